@@ -1,0 +1,160 @@
+/*
+ * conv2d.h -- C ABI of the GB300 (sm_103a) implicit-GEMM 2-D convolution forward.
+ *
+ * The operation: y = conv2d(x, w) + bias, computed as an implicit GEMM
+ *   M = N*P*Q output pixels, GEMM-N = K output channels, reduction over C*R*S,
+ * with the im2col operand formed on the fly in the loader and never written to
+ * memory.  Sources for the definition and its pieces:
+ *   - the convolution itself and its NHWC/KRSC layouts: docs.rs burn-cubecl 0.20.0,
+ *     burn_cubecl/kernel/conv/base.rs, conv_forward / conv_forward_nhwc (input and
+ *     weight both permuted NCHW->NHWC, i.e. weight [K][R][S][C]);
+ *   - "The bias added to each channel": the same page, conv_forward's doc comment;
+ *   - implicit GEMM as the conv algorithm: burn PR #2287 "Introduce autotuning to
+ *     conv2d and conv_transpose2d ..." (Changes) and burn PR #2545 "[Optimization]
+ *     Implicit gemm rewrite" (Changes);
+ *   - split-K with an in-place, serialised reduction on a per-tile semaphore, the
+ *     fp32 output doubling as the work buffer: NVIDIA/Fuser issue #1316 "Split-K
+ *     matmul is slow even for few partitions" (Eliminating the workspace, and the
+ *     comment on aliasing the output buffer).
+ *
+ * Math (cross-correlation, zero padding, groups = 1):
+ *   y[n][p][q][k] = bias[k] + sum_{r,s,c} x[n][p*sh-ph+r*dh][q*sw-pw+s*dw][c] * w[k][r][s][c]
+ *   P = floor((H + 2*ph - dh*(R-1) - 1)/sh) + 1,  Q likewise.
+ * Inputs are bf16, products are exact in fp32, accumulation is fp32 (tensor
+ * cores, TMEM), the output is fp32.
+ *
+ * Conventions for every entry point:
+ *   - Status is returned as an int (conv2d_status); nothing throws across the ABI.
+ *   - Pointers named *_dev are device pointers owned by the caller; pointers
+ *     named *_host are host pointers owned by the caller.  The library never
+ *     frees or retains them beyond the call.
+ *   - Tensors are dense and contiguous: x is [N][H][W][C] bf16, w is [K][R][S][C]
+ *     bf16, bias is [K] fp32, y is [N][P][Q][K] fp32.
+ *   - Device pointers must be 16-byte aligned, or the call returns
+ *     CONV2D_ERR_ALIGNMENT.
+ *   - Device work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting for it.
+ *   - Nothing is allocated on the device by these calls.
+ */
+#ifndef SPLIT_GEMM_GB300_CONV2D_H
+#define SPLIT_GEMM_GB300_CONV2D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA headers. */
+typedef struct CUstream_st* conv2d_stream_t;
+
+/* Problem description.  Options follow burn's ConvOptions (stride, padding,
+ * dilation, groups); padding is symmetric (pad_h rows above and below). */
+typedef struct {
+    int64_t n, h, w, c;  /* input  NHWC */
+    int64_t k, r, s;     /* weight KRSC: k output channels, r x s filter */
+    int32_t stride_h, stride_w;
+    int32_t pad_h, pad_w;
+    int32_t dil_h, dil_w;
+    int32_t groups;      /* must be 1 */
+} conv2d_params;
+
+typedef enum {
+    CONV2D_OK = 0,
+    CONV2D_ERR_INVALID = 1,     /* bad sizes/options, NULL pointer, empty window */
+    CONV2D_ERR_UNSUPPORTED = 2, /* groups != 1, sizes beyond 32-bit index range, or a forced algo that cannot run */
+    CONV2D_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned */
+    CONV2D_ERR_WORKSPACE = 4,   /* workspace missing or smaller than conv2d_fwd_workspace_bytes() */
+    CONV2D_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+    CONV2D_ERR_TIMEOUT = 6      /* a device-side wait ran out (reported by conv2d_fwd_status) */
+} conv2d_status;
+
+/* Loader kinds for the im2col (activation) operand. */
+typedef enum {
+    CONV2D_LOADER_AUTO = 0,
+    CONV2D_LOADER_TMA_IM2COL = 1, /* TMA im2col-mode descriptor; needs C % 64 == 0 */
+    CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C % 8 == 0 */
+    CONV2D_LOADER_SCALAR = 3      /* element gather; any C (also gathers the weight) */
+} conv2d_loader;
+
+/* Kernel configuration.  All-zero fields mean "let the heuristic choose". */
+typedef struct {
+    int32_t block_n;   /* output channels per CTA tile: 64, 128 or 256 */
+    int32_t splits;    /* split-K factor S >= 1 (CTAs per output tile, serialised in place) */
+    int32_t loader;    /* conv2d_loader */
+    int32_t reserved0;
+    int32_t debug_flags;      /* test hook, 0 in normal use; see CONV2D_DEBUG_* */
+    int32_t reserved1;
+    int64_t wait_limit_ns;    /* bound on every device-side wait; 0 = default (1 s) */
+} conv2d_algo;
+
+/* Test hook: split 0 of every tile skips its semaphore signal, so later splits'
+ * bounded waits run out and the call reports CONV2D_ERR_TIMEOUT. */
+#define CONV2D_DEBUG_SKIP_SIGNAL 1
+
+/* Output extents P and Q (pure host computation).  Returns CONV2D_OK or
+ * CONV2D_ERR_INVALID (bad options, or the filter window does not fit). */
+int conv2d_fwd_output_shape(const conv2d_params* params, int64_t* p, int64_t* q);
+
+/* Bytes of device workspace conv2d_fwd needs for these params with any
+ * algorithm: a status word plus one semaphore per output tile.  The workspace
+ * must be zero-filled before its first use; the kernels leave it zeroed after
+ * every successful call (the last split of a tile resets its semaphore). */
+size_t conv2d_fwd_workspace_bytes(const conv2d_params* params);
+
+/* The forward convolution.  x_dev, w_dev, y_dev: device tensors as above;
+ * bias_dev: [K] fp32 or NULL.  y is fully overwritten (its prior contents are
+ * ignored, also under split-K).  workspace_dev/workspace_bytes: see
+ * conv2d_fwd_workspace_bytes (may be NULL/0 only if the chosen split factor is 1).
+ * The algorithm is chosen by the host heuristic (conv2d_fwd_query_algo). */
+int conv2d_fwd(const conv2d_params* params, const void* x_dev, const void* w_dev,
+               const float* bias_dev, float* y_dev, void* workspace_dev,
+               size_t workspace_bytes, conv2d_stream_t stream);
+
+/* As conv2d_fwd with a forced configuration (any zero field is chosen by the
+ * heuristic).  Returns CONV2D_ERR_UNSUPPORTED if the forced configuration
+ * cannot run these params (e.g. the TMA loader with C % 64 != 0). */
+int conv2d_fwd_ex(const conv2d_params* params, const void* x_dev, const void* w_dev,
+                  const float* bias_dev, float* y_dev, void* workspace_dev,
+                  size_t workspace_bytes, conv2d_stream_t stream, const conv2d_algo* algo);
+
+/* What the heuristic picks for these params (tile width, split factor, loader),
+ * without launching anything.  Needs no device pointers; uses the current
+ * device's SM count. */
+int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out);
+
+/* Synchronises `stream`, then reads the workspace's device status word.
+ * Returns CONV2D_OK, CONV2D_ERR_TIMEOUT if a device-side wait ran out during a
+ * call that used this workspace, or CONV2D_ERR_CUDA.  After a timeout it zeroes
+ * the whole workspace (status and semaphores) so that it can be used again; the
+ * output of the failed call is undefined. */
+int conv2d_fwd_status(void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream);
+
+/* Bytes of device staging memory conv2d_fwd_host needs: room for x, w, bias,
+ * y and the workspace, each 256-byte aligned. */
+size_t conv2d_fwd_host_staging_bytes(const conv2d_params* params);
+
+/* End-to-end call for callers whose tensors live in host memory: enqueues on
+ * `stream` the host->device copies of x_host, w_host and bias_host (NULL for no
+ * bias), the convolution, and the device->host copy of y into y_host.  The
+ * caller provides `staging_dev` (conv2d_fwd_host_staging_bytes bytes of device
+ * memory that the library partitions; its workspace part must be zero before
+ * the first call and stays zero afterwards).  Host buffers should be pinned for
+ * the copies to be asynchronous; y_host is valid after the stream synchronises. */
+int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void* w_host,
+                    const float* bias_host, float* y_host, void* staging_dev,
+                    size_t staging_bytes, conv2d_stream_t stream);
+
+/* Number of kernel launches the last successful conv2d_fwd* call on this host
+ * thread enqueued (1 for every algorithm; 0 before any call and for empty problems). */
+int conv2d_last_launch_count(void);
+
+/* A static, human-readable message for a conv2d_status value. */
+const char* conv2d_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLIT_GEMM_GB300_CONV2D_H */

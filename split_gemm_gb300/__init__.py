@@ -1,0 +1,250 @@
+"""GB300 (sm_103a) implicit-GEMM 2-D convolution forward: Python binding.
+
+This module only marshals arguments to the C ABI in ``include/conv2d.h``
+(``libconv2d.so``, built in-tree by ``split_gemm_gb300._build``).  Every step of
+the computation runs in the library's CUDA kernels; PyTorch provides device
+memory and the current stream.  There is no fallback: if the library cannot be
+loaded, every call raises.
+
+    y = conv2d_fwd(x, w, bias, stride=1, padding=0, dilation=1)
+      x: [N,H,W,C] bf16 CUDA tensor (NHWC), w: [K,R,S,C] bf16 (KRSC),
+      bias: [K] fp32 or None  ->  y: [N,P,Q,K] fp32 (NHWC)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+from . import _build
+
+__all__ = [
+    "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
+    "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
+    "query_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
+    "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
+]
+
+LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR = 0, 1, 2, 3
+DEBUG_SKIP_SIGNAL = 1
+STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
+                4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT"}
+
+EXPORTED_SYMBOLS = [
+    "conv2d_fwd_output_shape", "conv2d_fwd_workspace_bytes", "conv2d_fwd", "conv2d_fwd_ex",
+    "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
+    "conv2d_last_launch_count", "conv2d_strerror",
+]
+
+
+class Conv2dError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_strerror_or_code(code)})")
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("h", ctypes.c_int64), ("w", ctypes.c_int64), ("c", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("r", ctypes.c_int64), ("s", ctypes.c_int64),
+                ("stride_h", ctypes.c_int32), ("stride_w", ctypes.c_int32),
+                ("pad_h", ctypes.c_int32), ("pad_w", ctypes.c_int32),
+                ("dil_h", ctypes.c_int32), ("dil_w", ctypes.c_int32), ("groups", ctypes.c_int32)]
+
+
+class Algo(ctypes.Structure):
+    _fields_ = [("block_n", ctypes.c_int32), ("splits", ctypes.c_int32), ("loader", ctypes.c_int32),
+                ("reserved0", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+    def as_dict(self):
+        return dict(block_n=self.block_n, splits=self.splits, loader=self.loader)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.POINTER(Params)
+    A = ctypes.POINTER(Algo)
+    vp, sz, i64p = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64)
+    lib.conv2d_fwd_output_shape.argtypes = [P, i64p, i64p]
+    lib.conv2d_fwd_output_shape.restype = ctypes.c_int
+    lib.conv2d_fwd_workspace_bytes.argtypes = [P]
+    lib.conv2d_fwd_workspace_bytes.restype = sz
+    lib.conv2d_fwd.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+    lib.conv2d_fwd.restype = ctypes.c_int
+    lib.conv2d_fwd_ex.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, A]
+    lib.conv2d_fwd_ex.restype = ctypes.c_int
+    lib.conv2d_fwd_query_algo.argtypes = [P, A]
+    lib.conv2d_fwd_query_algo.restype = ctypes.c_int
+    lib.conv2d_fwd_status.argtypes = [vp, sz, vp]
+    lib.conv2d_fwd_status.restype = ctypes.c_int
+    lib.conv2d_fwd_host_staging_bytes.argtypes = [P]
+    lib.conv2d_fwd_host_staging_bytes.restype = sz
+    lib.conv2d_fwd_host.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+    lib.conv2d_fwd_host.restype = ctypes.c_int
+    lib.conv2d_last_launch_count.argtypes = []
+    lib.conv2d_last_launch_count.restype = ctypes.c_int
+    lib.conv2d_strerror.argtypes = [ctypes.c_int]
+    lib.conv2d_strerror.restype = ctypes.c_char_p
+    return lib
+
+
+def load_library(build_if_stale: bool = True):
+    """Load (building first if needed) the CUDA library; raises if that is impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_stale and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"split_gemm_gb300: CUDA library {path} is missing; run __graft_entry__.build()")
+        _lib = _bind(ctypes.CDLL(path))
+        return _lib
+
+
+def _strerror_or_code(code: int) -> str:
+    try:
+        return load_library(build_if_stale=False).conv2d_strerror(code).decode()
+    except Exception:  # the message is best effort; the code is in the exception
+        return str(code)
+
+
+def strerror(code: int) -> str:
+    return load_library().conv2d_strerror(code).decode()
+
+
+def _pair(v) -> Tuple[int, int]:
+    if isinstance(v, (tuple, list)):
+        return int(v[0]), int(v[1])
+    return int(v), int(v)
+
+
+def make_params(x_shape, w_shape, stride=1, padding=0, dilation=1, groups=1) -> Params:
+    n, h, w, c = (int(v) for v in x_shape)
+    k, r, s, c2 = (int(v) for v in w_shape)
+    if groups == 1 and c2 != c:
+        raise ValueError(f"channel mismatch: input C={c}, weight C={c2}")
+    sh, sw = _pair(stride)
+    ph, pw = _pair(padding)
+    dh, dw = _pair(dilation)
+    return Params(n, h, w, c, k, r, s, sh, sw, ph, pw, dh, dw, int(groups))
+
+
+def output_shape(params: Params) -> Tuple[int, int]:
+    p, q = ctypes.c_int64(), ctypes.c_int64()
+    rc = load_library().conv2d_fwd_output_shape(ctypes.byref(params), ctypes.byref(p), ctypes.byref(q))
+    if rc:
+        raise Conv2dError(rc, "conv2d_fwd_output_shape")
+    return p.value, q.value
+
+
+def workspace_bytes(params: Params) -> int:
+    return int(load_library().conv2d_fwd_workspace_bytes(ctypes.byref(params)))
+
+
+def host_staging_bytes(params: Params) -> int:
+    return int(load_library().conv2d_fwd_host_staging_bytes(ctypes.byref(params)))
+
+
+def query_algo(params: Params) -> Algo:
+    out = Algo()
+    rc = load_library().conv2d_fwd_query_algo(ctypes.byref(params), ctypes.byref(out))
+    if rc:
+        raise Conv2dError(rc, "conv2d_fwd_query_algo")
+    return out
+
+
+def last_launch_count() -> int:
+    return int(load_library().conv2d_last_launch_count())
+
+
+# Per-device zero-filled workspaces (the kernels leave them zeroed after each call).
+# They assume one stream at a time per device; pass `workspace=` for concurrent streams.
+_ws_cache = {}
+
+
+def _default_workspace(nbytes: int, device):
+    import torch
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _check_tensor(t, name, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def conv2d_fwd_into(y, x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+                    algo: Optional[Algo] = None, stream=None) -> None:
+    """Writes conv2d(x, w) + bias into the preallocated fp32 NHWC tensor ``y`` (asynchronous)."""
+    import torch
+    _check_tensor(x, "x", torch.bfloat16, 4)
+    _check_tensor(w, "w", torch.bfloat16, 4)
+    _check_tensor(y, "y", torch.float32, 4)
+    if bias is not None:
+        _check_tensor(bias, "bias", torch.float32, 1)
+    params = make_params(x.shape, w.shape, stride, padding, dilation, groups)
+    lib = load_library()
+    if workspace is None:
+        workspace = _default_workspace(workspace_bytes(params), x.device)
+    ws_ptr, ws_len = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    args = (ctypes.byref(params), x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+            y.data_ptr(), ws_ptr, ws_len, st.cuda_stream)
+    rc = lib.conv2d_fwd(*args) if algo is None else lib.conv2d_fwd_ex(*args, ctypes.byref(algo))
+    if rc:
+        raise Conv2dError(rc, "conv2d_fwd")
+
+
+def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+               algo: Optional[Algo] = None, stream=None):
+    """Returns y = conv2d(x, w) + bias as a new fp32 NHWC CUDA tensor (asynchronous)."""
+    import torch
+    params = make_params(x.shape, w.shape, stride, padding, dilation, groups)
+    p, q = output_shape(params)
+    y = torch.empty((params.n, p, q, params.k), dtype=torch.float32, device=x.device)
+    conv2d_fwd_into(y, x, w, bias, stride, padding, dilation, groups, workspace=workspace, algo=algo,
+                    stream=stream)
+    return y
+
+
+def conv2d_fwd_host(x_host, w_host, bias_host, y_host, params: Params, staging, stream=None) -> None:
+    """End-to-end call on host tensors (pinned for async copies): H2D, conv, D2H on ``stream``."""
+    import torch
+    st = torch.cuda.current_stream() if stream is None else stream
+    rc = load_library().conv2d_fwd_host(
+        ctypes.byref(params), x_host.data_ptr(), w_host.data_ptr(),
+        None if bias_host is None else bias_host.data_ptr(), y_host.data_ptr(), staging.data_ptr(),
+        staging.numel() * staging.element_size(), st.cuda_stream)
+    if rc:
+        raise Conv2dError(rc, "conv2d_fwd_host")
+
+
+def status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's status (0 or CONV2D_ERR_TIMEOUT)."""
+    import torch
+    st = torch.cuda.current_stream() if stream is None else stream
+    return int(load_library().conv2d_fwd_status(workspace.data_ptr(),
+                                                workspace.numel() * workspace.element_size(), st.cuda_stream))

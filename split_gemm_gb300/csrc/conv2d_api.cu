@@ -1,0 +1,447 @@
+// Host side of the C ABI declared in include/conv2d.h: argument validation,
+// output shape, the tile / split / loader heuristic, TMA descriptor encoding
+// and the kernel launch.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "conv2d.h"
+#include "conv2d_kernel.cuh"
+
+namespace sgb {
+SGB_DECLARE_CONV2D(64)
+SGB_DECLARE_CONV2D(128)
+SGB_DECLARE_CONV2D(256)
+}  // namespace sgb
+
+namespace {
+
+using sgb::BK;
+using sgb::BM;
+
+constexpr int64_t kIndexLimit = (int64_t(1) << 31) - 1;
+constexpr size_t kStatusBytes = 256;  // status word, padded so the semaphores start 256-B aligned
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // 1 s
+
+thread_local int g_last_launches = 0;
+
+// ------------------------------------------------------------------ shape
+struct Shape {
+    int64_t n, h, w, c, k, r, s;
+    int64_t sh, sw, ph, pw, dh, dw;
+    int64_t p, q, m, crs;
+};
+
+int64_t out_extent(int64_t in, int64_t pad, int64_t dil, int64_t ker, int64_t stride)
+{
+    const int64_t span = dil * (ker - 1) + 1;
+    const int64_t room = in + 2 * pad - span;
+    if (room < 0) return 0;
+    return room / stride + 1;
+}
+
+int make_shape(const conv2d_params* prm, Shape* sh)
+{
+    if (!prm) return CONV2D_ERR_INVALID;
+    if (prm->groups != 1) return prm->groups < 1 ? CONV2D_ERR_INVALID : CONV2D_ERR_UNSUPPORTED;
+    if (prm->n < 0 || prm->k < 0 || prm->h < 1 || prm->w < 1 || prm->c < 1 || prm->r < 1 || prm->s < 1)
+        return CONV2D_ERR_INVALID;
+    if (prm->stride_h < 1 || prm->stride_w < 1 || prm->dil_h < 1 || prm->dil_w < 1 || prm->pad_h < 0 ||
+        prm->pad_w < 0)
+        return CONV2D_ERR_INVALID;
+    sh->n = prm->n; sh->h = prm->h; sh->w = prm->w; sh->c = prm->c;
+    sh->k = prm->k; sh->r = prm->r; sh->s = prm->s;
+    sh->sh = prm->stride_h; sh->sw = prm->stride_w;
+    sh->ph = prm->pad_h; sh->pw = prm->pad_w;
+    sh->dh = prm->dil_h; sh->dw = prm->dil_w;
+    // Guard the extent arithmetic itself against overflow before using it.
+    if (sh->h > kIndexLimit || sh->w > kIndexLimit || sh->r > kIndexLimit || sh->s > kIndexLimit ||
+        sh->c > kIndexLimit || sh->n > kIndexLimit || sh->k > kIndexLimit)
+        return CONV2D_ERR_UNSUPPORTED;
+    sh->p = out_extent(sh->h, sh->ph, sh->dh, sh->r, sh->sh);
+    sh->q = out_extent(sh->w, sh->pw, sh->dw, sh->s, sh->sw);
+    if (sh->p < 1 || sh->q < 1) return CONV2D_ERR_INVALID;
+    sh->crs = sh->c * sh->r * sh->s;
+    sh->m = sh->n * sh->p * sh->q;
+    // 32-bit device indexing: every element count must fit in int32.
+    if (sh->crs > kIndexLimit || sh->n * sh->h * sh->w * sh->c > kIndexLimit || sh->m > kIndexLimit ||
+        sh->m * sh->k > kIndexLimit || sh->k * sh->crs > kIndexLimit)
+        return CONV2D_ERR_UNSUPPORTED;
+    return CONV2D_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ device facts
+int sm_count_current()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cached[dev] = sms;
+    return sms;
+}
+
+// ------------------------------------------------------------------ TMA encoders (driver entry points)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_encode_im2col = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encoders()
+{
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q{};
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(fn);
+    });
+    return g_encode_tiled != nullptr && g_encode_im2col != nullptr;
+}
+
+// im2col-mode TMA limits for a rank-4 tensor: bounding-box corners in [-128, 127],
+// per-tap offsets that fit the instruction's offset field, traversal strides <= 8.
+bool tma_im2col_eligible(const Shape& s)
+{
+    if (s.c % BK != 0) return false;
+    const int64_t lo_w = -s.pw, lo_h = -s.ph;
+    const int64_t up_w = s.pw - (s.s - 1) * s.dw, up_h = s.ph - (s.r - 1) * s.dh;
+    auto in8 = [](int64_t v) { return v >= -128 && v <= 127; };
+    if (!in8(lo_w) || !in8(lo_h) || !in8(up_w) || !in8(up_h)) return false;
+    if ((s.s - 1) * s.dw > 255 || (s.r - 1) * s.dh > 255) return false;
+    if (s.sh > 8 || s.sw > 8) return false;
+    return true;
+}
+
+// ------------------------------------------------------------------ heuristic
+struct Plan {
+    int block_n;
+    int splits;
+    int loader;
+    int m_tiles, n_tiles, num_kb;
+};
+
+int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
+{
+    const int sms = sm_count_current();
+    // Loader.
+    int loader = force ? force->loader : 0;
+    if (loader == CONV2D_LOADER_AUTO) {
+        if (tma_im2col_eligible(s)) loader = CONV2D_LOADER_TMA_IM2COL;
+        else if (s.c % 8 == 0) loader = CONV2D_LOADER_CPASYNC;
+        else loader = CONV2D_LOADER_SCALAR;
+    } else if (loader == CONV2D_LOADER_TMA_IM2COL) {
+        if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader == CONV2D_LOADER_CPASYNC) {
+        if (s.c % 8 != 0) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader != CONV2D_LOADER_SCALAR) {
+        return CONV2D_ERR_INVALID;
+    }
+    // Tile width.
+    int bn = force ? force->block_n : 0;
+    if (bn == 0) bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    const int64_t m_tiles = cdiv(s.m, BM);
+    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t num_kb = cdiv(s.crs, BK);
+    const int64_t tiles = m_tiles * n_tiles;
+    // Split factor: spread a small tile grid over the SMs when the reduction is
+    // long enough that every split keeps at least four k-blocks.
+    int64_t splits = force ? force->splits : 0;
+    if (splits == 0) {
+        splits = 1;
+        if (sms > 0 && tiles < sms && num_kb >= 8) {
+            splits = sms / tiles;
+            if (splits > num_kb / 4) splits = num_kb / 4;
+            if (splits > 32) splits = 32;
+            if (splits < 1) splits = 1;
+        }
+    }
+    if (splits < 1) return CONV2D_ERR_INVALID;
+    if (splits > num_kb) return CONV2D_ERR_UNSUPPORTED;  // every split needs at least one k-block
+    if (tiles * splits > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
+    plan->block_n = bn;
+    plan->splits = static_cast<int>(splits);
+    plan->loader = loader;
+    plan->m_tiles = static_cast<int>(m_tiles);
+    plan->n_tiles = static_cast<int>(n_tiles);
+    plan->num_kb = static_cast<int>(num_kb);
+    return CONV2D_OK;
+}
+
+size_t workspace_bytes_for(const Shape& s)
+{
+    // Enough semaphores for the narrowest tile width.
+    const int64_t tiles = cdiv(s.m, BM) * cdiv(s.k, 64);
+    return kStatusBytes + static_cast<size_t>(tiles) * sizeof(uint32_t);
+}
+
+// ------------------------------------------------------------------ descriptors
+int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, float* y, bool tma_store,
+                CUtensorMap* tm_a, CUtensorMap* tm_b, CUtensorMap* tm_y)
+{
+    std::memset(tm_a, 0, sizeof(*tm_a));
+    std::memset(tm_b, 0, sizeof(*tm_b));
+    std::memset(tm_y, 0, sizeof(*tm_y));
+    if (!load_encoders()) return CONV2D_ERR_CUDA;
+    if (plan.loader == CONV2D_LOADER_TMA_IM2COL) {
+        const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                       (cuuint64_t)(s.h * s.w * s.c * 2)};
+        // Bounding box of window origins: lower corner -pad; upper corner measured
+        // from the last element, pad - (filter-1)*dilation.  Order {W, H}.
+        const int lower[2] = {(int)-s.pw, (int)-s.ph};
+        const int upper[2] = {(int)(s.pw - (s.s - 1) * s.dw), (int)(s.ph - (s.r - 1) * s.dh)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1};
+        CUresult rc = g_encode_im2col(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                                      strides, lower, upper, BK, BM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    }
+    if (plan.loader != CONV2D_LOADER_SCALAR) {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.crs, (cuuint64_t)s.k};
+        const cuuint64_t strides[1] = {(cuuint64_t)(s.crs * 2)};
+        const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)plan.block_n};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides,
+                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    }
+    if (tma_store) {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.k, (cuuint64_t)s.m};
+        const cuuint64_t strides[1] = {(cuuint64_t)(s.k * 4)};
+        const cuuint32_t box[2] = {32, (cuuint32_t)BM};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult rc = g_encode_tiled(tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    }
+    return CONV2D_OK;
+}
+
+cudaError_t dispatch(int bn, int loader, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                     const sgb::ConvKernelParams& kp, int grid, cudaStream_t st)
+{
+    using namespace sgb;
+#define SGB_CASE(BN_)                                                                                         \
+    if (bn == BN_) {                                                                                          \
+        if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<BN_, LOADER_TMA>(a, b, y, kp, grid, st); \
+        if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<BN_, LOADER_CPASYNC>(a, b, y, kp, grid, st); \
+        return launch_conv2d_tc<BN_, LOADER_SCALAR>(a, b, y, kp, grid, st);                                     \
+    }
+    SGB_CASE(64)
+    SGB_CASE(128)
+    SGB_CASE(256)
+#undef SGB_CASE
+    return cudaErrorInvalidValue;
+}
+
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("CONV2D_LOG");
+        return v && v[0] == '1';
+    }();
+    return on;
+}
+
+int run_conv(const conv2d_params* params, const void* x, const void* w, const float* bias, float* y,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.m == 0 || s.k == 0) return CONV2D_OK;  // empty batch or no filters: nothing to compute
+    if (!x || !w || !y) return CONV2D_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_ALIGNMENT;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->wait_limit_ns < 0)) return CONV2D_ERR_INVALID;
+    Plan plan;
+    rc = choose_plan(s, algo, &plan);
+    if (rc != CONV2D_OK) return rc;
+    const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(s);
+    if (plan.splits > 1 && !have_ws) return CONV2D_ERR_WORKSPACE;
+    if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
+    const bool tma_store = plan.splits == 1 && (s.k % 4) == 0;
+
+    CUtensorMap tm_a, tm_b, tm_y;
+    rc = encode_maps(s, plan, x, w, y, tma_store, &tm_a, &tm_b, &tm_y);
+    if (rc != CONV2D_OK) return rc;
+
+    sgb::ConvKernelParams kp{};
+    kp.x = static_cast<const uint16_t*>(x);
+    kp.w = static_cast<const uint16_t*>(w);
+    kp.bias = bias;
+    kp.y = y;
+    kp.status = have_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+    kp.sems = have_ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kStatusBytes) : nullptr;
+    kp.N = (int)s.n; kp.H = (int)s.h; kp.W = (int)s.w; kp.C = (int)s.c;
+    kp.K = (int)s.k; kp.R = (int)s.r; kp.S = (int)s.s; kp.P = (int)s.p; kp.Q = (int)s.q;
+    kp.sh = (int)s.sh; kp.sw = (int)s.sw; kp.ph = (int)s.ph; kp.pw = (int)s.pw; kp.dh = (int)s.dh; kp.dw = (int)s.dw;
+    kp.M = (int)s.m;
+    kp.CRS = (int)s.crs;
+    kp.num_kb = plan.num_kb;
+    kp.splits = plan.splits;
+    kp.m_tiles = plan.m_tiles;
+    kp.n_tiles = plan.n_tiles;
+    kp.use_tma_store = tma_store ? 1 : 0;
+    kp.debug_flags = algo ? algo->debug_flags : 0;
+    kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+
+    const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
+    if (log_enabled())
+        std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BN=%d splits=%d loader=%d grid=%lld tma_store=%d\n",
+                     (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_n, plan.splits, plan.loader,
+                     (long long)grid, (int)tma_store);
+    cudaError_t err = dispatch(plan.block_n, plan.loader, tm_a, tm_b, tm_y, kp, (int)grid, stream);
+    if (err != cudaSuccess) return CONV2D_ERR_CUDA;
+    g_last_launches = 1;
+    return CONV2D_OK;
+}
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+int conv2d_fwd_output_shape(const conv2d_params* params, int64_t* p, int64_t* q)
+{
+    Shape s;
+    const int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (p) *p = s.p;
+    if (q) *q = s.q;
+    return CONV2D_OK;
+}
+
+size_t conv2d_fwd_workspace_bytes(const conv2d_params* params)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    return workspace_bytes_for(s);
+}
+
+int conv2d_fwd_ex(const conv2d_params* params, const void* x_dev, const void* w_dev, const float* bias_dev,
+                  float* y_dev, void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream,
+                  const conv2d_algo* algo)
+{
+    return run_conv(params, x_dev, w_dev, bias_dev, y_dev, workspace_dev, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream), algo);
+}
+
+int conv2d_fwd(const conv2d_params* params, const void* x_dev, const void* w_dev, const float* bias_dev,
+               float* y_dev, void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream)
+{
+    return run_conv(params, x_dev, w_dev, bias_dev, y_dev, workspace_dev, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
+{
+    if (!out) return CONV2D_ERR_INVALID;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    Plan plan;
+    rc = choose_plan(s, nullptr, &plan);
+    if (rc != CONV2D_OK) return rc;
+    std::memset(out, 0, sizeof(*out));
+    out->block_n = plan.block_n;
+    out->splits = plan.splits;
+    out->loader = plan.loader;
+    return CONV2D_OK;
+}
+
+int conv2d_fwd_status(void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream)
+{
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (!workspace_dev) return CONV2D_OK;
+    if (workspace_bytes < sizeof(uint32_t)) return CONV2D_ERR_WORKSPACE;
+    uint32_t status = 0;
+    if (cudaMemcpy(&status, workspace_dev, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    if (status == 0) return CONV2D_OK;
+    if (cudaMemset(workspace_dev, 0, workspace_bytes) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CONV2D_ERR_CUDA;
+    return status == CONV2D_ERR_TIMEOUT ? CONV2D_ERR_TIMEOUT : CONV2D_ERR_CUDA;
+}
+
+size_t conv2d_fwd_host_staging_bytes(const conv2d_params* params)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    return round256(s.n * s.h * s.w * s.c * 2) + round256(s.k * s.crs * 2) + round256(s.k * 4) +
+           round256(s.m * s.k * 4) + round256(workspace_bytes_for(s));
+}
+
+int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void* w_host, const float* bias_host,
+                    float* y_host, void* staging_dev, size_t staging_bytes, conv2d_stream_t stream)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.m == 0 || s.k == 0) return CONV2D_OK;
+    if (!x_host || !w_host || !y_host || !staging_dev) return CONV2D_ERR_INVALID;
+    if (staging_bytes < conv2d_fwd_host_staging_bytes(params)) return CONV2D_ERR_WORKSPACE;
+    if (!aligned16(staging_dev)) return CONV2D_ERR_ALIGNMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(staging_dev);
+    const size_t xb = s.n * s.h * s.w * s.c * 2, wb = s.k * s.crs * 2, bb = s.k * 4, yb = s.m * s.k * 4;
+    char* xd = base;
+    char* wd = xd + round256(xb);
+    char* bd = wd + round256(wb);
+    char* yd = bd + round256(bb);
+    char* ws = yd + round256(yb);
+    if (cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (cudaMemcpyAsync(wd, w_host, wb, cudaMemcpyHostToDevice, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (bias_host && cudaMemcpyAsync(bd, bias_host, bb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return CONV2D_ERR_CUDA;
+    rc = run_conv(params, xd, wd, bias_host ? reinterpret_cast<float*>(bd) : nullptr, reinterpret_cast<float*>(yd),
+                  ws, workspace_bytes_for(s), st, nullptr);
+    if (rc != CONV2D_OK) return rc;
+    if (cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return CONV2D_ERR_CUDA;
+    return CONV2D_OK;
+}
+
+int conv2d_last_launch_count(void) { return g_last_launches; }
+
+const char* conv2d_strerror(int status)
+{
+    switch (status) {
+        case CONV2D_OK: return "ok";
+        case CONV2D_ERR_INVALID: return "invalid argument (sizes, options or pointers)";
+        case CONV2D_ERR_UNSUPPORTED: return "unsupported (groups != 1, sizes beyond 32-bit indexing, or forced algo)";
+        case CONV2D_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case CONV2D_ERR_WORKSPACE: return "workspace missing or too small";
+        case CONV2D_ERR_CUDA: return "CUDA runtime or driver error";
+        case CONV2D_ERR_TIMEOUT: return "a device-side wait ran out (workspace reset)";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,6 @@
+// Kernel instantiations for 64-channel output tiles (all three loaders).
+#include "conv2d_kernel.cuh"
+
+namespace sgb {
+SGB_INSTANTIATE_CONV2D(64)
+}  // namespace sgb
