@@ -64,6 +64,8 @@ def _bind(path: str):
     lib.oracle_conv2d_bf16.argtypes = [i64p, i64p, vp, vp, vp, vp, ctypes.c_int]
     lib.oracle_conv2d_points_bf16.restype = ctypes.c_int
     lib.oracle_conv2d_points_bf16.argtypes = [i64p, i64p, vp, vp, vp, vp, vp, ctypes.c_int64, vp]
+    lib.oracle_conv2d_points_f64.restype = ctypes.c_int
+    lib.oracle_conv2d_points_f64.argtypes = [i64p, i64p, vp, vp, vp, vp, vp, ctypes.c_int64, vp]
     return lib
 
 
@@ -194,6 +196,32 @@ def conv2d_fwd_points(x, w, bias, stride, padding, dilation, m_idx: Sequence[int
     if rc != 0:
         raise ValueError(f"oracle_conv2d_points_bf16 failed with code {rc}")
     return out
+
+
+def conv2d_fwd_points_f64(x: np.ndarray, w: np.ndarray, bias, stride, padding, dilation, m_idx, k_idx,
+                          lib=None) -> np.ndarray:
+    """As conv2d_fwd_points over float64 inputs (widen once, sample many times)."""
+    lib = lib or load()
+    xs = np.ascontiguousarray(x, dtype=np.float64)
+    ws = np.ascontiguousarray(w, dtype=np.float64)
+    b = _bias_f32(bias)
+    _, _, dims, opts = _dims_opts(xs.shape, ws.shape, stride, padding, dilation)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64)
+    ki = np.ascontiguousarray(k_idx, dtype=np.int64)
+    if mi.shape != ki.shape:
+        raise ValueError("m_idx and k_idx must have the same length")
+    out = np.zeros(mi.shape, dtype=np.float64)
+    rc = lib.oracle_conv2d_points_f64(dims, opts, _ptr(xs), _ptr(ws), _ptr(b), _ptr(mi), _ptr(ki),
+                                      int(mi.size), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_conv2d_points_f64 failed with code {rc}")
+    return out
+
+
+def widen_bf16(t) -> np.ndarray:
+    """bf16 tensor -> float64 array holding exactly the same values."""
+    bits = _bf16_bits(t).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
 
 
 def tolerance(c: int, r: int, s: int) -> Tuple[float, float]:

@@ -176,6 +176,27 @@ int oracle_conv2d_bf16(const int64_t dims[7], const int64_t opts[6], const uint1
     return rc;
 }
 
+/* Selected output elements y[m_idx[i]][k_idx[i]] over already-widened inputs. */
+static void points_f64(const oracle_shape* sp, const double* x, const double* w, const float* bias,
+                       const int64_t* m_idx, const int64_t* k_idx, int64_t npts, double* out)
+{
+    for (int64_t i = 0; i < npts; ++i) {
+        int64_t m = m_idx[i];
+        int64_t q = m % sp->q;
+        int64_t p = (m / sp->q) % sp->p;
+        int64_t n = m / (sp->q * sp->p);
+        out[i] = conv_point(sp, x, w, bias, n, p, q, k_idx[i]);
+    }
+}
+
+static int check_points(const oracle_shape* sp, const int64_t* m_idx, const int64_t* k_idx, int64_t npts)
+{
+    int64_t mtot = sp->n * sp->p * sp->q;
+    for (int64_t i = 0; i < npts; ++i)
+        if (m_idx[i] < 0 || m_idx[i] >= mtot || k_idx[i] < 0 || k_idx[i] >= sp->k) return 1;
+    return 0;
+}
+
 /*
  * Selected output elements only: for each i, out[i] = y[m_idx[i]][k_idx[i]] where
  * m = (n*P + p)*Q + q is the row of the NHWC output viewed as [N*P*Q][K].
@@ -186,23 +207,23 @@ int oracle_conv2d_points_bf16(const int64_t dims[7], const int64_t opts[6], cons
                               const int64_t* k_idx, int64_t npts, double* out)
 {
     oracle_shape sp;
-    if (make_shape(&sp, dims, opts)) return 1;
-    int64_t mtot = sp.n * sp.p * sp.q;
-    for (int64_t i = 0; i < npts; ++i)
-        if (m_idx[i] < 0 || m_idx[i] >= mtot || k_idx[i] < 0 || k_idx[i] >= sp.k) return 1;
-    int64_t nx = sp.n * sp.h * sp.w * sp.c;
-    int64_t nw = sp.k * sp.r * sp.s * sp.c;
-    double* xd = widen_bf16(x, nx);
-    double* wd = widen_bf16(w, nw);
+    if (make_shape(&sp, dims, opts) || check_points(&sp, m_idx, k_idx, npts)) return 1;
+    double* xd = widen_bf16(x, sp.n * sp.h * sp.w * sp.c);
+    double* wd = widen_bf16(w, sp.k * sp.r * sp.s * sp.c);
     if (!xd || !wd) { free(xd); free(wd); return 2; }
-    for (int64_t i = 0; i < npts; ++i) {
-        int64_t m = m_idx[i];
-        int64_t q = m % sp.q;
-        int64_t p = (m / sp.q) % sp.p;
-        int64_t n = m / (sp.q * sp.p);
-        out[i] = conv_point(&sp, xd, wd, bias, n, p, q, k_idx[i]);
-    }
+    points_f64(&sp, xd, wd, bias, m_idx, k_idx, npts, out);
     free(xd);
     free(wd);
+    return 0;
+}
+
+/* As oracle_conv2d_points_bf16 over double inputs (for repeated sampling of one problem). */
+int oracle_conv2d_points_f64(const int64_t dims[7], const int64_t opts[6], const double* x,
+                             const double* w, const float* bias, const int64_t* m_idx,
+                             const int64_t* k_idx, int64_t npts, double* out)
+{
+    oracle_shape sp;
+    if (make_shape(&sp, dims, opts) || check_points(&sp, m_idx, k_idx, npts)) return 1;
+    points_f64(&sp, x, w, bias, m_idx, k_idx, npts, out);
     return 0;
 }

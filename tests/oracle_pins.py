@@ -278,6 +278,8 @@ def pin_points_and_bf16(lib):
     ki = rng.integers(0, flat.shape[1], size=64)
     pts = oracle.conv2d_fwd_points(xb, wb, b, st, pd, dl, mi, ki, lib=lib)
     assert np.array_equal(pts, flat[mi, ki])
+    pts64 = oracle.conv2d_fwd_points_f64(x, w, b, st, pd, dl, mi, ki, lib=lib)
+    assert np.array_equal(pts64, flat[mi, ki])
     # bf16 widening of non-integer patterns: 1.5, -0.375, 2^-10, 3.0e38-ish
     vals = np.array([1.5, -0.375, 2.0 ** -10, 1.0e30], dtype=np.float32)
     bits = (vals.view(np.uint32) >> 16).astype(np.uint16)

@@ -34,7 +34,7 @@ MUTANTS = {
     "bf16_shift_wrong": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
     "thread_block_gap": ("jobs[t].row_end = rows * (t + 1) / threads;",
                          "jobs[t].row_end = rows * (t + 1) / threads - (t == 1);"),
-    "points_q_index": ("int64_t q = m % sp.q;", "int64_t q = m % sp.p;"),
+    "points_q_index": ("int64_t q = m % sp->q;", "int64_t q = m % sp->p;"),
     "output_k_stride": ("* sp->q + q) * sp->k + k]", "* sp->q + q) * sp->k + (k + 1) % sp->k]"),
 }
 
