@@ -31,6 +31,10 @@ constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // 1 s
 
 thread_local int g_last_launches = 0;
 
+#ifdef SGB_TRACE_ENABLED
+unsigned long long* g_trace = nullptr;  // profiling builds only: per-CTA phase timestamps
+#endif
+
 // ------------------------------------------------------------------ shape
 struct Shape {
     int64_t n, h, w, c, k, r, s;
@@ -284,7 +288,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(s);
     if (plan.splits > 1 && !have_ws) return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
-    const bool tma_store = plan.splits == 1 && (s.k % 4) == 0;
+    const bool tma_store = (s.k % 4) == 0;
 
     CUtensorMap tm_a, tm_b, tm_y;
     rc = encode_maps(s, plan, x, w, y, tma_store, &tm_a, &tm_b, &tm_y);
@@ -309,6 +313,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.use_tma_store = tma_store ? 1 : 0;
     kp.debug_flags = algo ? algo->debug_flags : 0;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+    kp.trace = nullptr;
+#ifdef SGB_TRACE_ENABLED
+    kp.trace = g_trace;
+#endif
 
     const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
     if (log_enabled())
@@ -429,6 +437,11 @@ int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void*
 }
 
 int conv2d_last_launch_count(void) { return g_last_launches; }
+
+#ifdef SGB_TRACE_ENABLED
+// Profiling builds only: device buffer of grid x 16 timestamps that later launches fill.
+void conv2d_debug_set_trace(void* trace_dev) { g_trace = static_cast<unsigned long long*>(trace_dev); }
+#endif
 
 const char* conv2d_strerror(int status)
 {

@@ -31,7 +31,7 @@
 // the last split resets it to 0.  The fp32 output is the work buffer, so the
 // only extra memory is one 32-bit word per tile.
 //
-// Every wait is bounded (wait_limit_ns of global time).  A wait that runs out
+// Every wait is bounded (about wait_limit_ns, counted in SM cycles).  A wait that runs out
 // records CONV2D_ERR_TIMEOUT in the status word, and the CTA drains its own
 // in-flight copies and MMAs, frees its tensor memory and exits.
 #pragma once
@@ -70,7 +70,22 @@ struct ConvKernelParams {
     int use_tma_store;
     int debug_flags;
     unsigned long long wait_limit_ns;
+    unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
 };
+
+// Phase timestamps for profiling builds (compiled with SGB_TRACE_ENABLED):
+// slot `slot` of CTA blockIdx.x gets the global timer when `cond` holds.
+#ifdef SGB_TRACE_ENABLED
+#define SGB_TRACE(kp, cond, slot)                                                               \
+    do {                                                                                        \
+        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 16 + (slot)] =   \
+            ::sgb::ptx::globaltimer();                                                          \
+    } while (0)
+#else
+#define SGB_TRACE(kp, cond, slot) \
+    do {                          \
+    } while (0)
+#endif
 
 template <int BN>
 struct TileConfig {
@@ -149,8 +164,10 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
             }
         }
         ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], (kb_begin + i) * BK, n0);
+        SGB_TRACE(kp, i == 0, 2);
         ++issued;
     }
+    SGB_TRACE(kp, true, 3);
     // Drain: the last loads of each stage must have landed before the CTA can exit.
     for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
         ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
@@ -172,6 +189,7 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
             break;
         }
         ptx::tc_fence_after();
+        SGB_TRACE(kp, i == 0, 4);
         const uint32_t a_addr = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
         const uint32_t b_addr = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
 #pragma unroll
@@ -185,8 +203,10 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     }
     // Signals the epilogue, and (waiting on it here too) guarantees no MMA is in
     // flight when the CTA reaches its teardown.
+    SGB_TRACE(kp, true, 5);
     ptx::mma_commit(sm.acc_full);
     ptx::mbar_wait(sm.acc_full, 0u, kp.wait_limit_ns);
+    SGB_TRACE(kp, true, 6);
 }
 
 // ---------------------------------------------------------------- gather producers (warps 2..5)
@@ -361,6 +381,33 @@ __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm
 }
 
 // ---------------------------------------------------------------- epilogue (warps 2..5)
+// Waits (thread et == 0, bounded) until the tile semaphore reads `split`.
+__device__ __forceinline__ bool wait_turn(const ConvKernelParams& kp, int tile, int split,
+                                          volatile uint32_t* abort_flag)
+{
+    const uint32_t* sem = kp.sems + tile;
+    if (ptx::ld_acquire_gpu(sem) == static_cast<uint32_t>(split)) return true;
+    const uint64_t t0 = ptx::clock64();
+    const uint64_t limit = ptx::ns_to_cycles(kp.wait_limit_ns);
+    while (ptx::ld_acquire_gpu(sem) != static_cast<uint32_t>(split)) {
+        __nanosleep(32);
+        if (ptx::clock64() - t0 > limit) {
+            record_timeout(kp, abort_flag);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Publishes the next split's turn (the last split resets the semaphore to 0).
+__device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, int tile, int split)
+{
+    const bool skip = (kp.debug_flags & 1) && split == 0;  // test hook: never signal
+    if (skip) return;
+    const uint32_t next = (split + 1 == kp.splits) ? 0u : static_cast<uint32_t>(split + 1);
+    ptx::st_release_gpu(kp.sems + tile, next);
+}
+
 template <int BN>
 __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp, const SmemView& sm,
                              uint32_t tmem_base, int m0, int n0, int split, int tile)
@@ -371,6 +418,7 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
     const int m = m0 + row;
     const bool row_ok = m < kp.M;
     const bool add_bias = kp.bias != nullptr && split == 0;
+    const bool serial = kp.splits > 1;
 
     const bool acc_ready = ptx::mbar_wait(sm.acc_full, 0u, kp.wait_limit_ns);
     if (!acc_ready) record_timeout(kp, sm.abort_flag);
@@ -380,12 +428,17 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
     if (et == 0) *sm.epi_go = (*sm.abort_flag == 0u) ? 1u : 0u;
     ptx::named_bar_sync(1, EPI_THREADS);
     if (!*sm.epi_go) return;
+    SGB_TRACE(kp, et == 0, 7);
     ptx::tc_fence_after();
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
 
-    if (kp.splits == 1 && kp.use_tma_store) {
-        // TMEM -> registers (+bias) -> 128-B swizzled shared slabs of 32 columns -> TMA store.
+    if (kp.use_tma_store) {
+        // TMEM -> registers (+bias) -> 128-B swizzled shared slabs of 32 columns.
+        // Split 0 (or no split) stores each slab as soon as it is complete; later
+        // splits stage every slab, wait for their turn, then let the TMA unit add
+        // the slabs into y in place.
         uint8_t* stage_base = sm.a;  // the ring is idle once the accumulator is complete
+        const bool store_now = split == 0;
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j) {
             uint32_t v[32];
@@ -404,42 +457,50 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
             for (int c = 0; c < 8; ++c)
                 ptx::st_shared_v4(slab + sw128_offset(row, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1, EPI_THREADS);
-            if (et == 0) {
-                ptx::tma_store_2d(tm_y, stage_base + j * (BM * 128), n0 + j * 32, m0);
-                ptx::bulk_commit();
+            if (store_now) {
+                ptx::named_bar_sync(1, EPI_THREADS);
+                if (et == 0) {
+                    ptx::tma_store_2d(tm_y, stage_base + j * (BM * 128), n0 + j * 32, m0);
+                    ptx::bulk_commit();
+                }
             }
         }
-        if (et == 0) ptx::bulk_wait_read_all();
+        if (!store_now) {
+            ptx::named_bar_sync(1, EPI_THREADS);
+            if (et == 0 && wait_turn(kp, tile, split, sm.abort_flag)) {
+                ptx::fence_proxy_async_global();
+#pragma unroll 1
+                for (int j = 0; j < BN / 32; ++j)
+                    ptx::tma_reduce_add_2d(tm_y, stage_base + j * (BM * 128), n0 + j * 32, m0);
+                ptx::bulk_commit();
+                ptx::bulk_wait_all();
+                ptx::fence_proxy_async_global();
+                __threadfence();
+                pass_turn(kp, tile, split);
+            }
+        } else if (et == 0) {
+            if (serial) {
+                ptx::bulk_wait_all();  // writes done before the next split may add to them
+                ptx::fence_proxy_async_global();
+                __threadfence();
+                pass_turn(kp, tile, split);
+            } else {
+                ptx::bulk_wait_read_all();
+            }
+        }
+        SGB_TRACE(kp, et == 0, 8);
         return;
     }
 
-    if (kp.splits > 1) {
-        // Wait for this split's turn on the tile semaphore.
-        if (et == 0) {
-            const uint32_t* sem = kp.sems + tile;
-            bool ok = true;
-            if (ptx::ld_acquire_gpu(sem) != static_cast<uint32_t>(split)) {
-                const uint64_t t0 = ptx::globaltimer();
-                while (ptx::ld_acquire_gpu(sem) != static_cast<uint32_t>(split)) {
-                    __nanosleep(64);
-                    if (ptx::globaltimer() - t0 > kp.wait_limit_ns) {
-                        record_timeout(kp, sm.abort_flag);
-                        ok = false;
-                        break;
-                    }
-                }
-            }
-            *sm.epi_go = ok ? 1u : 0u;
-        }
+    // K % 4 != 0: row-per-thread stores (split 0 / no split) or read-add-write
+    // (later splits, in turn).
+    if (serial && split > 0) {
+        if (et == 0) *sm.epi_go = wait_turn(kp, tile, split, sm.abort_flag) ? 1u : 0u;
         ptx::named_bar_sync(1, EPI_THREADS);
         if (!*sm.epi_go) return;
     }
-
-    // Row-per-thread stores (split 0 / no split) or read-add-write (later splits).
     const bool accumulate = split > 0;
     float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
-    const bool vec_ok = (kp.K % 4) == 0;
 #pragma unroll 1
     for (int j = 0; j < BN / 32; ++j) {
         uint32_t v[32];
@@ -447,50 +508,27 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
         ptx::tmem_ld_wait();
         if (!row_ok) continue;
         const int nb = n0 + j * 32;
+        float old[32];
+        if (accumulate) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
+            for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
             const int n = nb + e;
-            if (vec_ok && n + 3 < kp.K) {
-                float4 o = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                       __uint_as_float(v[e + 3]));
-                if (add_bias) {
-                    o.x += __ldg(kp.bias + n);
-                    o.y += __ldg(kp.bias + n + 1);
-                    o.z += __ldg(kp.bias + n + 2);
-                    o.w += __ldg(kp.bias + n + 3);
-                }
-                float4* dst = reinterpret_cast<float4*>(yrow + n);
-                if (accumulate) {
-                    const float4 old = *dst;
-                    o.x = old.x + o.x;
-                    o.y = old.y + o.y;
-                    o.z = old.z + o.z;
-                    o.w = old.w + o.w;
-                }
-                *dst = o;
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int nn = n + u;
-                    if (nn >= kp.K) break;
-                    float o = __uint_as_float(v[e + u]);
-                    if (add_bias) o += __ldg(kp.bias + nn);
-                    if (accumulate) o = yrow[nn] + o;
-                    yrow[nn] = o;
-                }
-            }
+            if (n >= kp.K) break;
+            float o = __uint_as_float(v[e]);
+            if (add_bias) o += __ldg(kp.bias + n);
+            if (accumulate) o = old[e] + o;
+            yrow[n] = o;
         }
     }
-
-    if (kp.splits > 1) {
+    if (serial) {
         __threadfence();
         ptx::named_bar_sync(1, EPI_THREADS);
-        const bool skip = (kp.debug_flags & 1) && split == 0;  // test hook: never signal
-        if (et == 0 && !skip) {
-            const uint32_t next = (split + 1 == kp.splits) ? 0u : static_cast<uint32_t>(split + 1);
-            ptx::st_release_gpu(kp.sems + tile, next);
-        }
+        if (et == 0) pass_turn(kp, tile, split);
     }
+    SGB_TRACE(kp, et == 0, 8);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -526,6 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int kb_begin = static_cast<int>(static_cast<int64_t>(split) * kp.num_kb / kp.splits);
     const int kb_end = static_cast<int>(static_cast<int64_t>(split + 1) * kp.num_kb / kp.splits);
     const int nkb = kb_end - kb_begin;
+    SGB_TRACE(kp, threadIdx.x == 0, 0);
 
     if (threadIdx.x == 0) {
         const uint32_t full_count =
@@ -552,6 +591,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
+    SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
         if (lane == 0 && LOADER != LOADER_SCALAR)
@@ -561,6 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         if (LOADER == LOADER_CPASYNC) run_gather_cpasync<BN>(kp, sm, m0, kb_begin, nkb);
         if (LOADER == LOADER_SCALAR) run_gather_scalar<BN>(kp, sm, m0, n0, kb_begin, nkb);
+        SGB_TRACE(kp, threadIdx.x == EPI_THREAD0, 9);
         run_epilogue<BN>(&tm_y, kp, sm, tmem_base, m0, n0, split, tile);
     }
 
@@ -570,6 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
+    SGB_TRACE(kp, threadIdx.x == 0, 10);
 }
 
 // Host-side launcher for one instantiation; explicitly instantiated in one

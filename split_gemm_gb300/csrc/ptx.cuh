@@ -21,6 +21,18 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+__device__ __forceinline__ uint64_t clock64()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+    return t;
+}
+
+// Bounds are kept in SM cycles (cheap to read) rather than global time: a
+// nanosecond limit becomes 2.5 cycles per ns, at least the limit at any SM
+// clock up to 2.5 GHz.
+__device__ __forceinline__ uint64_t ns_to_cycles(uint64_t ns) { return ns * 5u / 2u; }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {
@@ -59,16 +71,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` nanoseconds of global time and returns false.
+// about `limit_ns` nanoseconds (counted in SM cycles) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    const uint64_t t0 = clock64();
+    const uint64_t limit = ns_to_cycles(limit_ns);
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > limit_ns) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 
@@ -109,7 +122,22 @@ __device__ __forceinline__ void tma_store_2d(const void* map, const void* src, i
                  : "memory");
 }
 
+// y[tile] += smem tile, element-wise fp32 add performed by the TMA unit.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* map, const void* src, int32_t x, int32_t y)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until all committed bulk operations have completed, writes included.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's async-proxy global accesses with its generic-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Waits until the shared-memory sources of all committed bulk stores have been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
