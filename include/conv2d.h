@@ -67,7 +67,8 @@ typedef enum {
     CONV2D_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned */
     CONV2D_ERR_WORKSPACE = 4,   /* workspace missing or smaller than conv2d_fwd_workspace_bytes() */
     CONV2D_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
-    CONV2D_ERR_TIMEOUT = 6      /* a device-side wait ran out (reported by conv2d_fwd_status) */
+    CONV2D_ERR_TIMEOUT = 6,     /* a device-side wait ran out (reported by conv2d_fwd_status) */
+    CONV2D_ERR_SCRATCH_LIMIT = 7 /* conv2d_fwd_noalloc: problem needs more than CONV2D_NOALLOC_SCRATCH_BYTES */
 } conv2d_status;
 
 /* Loader kinds for the im2col (activation) operand. */
@@ -149,6 +150,34 @@ int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void*
 /* Number of kernel launches the last successful conv2d_fwd* call on this host
  * thread enqueued (1 for every algorithm; 0 before any call and for empty problems). */
 int conv2d_last_launch_count(void);
+
+/* Size of the library's built-in device scratch array used by conv2d_fwd_noalloc. */
+#define CONV2D_NOALLOC_SCRATCH_BYTES 65536
+
+/* The pages have no counterpart to this entry point.  It is conv2d_fwd for
+ * callers that cannot allocate device memory, so cannot pass a workspace: for
+ * example plugins whose host framework owns every device allocation, deployments
+ * that forbid allocation after start-up, or latency-critical loops that must not
+ * call cudaMalloc/cudaFree because those can synchronise the device.  It takes
+ * the same inputs and outputs as conv2d_fwd (caller-owned device memory) and
+ * allocates nothing; the workspace is a static device array of
+ * CONV2D_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *   - Problems whose conv2d_fwd_workspace_bytes() exceeds that size are rejected
+ *     with CONV2D_ERR_SCRATCH_LIMIT before anything is enqueued (65536 bytes
+ *     cover 16320 output tiles of 128 pixels x 64 channels).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - Every call clears the part of the array it uses (cudaMemsetAsync on
+ *     `stream`) and then enqueues the kernel.  All calls on one device share
+ *     that device's copy of the array, and it keeps the previous call's
+ *     contents, so calls that can overlap on the GPU (for example on two
+ *     streams) race with each other: serialise them.
+ *   - Device-side timeouts are not reported here (the status word is cleared by
+ *     the next call); use conv2d_fwd + conv2d_fwd_status where that matters. */
+int conv2d_fwd_noalloc(const conv2d_params* params, const void* x_dev, const void* w_dev,
+                       const float* bias_dev, float* y_dev, conv2d_stream_t stream);
 
 /* A static, human-readable message for a conv2d_status value. */
 const char* conv2d_strerror(int status);

@@ -29,12 +29,13 @@ __all__ = [
 LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR = 0, 1, 2, 3
 DEBUG_SKIP_SIGNAL = 1
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
-                4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT"}
+                4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT",
+                7: "CONV2D_ERR_SCRATCH_LIMIT"}
 
 EXPORTED_SYMBOLS = [
     "conv2d_fwd_output_shape", "conv2d_fwd_workspace_bytes", "conv2d_fwd", "conv2d_fwd_ex",
     "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
-    "conv2d_last_launch_count", "conv2d_strerror",
+    "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc",
 ]
 
 
@@ -91,6 +92,8 @@ def _bind(lib):
     lib.conv2d_fwd_host.restype = ctypes.c_int
     lib.conv2d_last_launch_count.argtypes = []
     lib.conv2d_last_launch_count.restype = ctypes.c_int
+    lib.conv2d_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
+    lib.conv2d_fwd_noalloc.restype = ctypes.c_int
     lib.conv2d_strerror.argtypes = [ctypes.c_int]
     lib.conv2d_strerror.restype = ctypes.c_char_p
     return lib

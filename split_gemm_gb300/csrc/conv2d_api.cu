@@ -453,6 +453,8 @@ const char* conv2d_strerror(int status)
         case CONV2D_ERR_WORKSPACE: return "workspace missing or too small";
         case CONV2D_ERR_CUDA: return "CUDA runtime or driver error";
         case CONV2D_ERR_TIMEOUT: return "a device-side wait ran out (workspace reset)";
+        case CONV2D_ERR_SCRATCH_LIMIT:
+            return "problem needs more workspace than the no-allocation entry point's static scratch array holds";
         default: return "unknown status";
     }
 }

@@ -67,6 +67,6 @@ def test_workspace_and_staging_sizes():
 
 
 def test_strerror_covers_codes():
-    for code in range(7):
+    for code in range(8):
         assert sg.strerror(code)
     assert sg.strerror(99) == "unknown status"
