@@ -289,7 +289,13 @@ def run_ours(args, wl, world, rank, local):
     x, w, b = workloads.make_inputs(wl)
     params = sg.make_params(x.shape, w.shape, **wl.options())
     p, q = sg.output_shape(params)
+    forced = None
+    if args.block_n or args.splits or args.loader:
+        forced = sg.Algo()
+        forced.block_n, forced.splits, forced.loader = args.block_n, args.splits, args.loader
     algo = sg.query_algo(params)
+    if forced is not None:
+        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits or algo.splits, forced.loader or algo.loader)
     set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * 4 + (0 if b is None else b.numel() * 4)
     n_sets = _sets_for(wl, set_bytes)
     sets = []
@@ -302,7 +308,7 @@ def run_ours(args, wl, world, rank, local):
 
     def step(i):
         xd, wd, bd, yd = sets[i % n_sets]
-        sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws)
+        sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws, algo=forced)
 
     K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
@@ -488,6 +494,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time for cpu_baseline")
+    ap.add_argument("--block-n", type=int, default=0, help="force the output-channel tile width (64/128/256)")
+    ap.add_argument("--splits", type=int, default=0, help="force the split-K factor")
+    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar)")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")

@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "ptx.cuh"
 
@@ -591,6 +592,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
+    // Everything above touches only shared memory, tensor memory and kernel
+    // parameters, so it may overlap the previous kernel in the stream.  Global
+    // memory (inputs it may have written, y and the workspace it may still read)
+    // is touched only after this wait.
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
@@ -614,6 +621,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 10);
 }
 
+// Overlap of consecutive launches (programmatic dependent launch) is on unless
+// the environment sets CONV2D_NO_PDL=1.
+inline bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("CONV2D_NO_PDL");
+        return !(v && v[0] == '1');
+    }();
+    return on;
+}
+
 // Host-side launcher for one instantiation; explicitly instantiated in one
 // translation unit per tile width so that the variants compile in parallel.
 template <int BN, int LOADER>
@@ -633,8 +651,20 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
         if (err != cudaSuccess) return err;
         if (bit) __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
-    kern<<<grid, NUM_THREADS, smem, stream>>>(tm_a, tm_b, tm_y, kp);
-    return cudaGetLastError();
+    // Programmatic stream serialization: this launch may start while the
+    // previous kernel in the stream drains; the kernel waits for it (see
+    // grid_dependency_wait) before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_y, kp);
 }
 
 #define SGB_LAUNCH_SIG(BN_, L_)                                                                                  \

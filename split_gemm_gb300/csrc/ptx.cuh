@@ -180,6 +180,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Blocks until the grids this one depends on have completed and their memory
+// writes are visible (a no-op when the launch carried no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid in the stream begin launching once every CTA of this grid
+// has executed this (its CTAs then run their prologue and wait in grid_dependency_wait).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_slot, uint32_t ncols)
 {
