@@ -76,15 +76,20 @@ typedef enum {
     CONV2D_LOADER_AUTO = 0,
     CONV2D_LOADER_TMA_IM2COL = 1, /* TMA im2col-mode descriptor; needs C % 64 == 0 */
     CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C % 8 == 0 */
-    CONV2D_LOADER_SCALAR = 3      /* element gather; any C (also gathers the weight) */
+    CONV2D_LOADER_SCALAR = 3,     /* element gather; any C (also gathers the weight) */
+    CONV2D_LOADER_HYBRID = 4      /* TMA im2col and cp.async gather on alternate k-blocks; needs C % 64 == 0 */
 } conv2d_loader;
 
-/* Kernel configuration.  All-zero fields mean "let the heuristic choose". */
+/* Kernel configuration.  All-zero fields mean "let the heuristic choose".
+ * Work is split stream-K style: the (tile, k-block) units are divided evenly
+ * over `grid` CTAs, and a tile cut between CTAs is reduced in place in y, the
+ * CTAs taking turns on a per-tile semaphore.  `splits` = S forces classic
+ * split-K instead (grid = tiles * S, every tile cut into S equal parts). */
 typedef struct {
     int32_t block_n;   /* output channels per CTA tile: 64, 128 or 256 */
-    int32_t splits;    /* split-K factor S >= 1 (CTAs per output tile, serialised in place) */
+    int32_t splits;    /* classic split-K factor S >= 1; 0 = stream-K */
     int32_t loader;    /* conv2d_loader */
-    int32_t reserved0;
+    int32_t grid;      /* CTAs for stream-K (1 .. tiles * k-blocks); 0 = heuristic */
     int32_t debug_flags;      /* test hook, 0 in normal use; see CONV2D_DEBUG_* */
     int32_t reserved1;
     int64_t wait_limit_ns;    /* bound on every device-side wait; 0 = default (1 s) */

@@ -137,10 +137,15 @@ bool tma_im2col_eligible(const Shape& s)
 // ------------------------------------------------------------------ heuristic
 struct Plan {
     int block_n;
-    int splits;
+    int splits;  // classic split-K factor, or 0 for stream-K
     int loader;
     int m_tiles, n_tiles, num_kb;
+    int grid;         // CTAs launched
+    long long units;  // (tile, k-block) work units
 };
+
+constexpr int kMinUnitsPerCta = 4;     // no split gets fewer k-blocks than this
+constexpr int kMaxSplitsPerTile = 6;   // longest serial in-place reduction chain the heuristic builds
 
 int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
 {
@@ -155,38 +160,67 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_CPASYNC) {
         if (s.c % 8 != 0) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader == CONV2D_LOADER_HYBRID) {
+        if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
-    // Tile width.
-    int bn = force ? force->block_n : 0;
-    if (bn == 0) bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
-    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
     const int64_t m_tiles = cdiv(s.m, BM);
-    const int64_t n_tiles = cdiv(s.k, bn);
     const int64_t num_kb = cdiv(s.crs, BK);
-    const int64_t tiles = m_tiles * n_tiles;
-    // Split factor: spread a small tile grid over the SMs when the reduction is
-    // long enough that every split keeps at least four k-blocks.
-    int64_t splits = force ? force->splits : 0;
-    if (splits == 0) {
-        splits = 1;
-        if (sms > 0 && tiles < sms && num_kb >= 8) {
-            splits = sms / tiles;
-            if (splits > num_kb / 4) splits = num_kb / 4;
-            if (splits > 32) splits = 32;
-            if (splits < 1) splits = 1;
+    const int64_t forced_splits = force ? force->splits : 0;
+    const int64_t forced_grid = force ? force->grid : 0;
+    if (forced_splits < 0 || forced_grid < 0 || (forced_splits > 0 && forced_grid > 0)) return CONV2D_ERR_INVALID;
+    const int64_t nsm = sms > 0 ? sms : 1;
+    // Tile width: as wide as the output channels allow (one A tile feeds more
+    // MMAs); narrower when that leaves so few tiles that a long reduction would
+    // need more than kMaxSplitsPerTile in-place turns per tile.
+    int bn = force ? force->block_n : 0;
+    if (bn == 0) {
+        bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+        while (bn > 64 && forced_splits == 0 && forced_grid == 0) {
+            const int64_t tiles = m_tiles * cdiv(s.k, bn);
+            if (tiles * 2 > nsm || num_kb < 8 || nsm / tiles <= kMaxSplitsPerTile) break;
+            bn /= 2;
         }
     }
-    if (splits < 1) return CONV2D_ERR_INVALID;
-    if (splits > num_kb) return CONV2D_ERR_UNSUPPORTED;  // every split needs at least one k-block
-    if (tiles * splits > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
+    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t tiles = m_tiles * n_tiles;
+    const int64_t units = tiles * num_kb;
+    int64_t splits = forced_splits;
+    int64_t grid = forced_grid;
+    if (splits == 0 && grid == 0) {
+        if (tiles >= nsm) {
+            // Persistent: every SM takes the same number of whole tiles where that
+            // divides out, otherwise an even share of (tile, k-block) units.
+            const int64_t per_cta = cdiv(tiles, nsm);
+            grid = cdiv(tiles, per_cta);
+        } else if (tiles * 2 <= nsm && num_kb >= 8) {
+            // Few tiles, long reduction: classic split-K (the "small M*N, large
+            // C*R*S" regime), every split keeping at least four k-blocks.
+            splits = nsm / tiles;
+            if (splits > kMaxSplitsPerTile) splits = kMaxSplitsPerTile;
+            if (splits > num_kb / kMinUnitsPerCta) splits = num_kb / kMinUnitsPerCta;
+            if (splits < 1) splits = 1;
+        } else {
+            grid = tiles;  // one tile per CTA: cutting tiles costs more than the idle SMs
+        }
+    }
+    if (splits > 0) {
+        if (splits > num_kb) return CONV2D_ERR_UNSUPPORTED;  // every split needs at least one k-block
+        grid = tiles * splits;
+    } else if (grid > units) {
+        return CONV2D_ERR_UNSUPPORTED;  // every CTA needs at least one unit
+    }
+    if (grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
     plan->block_n = bn;
     plan->splits = static_cast<int>(splits);
     plan->loader = loader;
     plan->m_tiles = static_cast<int>(m_tiles);
     plan->n_tiles = static_cast<int>(n_tiles);
     plan->num_kb = static_cast<int>(num_kb);
+    plan->grid = static_cast<int>(grid);
+    plan->units = units;
     return CONV2D_OK;
 }
 
@@ -205,7 +239,7 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     std::memset(tm_b, 0, sizeof(*tm_b));
     std::memset(tm_y, 0, sizeof(*tm_y));
     if (!load_encoders()) return CONV2D_ERR_CUDA;
-    if (plan.loader == CONV2D_LOADER_TMA_IM2COL) {
+    if (plan.loader == CONV2D_LOADER_TMA_IM2COL || plan.loader == CONV2D_LOADER_HYBRID) {
         const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
         const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
                                        (cuuint64_t)(s.h * s.w * s.c * 2)};
@@ -233,7 +267,7 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     if (tma_store) {
         const cuuint64_t dims[2] = {(cuuint64_t)s.k, (cuuint64_t)s.m};
         const cuuint64_t strides[1] = {(cuuint64_t)(s.k * 4)};
-        const cuuint32_t box[2] = {32, (cuuint32_t)BM};
+        const cuuint32_t box[2] = {32, 32};  // one epilogue warp's 32 rows x 32 columns
         const cuuint32_t estr[2] = {1, 1};
         CUresult rc = g_encode_tiled(tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
                                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -251,6 +285,7 @@ cudaError_t dispatch(int bn, int loader, const CUtensorMap& a, const CUtensorMap
     if (bn == BN_) {                                                                                          \
         if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<BN_, LOADER_TMA>(a, b, y, kp, grid, st); \
         if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<BN_, LOADER_CPASYNC>(a, b, y, kp, grid, st); \
+        if (loader == CONV2D_LOADER_HYBRID) return launch_conv2d_tc<BN_, LOADER_HYBRID>(a, b, y, kp, grid, st); \
         return launch_conv2d_tc<BN_, LOADER_SCALAR>(a, b, y, kp, grid, st);                                     \
     }
     SGB_CASE(64)
@@ -281,14 +316,17 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
         (workspace && !aligned16(workspace)))
         return CONV2D_ERR_ALIGNMENT;
-    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->wait_limit_ns < 0)) return CONV2D_ERR_INVALID;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->grid < 0 || algo->wait_limit_ns < 0))
+        return CONV2D_ERR_INVALID;
     Plan plan;
     rc = choose_plan(s, algo, &plan);
     if (rc != CONV2D_OK) return rc;
     const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(s);
-    if (plan.splits > 1 && !have_ws) return CONV2D_ERR_WORKSPACE;
+    // Any tile cut between CTAs needs the semaphores.
+    const bool cuts_tiles = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
+    if (cuts_tiles && !have_ws) return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
-    const bool tma_store = (s.k % 4) == 0;
+    const bool tma_store = (s.k % 4) == 0;  // y rows must be 16-byte multiples for the TMA store
 
     CUtensorMap tm_a, tm_b, tm_y;
     rc = encode_maps(s, plan, x, w, y, tma_store, &tm_a, &tm_b, &tm_y);
@@ -307,9 +345,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.M = (int)s.m;
     kp.CRS = (int)s.crs;
     kp.num_kb = plan.num_kb;
-    kp.splits = plan.splits;
     kp.m_tiles = plan.m_tiles;
     kp.n_tiles = plan.n_tiles;
+    kp.grid = plan.grid;
+    kp.units = plan.units;
     kp.use_tma_store = tma_store ? 1 : 0;
     kp.debug_flags = algo ? algo->debug_flags : 0;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
@@ -318,7 +357,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.trace = g_trace;
 #endif
 
-    const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
+    const int64_t grid = plan.grid;
     if (log_enabled())
         std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BN=%d splits=%d loader=%d grid=%lld tma_store=%d\n",
                      (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_n, plan.splits, plan.loader,
@@ -380,6 +419,7 @@ int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
     out->block_n = plan.block_n;
     out->splits = plan.splits;
     out->loader = plan.loader;
+    out->grid = plan.grid;
     return CONV2D_OK;
 }
 

@@ -10,30 +10,42 @@
 //              written to global memory;
 //   B[j][kk] = w[j][r][s][c]               -- the KRSC weight viewed as [K][C*R*S].
 //
-// One CTA computes one BM x BN output tile over one slice of the reduction
-// (split-K).  Warp roles (192 threads):
+// Work decomposition (stream-K).  The output is cut into BM x BN tiles and the
+// reduction into BK-wide k-blocks; a work unit is one (tile, k-block) pair and
+// the units are numbered tile-major.  CTA c of G takes the contiguous unit range
+// [c*U/G, (c+1)*U/G), so every CTA gets the same number of MMAs however the tile
+// count falls against the SM count.  A range covers a tail of one tile, whole
+// tiles, and a head of another: a tile cut by range boundaries is split over
+// consecutive CTAs, its "splits" in k-block order.  Classic split-K with S
+// splits is the special case G = tiles * S.
+//
+// Splits of a tile are reduced in place in y (NVIDIA/Fuser issue #1316
+// "Split-K matmul is slow even for few partitions", Eliminating the workspace):
+// the CTAs take turns on a per-tile semaphore -- split j waits until it reads j,
+// adds its partial tile into y (split 0 stores acc + bias), then publishes j+1;
+// the last split resets it to 0.  The fp32 output is the work buffer; the only
+// extra memory is one 32-bit word per tile.  Each CTA walks its segments in
+// reverse order, so the head of a cut tile (split 0, owned by the lower CTA) is
+// computed first and the tail (a later split) last: turns are normally granted
+// before they are asked for.
+//
+// Warp roles:
 //   warp 0      TMA producer: weight tile (tiled TMA) and, for the TMA loader,
-//               the im2col activation tile (im2col-mode TMA), into a STAGES-deep
-//               ring of shared-memory buffers guarded by full/empty mbarriers;
+//               the im2col activation tile (im2col-mode TMA) into a STAGES-deep
+//               shared-memory ring guarded by full/empty mbarriers;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer (128 x BN x 16
-//               per instruction, fp32 accumulator in tensor memory);
-//   warps 2..5  gather producers for the cp.async / scalar loaders, then the
-//               epilogue: TMEM -> registers (+ bias) -> shared memory -> TMA store,
-//               or, under split-K, the serialised in-place reduction into y.
-// The shared-memory ring replaces block-wide syncs between load and MMA (burn
-// PR #2545's sync-placement discussion; ROCm/rocMLIR PR #1511 "Double buffering
+//               per instruction) into two fp32 TMEM accumulators used in turn;
+//   warps 2..5  epilogue: TMEM -> registers (+ bias) -> swizzled shared staging ->
+//               per-warp TMA store (or TMA reduce-add for later splits), while
+//               the MMA warp already fills the other accumulator;
+//   warps 6..9  (cp.async and scalar loaders only) im2col gather into the ring.
+// The ring replaces block-wide syncs between load and MMA (burn PR #2545's
+// sync-placement discussion; ROCm/rocMLIR PR #1511 "Double buffering
 // improvements" splits loads and MMAs into overlapping stages the same way).
 //
-// Split-K (NVIDIA/Fuser issue #1316 "Split-K matmul is slow even for few
-// partitions", Eliminating the workspace): the S CTAs of one output tile take
-// turns on a per-tile semaphore.  Split j waits until the semaphore reads j,
-// adds its partial tile into y (split 0 stores acc + bias), then publishes j+1;
-// the last split resets it to 0.  The fp32 output is the work buffer, so the
-// only extra memory is one 32-bit word per tile.
-//
-// Every wait is bounded (about wait_limit_ns, counted in SM cycles).  A wait that runs out
-// records CONV2D_ERR_TIMEOUT in the status word, and the CTA drains its own
-// in-flight copies and MMAs, frees its tensor memory and exits.
+// Every wait is bounded (about wait_limit_ns, counted in SM cycles).  A wait
+// that runs out records CONV2D_ERR_TIMEOUT in the status word; the CTA then
+// drains its own in-flight copies and MMAs, frees its tensor memory and exits.
 #pragma once
 
 #include <cuda.h>
@@ -49,13 +61,31 @@ namespace sgb {
 constexpr int BM = 128;          // output pixels per tile (MMA M)
 constexpr int BK = 64;           // reduction elements per stage: one 128-byte bf16 row
 constexpr int UMMA_K = 16;       // reduction per tcgen05.mma of kind::f16
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;     // epilogue warps 2..5
 constexpr int EPI_THREADS = 128;
-constexpr int EPI_THREAD0 = 64;  // first thread of warp 2
+constexpr int GATHER_WARP0 = 6;  // gather warps 6..9 (gather loaders only)
+constexpr int GATHER_THREADS = 128;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
+constexpr int EPI_SLOTS = 2;                 // staging slots per epilogue warp
+constexpr int EPI_BYTES = 4 * EPI_SLOTS * EPI_SLOT_BYTES;
 constexpr uint32_t STATUS_TIMEOUT = 6;  // same value as CONV2D_ERR_TIMEOUT
 
-enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3 };
+enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4 };
+
+// Which engine brings in the im2col tile of the CTA's k-block number `it`:
+// the TMA unit (im2col mode) or the gather warps (cp.async).  The hybrid
+// loader alternates so that both engines work in parallel.
+template <int LOADER>
+__device__ __forceinline__ bool a_by_tma(int it)
+{
+    return LOADER == LOADER_TMA || (LOADER == LOADER_HYBRID && (it & 1) == 0);
+}
+template <int LOADER>
+__device__ __forceinline__ bool a_by_gather(int it)
+{
+    return LOADER == LOADER_CPASYNC || (LOADER == LOADER_HYBRID && (it & 1) == 1);
+}
 
 struct ConvKernelParams {
     const uint16_t* x;  // bf16 NHWC
@@ -63,11 +93,13 @@ struct ConvKernelParams {
     const float* bias;  // [K] or nullptr
     float* y;           // fp32 NHWC = [M][K]
     uint32_t* status;   // device status word or nullptr
-    uint32_t* sems;     // one per output tile (split-K only)
+    uint32_t* sems;     // one per output tile (needed whenever a tile is split)
     int N, H, W, C, K, R, S, P, Q;
     int sh, sw, ph, pw, dh, dw;
     int M, CRS, num_kb;
-    int splits, m_tiles, n_tiles;
+    int m_tiles, n_tiles;
+    int grid;                 // G: CTAs sharing the unit range
+    long long units;          // U = m_tiles * n_tiles * num_kb
     int use_tma_store;
     int debug_flags;
     unsigned long long wait_limit_ns;
@@ -79,35 +111,56 @@ struct ConvKernelParams {
 #ifdef SGB_TRACE_ENABLED
 #define SGB_TRACE(kp, cond, slot)                                                               \
     do {                                                                                        \
-        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 16 + (slot)] =   \
+        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 32 + (slot)] =   \
             ::sgb::ptx::globaltimer();                                                          \
+    } while (0)
+// Cycle accounting for profiling builds: SGB_CYCLES_BEGIN(t) starts a stopwatch,
+// SGB_CYCLES_END(acc, t) adds the elapsed SM cycles to a local accumulator that
+// SGB_TRACE_VALUE stores in the trace slot at the end.
+#define SGB_CYCLES_BEGIN(t) const uint64_t t = ::sgb::ptx::clock64()
+#define SGB_CYCLES_END(acc, t) (acc) += ::sgb::ptx::clock64() - (t)
+#define SGB_TRACE_VALUE(kp, cond, slot, value)                                                   \
+    do {                                                                                        \
+        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 32 + (slot)] = (value); \
     } while (0)
 #else
 #define SGB_TRACE(kp, cond, slot) \
     do {                          \
     } while (0)
+#define SGB_CYCLES_BEGIN(t) \
+    do {                    \
+    } while (0)
+#define SGB_CYCLES_END(acc, t) \
+    do {                       \
+    } while (0)
+#define SGB_TRACE_VALUE(kp, cond, slot, value) \
+    do {                                       \
+    } while (0)
 #endif
 
-template <int BN>
+template <int BN, int LOADER>
 struct TileConfig {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int EPI_BYTES = BM * BN * 4;  // fp32 output tile staged for the TMA store
-    static_assert(RING_BYTES >= EPI_BYTES, "output staging reuses the ring");
-    static constexpr int BAR_BYTES = (2 * STAGES + 1) * 8 + 16;
-    static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = BN;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared-memory limit");
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+    static constexpr int THREADS = (LOADER == LOADER_TMA ? 6 : 10) * 32;
 };
 
 struct SmemView {
-    uint8_t* a;       // STAGES x A tile
-    uint8_t* b;       // STAGES x B tile
-    uint64_t* full;   // STAGES
-    uint64_t* empty;  // STAGES
-    uint64_t* acc_full;
+    uint8_t* a;          // STAGES x A tile
+    uint8_t* b;          // STAGES x B tile
+    uint8_t* epi;        // 4 warps x EPI_SLOTS staging slots
+    uint64_t* full;      // STAGES
+    uint64_t* empty;     // STAGES
+    uint64_t* acc_full;  // 2: accumulator ready for the epilogue
+    uint64_t* acc_empty; // 2: accumulator drained by the epilogue
+    uint64_t* mma_done;  // teardown drain of the MMA pipe
     uint32_t* tmem_slot;
     volatile uint32_t* abort_flag;
     volatile uint32_t* epi_go;  // epilogue decision, written by one thread between two barriers
@@ -119,248 +172,316 @@ __device__ __forceinline__ void record_timeout(const ConvKernelParams& kp, volat
     if (kp.status) atomicMax(kp.status, STATUS_TIMEOUT);
 }
 
-// ---------------------------------------------------------------- TMA producer (warp 0, one thread)
-template <int BN, int LOADER>
-__device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
-                                 const SmemView& sm, int m0, int n0, int kb_begin, int nkb)
+// ---------------------------------------------------------------- work partition
+struct Segment {
+    int tile;      // output tile index (m_tile * n_tiles + n_tile)
+    int kb_begin;  // k-block range of this segment inside the tile
+    int kb_end;
+    int split;     // position among the CTAs sharing the tile (k-block order)
+    int nsplits;   // number of CTAs sharing the tile
+};
+
+// The CTA whose unit range contains unit u: the largest c with floor(c*U/G) <= u.
+__device__ __forceinline__ int cta_of_unit(long long u, long long units, int grid)
 {
-    using Cfg = TileConfig<BN>;
-    constexpr int STAGES = Cfg::STAGES;
-    constexpr uint32_t TX = (LOADER == LOADER_TMA ? A_STAGE_BYTES : 0) + Cfg::B_STAGE_BYTES;
-
-    // Window origin of the tile's first pixel and the first (r, s, c) of this split.
-    const int pq = kp.P * kp.Q;
-    const int n_img = m0 / pq;
-    const int rem = m0 - n_img * pq;
-    const int p0 = rem / kp.Q;
-    const int q0 = rem - p0 * kp.Q;
-    const int w_org = q0 * kp.sw - kp.pw;
-    const int h_org = p0 * kp.sh - kp.ph;
-    const int kk0 = kb_begin * BK;
-    const int rs0 = kk0 / kp.C;
-    int c = kk0 - rs0 * kp.C;
-    int r = rs0 / kp.S;
-    int s = rs0 - r * kp.S;
-
-    int issued = 0;
-    for (int i = 0; i < nkb; ++i) {
-        const int stage = i % STAGES;
-        const uint32_t parity = static_cast<uint32_t>(i / STAGES) & 1u;
-        if (*sm.abort_flag) break;
-        if (!ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
-            record_timeout(kp, sm.abort_flag);
-            break;
-        }
-        ptx::mbar_arrive_expect_tx(&sm.full[stage], TX);
-        if (LOADER == LOADER_TMA) {
-            ptx::tma_load_im2col_4d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], c, w_org, h_org, n_img,
-                                    static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
-            c += BK;
-            if (c == kp.C) {
-                c = 0;
-                if (++s == kp.S) {
-                    s = 0;
-                    ++r;
-                }
-            }
-        }
-        ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], (kb_begin + i) * BK, n0);
-        SGB_TRACE(kp, i == 0, 2);
-        ++issued;
-    }
-    SGB_TRACE(kp, true, 3);
-    // Drain: the last loads of each stage must have landed before the CTA can exit.
-    for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
-        ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
+    return static_cast<int>(((u + 1) * grid + units - 1) / units - 1);
 }
 
-// ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
-template <int BN>
-__device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, uint32_t tmem_d, int nkb)
-{
-    using Cfg = TileConfig<BN>;
-    constexpr int STAGES = Cfg::STAGES;
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
-    for (int i = 0; i < nkb; ++i) {
-        const int stage = i % STAGES;
-        const uint32_t parity = static_cast<uint32_t>(i / STAGES) & 1u;
-        if (*sm.abort_flag) break;
-        if (!ptx::mbar_wait(&sm.full[stage], parity, kp.wait_limit_ns)) {
-            record_timeout(kp, sm.abort_flag);
-            break;
-        }
-        ptx::tc_fence_after();
-        SGB_TRACE(kp, i == 0, 4);
-        const uint32_t a_addr = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
-        const uint32_t b_addr = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
-#pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k) {
-            // Advancing along K inside a 128-B swizzled row moves the start address by 32 B.
-            const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2);
-            const uint64_t bd = ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2);
-            ptx::mma_bf16(tmem_d, ad, bd, IDESC, (i > 0 || k > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(&sm.empty[stage]);
+// Walks this CTA's segments from the end of its unit range to the start.
+struct SegmentWalker {
+    long long lo, cur;
+    __device__ __forceinline__ explicit SegmentWalker(const ConvKernelParams& kp)
+    {
+        lo = static_cast<long long>(blockIdx.x) * kp.units / kp.grid;
+        cur = (static_cast<long long>(blockIdx.x) + 1) * kp.units / kp.grid;
     }
-    // Signals the epilogue, and (waiting on it here too) guarantees no MMA is in
-    // flight when the CTA reaches its teardown.
-    SGB_TRACE(kp, true, 5);
-    ptx::mma_commit(sm.acc_full);
-    ptx::mbar_wait(sm.acc_full, 0u, kp.wait_limit_ns);
-    SGB_TRACE(kp, true, 6);
-}
+    __device__ __forceinline__ bool next(const ConvKernelParams& kp, Segment& sg)
+    {
+        if (cur <= lo) return false;
+        const int t = static_cast<int>((cur - 1) / kp.num_kb);
+        const long long base = static_cast<long long>(t) * kp.num_kb;
+        const long long seg_lo = lo > base ? lo : base;
+        sg.tile = t;
+        sg.kb_begin = static_cast<int>(seg_lo - base);
+        sg.kb_end = static_cast<int>(cur - base);
+        const int first = cta_of_unit(base, kp.units, kp.grid);
+        const int last = cta_of_unit(base + kp.num_kb - 1, kp.units, kp.grid);
+        sg.split = static_cast<int>(blockIdx.x) - first;
+        sg.nsplits = last - first + 1;
+        cur = seg_lo;
+        return true;
+    }
+};
 
-// ---------------------------------------------------------------- gather producers (warps 2..5)
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16)
 {
     return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
 }
 
-// A tile by 16-byte cp.async: each thread owns one tile row (output pixel); a
-// 16-byte chunk is 8 consecutive channels of one filter tap (needs C % 8 == 0).
-template <int BN>
-__device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& sm, int m0, int kb_begin, int nkb)
+// Pixel (n, p, q) of GEMM row m.
+__device__ __forceinline__ void decode_pixel(const ConvKernelParams& kp, int m, int& n_img, int& p, int& q)
 {
-    using Cfg = TileConfig<BN>;
-    constexpr int STAGES = Cfg::STAGES;
-    constexpr int LAG = STAGES - 1 < 3 ? STAGES - 1 : 3;  // stages in flight per thread
-    const int row = threadIdx.x - EPI_THREAD0;
-    const int m = m0 + row;
-    const bool row_ok = m < kp.M;
-    int n_img = 0, p = 0, q = 0;
-    if (row_ok) {
-        const int pq = kp.P * kp.Q;
-        n_img = m / pq;
-        const int rem = m - n_img * pq;
-        p = rem / kp.Q;
-        q = rem - p * kp.Q;
-    }
-    const int ih0 = p * kp.sh - kp.ph;
-    const int iw0 = q * kp.sw - kp.pw;
-    const uint16_t* xb = kp.x + static_cast<int64_t>(n_img) * kp.H * kp.W * kp.C;
+    const int pq = kp.P * kp.Q;
+    n_img = m / pq;
+    const int rem = m - n_img * pq;
+    p = rem / kp.Q;
+    q = rem - p * kp.Q;
+}
 
-    int issued = 0, arrived = 0;
-    for (int i = 0; i < nkb; ++i) {
-        const int stage = i % STAGES;
-        const uint32_t parity = static_cast<uint32_t>(i / STAGES) & 1u;
-        if (*sm.abort_flag) break;
-        if (!ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
+// ---------------------------------------------------------------- TMA producer (warp 0, one thread)
+template <int BN, int LOADER>
+__device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
+                                 const SmemView& sm)
+{
+    using Cfg = TileConfig<BN, LOADER>;
+    constexpr int STAGES = Cfg::STAGES;
+    int it = 0;  // k-blocks issued so far (all segments)
+    bool ok = true;
+    uint64_t wait_cycles = 0;
+    (void)wait_cycles;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        const int m_tile = sg.tile / kp.n_tiles;
+        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        const int m0 = m_tile * BM;
+        // Window origin of the tile's first pixel and the first (r, s, c) of the segment.
+        int n_img, p0, q0;
+        decode_pixel(kp, m0, n_img, p0, q0);
+        const int w_org = q0 * kp.sw - kp.pw;
+        const int h_org = p0 * kp.sh - kp.ph;
+        const int kk0 = sg.kb_begin * BK;
+        const int rs0 = kk0 / kp.C;
+        int c = kk0 - rs0 * kp.C;
+        int r = rs0 / kp.S;
+        int s = rs0 - r * kp.S;
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            const int stage = it % STAGES;
+            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
+            if (*sm.abort_flag) { ok = false; break; }
+            SGB_CYCLES_BEGIN(tw);
+            if (!ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
+                record_timeout(kp, sm.abort_flag);
+                ok = false;
+                break;
+            }
+            SGB_CYCLES_END(wait_cycles, tw);
+            const bool a_tma = a_by_tma<LOADER>(it);
+            ptx::mbar_arrive_expect_tx(&sm.full[stage], (a_tma ? A_STAGE_BYTES : 0) + Cfg::B_STAGE_BYTES);
+            if (a_tma)
+                ptx::tma_load_im2col_4d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], c, w_org, h_org,
+                                        n_img, static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
+            if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID) {
+                c += BK;
+                if (c == kp.C) {
+                    c = 0;
+                    if (++s == kp.S) {
+                        s = 0;
+                        ++r;
+                    }
+                }
+            }
+            ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], kb * BK, n0);
+        }
+    }
+    SGB_TRACE(kp, true, 3);
+    SGB_TRACE_VALUE(kp, true, 2, wait_cycles);
+    // Drain: the last load of each stage must have landed before the CTA can exit.
+    for (int i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+        ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
+template <int BN, int LOADER>
+__device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, uint32_t tmem_base)
+{
+    using Cfg = TileConfig<BN, LOADER>;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+    int it = 0, seg_idx = 0;
+    bool ok = true;
+    uint64_t full_cycles = 0, acc_cycles = 0;
+    (void)full_cycles;
+    (void)acc_cycles;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        const int buf = seg_idx & 1;
+        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        // The epilogue must have drained this accumulator's previous segment.
+        SGB_CYCLES_BEGIN(ta);
+        if (!ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
             record_timeout(kp, sm.abort_flag);
             break;
         }
-        uint8_t* dst = sm.a + stage * A_STAGE_BYTES;
-        const int kk0 = (kb_begin + i) * BK;
+        SGB_CYCLES_END(acc_cycles, ta);
+        ptx::tc_fence_after();
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            const int stage = it % STAGES;
+            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
+            if (*sm.abort_flag) { ok = false; break; }
+            SGB_CYCLES_BEGIN(tf);
+            if (!ptx::mbar_wait(&sm.full[stage], parity, kp.wait_limit_ns)) {
+                record_timeout(kp, sm.abort_flag);
+                ok = false;
+                break;
+            }
+            SGB_CYCLES_END(full_cycles, tf);
+            ptx::tc_fence_after();
+            // Gathered tiles were written through the generic proxy (cp.async);
+            // order them before the tensor cores read the stage.
+            if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) ptx::fence_proxy_async_smem();
+            const uint32_t a_addr = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
+            const uint32_t b_addr = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
 #pragma unroll
-        for (int j = 0; j < BK / 8; ++j) {
-            const int kk = kk0 + j * 8;
-            const void* src = kp.x;
-            uint32_t bytes = 0;
-            if (row_ok && kk < kp.CRS) {
-                const int rs = kk / kp.C;
-                const int c = kk - rs * kp.C;
-                const int r = rs / kp.S;
-                const int s = rs - r * kp.S;
-                const int ih = ih0 + r * kp.dh;
-                const int iw = iw0 + s * kp.dw;
-                if (static_cast<unsigned>(ih) < static_cast<unsigned>(kp.H) &&
-                    static_cast<unsigned>(iw) < static_cast<unsigned>(kp.W)) {
-                    src = xb + (static_cast<int64_t>(ih) * kp.W + iw) * kp.C + c;
-                    bytes = 16;
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+                // Advancing along K inside a 128-B swizzled row moves the start address by 32 B.
+                const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2);
+                const uint64_t bd = ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2);
+                ptx::mma_bf16(tmem_d, ad, bd, IDESC, (kb > sg.kb_begin || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&sm.empty[stage]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&sm.acc_full[buf]);
+        ++seg_idx;
+    }
+    SGB_TRACE(kp, true, 5);
+    SGB_TRACE_VALUE(kp, true, 4, full_cycles);
+    SGB_TRACE_VALUE(kp, true, 6, acc_cycles);
+    // No MMA may be in flight when the CTA reaches its teardown.
+    ptx::mma_commit(sm.mma_done);
+    ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------- gather producers (warps 6..9)
+// A tile by 16-byte cp.async (needs C % 8 == 0).  Thread t copies 16-byte
+// chunk (t % 8) -- 8 consecutive channels -- of tile rows t/8 + 16*i, i = 0..7,
+// so each warp instruction moves four whole 128-byte rows (one per pixel) and
+// the filter-tap decode (r, s, c) happens once per k-block per thread.  Every
+// thread hands its copies to the stage's full barrier with a non-blocking
+// cp.async arrive, so the gather runs as far ahead as the ring allows; the MMA
+// thread fences the async proxy after its wait (run_mma_issuer).
+template <int BN, int LOADER>
+__device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& sm)
+{
+    using Cfg = TileConfig<BN, LOADER>;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int ROWS = BM / 16;  // tile rows per thread
+    const int gt = threadIdx.x - GATHER_WARP0 * 32;
+    const int lane = threadIdx.x & 31;
+    const int chunk = gt & 7;
+    const int row0 = gt >> 3;
+    int it = 0;
+    bool ok = true;
+    uint64_t g_empty = 0, g_issue = 0;
+    (void)g_empty; (void)g_issue;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        const int m_base = (sg.tile / kp.n_tiles) * BM;
+        int ih0[ROWS], iw0[ROWS], img[ROWS];
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i) {
+            const int m = m_base + row0 + 16 * i;
+            int n_img = 0, p = 0, q = 0;
+            if (m < kp.M) decode_pixel(kp, m, n_img, p, q);
+            // Rows past M get an origin far outside the image, so every tap zero-fills.
+            ih0[i] = m < kp.M ? p * kp.sh - kp.ph : -(1 << 28);
+            iw0[i] = q * kp.sw - kp.pw;
+            img[i] = n_img * kp.H * kp.W * kp.C;
+        }
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            const int stage = it % STAGES;
+            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
+            // One lane waits for the slot; the warp follows its verdict.
+            int go = 0;
+            SGB_CYCLES_BEGIN(t_e);
+            if (lane == 0) {
+                go = *sm.abort_flag == 0u;
+                if (go && !ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
+                    record_timeout(kp, sm.abort_flag);
+                    go = 0;
                 }
             }
-            ptx::cp_async_16(dst + sw128_offset(row, j), src, bytes);
-        }
-        ptx::cp_async_commit();
-        ++issued;
-        if (issued - arrived > LAG) {
-            ptx::cp_async_wait<LAG>();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&sm.full[arrived % STAGES]);
-            ++arrived;
+            if (!__shfl_sync(0xffffffffu, go, 0)) { ok = false; break; }
+            SGB_CYCLES_END(g_empty, t_e);
+            SGB_CYCLES_BEGIN(t_i);
+            if (a_by_gather<LOADER>(it)) {  // otherwise the TMA unit loads this k-block
+                uint8_t* dst = sm.a + stage * A_STAGE_BYTES;
+                const int kk = kb * BK + chunk * 8;
+                const bool col_ok = kk < kp.CRS;
+                int dih = 0, diw = 0, c = 0;
+                if (col_ok) {
+                    const int rs = kk / kp.C;
+                    c = kk - rs * kp.C;
+                    const int r = rs / kp.S;
+                    dih = r * kp.dh;
+                    diw = (rs - r * kp.S) * kp.dw;
+                }
+#pragma unroll
+                for (int i = 0; i < ROWS; ++i) {
+                    const int ih = ih0[i] + dih;
+                    const int iw = iw0[i] + diw;
+                    const bool in = col_ok && static_cast<unsigned>(ih) < static_cast<unsigned>(kp.H) &&
+                                    static_cast<unsigned>(iw) < static_cast<unsigned>(kp.W);
+                    const uint16_t* src = in ? kp.x + img[i] + (ih * kp.W + iw) * kp.C + c : kp.x;
+                    ptx::cp_async_16(dst + sw128_offset(row0 + 16 * i, chunk), src, in ? 16u : 0u);
+                }
+            }
+            ptx::cp_async_arrive_noinc(&sm.full[stage]);
+            SGB_CYCLES_END(g_issue, t_i);
         }
     }
-    ptx::cp_async_wait_all();
-    ptx::fence_proxy_async_smem();
-    while (arrived < issued) {
-        ptx::mbar_arrive(&sm.full[arrived % STAGES]);
-        ++arrived;
-    }
+    SGB_TRACE_VALUE(kp, gt == 0, 16, g_empty);
+    SGB_TRACE_VALUE(kp, gt == 0, 17, g_issue);
+    ptx::cp_async_wait_all();  // no copy may be in flight when the CTA exits
 }
 
 // A and B tiles element by element (any C, any C*R*S): plain loads, then
 // 16-byte shared stores in the swizzled layout.
-template <int BN>
-__device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm, int m0, int n0, int kb_begin,
-                                  int nkb)
+template <int BN, int LOADER>
+__device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm)
 {
-    using Cfg = TileConfig<BN>;
+    using Cfg = TileConfig<BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
-    const int row = threadIdx.x - EPI_THREAD0;
-    const int m = m0 + row;
-    const bool row_ok = m < kp.M;
-    int n_img = 0, p = 0, q = 0;
-    if (row_ok) {
-        const int pq = kp.P * kp.Q;
-        n_img = m / pq;
-        const int rem = m - n_img * pq;
-        p = rem / kp.Q;
-        q = rem - p * kp.Q;
-    }
-    const int ih0 = p * kp.sh - kp.ph;
-    const int iw0 = q * kp.sw - kp.pw;
-    const uint16_t* xb = kp.x + static_cast<int64_t>(n_img) * kp.H * kp.W * kp.C;
-
-    for (int i = 0; i < nkb; ++i) {
-        const int stage = i % STAGES;
-        const uint32_t parity = static_cast<uint32_t>(i / STAGES) & 1u;
-        if (*sm.abort_flag) break;
-        if (!ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
-            record_timeout(kp, sm.abort_flag);
-            break;
-        }
-        const int kk0 = (kb_begin + i) * BK;
-        // A row: walk (r, s, c) incrementally from kk0.
-        {
-            const int rs0 = kk0 / kp.C;
-            int c = kk0 - rs0 * kp.C;
-            int r = rs0 / kp.S;
-            int s = rs0 - r * kp.S;
-            const uint32_t base = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
-#pragma unroll 1
-            for (int j = 0; j < BK / 8; ++j) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int kk = kk0 + j * 8 + e;
-                    uint32_t v = 0;
-                    if (row_ok && kk < kp.CRS) {
-                        const int ih = ih0 + r * kp.dh;
-                        const int iw = iw0 + s * kp.dw;
-                        if (static_cast<unsigned>(ih) < static_cast<unsigned>(kp.H) &&
-                            static_cast<unsigned>(iw) < static_cast<unsigned>(kp.W))
-                            v = __ldg(reinterpret_cast<const unsigned short*>(
-                                xb + (static_cast<int64_t>(ih) * kp.W + iw) * kp.C + c));
-                    }
-                    if (e & 1) packed[e >> 1] |= v << 16;
-                    else packed[e >> 1] = v;
-                    if (++c == kp.C) {
-                        c = 0;
-                        if (++s == kp.S) {
-                            s = 0;
-                            ++r;
-                        }
-                    }
+    const int row = threadIdx.x - GATHER_WARP0 * 32;
+    const int lane = threadIdx.x & 31;
+    int it = 0;
+    bool ok = true;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        const int m_tile = sg.tile / kp.n_tiles;
+        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        const int m = m_tile * BM + row;
+        const bool row_ok = m < kp.M;
+        int n_img = 0, p = 0, q = 0;
+        if (row_ok) decode_pixel(kp, m, n_img, p, q);
+        const int ih0 = p * kp.sh - kp.ph;
+        const int iw0 = q * kp.sw - kp.pw;
+        const uint16_t* xb = kp.x + static_cast<int64_t>(n_img) * kp.H * kp.W * kp.C;
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            const int stage = it % STAGES;
+            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
+            int go = 0;
+            if (lane == 0) {
+                go = *sm.abort_flag == 0u;
+                if (go && !ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
+                    record_timeout(kp, sm.abort_flag);
+                    go = 0;
                 }
-                ptx::st_shared_v4(base + sw128_offset(row, j), packed[0], packed[1], packed[2], packed[3]);
             }
-        }
-        // B rows: thread t fills weight rows t, t + 128, ...
-        {
-            const uint32_t base = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
-#pragma unroll 1
-            for (int b = row; b < BN; b += EPI_THREADS) {
-                const int n = n0 + b;
-                const uint16_t* wr = kp.w + static_cast<int64_t>(n) * kp.CRS;
+            if (!__shfl_sync(0xffffffffu, go, 0)) { ok = false; break; }
+            const int kk0 = kb * BK;
+            // A row: walk (r, s, c) incrementally from kk0.
+            {
+                const int rs0 = kk0 / kp.C;
+                int c = kk0 - rs0 * kp.C;
+                int r = rs0 / kp.S;
+                int s = rs0 - r * kp.S;
+                const uint32_t base = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
 #pragma unroll 1
                 for (int j = 0; j < BK / 8; ++j) {
                     uint32_t packed[4];
@@ -368,21 +489,58 @@ __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm
                     for (int e = 0; e < 8; ++e) {
                         const int kk = kk0 + j * 8 + e;
                         uint32_t v = 0;
-                        if (n < kp.K && kk < kp.CRS) v = __ldg(reinterpret_cast<const unsigned short*>(wr + kk));
+                        if (row_ok && kk < kp.CRS) {
+                            const int ih = ih0 + r * kp.dh;
+                            const int iw = iw0 + s * kp.dw;
+                            if (static_cast<unsigned>(ih) < static_cast<unsigned>(kp.H) &&
+                                static_cast<unsigned>(iw) < static_cast<unsigned>(kp.W))
+                                v = __ldg(reinterpret_cast<const unsigned short*>(
+                                    xb + (static_cast<int64_t>(ih) * kp.W + iw) * kp.C + c));
+                        }
                         if (e & 1) packed[e >> 1] |= v << 16;
                         else packed[e >> 1] = v;
+                        if (++c == kp.C) {
+                            c = 0;
+                            if (++s == kp.S) {
+                                s = 0;
+                                ++r;
+                            }
+                        }
                     }
-                    ptx::st_shared_v4(base + sw128_offset(b, j), packed[0], packed[1], packed[2], packed[3]);
+                    ptx::st_shared_v4(base + sw128_offset(row, j), packed[0], packed[1], packed[2], packed[3]);
                 }
             }
+            // B rows: thread t fills weight rows t, t + 128, ...
+            {
+                const uint32_t base = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
+#pragma unroll 1
+                for (int b = row; b < BN; b += GATHER_THREADS) {
+                    const int n = n0 + b;
+                    const uint16_t* wr = kp.w + static_cast<int64_t>(n) * kp.CRS;
+#pragma unroll 1
+                    for (int j = 0; j < BK / 8; ++j) {
+                        uint32_t packed[4];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int kk = kk0 + j * 8 + e;
+                            uint32_t v = 0;
+                            if (n < kp.K && kk < kp.CRS) v = __ldg(reinterpret_cast<const unsigned short*>(wr + kk));
+                            if (e & 1) packed[e >> 1] |= v << 16;
+                            else packed[e >> 1] = v;
+                        }
+                        ptx::st_shared_v4(base + sw128_offset(b, j), packed[0], packed[1], packed[2], packed[3]);
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.full[stage]);
         }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&sm.full[stage]);
     }
 }
 
 // ---------------------------------------------------------------- epilogue (warps 2..5)
-// Waits (thread et == 0, bounded) until the tile semaphore reads `split`.
+// Waits (bounded) until the tile semaphore reads `split`.  One thread only.
 __device__ __forceinline__ bool wait_turn(const ConvKernelParams& kp, int tile, int split,
                                           volatile uint32_t* abort_flag)
 {
@@ -400,187 +558,215 @@ __device__ __forceinline__ bool wait_turn(const ConvKernelParams& kp, int tile, 
     return true;
 }
 
-// Publishes the next split's turn (the last split resets the semaphore to 0).
-__device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, int tile, int split)
+// Publishes the next split's turn (the last split resets the semaphore to 0).  One thread only.
+__device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, const Segment& sg)
 {
-    const bool skip = (kp.debug_flags & 1) && split == 0;  // test hook: never signal
-    if (skip) return;
-    const uint32_t next = (split + 1 == kp.splits) ? 0u : static_cast<uint32_t>(split + 1);
-    ptx::st_release_gpu(kp.sems + tile, next);
+    if ((kp.debug_flags & 1) && sg.split == 0) return;  // test hook: never signal
+    const uint32_t next = (sg.split + 1 == sg.nsplits) ? 0u : static_cast<uint32_t>(sg.split + 1);
+    ptx::st_release_gpu(kp.sems + sg.tile, next);
 }
 
 template <int BN>
 __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp, const SmemView& sm,
-                             uint32_t tmem_base, int m0, int n0, int split, int tile)
+                             uint32_t tmem_base)
 {
-    const int et = threadIdx.x - EPI_THREAD0;  // 0..127
-    const int quad = (threadIdx.x >> 5) & 3;   // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + (threadIdx.x & 31);
-    const int m = m0 + row;
-    const bool row_ok = m < kp.M;
-    const bool add_bias = kp.bias != nullptr && split == 0;
-    const bool serial = kp.splits > 1;
-
-    const bool acc_ready = ptx::mbar_wait(sm.acc_full, 0u, kp.wait_limit_ns);
-    if (!acc_ready) record_timeout(kp, sm.abort_flag);
-    // One thread decides for all 128, so that every epilogue warp takes the same
-    // path through the named barriers below.
-    ptx::named_bar_sync(1, EPI_THREADS);
-    if (et == 0) *sm.epi_go = (*sm.abort_flag == 0u) ? 1u : 0u;
-    ptx::named_bar_sync(1, EPI_THREADS);
-    if (!*sm.epi_go) return;
-    SGB_TRACE(kp, et == 0, 7);
-    ptx::tc_fence_after();
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-
-    if (kp.use_tma_store) {
-        // TMEM -> registers (+bias) -> 128-B swizzled shared slabs of 32 columns.
-        // Split 0 (or no split) stores each slab as soon as it is complete; later
-        // splits stage every slab, wait for their turn, then let the TMA unit add
-        // the slabs into y in place.
-        uint8_t* stage_base = sm.a;  // the ring is idle once the accumulator is complete
-        const bool store_now = split == 0;
-#pragma unroll 1
+    const int et = threadIdx.x - EPI_WARP0 * 32;  // 0..127
+    const int ew = et >> 5;                        // epilogue warp 0..3
+    const int lane = threadIdx.x & 31;
+    const int quad = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;          // tile row owned by this thread
+    uint8_t* slots = sm.epi + ew * (EPI_SLOTS * EPI_SLOT_BYTES);
+    int seg_idx = 0;
+    int slabs = 0;  // slabs this warp has handed to the TMA unit (staging-slot rotation)
+    uint64_t c_acc = 0, c_ld = 0, c_slot = 0, c_st = 0, c_turn = 0, c_done = 0;
+    (void)c_acc; (void)c_ld; (void)c_slot; (void)c_st; (void)c_turn; (void)c_done;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        const int buf = seg_idx & 1;
+        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        const int m_tile = sg.tile / kp.n_tiles;
+        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        const int m0 = m_tile * BM;
+        const bool add_bias = kp.bias != nullptr && sg.split == 0;
+        // Bias for this tile, fetched before the accumulator wait so that its
+        // latency is hidden: lane l holds columns n0 + 32*j + l.
+        float bias_r[BN / 32];
+#pragma unroll
         for (int j = 0; j < BN / 32; ++j) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
-            ptx::tmem_ld_wait();
-            if (add_bias) {
+            const int n = n0 + j * 32 + lane;
+            bias_r[j] = (add_bias && n < kp.K) ? __ldg(kp.bias + n) : 0.0f;
+        }
+        SGB_CYCLES_BEGIN(t_acc);
+        if (!ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) record_timeout(kp, sm.abort_flag);
+        SGB_CYCLES_END(c_acc, t_acc);
+        // One thread decides for all 128 (including, for a later split, waiting
+        // for its turn), so that every epilogue warp takes the same path.
+        SGB_CYCLES_BEGIN(t_turn);
+        ptx::named_bar_sync(1, EPI_THREADS);
+        if (et == 0) {
+            bool go = *sm.abort_flag == 0u;
+            if (go && sg.split > 0) go = wait_turn(kp, sg.tile, sg.split, sm.abort_flag);
+            *sm.epi_go = go ? 1u : 0u;
+        }
+        ptx::named_bar_sync(1, EPI_THREADS);
+        SGB_CYCLES_END(c_turn, t_turn);
+        if (!*sm.epi_go) break;
+        ptx::tc_fence_after();
+        SGB_TRACE(kp, et == 0 && seg_idx == 0, 7);
+
+        const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+
+        if (kp.use_tma_store) {
+            // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
+            // TMA store (split 0) or TMA reduce-add (later splits, in turn).
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int n = n0 + j * 32 + e;
-                    const float b = n < kp.K ? __ldg(kp.bias + n) : 0.0f;
-                    v[e] = __float_as_uint(__uint_as_float(v[e]) + b);
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t v[32];
+                SGB_CYCLES_BEGIN(t_ld);
+                ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                ptx::tmem_ld_wait();
+                SGB_CYCLES_END(c_ld, t_ld);
+                if (j == BN / 32 - 1) {  // accumulator drained: the MMA warp may reuse it
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&sm.acc_empty[buf]);
                 }
-            }
-            const uint32_t slab = ptx::smem_addr(stage_base + j * (BM * 128));
+                if (add_bias) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                ptx::st_shared_v4(slab + sw128_offset(row, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            ptx::fence_proxy_async_smem();
-            if (store_now) {
-                ptx::named_bar_sync(1, EPI_THREADS);
-                if (et == 0) {
-                    ptx::tma_store_2d(tm_y, stage_base + j * (BM * 128), n0 + j * 32, m0);
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
+                }
+                uint8_t* slot = slots + (slabs % EPI_SLOTS) * EPI_SLOT_BYTES;
+                SGB_CYCLES_BEGIN(t_slot);
+                if (slabs >= EPI_SLOTS) {  // the slot's previous slab must have been read by the TMA unit
+                    if (lane == 0) ptx::bulk_wait_read<EPI_SLOTS - 1>();
+                    __syncwarp();
+                }
+                SGB_CYCLES_END(c_slot, t_slot);
+                SGB_CYCLES_BEGIN(t_st);
+                const uint32_t saddr = ptx::smem_addr(slot);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                      v[4 * c + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                SGB_CYCLES_END(c_st, t_st);
+                if (lane == 0) {
+                    if (sg.split == 0) ptx::tma_store_2d(tm_y, slot, n0 + j * 32, m0 + quad * 32);
+                    else ptx::tma_reduce_add_2d(tm_y, slot, n0 + j * 32, m0 + quad * 32);
                     ptx::bulk_commit();
                 }
+                ++slabs;
+            }
+        } else {
+            // K % 4 != 0: row-per-thread stores (split 0) or read-add-write (later splits).
+            const int m = m0 + row;
+            const bool row_ok = m < kp.M;
+            const bool accumulate = sg.split > 0;
+            float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                ptx::tmem_ld_wait();
+                if (j == BN / 32 - 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&sm.acc_empty[buf]);
+                }
+                if (add_bias) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
+                }
+                if (!row_ok) continue;
+                const int nb = n0 + j * 32;
+                float old[32];
+                if (accumulate) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int n = nb + e;
+                    if (n >= kp.K) break;
+                    float o = __uint_as_float(v[e]);
+                    if (accumulate) o = old[e] + o;
+                    yrow[n] = o;
+                }
             }
         }
-        if (!store_now) {
-            ptx::named_bar_sync(1, EPI_THREADS);
-            if (et == 0 && wait_turn(kp, tile, split, sm.abort_flag)) {
-                ptx::fence_proxy_async_global();
-#pragma unroll 1
-                for (int j = 0; j < BN / 32; ++j)
-                    ptx::tma_reduce_add_2d(tm_y, stage_base + j * (BM * 128), n0 + j * 32, m0);
-                ptx::bulk_commit();
+
+        if (sg.nsplits > 1) {
+            SGB_CYCLES_BEGIN(t_done);
+            // Every write of this split must be complete and visible before the next split's turn.
+            if (kp.use_tma_store && lane == 0) {
                 ptx::bulk_wait_all();
                 ptx::fence_proxy_async_global();
-                __threadfence();
-                pass_turn(kp, tile, split);
             }
-        } else if (et == 0) {
-            if (serial) {
-                ptx::bulk_wait_all();  // writes done before the next split may add to them
-                ptx::fence_proxy_async_global();
-                __threadfence();
-                pass_turn(kp, tile, split);
-            } else {
-                ptx::bulk_wait_read_all();
-            }
+            __threadfence();
+            ptx::named_bar_sync(1, EPI_THREADS);
+            if (et == 0) pass_turn(kp, sg);
+            SGB_CYCLES_END(c_done, t_done);
         }
-        SGB_TRACE(kp, et == 0, 8);
-        return;
-    }
-
-    // K % 4 != 0: row-per-thread stores (split 0 / no split) or read-add-write
-    // (later splits, in turn).
-    if (serial && split > 0) {
-        if (et == 0) *sm.epi_go = wait_turn(kp, tile, split, sm.abort_flag) ? 1u : 0u;
-        ptx::named_bar_sync(1, EPI_THREADS);
-        if (!*sm.epi_go) return;
-    }
-    const bool accumulate = split > 0;
-    float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
-#pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
-        ptx::tmem_ld_wait();
-        if (!row_ok) continue;
-        const int nb = n0 + j * 32;
-        float old[32];
-        if (accumulate) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const int n = nb + e;
-            if (n >= kp.K) break;
-            float o = __uint_as_float(v[e]);
-            if (add_bias) o += __ldg(kp.bias + n);
-            if (accumulate) o = old[e] + o;
-            yrow[n] = o;
-        }
-    }
-    if (serial) {
-        __threadfence();
-        ptx::named_bar_sync(1, EPI_THREADS);
-        if (et == 0) pass_turn(kp, tile, split);
+        ++seg_idx;
     }
     SGB_TRACE(kp, et == 0, 8);
+    SGB_TRACE_VALUE(kp, et == 0, 11, c_acc);
+    SGB_TRACE_VALUE(kp, et == 0, 12, c_ld);
+    SGB_TRACE_VALUE(kp, et == 0, 13, c_slot);
+    SGB_TRACE_VALUE(kp, et == 0, 14, c_st);
+    SGB_TRACE_VALUE(kp, et == 0, 15, c_turn + (c_done << 32));
+    if (lane == 0) ptx::bulk_wait_read_all();  // staging slots must be read before the CTA exits
 }
 
 // ---------------------------------------------------------------- the kernel
 template <int BN, int LOADER>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(TileConfig<BN, LOADER>::THREADS, 1)
     conv2d_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_y, const ConvKernelParams kp)
 {
-    using Cfg = TileConfig<BN>;
+    using Cfg = TileConfig<BN, LOADER>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmemView sm;
     sm.a = smem;
     sm.b = smem + Cfg::STAGES * A_STAGE_BYTES;
-    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES);
+    sm.epi = smem + Cfg::RING_BYTES;
+    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + EPI_BYTES);
     sm.empty = sm.full + Cfg::STAGES;
     sm.acc_full = sm.empty + Cfg::STAGES;
-    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.acc_full + 1);
+    sm.acc_empty = sm.acc_full + 2;
+    sm.mma_done = sm.acc_empty + 2;
+    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
     sm.abort_flag = sm.tmem_slot + 1;
     sm.epi_go = sm.tmem_slot + 2;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tiles = kp.m_tiles * kp.n_tiles;
-    // Split-major block order: every split-j CTA has a lower id than any
-    // split-(j+1) CTA, so a tile's predecessors are scheduled first.
-    const int split = blockIdx.x / tiles;
-    const int tile = blockIdx.x - split * tiles;
-    const int m_tile = tile / kp.n_tiles;
-    const int n_tile = tile - m_tile * kp.n_tiles;
-    const int m0 = m_tile * BM;
-    const int n0 = n_tile * BN;
-    const int kb_begin = static_cast<int>(static_cast<int64_t>(split) * kp.num_kb / kp.splits);
-    const int kb_end = static_cast<int>(static_cast<int64_t>(split + 1) * kp.num_kb / kp.splits);
-    const int nkb = kb_end - kb_begin;
     SGB_TRACE(kp, threadIdx.x == 0, 0);
 
     if (threadIdx.x == 0) {
+        // TMA producer: one arrive (with the byte count); cp.async gather: one
+        // arrive per thread (issued by its copies); scalar gather: one per warp.
+        constexpr uint32_t GATHER_WARPS = GATHER_THREADS / 32;
         const uint32_t full_count =
-            LOADER == LOADER_TMA ? 1u : (LOADER == LOADER_CPASYNC ? 1u + EPI_THREADS : EPI_THREADS);
+            LOADER == LOADER_TMA ? 1u : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
         for (int i = 0; i < Cfg::STAGES; ++i) {
             ptx::mbar_init(&sm.full[i], full_count);
             ptx::mbar_init(&sm.empty[i], 1);
         }
-        ptx::mbar_init(sm.acc_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sm.acc_full[i], 1);
+            ptx::mbar_init(&sm.acc_empty[i], EPI_THREADS);
+        }
+        ptx::mbar_init(sm.mma_done, 1);
         *sm.abort_flag = 0u;
         *sm.epi_go = 0u;
         ptx::mbar_init_fence();
     }
     if (warp == 0 && lane == 0) {
-        if (LOADER == LOADER_TMA) ptx::prefetch_tensormap(&tm_a);
+        if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID) ptx::prefetch_tensormap(&tm_a);
         if (LOADER != LOADER_SCALAR) ptx::prefetch_tensormap(&tm_b);
         if (kp.use_tma_store) ptx::prefetch_tensormap(&tm_y);
     }
@@ -601,15 +787,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
-        if (lane == 0 && LOADER != LOADER_SCALAR)
-            run_tma_producer<BN, LOADER>(&tm_a, &tm_b, kp, sm, m0, n0, kb_begin, nkb);
+        if (lane == 0 && LOADER != LOADER_SCALAR) run_tma_producer<BN, LOADER>(&tm_a, &tm_b, kp, sm);
     } else if (warp == 1) {
-        if (lane == 0) run_mma_issuer<BN>(kp, sm, tmem_base, nkb);
+        if (lane == 0) run_mma_issuer<BN, LOADER>(kp, sm, tmem_base);
+    } else if (warp < GATHER_WARP0) {
+        run_epilogue<BN>(&tm_y, kp, sm, tmem_base);
     } else {
-        if (LOADER == LOADER_CPASYNC) run_gather_cpasync<BN>(kp, sm, m0, kb_begin, nkb);
-        if (LOADER == LOADER_SCALAR) run_gather_scalar<BN>(kp, sm, m0, n0, kb_begin, nkb);
-        SGB_TRACE(kp, threadIdx.x == EPI_THREAD0, 9);
-        run_epilogue<BN>(&tm_y, kp, sm, tmem_base, m0, n0, split, tile);
+        if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BN, LOADER>(kp, sm);
+        if (LOADER == LOADER_SCALAR) run_gather_scalar<BN, LOADER>(kp, sm);
+        SGB_TRACE(kp, threadIdx.x == GATHER_WARP0 * 32, 9);
     }
 
     ptx::tc_fence_before();
@@ -638,8 +824,8 @@ template <int BN, int LOADER>
 cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
                              const ConvKernelParams& kp, int grid, cudaStream_t stream)
 {
+    using Cfg = TileConfig<BN, LOADER>;
     auto kern = conv2d_fwd_tc_kernel<BN, LOADER>;
-    constexpr int smem = TileConfig<BN>::SMEM_BYTES;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -647,7 +833,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     static unsigned long long configured = 0ull;
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
     if (!bit || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (err != cudaSuccess) return err;
         if (bit) __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
@@ -656,8 +842,8 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     // grid_dependency_wait) before touching global memory.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -667,19 +853,21 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_y, kp);
 }
 
-#define SGB_LAUNCH_SIG(BN_, L_)                                                                                  \
-    cudaError_t launch_conv2d_tc<BN_, L_>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,          \
+#define SGB_LAUNCH_SIG(BN_, L_)                                                                         \
+    cudaError_t launch_conv2d_tc<BN_, L_>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
                                           const ConvKernelParams&, int, cudaStream_t)
 
-#define SGB_INSTANTIATE_CONV2D(BN_)                 \
-    template SGB_LAUNCH_SIG(BN_, LOADER_TMA);       \
-    template SGB_LAUNCH_SIG(BN_, LOADER_CPASYNC);   \
-    template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);
+#define SGB_INSTANTIATE_CONV2D(BN_)               \
+    template SGB_LAUNCH_SIG(BN_, LOADER_TMA);     \
+    template SGB_LAUNCH_SIG(BN_, LOADER_CPASYNC); \
+    template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);  \
+    template SGB_LAUNCH_SIG(BN_, LOADER_HYBRID);
 
 // Declarations of the instantiations that live in other translation units.
 #define SGB_DECLARE_CONV2D(BN_)                          \
     extern template SGB_LAUNCH_SIG(BN_, LOADER_TMA);     \
     extern template SGB_LAUNCH_SIG(BN_, LOADER_CPASYNC); \
-    extern template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);
+    extern template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);  \
+    extern template SGB_LAUNCH_SIG(BN_, LOADER_HYBRID);
 
 }  // namespace sgb

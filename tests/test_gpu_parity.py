@@ -54,7 +54,7 @@ def test_tiny_workload_gather_loaders(sg, loader):
     _run_and_check(sg, wl, x, w, b, make_algo(sg, loader=loader, wait_limit_ns=WAIT))
 
 
-@pytest.mark.parametrize("loader", [1, 2, 3])
+@pytest.mark.parametrize("loader", [1, 2, 3, 4])
 @pytest.mark.parametrize("bn", [64, 128, 256])
 def test_c64_each_loader_each_width(sg, loader, bn):
     # 2 images of 10x10, 3x3 pad 1: M = 200 (one full tile + a ragged tail), K = 80 (ragged in N).
@@ -69,7 +69,7 @@ def test_c64_each_loader_each_width(sg, loader, bn):
     dict(stride=(1, 3), pad=(0, 2), dil=(1, 2)),
     dict(stride=2, pad=3, dil=1),
 ])
-@pytest.mark.parametrize("loader", [1, 2])
+@pytest.mark.parametrize("loader", [1, 2, 4])
 def test_asymmetric_windows(sg, geom, loader):
     wl, x, w, b = _case(2, 13, 11, 64, 64, 3, 5, seed=2, **geom)
     _run_and_check(sg, wl, x, w, b, make_algo(sg, loader=loader, wait_limit_ns=WAIT), f"{geom} loader={loader}")

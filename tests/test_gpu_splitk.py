@@ -33,7 +33,7 @@ def long_k_case():
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 36])
-@pytest.mark.parametrize("loader", [1, 2])
+@pytest.mark.parametrize("loader", [1, 2, 4])
 def test_forced_splits_match_oracle(sg, long_k_case, splits, loader):
     wl, x, w, b, ref = long_k_case
     got = gpu_conv(sg, x, w, b, wl.options(), algo=make_algo(sg, splits=splits, loader=loader, wait_limit_ns=WAIT))
