@@ -290,13 +290,14 @@ def run_ours(args, wl, world, rank, local):
     params = sg.make_params(x.shape, w.shape, **wl.options())
     p, q = sg.output_shape(params)
     forced = None
-    if args.block_n or args.splits or args.loader or args.grid:
+    if args.block_n or args.splits or args.loader or args.grid or args.block_m:
         forced = sg.Algo()
         forced.block_n, forced.splits, forced.loader, forced.grid = args.block_n, args.splits, args.loader, args.grid
+        forced.block_m = args.block_m
     algo = sg.query_algo(params)
     if forced is not None:
         algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, forced.loader or algo.loader,
-                       forced.grid or (0 if forced.splits else algo.grid))
+                       forced.grid or (0 if forced.splits else algo.grid), 0, forced.block_m or algo.block_m)
     set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * 4 + (0 if b is None else b.numel() * 4)
     n_sets = _sets_for(wl, set_bytes)
     sets = []
@@ -499,6 +500,7 @@ def parse_args(argv=None):
     ap.add_argument("--splits", type=int, default=0, help="force the split-K factor")
     ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
+    ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")

@@ -91,7 +91,7 @@ typedef struct {
     int32_t loader;    /* conv2d_loader */
     int32_t grid;      /* CTAs for stream-K (1 .. tiles * k-blocks); 0 = heuristic */
     int32_t debug_flags;      /* test hook, 0 in normal use; see CONV2D_DEBUG_* */
-    int32_t reserved1;
+    int32_t block_m;          /* output pixels per CTA tile: 128, or 256 (TMA im2col loader only) */
     int64_t wait_limit_ns;    /* bound on every device-side wait; 0 = default (1 s) */
 } conv2d_algo;
 

@@ -55,11 +55,12 @@ class Params(ctypes.Structure):
 
 class Algo(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("splits", ctypes.c_int32), ("loader", ctypes.c_int32),
-                ("grid", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("block_m", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64)]
 
     def as_dict(self):
-        return dict(block_n=self.block_n, splits=self.splits, loader=self.loader, grid=self.grid)
+        return dict(block_m=self.block_m, block_n=self.block_n, splits=self.splits, loader=self.loader,
+                    grid=self.grid)
 
 
 _lock = threading.Lock()

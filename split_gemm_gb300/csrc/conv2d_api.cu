@@ -23,7 +23,7 @@ SGB_DECLARE_CONV2D(256)
 namespace {
 
 using sgb::BK;
-using sgb::BM;
+constexpr int64_t kMinTileM = 128;  // the narrowest tile height (sizes the semaphore array)
 
 constexpr int64_t kIndexLimit = (int64_t(1) << 31) - 1;
 constexpr size_t kStatusBytes = 256;  // status word, padded so the semaphores start 256-B aligned
@@ -136,6 +136,7 @@ bool tma_im2col_eligible(const Shape& s)
 
 // ------------------------------------------------------------------ heuristic
 struct Plan {
+    int block_m;
     int block_n;
     int splits;  // classic split-K factor, or 0 for stream-K
     int loader;
@@ -165,7 +166,20 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
-    const int64_t m_tiles = cdiv(s.m, BM);
+    int bm = force ? force->block_m : 0;
+    if (bm == 0) {
+        // 256-pixel tiles halve the im2col operations per MMA (the TMA unit's cost
+        // is per operation); worth it when the output channels are few (<= 128,
+        // so the MMA per k-block is short) and the tiles still cover the SMs.
+        bm = 128;
+        const int64_t bn_guess = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+        if (loader == CONV2D_LOADER_TMA_IM2COL && bn_guess <= 128 && (!force || force->splits == 0) &&
+            cdiv(s.m, 256) * cdiv(s.k, bn_guess) * 5 >= (sms > 0 ? sms : 1) * 4)
+            bm = 256;
+    }
+    if (bm != 128 && bm != 256) return CONV2D_ERR_INVALID;
+    if (bm == 256 && loader != CONV2D_LOADER_TMA_IM2COL) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t m_tiles = cdiv(s.m, bm);
     const int64_t num_kb = cdiv(s.crs, BK);
     const int64_t forced_splits = force ? force->splits : 0;
     const int64_t forced_grid = force ? force->grid : 0;
@@ -213,6 +227,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         return CONV2D_ERR_UNSUPPORTED;  // every CTA needs at least one unit
     }
     if (grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
+    plan->block_m = bm;
     plan->block_n = bn;
     plan->splits = static_cast<int>(splits);
     plan->loader = loader;
@@ -227,7 +242,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
 size_t workspace_bytes_for(const Shape& s)
 {
     // Enough semaphores for the narrowest tile width.
-    const int64_t tiles = cdiv(s.m, BM) * cdiv(s.k, 64);
+    const int64_t tiles = cdiv(s.m, kMinTileM) * cdiv(s.k, 64);
     return kStatusBytes + static_cast<size_t>(tiles) * sizeof(uint32_t);
 }
 
@@ -249,7 +264,7 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
         const int upper[2] = {(int)(s.pw - (s.s - 1) * s.dw), (int)(s.ph - (s.r - 1) * s.dh)};
         const cuuint32_t estr[4] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1};
         CUresult rc = g_encode_im2col(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
-                                      strides, lower, upper, BK, BM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      strides, lower, upper, BK, static_cast<cuuint32_t>(plan.block_m), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
@@ -277,16 +292,17 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     return CONV2D_OK;
 }
 
-cudaError_t dispatch(int bn, int loader, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+cudaError_t dispatch(int bm, int bn, int loader, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
                      const sgb::ConvKernelParams& kp, int grid, cudaStream_t st)
 {
     using namespace sgb;
-#define SGB_CASE(BN_)                                                                                         \
-    if (bn == BN_) {                                                                                          \
-        if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<BN_, LOADER_TMA>(a, b, y, kp, grid, st); \
-        if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<BN_, LOADER_CPASYNC>(a, b, y, kp, grid, st); \
-        if (loader == CONV2D_LOADER_HYBRID) return launch_conv2d_tc<BN_, LOADER_HYBRID>(a, b, y, kp, grid, st); \
-        return launch_conv2d_tc<BN_, LOADER_SCALAR>(a, b, y, kp, grid, st);                                     \
+#define SGB_CASE(BN_)                                                                                          \
+    if (bn == BN_) {                                                                                           \
+        if (bm == 256) return launch_conv2d_tc<256, BN_, LOADER_TMA>(a, b, y, kp, grid, st);                 \
+        if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<128, BN_, LOADER_TMA>(a, b, y, kp, grid, st); \
+        if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<128, BN_, LOADER_CPASYNC>(a, b, y, kp, grid, st); \
+        if (loader == CONV2D_LOADER_HYBRID) return launch_conv2d_tc<128, BN_, LOADER_HYBRID>(a, b, y, kp, grid, st); \
+        return launch_conv2d_tc<128, BN_, LOADER_SCALAR>(a, b, y, kp, grid, st);                               \
     }
     SGB_CASE(64)
     SGB_CASE(128)
@@ -316,7 +332,8 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
         (workspace && !aligned16(workspace)))
         return CONV2D_ERR_ALIGNMENT;
-    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->grid < 0 || algo->wait_limit_ns < 0))
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
+                 algo->wait_limit_ns < 0))
         return CONV2D_ERR_INVALID;
     Plan plan;
     rc = choose_plan(s, algo, &plan);
@@ -359,10 +376,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
 
     const int64_t grid = plan.grid;
     if (log_enabled())
-        std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BN=%d splits=%d loader=%d grid=%lld tma_store=%d\n",
-                     (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_n, plan.splits, plan.loader,
+        std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BM=%d BN=%d splits=%d loader=%d grid=%lld tma_store=%d\n",
+                     (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_m, plan.block_n, plan.splits, plan.loader,
                      (long long)grid, (int)tma_store);
-    cudaError_t err = dispatch(plan.block_n, plan.loader, tm_a, tm_b, tm_y, kp, (int)grid, stream);
+    cudaError_t err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, tm_y, kp, (int)grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;
     g_last_launches = 1;
     return CONV2D_OK;
@@ -416,6 +433,7 @@ int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
     rc = choose_plan(s, nullptr, &plan);
     if (rc != CONV2D_OK) return rc;
     std::memset(out, 0, sizeof(*out));
+    out->block_m = plan.block_m;
     out->block_n = plan.block_n;
     out->splits = plan.splits;
     out->loader = plan.loader;

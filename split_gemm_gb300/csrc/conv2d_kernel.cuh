@@ -58,14 +58,13 @@
 
 namespace sgb {
 
-constexpr int BM = 128;          // output pixels per tile (MMA M)
+constexpr int MMA_M = 128;       // rows per tcgen05.mma (cta_group::1); a tile has BM/128 row blocks
 constexpr int BK = 64;           // reduction elements per stage: one 128-byte bf16 row
 constexpr int UMMA_K = 16;       // reduction per tcgen05.mma of kind::f16
 constexpr int EPI_WARP0 = 2;     // epilogue warps 2..5
 constexpr int EPI_THREADS = 128;
 constexpr int GATHER_WARP0 = 6;  // gather warps 6..9 (gather loaders only)
 constexpr int GATHER_THREADS = 128;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
 constexpr int EPI_SLOTS = 2;                 // staging slots per epilogue warp
 constexpr int EPI_BYTES = 4 * EPI_SLOTS * EPI_SLOT_BYTES;
@@ -138,17 +137,28 @@ struct ConvKernelParams {
     } while (0)
 #endif
 
-template <int BN, int LOADER>
+// Tile BM x BN (BM = 128 or 256 output pixels, BN = 64/128/256 channels).  A
+// 256-pixel tile is loaded with one im2col operation per k-block and computed
+// as two 128-row MMAs into two TMEM accumulators: the TMA unit's cost is per
+// operation, so this doubles the MMA work each activation load feeds.
+template <int BM, int BN, int LOADER>
 struct TileConfig {
+    static_assert(BM == 128 || BM == 256, "BM must be 128 or 256");
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+    static_assert(BM == 128 || LOADER == LOADER_TMA, "256-pixel tiles use the TMA im2col loader");
+    static constexpr int M_SUB = BM / MMA_M;  // 128-row MMA blocks per tile
+    static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int STAGES =
+        BM == 128 ? (BN == 256 ? 4 : (BN == 128 ? 6 : 8)) : (BN == 256 ? 3 : 4);
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared-memory limit");
-    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+    static constexpr int ACC_COLS = M_SUB * BN;                   // TMEM columns of one accumulator set
+    static constexpr int NUM_ACC = 2 * ACC_COLS <= 512 ? 2 : 1;   // double-buffered when TMEM allows
+    static constexpr uint32_t TMEM_COLS = NUM_ACC * ACC_COLS;
     static constexpr int THREADS = (LOADER == LOADER_TMA ? 6 : 10) * 32;
 };
 
@@ -229,12 +239,13 @@ __device__ __forceinline__ void decode_pixel(const ConvKernelParams& kp, int m, 
 }
 
 // ---------------------------------------------------------------- TMA producer (warp 0, one thread)
-template <int BN, int LOADER>
+template <int BM, int BN, int LOADER>
 __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
                                  const SmemView& sm)
 {
-    using Cfg = TileConfig<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
     int it = 0;  // k-blocks issued so far (all segments)
     bool ok = true;
     uint64_t wait_cycles = 0;
@@ -292,12 +303,13 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
 }
 
 // ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
-template <int BN, int LOADER>
+template <int BM, int BN, int LOADER>
 __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, uint32_t tmem_base)
 {
-    using Cfg = TileConfig<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+    constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(MMA_M, BN);
     int it = 0, seg_idx = 0;
     bool ok = true;
     uint64_t full_cycles = 0, acc_cycles = 0;
@@ -306,8 +318,8 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     SegmentWalker walk(kp);
     Segment sg;
     while (ok && walk.next(kp, sg)) {
-        const int buf = seg_idx & 1;
-        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        const int buf = seg_idx % Cfg::NUM_ACC;
+        const uint32_t use = static_cast<uint32_t>(seg_idx / Cfg::NUM_ACC) & 1u;
         // The epilogue must have drained this accumulator's previous segment.
         SGB_CYCLES_BEGIN(ta);
         if (!ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
@@ -316,7 +328,7 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
         }
         SGB_CYCLES_END(acc_cycles, ta);
         ptx::tc_fence_after();
-        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * BN);
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * Cfg::ACC_COLS);
         for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
             const int stage = it % STAGES;
             const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -337,9 +349,12 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
                 // Advancing along K inside a 128-B swizzled row moves the start address by 32 B.
-                const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + k * UMMA_K * 2);
                 const uint64_t bd = ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2);
-                ptx::mma_bf16(tmem_d, ad, bd, IDESC, (kb > sg.kb_begin || k > 0) ? 1u : 0u);
+#pragma unroll
+                for (int sub = 0; sub < Cfg::M_SUB; ++sub) {  // 128-row blocks share the B tile
+                    const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + sub * MMA_M * 128 + k * UMMA_K * 2);
+                    ptx::mma_bf16(tmem_d + sub * BN, ad, bd, IDESC, (kb > sg.kb_begin || k > 0) ? 1u : 0u);
+                }
             }
             ptx::mma_commit(&sm.empty[stage]);
         }
@@ -363,11 +378,12 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
 // thread hands its copies to the stage's full barrier with a non-blocking
 // cp.async arrive, so the gather runs as far ahead as the ring allows; the MMA
 // thread fences the async proxy after its wait (run_mma_issuer).
-template <int BN, int LOADER>
+template <int BM, int BN, int LOADER>
 __device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& sm)
 {
-    using Cfg = TileConfig<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
     constexpr int ROWS = BM / 16;  // tile rows per thread
     const int gt = threadIdx.x - GATHER_WARP0 * 32;
     const int lane = threadIdx.x & 31;
@@ -441,11 +457,13 @@ __device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& s
 
 // A and B tiles element by element (any C, any C*R*S): plain loads, then
 // 16-byte shared stores in the swizzled layout.
-template <int BN, int LOADER>
+template <int BM, int BN, int LOADER>
 __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm)
 {
-    using Cfg = TileConfig<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    static_assert(BM == GATHER_THREADS, "one tile row per gather thread");
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
     const int row = threadIdx.x - GATHER_WARP0 * 32;
     const int lane = threadIdx.x & 31;
     int it = 0;
@@ -566,15 +584,16 @@ __device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, const Segm
     ptx::st_release_gpu(kp.sems + sg.tile, next);
 }
 
-template <int BN>
+template <int BM, int BN, int LOADER>
 __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp, const SmemView& sm,
                              uint32_t tmem_base)
 {
+    using Cfg = TileConfig<BM, BN, LOADER>;
     const int et = threadIdx.x - EPI_WARP0 * 32;  // 0..127
     const int ew = et >> 5;                        // epilogue warp 0..3
     const int lane = threadIdx.x & 31;
     const int quad = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;          // tile row owned by this thread
+    const int row = quad * 32 + lane;          // row of each 128-row block owned by this thread
     uint8_t* slots = sm.epi + ew * (EPI_SLOTS * EPI_SLOT_BYTES);
     int seg_idx = 0;
     int slabs = 0;  // slabs this warp has handed to the TMA unit (staging-slot rotation)
@@ -583,8 +602,8 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
     SegmentWalker walk(kp);
     Segment sg;
     while (walk.next(kp, sg)) {
-        const int buf = seg_idx & 1;
-        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        const int buf = seg_idx % Cfg::NUM_ACC;
+        const uint32_t use = static_cast<uint32_t>(seg_idx / Cfg::NUM_ACC) & 1u;
         const int m_tile = sg.tile / kp.n_tiles;
         const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
         const int m0 = m_tile * BM;
@@ -615,84 +634,89 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
         ptx::tc_fence_after();
         SGB_TRACE(kp, et == 0 && seg_idx == 0, 7);
 
-        const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
-
-        if (kp.use_tma_store) {
-            // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
-            // TMA store (split 0) or TMA reduce-add (later splits, in turn).
+#pragma unroll 1
+        for (int sub = 0; sub < Cfg::M_SUB; ++sub) {
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * Cfg::ACC_COLS + sub * BN) +
+                                   (static_cast<uint32_t>(quad * 32) << 16);
+            const int mrow0 = m0 + sub * MMA_M;  // first output row of this 128-row block
+            const bool last_sub = sub == Cfg::M_SUB - 1;
+            if (kp.use_tma_store) {
+                // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
+                // TMA store (split 0) or TMA reduce-add (later splits, in turn).
 #pragma unroll
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t v[32];
-                SGB_CYCLES_BEGIN(t_ld);
-                ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
-                ptx::tmem_ld_wait();
-                SGB_CYCLES_END(c_ld, t_ld);
-                if (j == BN / 32 - 1) {  // accumulator drained: the MMA warp may reuse it
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(&sm.acc_empty[buf]);
-                }
-                if (add_bias) {
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t v[32];
+                    SGB_CYCLES_BEGIN(t_ld);
+                    ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                    ptx::tmem_ld_wait();
+                    SGB_CYCLES_END(c_ld, t_ld);
+                    if (last_sub && j == BN / 32 - 1) {  // accumulator drained: the MMA warp may reuse it
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(&sm.acc_empty[buf]);
+                    }
+                    if (add_bias) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
-                }
-                uint8_t* slot = slots + (slabs % EPI_SLOTS) * EPI_SLOT_BYTES;
-                SGB_CYCLES_BEGIN(t_slot);
-                if (slabs >= EPI_SLOTS) {  // the slot's previous slab must have been read by the TMA unit
-                    if (lane == 0) ptx::bulk_wait_read<EPI_SLOTS - 1>();
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
+                    }
+                    uint8_t* slot = slots + (slabs % EPI_SLOTS) * EPI_SLOT_BYTES;
+                    SGB_CYCLES_BEGIN(t_slot);
+                    if (slabs >= EPI_SLOTS) {  // the slot's previous slab must have been read by the TMA unit
+                        if (lane == 0) ptx::bulk_wait_read<EPI_SLOTS - 1>();
+                        __syncwarp();
+                    }
+                    SGB_CYCLES_END(c_slot, t_slot);
+                    SGB_CYCLES_BEGIN(t_st);
+                    const uint32_t saddr = ptx::smem_addr(slot);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                          v[4 * c + 3]);
+                    ptx::fence_proxy_async_smem();
                     __syncwarp();
+                    SGB_CYCLES_END(c_st, t_st);
+                    if (lane == 0) {
+                        if (sg.split == 0) ptx::tma_store_2d(tm_y, slot, n0 + j * 32, mrow0 + quad * 32);
+                        else ptx::tma_reduce_add_2d(tm_y, slot, n0 + j * 32, mrow0 + quad * 32);
+                        ptx::bulk_commit();
+                    }
+                    ++slabs;
                 }
-                SGB_CYCLES_END(c_slot, t_slot);
-                SGB_CYCLES_BEGIN(t_st);
-                const uint32_t saddr = ptx::smem_addr(slot);
+            } else {
+                // K % 4 != 0: row-per-thread stores (split 0) or read-add-write (later splits).
+                const int m = mrow0 + row;
+                const bool row_ok = m < kp.M;
+                const bool accumulate = sg.split > 0;
+                float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
-                                      v[4 * c + 3]);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                SGB_CYCLES_END(c_st, t_st);
-                if (lane == 0) {
-                    if (sg.split == 0) ptx::tma_store_2d(tm_y, slot, n0 + j * 32, m0 + quad * 32);
-                    else ptx::tma_reduce_add_2d(tm_y, slot, n0 + j * 32, m0 + quad * 32);
-                    ptx::bulk_commit();
-                }
-                ++slabs;
-            }
-        } else {
-            // K % 4 != 0: row-per-thread stores (split 0) or read-add-write (later splits).
-            const int m = m0 + row;
-            const bool row_ok = m < kp.M;
-            const bool accumulate = sg.split > 0;
-            float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                    ptx::tmem_ld_wait();
+                    if (last_sub && j == BN / 32 - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(&sm.acc_empty[buf]);
+                    }
+                    if (add_bias) {
 #pragma unroll
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
-                ptx::tmem_ld_wait();
-                if (j == BN / 32 - 1) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(&sm.acc_empty[buf]);
-                }
-                if (add_bias) {
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
+                    }
+                    if (!row_ok) continue;
+                    const int nb = n0 + j * 32;
+                    float old[32];
+                    if (accumulate) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
-                }
-                if (!row_ok) continue;
-                const int nb = n0 + j * 32;
-                float old[32];
-                if (accumulate) {
+                        for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
+                    }
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int n = nb + e;
-                    if (n >= kp.K) break;
-                    float o = __uint_as_float(v[e]);
-                    if (accumulate) o = old[e] + o;
-                    yrow[n] = o;
+                    for (int e = 0; e < 32; ++e) {
+                        const int n = nb + e;
+                        if (n >= kp.K) break;
+                        float o = __uint_as_float(v[e]);
+                        if (accumulate) o = old[e] + o;
+                        yrow[n] = o;
+                    }
                 }
             }
         }
@@ -721,17 +745,17 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, int LOADER>
-__global__ void __launch_bounds__(TileConfig<BN, LOADER>::THREADS, 1)
+template <int BM, int BN, int LOADER>
+__global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     conv2d_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_y, const ConvKernelParams kp)
 {
-    using Cfg = TileConfig<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmemView sm;
     sm.a = smem;
-    sm.b = smem + Cfg::STAGES * A_STAGE_BYTES;
+    sm.b = smem + Cfg::STAGES * Cfg::A_STAGE_BYTES;
     sm.epi = smem + Cfg::RING_BYTES;
     sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + EPI_BYTES);
     sm.empty = sm.full + Cfg::STAGES;
@@ -787,14 +811,14 @@ __global__ void __launch_bounds__(TileConfig<BN, LOADER>::THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
-        if (lane == 0 && LOADER != LOADER_SCALAR) run_tma_producer<BN, LOADER>(&tm_a, &tm_b, kp, sm);
+        if (lane == 0 && LOADER != LOADER_SCALAR) run_tma_producer<BM, BN, LOADER>(&tm_a, &tm_b, kp, sm);
     } else if (warp == 1) {
-        if (lane == 0) run_mma_issuer<BN, LOADER>(kp, sm, tmem_base);
+        if (lane == 0) run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
     } else if (warp < GATHER_WARP0) {
-        run_epilogue<BN>(&tm_y, kp, sm, tmem_base);
+        run_epilogue<BM, BN, LOADER>(&tm_y, kp, sm, tmem_base);
     } else {
-        if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BN, LOADER>(kp, sm);
-        if (LOADER == LOADER_SCALAR) run_gather_scalar<BN, LOADER>(kp, sm);
+        if constexpr (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BM, BN, LOADER>(kp, sm);
+        if constexpr (LOADER == LOADER_SCALAR) run_gather_scalar<BM, BN, LOADER>(kp, sm);
         SGB_TRACE(kp, threadIdx.x == GATHER_WARP0 * 32, 9);
     }
 
@@ -820,12 +844,12 @@ inline bool pdl_enabled()
 
 // Host-side launcher for one instantiation; explicitly instantiated in one
 // translation unit per tile width so that the variants compile in parallel.
-template <int BN, int LOADER>
+template <int BM, int BN, int LOADER>
 cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
                              const ConvKernelParams& kp, int grid, cudaStream_t stream)
 {
-    using Cfg = TileConfig<BN, LOADER>;
-    auto kern = conv2d_fwd_tc_kernel<BN, LOADER>;
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    auto kern = conv2d_fwd_tc_kernel<BM, BN, LOADER>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -853,21 +877,24 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_y, kp);
 }
 
-#define SGB_LAUNCH_SIG(BN_, L_)                                                                         \
-    cudaError_t launch_conv2d_tc<BN_, L_>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
-                                          const ConvKernelParams&, int, cudaStream_t)
+#define SGB_LAUNCH_SIG(BM_, BN_, L_)                                                                        \
+    cudaError_t launch_conv2d_tc<BM_, BN_, L_>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
+                                               const ConvKernelParams&, int, cudaStream_t)
 
-#define SGB_INSTANTIATE_CONV2D(BN_)               \
-    template SGB_LAUNCH_SIG(BN_, LOADER_TMA);     \
-    template SGB_LAUNCH_SIG(BN_, LOADER_CPASYNC); \
-    template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);  \
-    template SGB_LAUNCH_SIG(BN_, LOADER_HYBRID);
+// Every loader with 128-pixel tiles, and the TMA loader with 256-pixel tiles.
+#define SGB_INSTANTIATE_CONV2D(BN_)                    \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_TMA);     \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_CPASYNC); \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
+    template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 
 // Declarations of the instantiations that live in other translation units.
-#define SGB_DECLARE_CONV2D(BN_)                          \
-    extern template SGB_LAUNCH_SIG(BN_, LOADER_TMA);     \
-    extern template SGB_LAUNCH_SIG(BN_, LOADER_CPASYNC); \
-    extern template SGB_LAUNCH_SIG(BN_, LOADER_SCALAR);  \
-    extern template SGB_LAUNCH_SIG(BN_, LOADER_HYBRID);
+#define SGB_DECLARE_CONV2D(BN_)                               \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_TMA);     \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_CPASYNC); \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
+    extern template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 
 }  // namespace sgb

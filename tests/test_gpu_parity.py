@@ -63,6 +63,16 @@ def test_c64_each_loader_each_width(sg, loader, bn):
                    f"loader={loader} bn={bn}")
 
 
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("grid", [0, 1, 3])
+def test_256_pixel_tiles(sg, bn, grid):
+    # M = 3*10*10 = 300: one full 256-row tile and a ragged one; K = 200 ragged in N.
+    # grid 1 and 3 put several tiles (and cut tiles) on one CTA.
+    wl, x, w, b = _case(3, 10, 10, 64, 200, 3, 3, pad=1, seed=4)
+    _run_and_check(sg, wl, x, w, b, make_algo(sg, block_m=256, block_n=bn, loader=1, grid=grid, wait_limit_ns=WAIT),
+                   f"BM=256 bn={bn} grid={grid}")
+
+
 @pytest.mark.parametrize("geom", [
     dict(stride=(2, 1), pad=(1, 0), dil=1),
     dict(stride=1, pad=(2, 1), dil=(2, 1)),

@@ -40,6 +40,14 @@ def test_forced_splits_match_oracle(sg, long_k_case, splits, loader):
     check_close(got, ref, wl.c, wl.r, wl.s, f"splits={splits} loader={loader}")
 
 
+@pytest.mark.parametrize("splits", [2, 5])
+def test_forced_splits_256_pixel_tiles(sg, long_k_case, splits):
+    wl, x, w, b, ref = long_k_case
+    got = gpu_conv(sg, x, w, b, wl.options(),
+                   algo=make_algo(sg, splits=splits, loader=1, block_m=256, wait_limit_ns=WAIT))
+    check_close(got, ref, wl.c, wl.r, wl.s, f"BM=256 splits={splits}")
+
+
 def test_splits_agree_and_are_deterministic(sg, long_k_case):
     wl, x, w, b, _ = long_k_case
     outs = {}
