@@ -247,12 +247,10 @@ size_t workspace_bytes_for(const Shape& s)
 }
 
 // ------------------------------------------------------------------ descriptors
-int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, float* y, bool tma_store,
-                CUtensorMap* tm_a, CUtensorMap* tm_b, CUtensorMap* tm_y)
+int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, CUtensorMap* tm_a, CUtensorMap* tm_b)
 {
     std::memset(tm_a, 0, sizeof(*tm_a));
     std::memset(tm_b, 0, sizeof(*tm_b));
-    std::memset(tm_y, 0, sizeof(*tm_y));
     if (!load_encoders()) return CONV2D_ERR_CUDA;
     if (plan.loader == CONV2D_LOADER_TMA_IM2COL || plan.loader == CONV2D_LOADER_HYBRID) {
         const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
@@ -279,30 +277,20 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     }
-    if (tma_store) {
-        const cuuint64_t dims[2] = {(cuuint64_t)s.k, (cuuint64_t)s.m};
-        const cuuint64_t strides[1] = {(cuuint64_t)(s.k * 4)};
-        const cuuint32_t box[2] = {32, 32};  // one epilogue warp's 32 rows x 32 columns
-        const cuuint32_t estr[2] = {1, 1};
-        CUresult rc = g_encode_tiled(tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
-                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
-    }
     return CONV2D_OK;
 }
 
-cudaError_t dispatch(int bm, int bn, int loader, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+cudaError_t dispatch(int bm, int bn, int loader, const CUtensorMap& a, const CUtensorMap& b,
                      const sgb::ConvKernelParams& kp, int grid, cudaStream_t st)
 {
     using namespace sgb;
 #define SGB_CASE(BN_)                                                                                          \
     if (bn == BN_) {                                                                                           \
-        if (bm == 256) return launch_conv2d_tc<256, BN_, LOADER_TMA>(a, b, y, kp, grid, st);                 \
-        if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<128, BN_, LOADER_TMA>(a, b, y, kp, grid, st); \
-        if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<128, BN_, LOADER_CPASYNC>(a, b, y, kp, grid, st); \
-        if (loader == CONV2D_LOADER_HYBRID) return launch_conv2d_tc<128, BN_, LOADER_HYBRID>(a, b, y, kp, grid, st); \
-        return launch_conv2d_tc<128, BN_, LOADER_SCALAR>(a, b, y, kp, grid, st);                               \
+        if (bm == 256) return launch_conv2d_tc<256, BN_, LOADER_TMA>(a, b, kp, grid, st);                 \
+        if (loader == CONV2D_LOADER_TMA_IM2COL) return launch_conv2d_tc<128, BN_, LOADER_TMA>(a, b, kp, grid, st); \
+        if (loader == CONV2D_LOADER_CPASYNC) return launch_conv2d_tc<128, BN_, LOADER_CPASYNC>(a, b, kp, grid, st); \
+        if (loader == CONV2D_LOADER_HYBRID) return launch_conv2d_tc<128, BN_, LOADER_HYBRID>(a, b, kp, grid, st); \
+        return launch_conv2d_tc<128, BN_, LOADER_SCALAR>(a, b, kp, grid, st);                               \
     }
     SGB_CASE(64)
     SGB_CASE(128)
@@ -343,10 +331,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     const bool cuts_tiles = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
     if (cuts_tiles && !have_ws) return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
-    const bool tma_store = (s.k % 4) == 0;  // y rows must be 16-byte multiples for the TMA store
+    const bool vec_store = (s.k % 4) == 0;  // 16-byte vector writes of y rows
 
-    CUtensorMap tm_a, tm_b, tm_y;
-    rc = encode_maps(s, plan, x, w, y, tma_store, &tm_a, &tm_b, &tm_y);
+    CUtensorMap tm_a, tm_b;
+    rc = encode_maps(s, plan, x, w, &tm_a, &tm_b);
     if (rc != CONV2D_OK) return rc;
 
     sgb::ConvKernelParams kp{};
@@ -366,7 +354,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.n_tiles = plan.n_tiles;
     kp.grid = plan.grid;
     kp.units = plan.units;
-    kp.use_tma_store = tma_store ? 1 : 0;
+    kp.vec_store = vec_store ? 1 : 0;
     kp.debug_flags = algo ? algo->debug_flags : 0;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
     kp.trace = nullptr;
@@ -376,10 +364,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
 
     const int64_t grid = plan.grid;
     if (log_enabled())
-        std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BM=%d BN=%d splits=%d loader=%d grid=%lld tma_store=%d\n",
+        std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BM=%d BN=%d splits=%d loader=%d grid=%lld vec_store=%d\n",
                      (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_m, plan.block_n, plan.splits, plan.loader,
-                     (long long)grid, (int)tma_store);
-    cudaError_t err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, tm_y, kp, (int)grid, stream);
+                     (long long)grid, (int)vec_store);
+    cudaError_t err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, kp, (int)grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;
     g_last_launches = 1;
     return CONV2D_OK;

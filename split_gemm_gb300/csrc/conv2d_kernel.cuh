@@ -36,8 +36,8 @@
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer (128 x BN x 16
 //               per instruction) into two fp32 TMEM accumulators used in turn;
 //   warps 2..5  epilogue: TMEM -> registers (+ bias) -> swizzled shared staging ->
-//               per-warp TMA store (or TMA reduce-add for later splits), while
-//               the MMA warp already fills the other accumulator;
+//               coalesced 16-byte global stores (vector atomic adds for later
+//               splits), while the MMA warp already fills the other accumulator;
 //   warps 6..9  (cp.async and scalar loaders only) im2col gather into the ring.
 // The ring replaces block-wide syncs between load and MMA (burn PR #2545's
 // sync-placement discussion; ROCm/rocMLIR PR #1511 "Double buffering
@@ -66,7 +66,7 @@ constexpr int EPI_THREADS = 128;
 constexpr int GATHER_WARP0 = 6;  // gather warps 6..9 (gather loaders only)
 constexpr int GATHER_THREADS = 128;
 constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
-constexpr int EPI_SLOTS = 2;                 // staging slots per epilogue warp
+constexpr int EPI_SLOTS = 1;                 // staging slots per epilogue warp
 constexpr int EPI_BYTES = 4 * EPI_SLOTS * EPI_SLOT_BYTES;
 constexpr uint32_t STATUS_TIMEOUT = 6;  // same value as CONV2D_ERR_TIMEOUT
 
@@ -99,7 +99,7 @@ struct ConvKernelParams {
     int m_tiles, n_tiles;
     int grid;                 // G: CTAs sharing the unit range
     long long units;          // U = m_tiles * n_tiles * num_kb
-    int use_tma_store;
+    int vec_store;            // K % 4 == 0: 16-byte vector writes of y
     int debug_flags;
     unsigned long long wait_limit_ns;
     unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
@@ -585,7 +585,7 @@ __device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, const Segm
 }
 
 template <int BM, int BN, int LOADER>
-__device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp, const SmemView& sm,
+__device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                              uint32_t tmem_base)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
@@ -596,7 +596,6 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
     const int row = quad * 32 + lane;          // row of each 128-row block owned by this thread
     uint8_t* slots = sm.epi + ew * (EPI_SLOTS * EPI_SLOT_BYTES);
     int seg_idx = 0;
-    int slabs = 0;  // slabs this warp has handed to the TMA unit (staging-slot rotation)
     uint64_t c_acc = 0, c_ld = 0, c_slot = 0, c_st = 0, c_turn = 0, c_done = 0;
     (void)c_acc; (void)c_ld; (void)c_slot; (void)c_st; (void)c_turn; (void)c_done;
     SegmentWalker walk(kp);
@@ -633,6 +632,7 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
         if (!*sm.epi_go) break;
         ptx::tc_fence_after();
         SGB_TRACE(kp, et == 0 && seg_idx == 0, 7);
+        SGB_TRACE(kp, et == 0 && seg_idx < 4, 20 + 3 * seg_idx);  // segment: turn granted, accumulator ready
 
 #pragma unroll 1
         for (int sub = 0; sub < Cfg::M_SUB; ++sub) {
@@ -640,9 +640,15 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
                                    (static_cast<uint32_t>(quad * 32) << 16);
             const int mrow0 = m0 + sub * MMA_M;  // first output row of this 128-row block
             const bool last_sub = sub == Cfg::M_SUB - 1;
-            if (kp.use_tma_store) {
+            if (kp.vec_store) {
                 // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
-                // TMA store (split 0) or TMA reduce-add (later splits, in turn).
+                // coalesced 16-byte global writes (8 lanes per 128-byte row): plain stores for
+                // split 0, vector atomic adds for later splits (in turn).  The writes use the
+                // load/store path, leaving the TMA unit to the im2col and weight loads.
+                uint8_t* slot = slots;  // one slot per warp: its reads finish before the next slab is written
+                const uint32_t saddr = ptx::smem_addr(slot);
+                const int rsub = lane >> 3;     // row within a group of four written per instruction
+                const int chunk = lane & 7;     // 16-byte chunk of the 128-byte row
 #pragma unroll
                 for (int j = 0; j < BN / 32; ++j) {
                     uint32_t v[32];
@@ -659,28 +665,28 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
                         for (int e = 0; e < 32; ++e)
                             v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
                     }
-                    uint8_t* slot = slots + (slabs % EPI_SLOTS) * EPI_SLOT_BYTES;
-                    SGB_CYCLES_BEGIN(t_slot);
-                    if (slabs >= EPI_SLOTS) {  // the slot's previous slab must have been read by the TMA unit
-                        if (lane == 0) ptx::bulk_wait_read<EPI_SLOTS - 1>();
-                        __syncwarp();
-                    }
-                    SGB_CYCLES_END(c_slot, t_slot);
                     SGB_CYCLES_BEGIN(t_st);
-                    const uint32_t saddr = ptx::smem_addr(slot);
+                    __syncwarp();  // the previous slab's reads of the slot are done
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
                                           v[4 * c + 3]);
-                    ptx::fence_proxy_async_smem();
                     __syncwarp();
                     SGB_CYCLES_END(c_st, t_st);
-                    if (lane == 0) {
-                        if (sg.split == 0) ptx::tma_store_2d(tm_y, slot, n0 + j * 32, mrow0 + quad * 32);
-                        else ptx::tma_reduce_add_2d(tm_y, slot, n0 + j * 32, mrow0 + quad * 32);
-                        ptx::bulk_commit();
+                    SGB_CYCLES_BEGIN(t_slot);
+                    const int col = n0 + j * 32 + chunk * 4;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 4 * i + rsub;  // row within the warp's 32 rows
+                        const int m = mrow0 + quad * 32 + r;
+                        const uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(r, chunk));
+                        if (m < kp.M && col < kp.K) {
+                            float* dst = kp.y + static_cast<int64_t>(m) * kp.K + col;
+                            if (sg.split == 0) *reinterpret_cast<uint4*>(dst) = val;
+                            else ptx::red_add_v4_f32(dst, val);
+                        }
                     }
-                    ++slabs;
+                    SGB_CYCLES_END(c_slot, t_slot);
                 }
             } else {
                 // K % 4 != 0: row-per-thread stores (split 0) or read-add-write (later splits).
@@ -724,15 +730,15 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
         if (sg.nsplits > 1) {
             SGB_CYCLES_BEGIN(t_done);
             // Every write of this split must be complete and visible before the next split's turn.
-            if (kp.use_tma_store && lane == 0) {
-                ptx::bulk_wait_all();
-                ptx::fence_proxy_async_global();
-            }
             __threadfence();
             ptx::named_bar_sync(1, EPI_THREADS);
             if (et == 0) pass_turn(kp, sg);
             SGB_CYCLES_END(c_done, t_done);
         }
+        SGB_TRACE(kp, et == 0 && seg_idx < 4, 21 + 3 * seg_idx);  // segment: epilogue done
+        SGB_TRACE_VALUE(kp, et == 0 && seg_idx < 4, 22 + 3 * seg_idx,
+                        (static_cast<unsigned long long>(sg.kb_end - sg.kb_begin) << 16) |
+                            (static_cast<unsigned long long>(sg.split) << 8) | sg.nsplits);
         ++seg_idx;
     }
     SGB_TRACE(kp, et == 0, 8);
@@ -741,14 +747,13 @@ __device__ void run_epilogue(const CUtensorMap* tm_y, const ConvKernelParams& kp
     SGB_TRACE_VALUE(kp, et == 0, 13, c_slot);
     SGB_TRACE_VALUE(kp, et == 0, 14, c_st);
     SGB_TRACE_VALUE(kp, et == 0, 15, c_turn + (c_done << 32));
-    if (lane == 0) ptx::bulk_wait_read_all();  // staging slots must be read before the CTA exits
 }
 
 // ---------------------------------------------------------------- the kernel
 template <int BM, int BN, int LOADER>
 __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     conv2d_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const __grid_constant__ CUtensorMap tm_y, const ConvKernelParams kp)
+                         const ConvKernelParams kp)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
     extern __shared__ uint8_t smem_raw[];
@@ -792,7 +797,6 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID) ptx::prefetch_tensormap(&tm_a);
         if (LOADER != LOADER_SCALAR) ptx::prefetch_tensormap(&tm_b);
-        if (kp.use_tma_store) ptx::prefetch_tensormap(&tm_y);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sm.tmem_slot, Cfg::TMEM_COLS);
@@ -815,7 +819,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
     } else if (warp < GATHER_WARP0) {
-        run_epilogue<BM, BN, LOADER>(&tm_y, kp, sm, tmem_base);
+        run_epilogue<BM, BN, LOADER>(kp, sm, tmem_base);
     } else {
         if constexpr (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BM, BN, LOADER>(kp, sm);
         if constexpr (LOADER == LOADER_SCALAR) run_gather_scalar<BM, BN, LOADER>(kp, sm);
@@ -845,8 +849,8 @@ inline bool pdl_enabled()
 // Host-side launcher for one instantiation; explicitly instantiated in one
 // translation unit per tile width so that the variants compile in parallel.
 template <int BM, int BN, int LOADER>
-cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_y,
-                             const ConvKernelParams& kp, int grid, cudaStream_t stream)
+cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const ConvKernelParams& kp, int grid,
+                             cudaStream_t stream)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
     auto kern = conv2d_fwd_tc_kernel<BM, BN, LOADER>;
@@ -874,12 +878,12 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, tm_y, kp);
+    return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, kp);
 }
 
 #define SGB_LAUNCH_SIG(BM_, BN_, L_)                                                                        \
-    cudaError_t launch_conv2d_tc<BM_, BN_, L_>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, \
-                                               const ConvKernelParams&, int, cudaStream_t)
+    cudaError_t launch_conv2d_tc<BM_, BN_, L_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, \
+                                               int, cudaStream_t)
 
 // Every loader with 128-pixel tiles, and the TMA loader with 256-pixel tiles.
 #define SGB_INSTANTIATE_CONV2D(BN_)                    \
