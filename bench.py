@@ -498,7 +498,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time for cpu_baseline")
     ap.add_argument("--block-n", type=int, default=0, help="force the output-channel tile width (64/128/256)")
     ap.add_argument("--splits", type=int, default=0, help="force the split-K factor")
-    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar)")
+    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
     args = ap.parse_args(argv)

@@ -77,7 +77,10 @@ typedef enum {
     CONV2D_LOADER_TMA_IM2COL = 1, /* TMA im2col-mode descriptor; needs C % 64 == 0 */
     CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C % 8 == 0 */
     CONV2D_LOADER_SCALAR = 3,     /* element gather; any C (also gathers the weight) */
-    CONV2D_LOADER_HYBRID = 4      /* TMA im2col and cp.async gather on alternate k-blocks; needs C % 64 == 0 */
+    CONV2D_LOADER_HYBRID = 4,     /* TMA im2col and cp.async gather on alternate k-blocks; needs C % 64 == 0 */
+    CONV2D_LOADER_ROW_WINDOW = 5  /* few channels: staged input rows read in place by the MMA as overlapping
+                                     16-byte-pitch windows; needs dil_w == 1, stride_w in {1,2,4,8},
+                                     C <= 8 / stride_w, K <= 256 (one tile of output channels), no split */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".

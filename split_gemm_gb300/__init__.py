@@ -21,12 +21,13 @@ from . import _build
 
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
+    "LOADER_HYBRID", "LOADER_ROW_WINDOW",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
     "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
 ]
 
-LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR = 0, 1, 2, 3
+LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR, LOADER_HYBRID, LOADER_ROW_WINDOW = 0, 1, 2, 3, 4, 5
 DEBUG_SKIP_SIGNAL = 1
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
                 4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT",

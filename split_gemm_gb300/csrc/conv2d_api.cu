@@ -13,11 +13,15 @@
 
 #include "conv2d.h"
 #include "conv2d_kernel.cuh"
+#include "conv2d_rowwin.cuh"
 
 namespace sgb {
 SGB_DECLARE_CONV2D(64)
 SGB_DECLARE_CONV2D(128)
 SGB_DECLARE_CONV2D(256)
+extern template SGB_ROWWIN_SIG(64);
+extern template SGB_ROWWIN_SIG(128);
+extern template SGB_ROWWIN_SIG(256);
 }  // namespace sgb
 
 namespace {
@@ -134,6 +138,100 @@ bool tma_im2col_eligible(const Shape& s)
     return true;
 }
 
+// ------------------------------------------------------------------ row-window loader (few channels)
+constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may opt in to
+
+struct RowWinCfg {
+    int bn, cp_log2, nch, seg_elems, raw_bytes, T, rt, new_rows, reuse, ncls, nblocks, row_slots, wtmp_filters;
+    int cls_k[sgb::RW_MAX_CLASSES], cls_base[sgb::RW_MAX_CLASSES];
+    int qblocks, pblocks, tiles;
+    uint32_t tmem_cols;
+    sgb::RowWinLayout lay;
+};
+
+// The row-window kernel's sizes for this shape, or false when it does not
+// apply: the padded pixel (Cp = 8 / stride_w channels) must hold C, the window
+// must be contiguous along W (dil_w == 1), all K channels must fit one channel
+// tile, and the resident weight plus one tile's window rows must fit in shared
+// memory.  T output rows share each MMA (T*BN <= 256); T drops to 1 for
+// dil_h > 1 or stride_h > 8, and further down while shared memory is short.
+bool rowwin_config(const Shape& s, int bn_force, RowWinCfg* o)
+{
+    if (s.dw != 1 || s.r > 64 || s.s > 64 || s.dh > 64) return false;
+    int cp_log2;
+    switch (s.sw) {
+        case 1: cp_log2 = 3; break;
+        case 2: cp_log2 = 2; break;
+        case 4: cp_log2 = 1; break;
+        case 8: cp_log2 = 0; break;
+        default: return false;
+    }
+    const int64_t cp = int64_t(1) << cp_log2;
+    if (s.c > cp || s.k > 256) return false;
+    const int bn = bn_force ? bn_force : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+    if (bn != 64 && bn != 128 && bn != 256) return false;
+    if (bn < s.k) return false;
+    o->bn = bn;
+    o->cp_log2 = cp_log2;
+    o->nch = static_cast<int>(cdiv(s.s * cp, 16));
+    o->seg_elems = 8 * (sgb::RW_TILE_M - 1) + 16 * o->nch;
+    const int64_t segpix = o->seg_elems / cp;
+    o->raw_bytes = static_cast<int>((segpix * s.c * 2 + 32 + 15) / 16 * 16);
+    o->qblocks = static_cast<int>(cdiv(s.q, sgb::RW_TILE_M));
+    const int64_t crs_bytes = s.crs * 2;
+    int t_max = 256 / bn;
+    if (s.dh != 1 || s.sh > sgb::RW_MAX_CLASSES) t_max = 1;
+    if (t_max > s.p) t_max = static_cast<int>(s.p);
+    for (int T = t_max; T >= 1; --T) {
+        const int64_t rt = (T - 1) * s.sh + (s.r - 1) * s.dh + 1;
+        if (rt > 4096) continue;
+        // Residue classes of filter rows and their zero-padded block sequences.
+        int ncls = T > 1 ? static_cast<int>(s.sh) : 1;
+        int nblocks = 0;
+        for (int rho = 0; rho < sgb::RW_MAX_CLASSES; ++rho) {
+            int k = 0;
+            if (rho < ncls) k = T > 1 ? (rho < s.r ? static_cast<int>(cdiv(s.r - rho, s.sh)) : 0) : static_cast<int>(s.r);
+            o->cls_k[rho] = k;
+            o->cls_base[rho] = nblocks;
+            if (k > 0) nblocks += k + 2 * (T - 1);
+        }
+        const bool reuse = rt > T * s.sh;
+        const int new_rows = reuse ? static_cast<int>(T * s.sh) : static_cast<int>(rt);
+        // Ring: one tile's window plus two tiles of look-ahead, fewer when shared memory is short.
+        // The weight is copied in through an area of its own in one pass when
+        // shared memory allows, else through the epilogue staging area in passes.
+        const int64_t w_all = (s.k * crs_bytes + 32 + 127) / 128 * 128;
+        for (int64_t slots = rt + 2 * new_rows; slots >= rt; --slots) {
+            sgb::RowWinLayout lay = sgb::rowwin_layout(bn, o->nch, nblocks, o->seg_elems, static_cast<int>(slots),
+                                                       static_cast<int>(rt), o->raw_bytes, static_cast<int>(w_all));
+            int64_t wtmp = s.k;
+            if (w_all > kSmemLimit || lay.total > kSmemLimit) {
+                lay = sgb::rowwin_layout(bn, o->nch, nblocks, o->seg_elems, static_cast<int>(slots),
+                                         static_cast<int>(rt), o->raw_bytes, 0);
+                wtmp = (4 * sgb::RW_EPI_SLOT_BYTES - 32) / crs_bytes;
+            }
+            if (lay.total > kSmemLimit) continue;
+            if (wtmp < 1) break;
+            o->T = T;
+            o->rt = static_cast<int>(rt);
+            o->new_rows = new_rows;
+            o->reuse = reuse ? 1 : 0;
+            o->ncls = ncls;
+            o->nblocks = nblocks;
+            o->row_slots = static_cast<int>(slots);
+            o->wtmp_filters = static_cast<int>(wtmp < 256 ? wtmp : 256);
+            o->pblocks = static_cast<int>(cdiv(s.p, T));
+            o->tiles = static_cast<int>(s.n * o->qblocks * o->pblocks);
+            uint32_t cols = 32;
+            while (cols < static_cast<uint32_t>(2 * T * bn)) cols <<= 1;
+            o->tmem_cols = cols;
+            o->lay = lay;
+            return true;
+        }
+    }
+    return false;
+}
+
 // ------------------------------------------------------------------ heuristic
 struct Plan {
     int block_m;
@@ -153,10 +251,14 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     const int sms = sm_count_current();
     // Loader.
     int loader = force ? force->loader : 0;
+    RowWinCfg rw;
     if (loader == CONV2D_LOADER_AUTO) {
         if (tma_im2col_eligible(s)) loader = CONV2D_LOADER_TMA_IM2COL;
         else if (s.c % 8 == 0) loader = CONV2D_LOADER_CPASYNC;
+        else if (rowwin_config(s, force ? force->block_n : 0, &rw)) loader = CONV2D_LOADER_ROW_WINDOW;
         else loader = CONV2D_LOADER_SCALAR;
+    } else if (loader == CONV2D_LOADER_ROW_WINDOW) {
+        if (!rowwin_config(s, force->block_n, &rw)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_TMA_IM2COL) {
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_CPASYNC) {
@@ -165,6 +267,23 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
+    }
+    if (loader == CONV2D_LOADER_ROW_WINDOW) {
+        // One tile = up to 128 pixels of one output row, all channels; never split.
+        if (force && (force->splits > 1 || (force->block_m != 0 && force->block_m != 128) || force->grid < 0))
+            return CONV2D_ERR_UNSUPPORTED;
+        int64_t grid = force && force->grid > 0 ? force->grid : (rw.tiles < sms ? rw.tiles : (sms > 0 ? sms : 1));
+        if (grid > rw.tiles) return CONV2D_ERR_UNSUPPORTED;
+        plan->block_m = sgb::RW_TILE_M;
+        plan->block_n = rw.bn;
+        plan->splits = 0;
+        plan->loader = loader;
+        plan->m_tiles = rw.tiles;
+        plan->n_tiles = 1;
+        plan->num_kb = 1;
+        plan->grid = static_cast<int>(grid);
+        plan->units = rw.tiles;
+        return CONV2D_OK;
     }
     int bm = force ? force->block_m : 0;
     if (bm == 0) {
@@ -332,6 +451,69 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     if (cuts_tiles && !have_ws) return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
     const bool vec_store = (s.k % 4) == 0;  // 16-byte vector writes of y rows
+    if (plan.loader == CONV2D_LOADER_ROW_WINDOW) {
+        RowWinCfg rw;
+        if (!rowwin_config(s, plan.block_n, &rw)) return CONV2D_ERR_UNSUPPORTED;
+        sgb::RowWinParams rp{};
+        rp.x = static_cast<const uint16_t*>(x);
+        rp.w = static_cast<const uint16_t*>(w);
+        rp.bias = bias;
+        rp.y = y;
+        rp.status = have_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+        rp.N = (int)s.n; rp.H = (int)s.h; rp.W = (int)s.w; rp.C = (int)s.c;
+        rp.K = (int)s.k; rp.R = (int)s.r; rp.S = (int)s.s; rp.P = (int)s.p; rp.Q = (int)s.q;
+        rp.sh = (int)s.sh; rp.sw = (int)s.sw; rp.ph = (int)s.ph; rp.pw = (int)s.pw; rp.dh = (int)s.dh;
+        rp.cp_log2 = rw.cp_log2;
+        rp.nch = rw.nch;
+        rp.seg_elems = rw.seg_elems;
+        rp.raw_bytes = rw.raw_bytes;
+        rp.T = rw.T;
+        rp.rt = rw.rt;
+        rp.new_rows = rw.new_rows;
+        rp.reuse = rw.reuse;
+        rp.ncls = rw.ncls;
+        for (int i = 0; i < sgb::RW_MAX_CLASSES; ++i) {
+            rp.cls_k[i] = rw.cls_k[i];
+            rp.cls_base[i] = rw.cls_base[i];
+        }
+        rp.nblocks = rw.nblocks;
+        rp.row_slots = rw.row_slots;
+        rp.wtmp_filters = rw.wtmp_filters;
+        rp.qblocks = rw.qblocks;
+        rp.pblocks = rw.pblocks;
+        rp.tiles = rw.tiles;
+        rp.grid = plan.grid;
+        rp.tmem_cols = rw.tmem_cols;
+        rp.vec_store = vec_store ? 1 : 0;
+        rp.x_bytes = s.n * s.h * s.w * s.c * 2;
+        rp.w_bytes = s.k * s.crs * 2;
+        rp.off_rows = rw.lay.off_rows;
+        rp.off_raw = rw.lay.off_raw;
+        rp.off_wtmp = rw.lay.off_wtmp;
+        rp.off_epi = rw.lay.off_epi;
+        rp.off_bar = rw.lay.off_bar;
+        rp.off_tab = rw.lay.off_tab;
+        rp.wait_limit_ns =
+            (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+        rp.trace = nullptr;
+#ifdef SGB_TRACE_ENABLED
+        rp.trace = g_trace;
+#endif
+        if (log_enabled())
+            std::fprintf(stderr,
+                         "[conv2d] M=%lld K=%lld CRS=%lld -> row window BN=%d T=%d rt=%d tiles=%d grid=%d slots=%d "
+                         "nch=%d blocks=%d reuse=%d smem=%d\n",
+                         (long long)s.m, (long long)s.k, (long long)s.crs, rw.bn, rw.T, rw.rt, rw.tiles, plan.grid,
+                         rw.row_slots, rw.nch, rw.nblocks, rw.reuse, rw.lay.total);
+        cudaError_t err;
+        const bool pdl = sgb::pdl_enabled();
+        if (rw.bn == 64) err = sgb::launch_conv2d_rowwin<64>(rp, rw.lay.total, pdl, stream);
+        else if (rw.bn == 128) err = sgb::launch_conv2d_rowwin<128>(rp, rw.lay.total, pdl, stream);
+        else err = sgb::launch_conv2d_rowwin<256>(rp, rw.lay.total, pdl, stream);
+        if (err != cudaSuccess) return CONV2D_ERR_CUDA;
+        g_last_launches = 1;
+        return CONV2D_OK;
+    }
 
     CUtensorMap tm_a, tm_b;
     rc = encode_maps(s, plan, x, w, &tm_a, &tm_b);

@@ -55,6 +55,7 @@
 #include <cstdlib>
 
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace sgb {
 
@@ -105,37 +106,6 @@ struct ConvKernelParams {
     unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
 };
 
-// Phase timestamps for profiling builds (compiled with SGB_TRACE_ENABLED):
-// slot `slot` of CTA blockIdx.x gets the global timer when `cond` holds.
-#ifdef SGB_TRACE_ENABLED
-#define SGB_TRACE(kp, cond, slot)                                                               \
-    do {                                                                                        \
-        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 32 + (slot)] =   \
-            ::sgb::ptx::globaltimer();                                                          \
-    } while (0)
-// Cycle accounting for profiling builds: SGB_CYCLES_BEGIN(t) starts a stopwatch,
-// SGB_CYCLES_END(acc, t) adds the elapsed SM cycles to a local accumulator that
-// SGB_TRACE_VALUE stores in the trace slot at the end.
-#define SGB_CYCLES_BEGIN(t) const uint64_t t = ::sgb::ptx::clock64()
-#define SGB_CYCLES_END(acc, t) (acc) += ::sgb::ptx::clock64() - (t)
-#define SGB_TRACE_VALUE(kp, cond, slot, value)                                                   \
-    do {                                                                                        \
-        if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 32 + (slot)] = (value); \
-    } while (0)
-#else
-#define SGB_TRACE(kp, cond, slot) \
-    do {                          \
-    } while (0)
-#define SGB_CYCLES_BEGIN(t) \
-    do {                    \
-    } while (0)
-#define SGB_CYCLES_END(acc, t) \
-    do {                       \
-    } while (0)
-#define SGB_TRACE_VALUE(kp, cond, slot, value) \
-    do {                                       \
-    } while (0)
-#endif
 
 // Tile BM x BN (BM = 128 or 256 output pixels, BN = 64/128/256 channels).  A
 // 256-pixel tile is loaded with one im2col operation per k-block and computed

@@ -181,6 +181,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Vector fp32 atomic add to global memory (no return value).
 __device__ __forceinline__ void red_add_v4_f32(float* dst, uint4 v)
 {
@@ -282,6 +289,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the unswizzled
+// ("interleaved") layout: core matrices of 8 rows x 16 bytes, the 8 rows 16 B
+// apart; `lbo` is the byte distance between core matrices adjacent along K and
+// `sbo` between core matrices adjacent along M/N (both multiples of 16), swizzle
+// mode 0.  Element (row, k) of a bf16 operand sits at
+//   start + (row % 8)*16 + (row / 8)*sbo + (k % 8)*2 + (k / 8)*lbo.
+__device__ __forceinline__ uint64_t plain_kmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
     return d;
 }
 
