@@ -280,6 +280,8 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     constexpr int STAGES = Cfg::STAGES;
     constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(MMA_M, BN);
+    const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
+    const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
     int it = 0, seg_idx = 0;
     bool ok = true;
     uint64_t full_cycles = 0, acc_cycles = 0;
@@ -314,17 +316,28 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
             // Gathered tiles were written through the generic proxy (cp.async);
             // order them before the tensor cores read the stage.
             if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) ptx::fence_proxy_async_smem();
-            const uint32_t a_addr = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
-            const uint32_t b_addr = ptx::smem_addr(sm.b + stage * Cfg::B_STAGE_BYTES);
+            // The MMA issue stalls until the tensor pipe takes the instruction, so
+            // all descriptors of the stage are formed before the first MMA and the
+            // MMAs then go out back to back.  Descriptor start addresses are
+            // address >> 4 in the low bits (no carry: shared addresses < 256 KB), so
+            // an offset is added to the descriptor itself; advancing along K inside
+            // a 128-B swizzled row moves the start address by 32 B.
+            const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
+            uint64_t adk[BK / UMMA_K][Cfg::M_SUB], bdk[BK / UMMA_K];
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
-                // Advancing along K inside a 128-B swizzled row moves the start address by 32 B.
-                const uint64_t bd = ptx::sw128_kmajor_desc(b_addr + k * UMMA_K * 2);
+                bdk[k] = bd + static_cast<uint64_t>((k * UMMA_K * 2) >> 4);
 #pragma unroll
-                for (int sub = 0; sub < Cfg::M_SUB; ++sub) {  // 128-row blocks share the B tile
-                    const uint64_t ad = ptx::sw128_kmajor_desc(a_addr + sub * MMA_M * 128 + k * UMMA_K * 2);
-                    ptx::mma_bf16(tmem_d + sub * BN, ad, bd, IDESC, (kb > sg.kb_begin || k > 0) ? 1u : 0u);
-                }
+                for (int sub = 0; sub < Cfg::M_SUB; ++sub)
+                    adk[k][sub] = ad + static_cast<uint64_t>((sub * MMA_M * 128 + k * UMMA_K * 2) >> 4);
+            }
+            const uint32_t acc0 = kb > sg.kb_begin ? 1u : 0u;
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+#pragma unroll
+                for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
+                    ptx::mma_bf16(tmem_d + sub * BN, adk[k][sub], bdk[k], IDESC, k > 0 ? 1u : acc0);
             }
             ptx::mma_commit(&sm.empty[stage]);
         }
