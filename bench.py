@@ -290,14 +290,15 @@ def run_ours(args, wl, world, rank, local):
     params = sg.make_params(x.shape, w.shape, **wl.options())
     p, q = sg.output_shape(params)
     forced = None
-    if args.block_n or args.splits or args.loader or args.grid or args.block_m:
+    if args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction:
         forced = sg.Algo()
         forced.block_n, forced.splits, forced.loader, forced.grid = args.block_n, args.splits, args.loader, args.grid
-        forced.block_m = args.block_m
+        forced.block_m, forced.reduction = args.block_m, args.reduction
     algo = sg.query_algo(params)
     if forced is not None:
         algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, forced.loader or algo.loader,
-                       forced.grid or (0 if forced.splits else algo.grid), 0, forced.block_m or algo.block_m)
+                       forced.grid or (0 if forced.splits else algo.grid), 0, forced.block_m or algo.block_m, 0,
+                       forced.reduction or algo.reduction)
     set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * 4 + (0 if b is None else b.numel() * 4)
     n_sets = _sets_for(wl, set_bytes)
     sets = []
@@ -498,7 +499,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time for cpu_baseline")
     ap.add_argument("--block-n", type=int, default=0, help="force the output-channel tile width (64/128/256)")
     ap.add_argument("--splits", type=int, default=0, help="force the split-K factor")
-    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window)")
+    ap.add_argument("--reduction", type=int, default=0,
+                    help="force the in-place reduction of cut tiles (1 ordered, 2 concurrent)")
+    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
     args = ap.parse_args(argv)

@@ -78,9 +78,13 @@ typedef enum {
     CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C % 8 == 0 */
     CONV2D_LOADER_SCALAR = 3,     /* element gather; any C (also gathers the weight) */
     CONV2D_LOADER_HYBRID = 4,     /* TMA im2col and cp.async gather on alternate k-blocks; needs C % 64 == 0 */
-    CONV2D_LOADER_ROW_WINDOW = 5  /* few channels: staged input rows read in place by the MMA as overlapping
+    CONV2D_LOADER_ROW_WINDOW = 5, /* few channels: staged input rows read in place by the MMA as overlapping
                                      16-byte-pitch windows; needs dil_w == 1, stride_w in {1,2,4,8},
                                      C <= 8 / stride_w, K <= 256 (one tile of output channels), no split */
+    CONV2D_LOADER_TMA_BOX = 6     /* tiles are rectangles of output pixels; each tiled TMA box carries two
+                                     64-channel chunks of one filter tap (and a 3-D box two weight k-blocks);
+                                     needs C % 128 == 0, strides <= 8, a rectangle whose pixel count is a
+                                     multiple of 8, and block_n <= 128 with 256-pixel tiles */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".
@@ -94,9 +98,20 @@ typedef struct {
     int32_t loader;    /* conv2d_loader */
     int32_t grid;      /* CTAs for stream-K (1 .. tiles * k-blocks); 0 = heuristic */
     int32_t debug_flags;      /* test hook, 0 in normal use; see CONV2D_DEBUG_* */
-    int32_t block_m;          /* output pixels per CTA tile: 128, or 256 (TMA im2col loader only) */
+    int32_t block_m;          /* output pixels per CTA tile: 128, or 256 (TMA im2col and TMA box loaders) */
     int64_t wait_limit_ns;    /* bound on every device-side wait; 0 = default (1 s) */
+    int32_t reduction;        /* conv2d_reduction: how the splits of a cut tile meet in y */
 } conv2d_algo;
+
+/* In-place reduction of a tile cut between CTAs.  Either way split 0 stores
+ * first (with the bias) and the only memory besides y is one semaphore per tile. */
+typedef enum {
+    CONV2D_REDUCTION_AUTO = 0,       /* the heuristic's choice (concurrent) */
+    CONV2D_REDUCTION_ORDERED = 1,    /* later splits add in k-order, one at a time: bitwise reproducible */
+    CONV2D_REDUCTION_CONCURRENT = 2  /* later splits add as they finish (fp32 atomic adds in L2): results
+                                        may differ between runs in the last bits, within the fp32
+                                        summation bound */
+} conv2d_reduction;
 
 /* Test hook: split 0 of every tile skips its semaphore signal, so later splits'
  * bounded waits run out and the call reports CONV2D_ERR_TIMEOUT. */

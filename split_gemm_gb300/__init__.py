@@ -21,13 +21,16 @@ from . import _build
 
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
-    "LOADER_HYBRID", "LOADER_ROW_WINDOW",
+    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "REDUCTION_AUTO", "REDUCTION_ORDERED",
+    "REDUCTION_CONCURRENT",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
     "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
 ]
 
 LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR, LOADER_HYBRID, LOADER_ROW_WINDOW = 0, 1, 2, 3, 4, 5
+LOADER_TMA_BOX = 6
+REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
 DEBUG_SKIP_SIGNAL = 1
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
                 4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT",
@@ -57,11 +60,11 @@ class Params(ctypes.Structure):
 class Algo(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("splits", ctypes.c_int32), ("loader", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("block_m", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64)]
+                ("wait_limit_ns", ctypes.c_int64), ("reduction", ctypes.c_int32)]
 
     def as_dict(self):
         return dict(block_m=self.block_m, block_n=self.block_n, splits=self.splits, loader=self.loader,
-                    grid=self.grid)
+                    grid=self.grid, reduction=self.reduction)
 
 
 _lock = threading.Lock()

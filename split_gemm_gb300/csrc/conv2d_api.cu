@@ -19,6 +19,8 @@ namespace sgb {
 SGB_DECLARE_CONV2D(64)
 SGB_DECLARE_CONV2D(128)
 SGB_DECLARE_CONV2D(256)
+SGB_DECLARE_CONV2D_BOX256(64)
+SGB_DECLARE_CONV2D_BOX256(128)
 extern template SGB_ROWWIN_SIG(64);
 extern template SGB_ROWWIN_SIG(128);
 extern template SGB_ROWWIN_SIG(256);
@@ -138,6 +140,63 @@ bool tma_im2col_eligible(const Shape& s)
     return true;
 }
 
+// ------------------------------------------------------------------ box loader (tile = rectangle of pixels)
+constexpr int kBoxChunks = 2;  // 64-channel chunks (k-blocks) per box, as in the kernel's TileConfig::KC
+
+struct BoxGeom {
+    int bw, bh, bn_img, px;      // rectangle: bn_img images x bh rows x bw columns, px pixels
+    int q_blocks, p_blocks, n_blocks;
+    int64_t m_tiles;
+};
+
+// Rectangle of at most bm output pixels for the box loader, or false when the
+// shape does not allow one: the chunks of a box must stay 1024-byte aligned in
+// shared memory (px % 8 == 0), a box spans at most 256 elements per dimension
+// (bw * stride_w, bh * stride_h), the traversal strides are at most 8, and two
+// 64-channel chunks must divide C.
+bool box_geometry(const Shape& s, int bm, BoxGeom* g)
+{
+    if (s.c % (kBoxChunks * BK) != 0 || s.sw > 8 || s.sh > 8) return false;
+    const int64_t wmax = 256 / s.sw, hmax = 256 / s.sh;
+    int64_t bw, bh = 1, bn = 1;
+    if (s.q >= bm || s.q > wmax) {
+        // Part of one output row per tile, split evenly, rounded up to 8 pixels.
+        const int64_t cap = bm < wmax ? bm : wmax;
+        const int64_t qb = cdiv(s.q, cap);
+        bw = (cdiv(s.q, qb) + 7) / 8 * 8;
+        if (bw > cap) bw = cap / 8 * 8;
+    } else if (s.p * s.q > bm) {
+        // Whole rows: as many as fit, balanced over the row blocks, with a pixel count that is a multiple of 8.
+        bw = s.q;
+        int64_t rows = bm / s.q;
+        if (rows > hmax) rows = hmax;
+        const int64_t pb = cdiv(s.p, rows);
+        bh = cdiv(s.p, pb);
+        while (bh > 1 && (bw * bh) % 8 != 0) --bh;
+        if ((bw * bh) % 8 != 0) bh = rows;
+        while (bh > 1 && (bw * bh) % 8 != 0) --bh;
+    } else {
+        // Whole images.
+        bw = s.q;
+        bh = s.p;
+        bn = bm / (s.p * s.q);
+        if (bn > s.n) bn = s.n;
+        while (bn > 1 && (bw * bh * bn) % 8 != 0) --bn;
+    }
+    if (bw < 1 || bh < 1 || bn < 1) return false;
+    const int64_t px = bw * bh * bn;
+    if (px % 8 != 0 || px > bm || bw > wmax || bh > hmax) return false;
+    g->bw = static_cast<int>(bw);
+    g->bh = static_cast<int>(bh);
+    g->bn_img = static_cast<int>(bn);
+    g->px = static_cast<int>(px);
+    g->q_blocks = static_cast<int>(cdiv(s.q, bw));
+    g->p_blocks = static_cast<int>(cdiv(s.p, bh));
+    g->n_blocks = static_cast<int>(cdiv(s.n, bn));
+    g->m_tiles = static_cast<int64_t>(g->q_blocks) * g->p_blocks * g->n_blocks;
+    return true;
+}
+
 // ------------------------------------------------------------------ row-window loader (few channels)
 constexpr int kSmemLimit = 232448;  // dynamic shared memory one CTA may opt in to
 
@@ -238,10 +297,23 @@ struct Plan {
     int block_n;
     int splits;  // classic split-K factor, or 0 for stream-K
     int loader;
-    int m_tiles, n_tiles, num_kb;
+    int m_tiles, n_tiles, num_kb;  // num_kb: pipeline stages per tile (two k-blocks each for the box loader)
     int grid;         // CTAs launched
-    long long units;  // (tile, k-block) work units
+    long long units;  // (tile, stage) work units
+    BoxGeom box;      // box loader only
 };
+
+// Semaphores the workspace holds: one per tile of the smallest tiles any plan
+// uses (128-pixel rows of M, or the box loader's 128-pixel rectangles, by
+// 64 output channels).
+int64_t semaphore_capacity(const Shape& s)
+{
+    int64_t m_tiles = cdiv(s.m, kMinTileM);
+    BoxGeom g;
+    if (box_geometry(s, 128, &g) && g.m_tiles > m_tiles) m_tiles = g.m_tiles;
+    return m_tiles * cdiv(s.k, 64);
+}
+
 
 constexpr int kMinUnitsPerCta = 4;     // no split gets fewer k-blocks than this
 constexpr int kMaxSplitsPerTile = 6;   // longest serial in-place reduction chain the heuristic builds
@@ -265,6 +337,9 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         if (s.c % 8 != 0) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_HYBRID) {
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader == CONV2D_LOADER_TMA_BOX) {
+        BoxGeom g;
+        if (!box_geometry(s, 128, &g) && !box_geometry(s, 256, &g)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
@@ -291,15 +366,25 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         // is per operation); worth it when the output channels are few (<= 128,
         // so the MMA per k-block is short) and the tiles still cover the SMs.
         bm = 128;
-        const int64_t bn_guess = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+        const int64_t bn_guess = (force && force->block_n) ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+        const int64_t cover = (sms > 0 ? sms : 1) * 4;
+        BoxGeom g256;
         if (loader == CONV2D_LOADER_TMA_IM2COL && bn_guess <= 128 && (!force || force->splits == 0) &&
-            cdiv(s.m, 256) * cdiv(s.k, bn_guess) * 5 >= (sms > 0 ? sms : 1) * 4)
+            cdiv(s.m, 256) * cdiv(s.k, bn_guess) * 5 >= cover)
             bm = 256;
+        if (loader == CONV2D_LOADER_TMA_BOX && bn_guess <= 128 && (!force || force->splits == 0) &&
+            box_geometry(s, 256, &g256) && g256.px * 4 >= 256 * 3 && g256.m_tiles * cdiv(s.k, bn_guess) * 5 >= cover)
+            bm = 256;
+        BoxGeom g128;
+        if (loader == CONV2D_LOADER_TMA_BOX && bm == 128 && !box_geometry(s, 128, &g128)) bm = 256;
     }
     if (bm != 128 && bm != 256) return CONV2D_ERR_INVALID;
-    if (bm == 256 && loader != CONV2D_LOADER_TMA_IM2COL) return CONV2D_ERR_UNSUPPORTED;
-    const int64_t m_tiles = cdiv(s.m, bm);
-    const int64_t num_kb = cdiv(s.crs, BK);
+    if (bm == 256 && loader != CONV2D_LOADER_TMA_IM2COL && loader != CONV2D_LOADER_TMA_BOX)
+        return CONV2D_ERR_UNSUPPORTED;
+    BoxGeom geom{};
+    if (loader == CONV2D_LOADER_TMA_BOX && !box_geometry(s, bm, &geom)) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t m_tiles = loader == CONV2D_LOADER_TMA_BOX ? geom.m_tiles : cdiv(s.m, bm);
+    const int64_t num_kb = loader == CONV2D_LOADER_TMA_BOX ? s.crs / (kBoxChunks * BK) : cdiv(s.crs, BK);
     const int64_t forced_splits = force ? force->splits : 0;
     const int64_t forced_grid = force ? force->grid : 0;
     if (forced_splits < 0 || forced_grid < 0 || (forced_splits > 0 && forced_grid > 0)) return CONV2D_ERR_INVALID;
@@ -317,6 +402,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         }
     }
     if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    if (loader == CONV2D_LOADER_TMA_BOX && bm == 256 && bn > 128) return CONV2D_ERR_UNSUPPORTED;
     const int64_t n_tiles = cdiv(s.k, bn);
     const int64_t tiles = m_tiles * n_tiles;
     const int64_t units = tiles * num_kb;
@@ -346,6 +432,10 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         return CONV2D_ERR_UNSUPPORTED;  // every CTA needs at least one unit
     }
     if (grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
+    // A plan that cuts tiles needs one semaphore per tile.
+    if (((units % grid) != 0 || (units / grid) % num_kb != 0) && tiles > semaphore_capacity(s))
+        return CONV2D_ERR_UNSUPPORTED;
+    plan->box = geom;
     plan->block_m = bm;
     plan->block_n = bn;
     plan->splits = static_cast<int>(splits);
@@ -361,8 +451,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
 size_t workspace_bytes_for(const Shape& s)
 {
     // Enough semaphores for the narrowest tile width.
-    const int64_t tiles = cdiv(s.m, kMinTileM) * cdiv(s.k, 64);
-    return kStatusBytes + static_cast<size_t>(tiles) * sizeof(uint32_t);
+    return kStatusBytes + static_cast<size_t>(semaphore_capacity(s)) * sizeof(uint32_t);
 }
 
 // ------------------------------------------------------------------ descriptors
@@ -386,6 +475,31 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     }
+    if (plan.loader == CONV2D_LOADER_TMA_BOX) {
+        // x as {64 channels, W, H, N, C/64}: a box is KC chunks of a bn_img x bh x bw pixel rectangle
+        // (traversal strides sh, sw), landing chunk-major; w as {64, K, C*R*S/64}: KC k-blocks of BN rows.
+        const BoxGeom& g = plan.box;
+        const cuuint64_t xd[5] = {(cuuint64_t)BK, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n,
+                                  (cuuint64_t)(s.c / BK)};
+        const cuuint64_t xs[4] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                  (cuuint64_t)(s.h * s.w * s.c * 2), (cuuint64_t)(BK * 2)};
+        const cuuint32_t xb[5] = {(cuuint32_t)BK, (cuuint32_t)(g.bw * s.sw), (cuuint32_t)(g.bh * s.sh),
+                                  (cuuint32_t)g.bn_img, (cuuint32_t)kBoxChunks};
+        const cuuint32_t xe[5] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1, 1};
+        CUresult rc = g_encode_tiled(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(x), xd, xs, xb, xe,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        const cuuint64_t wd[3] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.crs / BK)};
+        const cuuint64_t ws[2] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2)};
+        const cuuint32_t wb[3] = {(cuuint32_t)BK, (cuuint32_t)plan.block_n, (cuuint32_t)kBoxChunks};
+        const cuuint32_t we[3] = {1, 1, 1};
+        rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), wd, ws, wb, we,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
     if (plan.loader != CONV2D_LOADER_SCALAR) {
         const cuuint64_t dims[2] = {(cuuint64_t)s.crs, (cuuint64_t)s.k};
         const cuuint64_t strides[1] = {(cuuint64_t)(s.crs * 2)};
@@ -403,6 +517,17 @@ cudaError_t dispatch(int bm, int bn, int loader, const CUtensorMap& a, const CUt
                      const sgb::ConvKernelParams& kp, int grid, cudaStream_t st)
 {
     using namespace sgb;
+    if (loader == CONV2D_LOADER_TMA_BOX) {
+        if (bm == 256) {
+            if (bn == 64) return launch_conv2d_tc<256, 64, LOADER_BOX>(a, b, kp, grid, st);
+            if (bn == 128) return launch_conv2d_tc<256, 128, LOADER_BOX>(a, b, kp, grid, st);
+            return cudaErrorInvalidValue;
+        }
+        if (bn == 64) return launch_conv2d_tc<128, 64, LOADER_BOX>(a, b, kp, grid, st);
+        if (bn == 128) return launch_conv2d_tc<128, 128, LOADER_BOX>(a, b, kp, grid, st);
+        if (bn == 256) return launch_conv2d_tc<128, 256, LOADER_BOX>(a, b, kp, grid, st);
+        return cudaErrorInvalidValue;
+    }
 #define SGB_CASE(BN_)                                                                                          \
     if (bn == BN_) {                                                                                           \
         if (bm == 256) return launch_conv2d_tc<256, BN_, LOADER_TMA>(a, b, kp, grid, st);                 \
@@ -440,7 +565,8 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
         (workspace && !aligned16(workspace)))
         return CONV2D_ERR_ALIGNMENT;
     if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
-                 algo->wait_limit_ns < 0))
+                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
+                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
         return CONV2D_ERR_INVALID;
     Plan plan;
     rc = choose_plan(s, algo, &plan);
@@ -537,7 +663,14 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.grid = plan.grid;
     kp.units = plan.units;
     kp.vec_store = vec_store ? 1 : 0;
+    kp.bw = plan.box.bw;
+    kp.bh = plan.box.bh;
+    kp.bn_img = plan.box.bn_img;
+    kp.px = plan.box.px;
+    kp.q_blocks = plan.box.q_blocks;
+    kp.p_blocks = plan.box.p_blocks;
     kp.debug_flags = algo ? algo->debug_flags : 0;
+    kp.reduce_concurrent = (algo && algo->reduction == CONV2D_REDUCTION_ORDERED) ? 0 : 1;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
     kp.trace = nullptr;
 #ifdef SGB_TRACE_ENABLED
@@ -608,6 +741,8 @@ int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
     out->splits = plan.splits;
     out->loader = plan.loader;
     out->grid = plan.grid;
+    const bool cuts = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
+    out->reduction = cuts ? CONV2D_REDUCTION_CONCURRENT : CONV2D_REDUCTION_AUTO;
     return CONV2D_OK;
 }
 

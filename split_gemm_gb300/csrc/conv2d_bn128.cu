@@ -3,4 +3,5 @@
 
 namespace sgb {
 SGB_INSTANTIATE_CONV2D(128)
+SGB_INSTANTIATE_CONV2D_BOX256(128)
 }  // namespace sgb

@@ -3,4 +3,5 @@
 
 namespace sgb {
 SGB_INSTANTIATE_CONV2D(64)
+SGB_INSTANTIATE_CONV2D_BOX256(64)
 }  // namespace sgb

@@ -20,14 +20,32 @@
 // splits is the special case G = tiles * S.
 //
 // Splits of a tile are reduced in place in y (NVIDIA/Fuser issue #1316
-// "Split-K matmul is slow even for few partitions", Eliminating the workspace):
-// the CTAs take turns on a per-tile semaphore -- split j waits until it reads j,
-// adds its partial tile into y (split 0 stores acc + bias), then publishes j+1;
-// the last split resets it to 0.  The fp32 output is the work buffer; the only
-// extra memory is one 32-bit word per tile.  Each CTA walks its segments in
+// "Split-K matmul is slow even for few partitions", Eliminating the workspace),
+// ordered by a per-tile semaphore; the fp32 output is the work buffer and the
+// only extra memory is one 32-bit word per tile.  Split 0 always goes first: it
+// stores acc + bias.  Then, in the ordered mode, the CTAs take turns -- split j
+// waits until the semaphore reads j, adds its partial tile into y and publishes
+// j+1 (bitwise reproducible); in the concurrent mode every later split waits only
+// for split 0, adds with vector atomic adds in L2 in whatever order the splits
+// finish, and counts itself done -- a chain of two steps instead of S.  The last
+// split of a tile resets its semaphore to 0.  Each CTA walks its segments in
 // reverse order, so the head of a cut tile (split 0, owned by the lower CTA) is
 // computed first and the tail (a later split) last: turns are normally granted
 // before they are asked for.
+//
+// Box loader (C % 128 == 0).  An im2col-mode TMA operation costs about as much
+// as a tiled one however few bytes it moves, so the box loader makes each
+// operation carry more: the tile is a rectangle of output pixels (bn_img images
+// x bh rows x bw columns, px = bn_img*bh*bw <= BM), and for filter tap (r, s)
+// its activation rows are one tiled box of the NHWC input viewed as 5-D
+// {64 channels, W, H, N, C/64}, starting at the window origin of the
+// rectangle's first pixel (traversal strides sh, sw; zero fill outside the
+// image gives the padding).  One box brings KC = 2 consecutive 64-channel
+// chunks, and one 3-D box of the weight viewed as {64, K, C*R*S/64} brings the
+// matching two k-blocks of B, so a pipeline stage holds two k-blocks.  Chunk j
+// of A lands px rows after chunk j-1 (px is a multiple of 8, keeping the
+// 128-byte swizzle atoms aligned); the MMA reads 128 rows from each chunk start
+// and the rows past px are ignored by the epilogue.
 //
 // Warp roles:
 //   warp 0      TMA producer: weight tile (tiled TMA) and, for the TMA loader,
@@ -62,16 +80,14 @@ namespace sgb {
 constexpr int MMA_M = 128;       // rows per tcgen05.mma (cta_group::1); a tile has BM/128 row blocks
 constexpr int BK = 64;           // reduction elements per stage: one 128-byte bf16 row
 constexpr int UMMA_K = 16;       // reduction per tcgen05.mma of kind::f16
-constexpr int EPI_WARP0 = 2;     // epilogue warps 2..5
-constexpr int EPI_THREADS = 128;
+constexpr int EPI_WARP0 = 2;     // epilogue warps 2..5 (2..9 with a TMA loader)
 constexpr int GATHER_WARP0 = 6;  // gather warps 6..9 (gather loaders only)
 constexpr int GATHER_THREADS = 128;
 constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
 constexpr int EPI_SLOTS = 1;                 // staging slots per epilogue warp
-constexpr int EPI_BYTES = 4 * EPI_SLOTS * EPI_SLOT_BYTES;
 constexpr uint32_t STATUS_TIMEOUT = 6;  // same value as CONV2D_ERR_TIMEOUT
 
-enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4 };
+enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6 };
 
 // Which engine brings in the im2col tile of the CTA's k-block number `it`:
 // the TMA unit (im2col mode) or the gather warps (cp.async).  The hybrid
@@ -79,7 +95,7 @@ enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, L
 template <int LOADER>
 __device__ __forceinline__ bool a_by_tma(int it)
 {
-    return LOADER == LOADER_TMA || (LOADER == LOADER_HYBRID && (it & 1) == 0);
+    return LOADER == LOADER_TMA || LOADER == LOADER_BOX || (LOADER == LOADER_HYBRID && (it & 1) == 0);
 }
 template <int LOADER>
 __device__ __forceinline__ bool a_by_gather(int it)
@@ -96,12 +112,16 @@ struct ConvKernelParams {
     uint32_t* sems;     // one per output tile (needed whenever a tile is split)
     int N, H, W, C, K, R, S, P, Q;
     int sh, sw, ph, pw, dh, dw;
-    int M, CRS, num_kb;
+    int M, CRS, num_kb;       // num_kb: pipeline stages per tile (KC k-blocks each)
     int m_tiles, n_tiles;
     int grid;                 // G: CTAs sharing the unit range
     long long units;          // U = m_tiles * n_tiles * num_kb
     int vec_store;            // K % 4 == 0: 16-byte vector writes of y
+    // Box loader only: the tile rectangle (bn_img images x bh rows x bw columns,
+    // px of its pixels) and the tile grid over (images, rows, columns).
+    int bw, bh, bn_img, px, q_blocks, p_blocks;
     int debug_flags;
+    int reduce_concurrent;    // 1: later splits add concurrently after split 0; 0: strict turns
     unsigned long long wait_limit_ns;
     unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
 };
@@ -115,27 +135,34 @@ template <int BM, int BN, int LOADER>
 struct TileConfig {
     static_assert(BM == 128 || BM == 256, "BM must be 128 or 256");
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
-    static_assert(BM == 128 || LOADER == LOADER_TMA, "256-pixel tiles use the TMA im2col loader");
+    static_assert(BM == 128 || LOADER == LOADER_TMA || LOADER == LOADER_BOX, "256-pixel tiles need a TMA loader");
     static constexpr int M_SUB = BM / MMA_M;  // 128-row MMA blocks per tile
-    static constexpr int A_STAGE_BYTES = BM * BK * 2;
-    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    static constexpr int KC = LOADER == LOADER_BOX ? 2 : 1;  // k-blocks per pipeline stage
+    static constexpr int A_STAGE_BYTES = KC * BM * BK * 2;
+    static constexpr int B_STAGE_BYTES = KC * BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int STAGES =
-        BM == 128 ? (BN == 256 ? 4 : (BN == 128 ? 6 : 8)) : (BN == 256 ? 3 : 4);
+        LOADER == LOADER_BOX ? (196608 / STAGE_BYTES > 8 ? 8 : 196608 / STAGE_BYTES)
+        : BM == 128 ? (BN == 256 ? 4 : (BN == 128 ? 6 : 8)) : (BN == 256 ? 3 : 4);
+    static_assert(STAGES >= 2, "the ring needs at least two stages");
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    // With a TMA loader the gather warps' places go to the epilogue: 8 warps, two
+    // per TMEM lane quadrant, each writing half of the tile's columns.
+    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 8 : 4;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOTS * EPI_SLOT_BYTES;
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared-memory limit");
     static constexpr int ACC_COLS = M_SUB * BN;                   // TMEM columns of one accumulator set
     static constexpr int NUM_ACC = 2 * ACC_COLS <= 512 ? 2 : 1;   // double-buffered when TMEM allows
     static constexpr uint32_t TMEM_COLS = NUM_ACC * ACC_COLS;
-    static constexpr int THREADS = (LOADER == LOADER_TMA ? 6 : 10) * 32;
+    static constexpr int THREADS = 10 * 32;
 };
 
 struct SmemView {
     uint8_t* a;          // STAGES x A tile
     uint8_t* b;          // STAGES x B tile
-    uint8_t* epi;        // 4 warps x EPI_SLOTS staging slots
+    uint8_t* epi;        // EPI_WARPS x EPI_SLOTS staging slots
     uint64_t* full;      // STAGES
     uint64_t* empty;     // STAGES
     uint64_t* acc_full;  // 2: accumulator ready for the epilogue
@@ -208,6 +235,38 @@ __device__ __forceinline__ void decode_pixel(const ConvKernelParams& kp, int m, 
     q = rem - p * kp.Q;
 }
 
+// Box loader: first image, row and column of the rectangle of tile row-block m_tile.
+__device__ __forceinline__ void box_origin(const ConvKernelParams& kp, int m_tile, int& n0, int& p0, int& q0)
+{
+    const int qb = m_tile % kp.q_blocks;
+    const int rest = m_tile / kp.q_blocks;
+    const int pb = rest % kp.p_blocks;
+    n0 = (rest / kp.p_blocks) * kp.bn_img;
+    p0 = pb * kp.bh;
+    q0 = qb * kp.bw;
+}
+
+// GEMM row (output pixel index) of row `row` of tile row-block m_tile, or -1
+// when the row lies past the output.  (n0, p0, q0) is the box origin (box
+// loader only).
+template <int BM, int LOADER>
+__device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile, int row, int n0, int p0, int q0)
+{
+    if constexpr (LOADER == LOADER_BOX) {
+        if (row >= kp.px) return -1;
+        const int q = q0 + row % kp.bw;
+        const int t = row / kp.bw;
+        const int p = p0 + t % kp.bh;
+        const int n = n0 + t / kp.bh;
+        if (q >= kp.Q || p >= kp.P || n >= kp.N) return -1;
+        return (n * kp.P + p) * kp.Q + q;
+    } else {
+        (void)n0; (void)p0; (void)q0;
+        const int m = m_tile * BM + row;
+        return m < kp.M ? m : -1;
+    }
+}
+
 // ---------------------------------------------------------------- TMA producer (warp 0, one thread)
 template <int BM, int BN, int LOADER>
 __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
@@ -222,16 +281,18 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
     (void)wait_cycles;
     SegmentWalker walk(kp);
     Segment sg;
+    constexpr int KC = Cfg::KC;
+    const uint32_t a_bytes = LOADER == LOADER_BOX ? static_cast<uint32_t>(KC * kp.px * BK * 2) : A_STAGE_BYTES;
     while (ok && walk.next(kp, sg)) {
         const int m_tile = sg.tile / kp.n_tiles;
         const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
-        const int m0 = m_tile * BM;
         // Window origin of the tile's first pixel and the first (r, s, c) of the segment.
         int n_img, p0, q0;
-        decode_pixel(kp, m0, n_img, p0, q0);
+        if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, n_img, p0, q0);
+        else decode_pixel(kp, m_tile * BM, n_img, p0, q0);
         const int w_org = q0 * kp.sw - kp.pw;
         const int h_org = p0 * kp.sh - kp.ph;
-        const int kk0 = sg.kb_begin * BK;
+        const int kk0 = sg.kb_begin * KC * BK;
         const int rs0 = kk0 / kp.C;
         int c = kk0 - rs0 * kp.C;
         int r = rs0 / kp.S;
@@ -248,12 +309,18 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
             }
             SGB_CYCLES_END(wait_cycles, tw);
             const bool a_tma = a_by_tma<LOADER>(it);
-            ptx::mbar_arrive_expect_tx(&sm.full[stage], (a_tma ? A_STAGE_BYTES : 0) + Cfg::B_STAGE_BYTES);
-            if (a_tma)
+            ptx::mbar_arrive_expect_tx(&sm.full[stage], (a_tma ? a_bytes : 0) + Cfg::B_STAGE_BYTES);
+            if constexpr (LOADER == LOADER_BOX) {
+                // KC channel chunks of the rectangle's windows at tap (r, s), then the matching KC weight k-blocks.
+                ptx::tma_load_5d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], 0, w_org + s * kp.dw,
+                                 h_org + r * kp.dh, n_img, c / BK);
+                ptx::tma_load_3d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], 0, n0, kb * KC);
+            } else if (a_tma) {
                 ptx::tma_load_im2col_4d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], c, w_org, h_org,
                                         n_img, static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
-            if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID) {
-                c += BK;
+            }
+            if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID || LOADER == LOADER_BOX) {
+                c += KC * BK;
                 if (c == kp.C) {
                     c = 0;
                     if (++s == kp.S) {
@@ -262,7 +329,8 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
                     }
                 }
             }
-            ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], kb * BK, n0);
+            if constexpr (LOADER != LOADER_BOX)
+                ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], kb * BK, n0);
         }
     }
     SGB_TRACE(kp, true, 3);
@@ -282,6 +350,7 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(MMA_M, BN);
     const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
     const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    const uint32_t a_chunk16 = LOADER == LOADER_BOX ? static_cast<uint32_t>(kp.px * 8) : 0u;
     int it = 0, seg_idx = 0;
     bool ok = true;
     uint64_t full_cycles = 0, acc_cycles = 0;
@@ -322,19 +391,23 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
             // address >> 4 in the low bits (no carry: shared addresses < 256 KB), so
             // an offset is added to the descriptor itself; advancing along K inside
             // a 128-B swizzled row moves the start address by 32 B.
+            // A stage with KC k-blocks holds them as KC chunks, a_chunk16 apart (in 16-B units).
             const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
             const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
-            uint64_t adk[BK / UMMA_K][Cfg::M_SUB], bdk[BK / UMMA_K];
+            constexpr int KSTEPS = Cfg::KC * BK / UMMA_K;
+            uint64_t adk[KSTEPS][Cfg::M_SUB], bdk[KSTEPS];
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-                bdk[k] = bd + static_cast<uint64_t>((k * UMMA_K * 2) >> 4);
+            for (int k = 0; k < KSTEPS; ++k) {
+                const int chunk = k / (BK / UMMA_K), kin = k % (BK / UMMA_K);
+                bdk[k] = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * UMMA_K * 2) >> 4);
 #pragma unroll
                 for (int sub = 0; sub < Cfg::M_SUB; ++sub)
-                    adk[k][sub] = ad + static_cast<uint64_t>((sub * MMA_M * 128 + k * UMMA_K * 2) >> 4);
+                    adk[k][sub] = ad + static_cast<uint64_t>(chunk) * a_chunk16 +
+                                  static_cast<uint64_t>((sub * MMA_M * 128 + kin * UMMA_K * 2) >> 4);
             }
             const uint32_t acc0 = kb > sg.kb_begin ? 1u : 0u;
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
+            for (int k = 0; k < KSTEPS; ++k) {
 #pragma unroll
                 for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
                     ptx::mma_bf16(tmem_d + sub * BN, adk[k][sub], bdk[k], IDESC, k > 0 ? 1u : acc0);
@@ -559,10 +632,35 @@ __device__ __forceinline__ bool wait_turn(const ConvKernelParams& kp, int tile, 
     return true;
 }
 
-// Publishes the next split's turn (the last split resets the semaphore to 0).  One thread only.
+// Concurrent mode: waits (bounded) until split 0 of the tile has stored its part.  One thread only.
+__device__ __forceinline__ bool wait_base(const ConvKernelParams& kp, int tile, volatile uint32_t* abort_flag)
+{
+    const uint32_t* sem = kp.sems + tile;
+    if (ptx::ld_acquire_gpu(sem) != 0u) return true;
+    const uint64_t t0 = ptx::clock64();
+    const uint64_t limit = ptx::ns_to_cycles(kp.wait_limit_ns);
+    while (ptx::ld_acquire_gpu(sem) == 0u) {
+        __nanosleep(32);
+        if (ptx::clock64() - t0 > limit) {
+            record_timeout(kp, abort_flag);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Marks this split's part of the tile done.  Ordered mode: publishes the next
+// split's turn.  Concurrent mode: counts the split in; the split that completes
+// the count is the last one.  The last split resets the semaphore to 0.  One
+// thread only, after the CTA's writes have been fenced.
 __device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, const Segment& sg)
 {
     if ((kp.debug_flags & 1) && sg.split == 0) return;  // test hook: never signal
+    if (kp.reduce_concurrent) {
+        const uint32_t before = atomicAdd(kp.sems + sg.tile, 1u);
+        if (before + 1u == static_cast<uint32_t>(sg.nsplits)) atomicExch(kp.sems + sg.tile, 0u);
+        return;
+    }
     const uint32_t next = (sg.split + 1 == sg.nsplits) ? 0u : static_cast<uint32_t>(sg.split + 1);
     ptx::st_release_gpu(kp.sems + sg.tile, next);
 }
@@ -572,15 +670,21 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                              uint32_t tmem_base)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
-    const int et = threadIdx.x - EPI_WARP0 * 32;  // 0..127
-    const int ew = et >> 5;                        // epilogue warp 0..3
+    constexpr int EPI_T = Cfg::EPI_WARPS * 32;
+    // Warps of the same TMEM lane quadrant split the tile's 32-column slabs.
+    constexpr int SLABS = BN / 32 / (Cfg::EPI_WARPS / 4);
+    const int et = threadIdx.x - EPI_WARP0 * 32;  // 0 .. EPI_T-1
+    const int ew = et >> 5;                        // epilogue warp
     const int lane = threadIdx.x & 31;
     const int quad = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;          // row of each 128-row block owned by this thread
+    const int jbeg = (ew >> 2) * SLABS;        // this warp's first slab
     uint8_t* slots = sm.epi + ew * (EPI_SLOTS * EPI_SLOT_BYTES);
     int seg_idx = 0;
     uint64_t c_acc = 0, c_ld = 0, c_slot = 0, c_st = 0, c_turn = 0, c_done = 0;
     (void)c_acc; (void)c_ld; (void)c_slot; (void)c_st; (void)c_turn; (void)c_done;
+    const int rsub = lane >> 3;  // vector stores: row within a group of four written per instruction
+    const int chunk = lane & 7;  // vector stores: 16-byte chunk of the 128-byte row slab
     SegmentWalker walk(kp);
     Segment sg;
     while (walk.next(kp, sg)) {
@@ -588,29 +692,38 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         const uint32_t use = static_cast<uint32_t>(seg_idx / Cfg::NUM_ACC) & 1u;
         const int m_tile = sg.tile / kp.n_tiles;
         const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
-        const int m0 = m_tile * BM;
+        int bx_n = 0, bx_p = 0, bx_q = 0;
+        if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, bx_n, bx_p, bx_q);
         const bool add_bias = kp.bias != nullptr && sg.split == 0;
-        // Bias for this tile, fetched before the accumulator wait so that its
-        // latency is hidden: lane l holds columns n0 + 32*j + l.
-        float bias_r[BN / 32];
+        // Bias of this warp's slabs, fetched before the accumulator wait so that
+        // its latency is hidden.  Vector stores: lane holds the four columns of its
+        // 16-byte chunk; row stores: lane l holds column 32*j + l.
+        float4 bias4[SLABS];
+        float bias_r[SLABS];
 #pragma unroll
-        for (int j = 0; j < BN / 32; ++j) {
-            const int n = n0 + j * 32 + lane;
-            bias_r[j] = (add_bias && n < kp.K) ? __ldg(kp.bias + n) : 0.0f;
+        for (int j = 0; j < SLABS; ++j) {
+            const int cbase = n0 + (jbeg + j) * 32;
+            bias4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            bias_r[j] = 0.f;
+            if (add_bias && kp.vec_store && cbase + chunk * 4 < kp.K)
+                bias4[j] = __ldg(reinterpret_cast<const float4*>(kp.bias + cbase + chunk * 4));
+            if (add_bias && !kp.vec_store && cbase + lane < kp.K) bias_r[j] = __ldg(kp.bias + cbase + lane);
         }
         SGB_CYCLES_BEGIN(t_acc);
         if (!ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) record_timeout(kp, sm.abort_flag);
         SGB_CYCLES_END(c_acc, t_acc);
-        // One thread decides for all 128 (including, for a later split, waiting
-        // for its turn), so that every epilogue warp takes the same path.
+        // One thread decides for all (including, for a later split, waiting for
+        // split 0 or for its turn), so that every epilogue warp takes the same path.
         SGB_CYCLES_BEGIN(t_turn);
-        ptx::named_bar_sync(1, EPI_THREADS);
+        ptx::named_bar_sync(1, EPI_T);
         if (et == 0) {
             bool go = *sm.abort_flag == 0u;
-            if (go && sg.split > 0) go = wait_turn(kp, sg.tile, sg.split, sm.abort_flag);
+            if (go && sg.split > 0)
+                go = kp.reduce_concurrent ? wait_base(kp, sg.tile, sm.abort_flag)
+                                          : wait_turn(kp, sg.tile, sg.split, sm.abort_flag);
             *sm.epi_go = go ? 1u : 0u;
         }
-        ptx::named_bar_sync(1, EPI_THREADS);
+        ptx::named_bar_sync(1, EPI_T);
         SGB_CYCLES_END(c_turn, t_turn);
         if (!*sm.epi_go) break;
         ptx::tc_fence_after();
@@ -621,32 +734,29 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         for (int sub = 0; sub < Cfg::M_SUB; ++sub) {
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * Cfg::ACC_COLS + sub * BN) +
                                    (static_cast<uint32_t>(quad * 32) << 16);
-            const int mrow0 = m0 + sub * MMA_M;  // first output row of this 128-row block
+            const int trow0 = sub * MMA_M;  // first tile row of this 128-row block
             const bool last_sub = sub == Cfg::M_SUB - 1;
             if (kp.vec_store) {
-                // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
-                // coalesced 16-byte global writes (8 lanes per 128-byte row): plain stores for
-                // split 0, vector atomic adds for later splits (in turn).  The writes use the
-                // load/store path, leaving the TMA unit to the im2col and weight loads.
-                uint8_t* slot = slots;  // one slot per warp: its reads finish before the next slab is written
-                const uint32_t saddr = ptx::smem_addr(slot);
-                const int rsub = lane >> 3;     // row within a group of four written per instruction
-                const int chunk = lane & 7;     // 16-byte chunk of the 128-byte row
+                // TMEM -> registers -> this warp's 32 x 32 swizzled staging slot ->
+                // coalesced 16-byte global writes (8 lanes per 128-byte row, bias added
+                // per chunk): plain stores for split 0, vector atomic adds for later
+                // splits.  The writes use the load/store path, leaving the TMA unit
+                // to the im2col and weight loads.
+                const uint32_t saddr = ptx::smem_addr(slots);
+                int mrow[8];  // output row of each of this lane's eight rows (-1: none)
 #pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
+                for (int i = 0; i < 8; ++i)
+                    mrow[i] = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + quad * 32 + 4 * i + rsub, bx_n, bx_p, bx_q);
+#pragma unroll
+                for (int j = 0; j < SLABS; ++j) {
                     uint32_t v[32];
                     SGB_CYCLES_BEGIN(t_ld);
-                    ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                    ptx::tmem_ld_32x32b_x32(taddr + (jbeg + j) * 32, v);
                     ptx::tmem_ld_wait();
                     SGB_CYCLES_END(c_ld, t_ld);
-                    if (last_sub && j == BN / 32 - 1) {  // accumulator drained: the MMA warp may reuse it
+                    if (last_sub && j == SLABS - 1) {  // accumulator drained: the MMA warp may reuse it
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&sm.acc_empty[buf]);
-                    }
-                    if (add_bias) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
                     }
                     SGB_CYCLES_BEGIN(t_st);
                     __syncwarp();  // the previous slab's reads of the slot are done
@@ -657,13 +767,19 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                     __syncwarp();
                     SGB_CYCLES_END(c_st, t_st);
                     SGB_CYCLES_BEGIN(t_slot);
-                    const int col = n0 + j * 32 + chunk * 4;
+                    const int col = n0 + (jbeg + j) * 32 + chunk * 4;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int r = 4 * i + rsub;  // row within the warp's 32 rows
-                        const int m = mrow0 + quad * 32 + r;
-                        const uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(r, chunk));
-                        if (m < kp.M && col < kp.K) {
+                        const int m = mrow[i];
+                        uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(r, chunk));
+                        if (add_bias) {
+                            val.x = __float_as_uint(__uint_as_float(val.x) + bias4[j].x);
+                            val.y = __float_as_uint(__uint_as_float(val.y) + bias4[j].y);
+                            val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
+                            val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
+                        }
+                        if (m >= 0 && col < kp.K) {
                             float* dst = kp.y + static_cast<int64_t>(m) * kp.K + col;
                             if (sg.split == 0) *reinterpret_cast<uint4*>(dst) = val;
                             else ptx::red_add_v4_f32(dst, val);
@@ -672,17 +788,18 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                     SGB_CYCLES_END(c_slot, t_slot);
                 }
             } else {
-                // K % 4 != 0: row-per-thread stores (split 0) or read-add-write (later splits).
-                const int m = mrow0 + row;
-                const bool row_ok = m < kp.M;
+                // K % 4 != 0: row-per-thread stores (split 0), and for later splits
+                // read-add-write in turn or scalar atomic adds when concurrent.
+                const int m = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + row, bx_n, bx_p, bx_q);
+                const bool row_ok = m >= 0;
                 const bool accumulate = sg.split > 0;
                 float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
 #pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
+                for (int j = 0; j < SLABS; ++j) {
                     uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + j * 32, v);
+                    ptx::tmem_ld_32x32b_x32(taddr + (jbeg + j) * 32, v);
                     ptx::tmem_ld_wait();
-                    if (last_sub && j == BN / 32 - 1) {
+                    if (last_sub && j == SLABS - 1) {
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&sm.acc_empty[buf]);
                     }
@@ -692,9 +809,9 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                             v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
                     }
                     if (!row_ok) continue;
-                    const int nb = n0 + j * 32;
+                    const int nb = n0 + (jbeg + j) * 32;
                     float old[32];
-                    if (accumulate) {
+                    if (accumulate && !kp.reduce_concurrent) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
                     }
@@ -703,6 +820,10 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                         const int n = nb + e;
                         if (n >= kp.K) break;
                         float o = __uint_as_float(v[e]);
+                        if (accumulate && kp.reduce_concurrent) {
+                            atomicAdd(yrow + n, o);
+                            continue;
+                        }
                         if (accumulate) o = old[e] + o;
                         yrow[n] = o;
                     }
@@ -712,9 +833,12 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
 
         if (sg.nsplits > 1) {
             SGB_CYCLES_BEGIN(t_done);
-            // Every write of this split must be complete and visible before the next split's turn.
-            __threadfence();
-            ptx::named_bar_sync(1, EPI_THREADS);
+            // Before the next split may read or add: split 0's stores (both modes)
+            // and every split's writes in the ordered mode must be complete and
+            // visible.  A later split of the concurrent mode only counts itself
+            // done; nothing waits for its adds inside this launch.
+            if (sg.split == 0 || !kp.reduce_concurrent) __threadfence();
+            ptx::named_bar_sync(1, EPI_T);
             if (et == 0) pass_turn(kp, sg);
             SGB_CYCLES_END(c_done, t_done);
         }
@@ -745,7 +869,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     sm.a = smem;
     sm.b = smem + Cfg::STAGES * Cfg::A_STAGE_BYTES;
     sm.epi = smem + Cfg::RING_BYTES;
-    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + EPI_BYTES);
+    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + Cfg::EPI_BYTES);
     sm.empty = sm.full + Cfg::STAGES;
     sm.acc_full = sm.empty + Cfg::STAGES;
     sm.acc_empty = sm.acc_full + 2;
@@ -763,14 +887,15 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         // arrive per thread (issued by its copies); scalar gather: one per warp.
         constexpr uint32_t GATHER_WARPS = GATHER_THREADS / 32;
         const uint32_t full_count =
-            LOADER == LOADER_TMA ? 1u : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
+            (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 1u
+                                                           : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
         for (int i = 0; i < Cfg::STAGES; ++i) {
             ptx::mbar_init(&sm.full[i], full_count);
             ptx::mbar_init(&sm.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&sm.acc_full[i], 1);
-            ptx::mbar_init(&sm.acc_empty[i], EPI_THREADS);
+            ptx::mbar_init(&sm.acc_empty[i], Cfg::EPI_WARPS * 32);
         }
         ptx::mbar_init(sm.mma_done, 1);
         *sm.abort_flag = 0u;
@@ -778,7 +903,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         ptx::mbar_init_fence();
     }
     if (warp == 0 && lane == 0) {
-        if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID) ptx::prefetch_tensormap(&tm_a);
+        if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID || LOADER == LOADER_BOX) ptx::prefetch_tensormap(&tm_a);
         if (LOADER != LOADER_SCALAR) ptx::prefetch_tensormap(&tm_b);
     }
     if (warp == 1) {
@@ -801,7 +926,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         if (lane == 0 && LOADER != LOADER_SCALAR) run_tma_producer<BM, BN, LOADER>(&tm_a, &tm_b, kp, sm);
     } else if (warp == 1) {
         if (lane == 0) run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
-    } else if (warp < GATHER_WARP0) {
+    } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
         run_epilogue<BM, BN, LOADER>(kp, sm, tmem_base);
     } else {
         if constexpr (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BM, BN, LOADER>(kp, sm);
@@ -868,13 +993,17 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     cudaError_t launch_conv2d_tc<BM_, BN_, L_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, \
                                                int, cudaStream_t)
 
-// Every loader with 128-pixel tiles, and the TMA loader with 256-pixel tiles.
+// Every loader with 128-pixel tiles, the TMA loader with 256-pixel tiles, and
+// the box loader with 256-pixel tiles where two k-blocks of both operands fit
+// a stage twice (BN <= 128).
 #define SGB_INSTANTIATE_CONV2D(BN_)                    \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_TMA);     \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_CPASYNC); \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
+#define SGB_INSTANTIATE_CONV2D_BOX256(BN_) template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 
 // Declarations of the instantiations that live in other translation units.
 #define SGB_DECLARE_CONV2D(BN_)                               \
@@ -882,6 +1011,8 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_CPASYNC); \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     extern template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
+#define SGB_DECLARE_CONV2D_BOX256(BN_) extern template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 
 }  // namespace sgb

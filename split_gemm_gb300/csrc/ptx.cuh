@@ -100,6 +100,27 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
         : "memory");
 }
 
+// Tiled loads of a 3-D / 5-D box (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t* bar, int32_t c0, int32_t c1,
+                                            int32_t c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* map, uint64_t* bar, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, int32_t c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
 // im2col-mode load of a 4-D NHWC tensor: coordinates {c, w, h, n} of the first
 // pixel's window origin, plus the filter-tap offsets {w_off, h_off}.
 __device__ __forceinline__ void tma_load_im2col_4d(void* dst, const void* map, uint64_t* bar, int32_t c,

@@ -35,8 +35,8 @@ def gpu_conv(sg, x, w, b, opts, algo=None, workspace=None):
     return y.cpu().numpy()
 
 
-def make_algo(sg, block_n=0, splits=0, loader=0, debug_flags=0, wait_limit_ns=0, block_m=0, grid=0):
+def make_algo(sg, block_n=0, splits=0, loader=0, debug_flags=0, wait_limit_ns=0, block_m=0, grid=0, reduction=0):
     a = sg.Algo()
     a.block_n, a.splits, a.loader, a.block_m, a.grid = block_n, splits, loader, block_m, grid
-    a.debug_flags, a.wait_limit_ns = debug_flags, wait_limit_ns
+    a.debug_flags, a.wait_limit_ns, a.reduction = debug_flags, wait_limit_ns, reduction
     return a
