@@ -268,6 +268,88 @@ __device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile
 }
 
 // ---------------------------------------------------------------- TMA producer (warp 0, one thread)
+// Coordinates of the TMA loads of one segment, stage by stage: the window
+// origin of the tile's first pixel, the filter tap (r, s) and channel c of the
+// stage's first k-block, and the tile's first output channel.
+template <int BM, int BN, int LOADER>
+struct LoadCursor {
+    static constexpr int KC = TileConfig<BM, BN, LOADER>::KC;
+    int n_img, w_org, h_org, c, r, s, n0, kb;
+    __device__ __forceinline__ LoadCursor(const ConvKernelParams& kp, const Segment& sg)
+    {
+        const int m_tile = sg.tile / kp.n_tiles;
+        n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int p0, q0;
+        if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, n_img, p0, q0);
+        else decode_pixel(kp, m_tile * BM, n_img, p0, q0);
+        w_org = q0 * kp.sw - kp.pw;
+        h_org = p0 * kp.sh - kp.ph;
+        kb = sg.kb_begin;
+        const int kk0 = kb * KC * BK;
+        const int rs0 = kk0 / kp.C;
+        c = kk0 - rs0 * kp.C;
+        r = rs0 / kp.S;
+        s = rs0 - r * kp.S;
+    }
+    __device__ __forceinline__ void advance(const ConvKernelParams& kp)
+    {
+        ++kb;
+        c += KC * BK;
+        if (c >= kp.C) {  // the im2col loaders need C % 64 == 0, the box loader C % 128 == 0
+            c = 0;
+            if (++s == kp.S) {
+                s = 0;
+                ++r;
+            }
+        }
+    }
+    // The stage's loads into shared memory, completing on `bar`.
+    __device__ __forceinline__ void load(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
+                                         uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar, bool a_tma) const
+    {
+        if constexpr (LOADER == LOADER_BOX) {
+            // KC channel chunks of the rectangle's windows at tap (r, s), then the matching KC weight k-blocks.
+            ptx::tma_load_5d(a_dst, tm_a, bar, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, c / BK);
+            ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);
+        } else {
+            if (a_tma)
+                ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+                                        static_cast<uint16_t>(r * kp.dh));
+            ptx::tma_load_2d(b_dst, tm_b, bar, kb * BK, n0);
+        }
+    }
+    // The same reads as L2 prefetches (nothing lands in shared memory).
+    __device__ __forceinline__ void prefetch(const CUtensorMap* tm_a, const CUtensorMap* tm_b,
+                                             const ConvKernelParams& kp) const
+    {
+        if constexpr (LOADER == LOADER_BOX) {
+            ptx::tma_prefetch_5d(tm_a, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, c / BK);
+            ptx::tma_prefetch_3d(tm_b, 0, n0, kb * KC);
+        } else {
+            ptx::tma_prefetch_im2col_4d(tm_a, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+                                        static_cast<uint16_t>(r * kp.dh));
+            ptx::tma_prefetch_2d(tm_b, kb * BK, n0);
+        }
+    }
+};
+
+// Before the wait for the previous kernel: L2 prefetches of the CTA's first
+// STAGES loads, so that its pipeline fills from L2 once the wait returns.  A
+// prefetch moves nothing into the CTA and reads through L2, the GPU's point of
+// coherence, so it cannot observe or disturb the previous kernel's writes.
+template <int BM, int BN, int LOADER>
+__device__ void prefetch_first_stages(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp)
+{
+    SegmentWalker walk(kp);
+    Segment sg;
+    if (!walk.next(kp, sg)) return;
+    LoadCursor<BM, BN, LOADER> cur(kp, sg);
+    for (int i = 0; i < TileConfig<BM, BN, LOADER>::STAGES && cur.kb < sg.kb_end; ++i) {
+        cur.prefetch(tm_a, tm_b, kp);
+        cur.advance(kp);
+    }
+}
+
 template <int BM, int BN, int LOADER>
 __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
                                  const SmemView& sm)
@@ -275,29 +357,17 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
     using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
-    int it = 0;  // k-blocks issued so far (all segments)
+    constexpr int KC = Cfg::KC;
+    const uint32_t a_bytes = LOADER == LOADER_BOX ? static_cast<uint32_t>(KC * kp.px * BK * 2) : A_STAGE_BYTES;
+    int it = 0;  // stages issued so far (all segments)
     bool ok = true;
     uint64_t wait_cycles = 0;
     (void)wait_cycles;
     SegmentWalker walk(kp);
     Segment sg;
-    constexpr int KC = Cfg::KC;
-    const uint32_t a_bytes = LOADER == LOADER_BOX ? static_cast<uint32_t>(KC * kp.px * BK * 2) : A_STAGE_BYTES;
     while (ok && walk.next(kp, sg)) {
-        const int m_tile = sg.tile / kp.n_tiles;
-        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
-        // Window origin of the tile's first pixel and the first (r, s, c) of the segment.
-        int n_img, p0, q0;
-        if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, n_img, p0, q0);
-        else decode_pixel(kp, m_tile * BM, n_img, p0, q0);
-        const int w_org = q0 * kp.sw - kp.pw;
-        const int h_org = p0 * kp.sh - kp.ph;
-        const int kk0 = sg.kb_begin * KC * BK;
-        const int rs0 = kk0 / kp.C;
-        int c = kk0 - rs0 * kp.C;
-        int r = rs0 / kp.S;
-        int s = rs0 - r * kp.S;
-        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+        LoadCursor<BM, BN, LOADER> cur(kp, sg);
+        for (; cur.kb < sg.kb_end; cur.advance(kp), ++it) {
             const int stage = it % STAGES;
             const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
             if (*sm.abort_flag) { ok = false; break; }
@@ -310,27 +380,8 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
             SGB_CYCLES_END(wait_cycles, tw);
             const bool a_tma = a_by_tma<LOADER>(it);
             ptx::mbar_arrive_expect_tx(&sm.full[stage], (a_tma ? a_bytes : 0) + Cfg::B_STAGE_BYTES);
-            if constexpr (LOADER == LOADER_BOX) {
-                // KC channel chunks of the rectangle's windows at tap (r, s), then the matching KC weight k-blocks.
-                ptx::tma_load_5d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], 0, w_org + s * kp.dw,
-                                 h_org + r * kp.dh, n_img, c / BK);
-                ptx::tma_load_3d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], 0, n0, kb * KC);
-            } else if (a_tma) {
-                ptx::tma_load_im2col_4d(sm.a + stage * A_STAGE_BYTES, tm_a, &sm.full[stage], c, w_org, h_org,
-                                        n_img, static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
-            }
-            if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID || LOADER == LOADER_BOX) {
-                c += KC * BK;
-                if (c == kp.C) {
-                    c = 0;
-                    if (++s == kp.S) {
-                        s = 0;
-                        ++r;
-                    }
-                }
-            }
-            if constexpr (LOADER != LOADER_BOX)
-                ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], kb * BK, n0);
+            cur.load(tm_a, tm_b, kp, sm.a + stage * A_STAGE_BYTES, sm.b + stage * Cfg::B_STAGE_BYTES,
+                     &sm.full[stage], a_tma);
         }
     }
     SGB_TRACE(kp, true, 3);
@@ -905,6 +956,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID || LOADER == LOADER_BOX) ptx::prefetch_tensormap(&tm_a);
         if (LOADER != LOADER_SCALAR) ptx::prefetch_tensormap(&tm_b);
+        if constexpr (LOADER == LOADER_TMA || LOADER == LOADER_BOX) prefetch_first_stages<BM, BN, LOADER>(&tm_a, &tm_b, kp);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sm.tmem_slot, Cfg::TMEM_COLS);
@@ -914,10 +966,11 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
-    // Everything above touches only shared memory, tensor memory and kernel
-    // parameters, so it may overlap the previous kernel in the stream.  Global
-    // memory (inputs it may have written, y and the workspace it may still read)
-    // is touched only after this wait.
+    // Everything above touches only shared memory, tensor memory, kernel
+    // parameters and (by L2 prefetches) the L2 cache, so it may overlap the
+    // previous kernel in the stream.  Global memory is read into the CTA or
+    // written (inputs it may have written, y and the workspace it may still
+    // read) only after this wait.
     ptx::grid_launch_dependents();
     ptx::grid_dependency_wait();
     SGB_TRACE(kp, threadIdx.x == 0, 1);

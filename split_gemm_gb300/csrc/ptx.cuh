@@ -121,6 +121,38 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* map, uint64_t
         : "memory");
 }
 
+// L2 prefetches of what the matching loads above will read (no shared memory,
+// no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_5d(const void* map, int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                                int32_t c4)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_im2col_4d(const void* map, int32_t c, int32_t w, int32_t h, int32_t n,
+                                                       uint16_t w_off, uint16_t h_off)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.im2col [%0, {%1, %2, %3, %4}], {%5, %6};" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "h"(w_off), "h"(h_off)
+                 : "memory");
+}
+
 // im2col-mode load of a 4-D NHWC tensor: coordinates {c, w, h, n} of the first
 // pixel's window origin, plus the filter-tap offsets {w_off, h_off}.
 __device__ __forceinline__ void tma_load_im2col_4d(void* dst, const void* map, uint64_t* bar, int32_t c,
