@@ -48,15 +48,22 @@
 // and the rows past px are ignored by the epilogue.
 //
 // Warp roles:
-//   warp 0      TMA producer: weight tile (tiled TMA) and, for the TMA loader,
-//               the im2col activation tile (im2col-mode TMA) into a STAGES-deep
-//               shared-memory ring guarded by full/empty mbarriers;
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer (128 x BN x 16
-//               per instruction) into two fp32 TMEM accumulators used in turn;
-//   warps 2..5  epilogue: TMEM -> registers (+ bias) -> swizzled shared staging ->
-//               coalesced 16-byte global stores (vector atomic adds for later
-//               splits), while the MMA warp already fills the other accumulator;
-//   warps 6..9  (cp.async and scalar loaders only) im2col gather into the ring.
+//   warp 0      TMA producer (one thread): the im2col activation tiles
+//               (im2col-mode or box TMA) into a STAGES-deep shared-memory ring
+//               guarded by full/empty mbarriers; with a gather loader, the
+//               weight tiles instead;
+//   warp 1      TMEM allocator and tcgen05.mma issuer (128 x BN x 16 per
+//               instruction, lane 0) into two fp32 TMEM accumulators used in
+//               turn; it learns that a stage has landed from a named barrier,
+//               never by touching shared memory between its MMAs;
+//   warps 2..9  epilogue (2..5 with a gather loader): TMEM -> registers (+ bias)
+//               -> swizzled shared staging -> coalesced 16-byte global stores
+//               (vector atomic adds for later splits), while the MMA warp
+//               already fills the other accumulator;
+//   warps 6..9  (cp.async and scalar loaders only) im2col gather into the ring;
+//   warp 10     stage waiter: waits for each stage's full barrier, releases the
+//               MMA warp by the stage's named barrier;
+//   warp 11     (TMA loaders) TMA producer of the weight tiles.
 // The ring replaces block-wide syncs between load and MMA (burn PR #2545's
 // sync-placement discussion; ROCm/rocMLIR PR #1511 "Double buffering
 // improvements" splits loads and MMAs into overlapping stages the same way).
@@ -82,6 +89,8 @@ constexpr int BK = 64;           // reduction elements per stage: one 128-byte b
 constexpr int UMMA_K = 16;       // reduction per tcgen05.mma of kind::f16
 constexpr int EPI_WARP0 = 2;     // epilogue warps 2..5 (2..9 with a TMA loader)
 constexpr int GATHER_WARP0 = 6;  // gather warps 6..9 (gather loaders only)
+constexpr int WAITER_WARP = 10;  // waits for each stage's data, releases the MMA warp by named barrier
+constexpr int STAGE_BAR0 = 2;    // named barrier of ring stage s: STAGE_BAR0 + s (1 is the epilogue's)
 constexpr int GATHER_THREADS = 128;
 constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
 constexpr int EPI_SLOTS = 1;                 // staging slots per epilogue warp
@@ -156,7 +165,18 @@ struct TileConfig {
     static constexpr int ACC_COLS = M_SUB * BN;                   // TMEM columns of one accumulator set
     static constexpr int NUM_ACC = 2 * ACC_COLS <= 512 ? 2 : 1;   // double-buffered when TMEM allows
     static constexpr uint32_t TMEM_COLS = NUM_ACC * ACC_COLS;
-    static constexpr int THREADS = 10 * 32;
+    // With a TMA loader two producer warps issue the loads: warp 0 the
+    // activation tiles, warp 11 the weight tiles.  One issuing thread completes
+    // only about one TMA operation per ~0.3 us whatever its size (about as long
+    // as the MMAs of a 128 x 256 stage take); giving each operand its own
+    // thread halves the issue time per stage.  Each operand of each ring slot
+    // thus has one issuer, loading its uses in order, and a slot's parity waits
+    // never run more than one phase ahead of the MMA's releases.  (Gather
+    // loaders: warp 0 issues the weight tiles.)
+    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX;
+    static constexpr int NPROD = TMA_A ? 2 : 1;
+    static_assert(STAGES <= 8, "one named barrier per stage: ids 2 .. 9");
+    static constexpr int THREADS = (WAITER_WARP + NPROD) * 32;
 };
 
 struct SmemView {
@@ -275,6 +295,7 @@ template <int BM, int BN, int LOADER>
 struct LoadCursor {
     static constexpr int KC = TileConfig<BM, BN, LOADER>::KC;
     int n_img, w_org, h_org, c, r, s, n0, kb;
+    LoadCursor() = default;
     __device__ __forceinline__ LoadCursor(const ConvKernelParams& kp, const Segment& sg)
     {
         const int m_tile = sg.tile / kp.n_tiles;
@@ -303,20 +324,23 @@ struct LoadCursor {
             }
         }
     }
-    // The stage's loads into shared memory, completing on `bar`.
-    __device__ __forceinline__ void load(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
-                                         uint8_t* a_dst, uint8_t* b_dst, uint64_t* bar, bool a_tma) const
+    // The stage's loads into shared memory, completing on `bar`: the activation
+    // tile (`a_tma`: by the TMA unit) and the weight tile.  One issuing thread
+    // has only about one TMA operation in flight at a time, so the two loads
+    // are issued by two lanes of the producer warp, A by lane 0 and B by lane 1.
+    __device__ __forceinline__ void load_a(const CUtensorMap* tm_a, const ConvKernelParams& kp, uint8_t* a_dst,
+                                           uint64_t* bar) const
     {
-        if constexpr (LOADER == LOADER_BOX) {
-            // KC channel chunks of the rectangle's windows at tap (r, s), then the matching KC weight k-blocks.
+        if constexpr (LOADER == LOADER_BOX)  // KC channel chunks of the rectangle's windows at tap (r, s)
             ptx::tma_load_5d(a_dst, tm_a, bar, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, c / BK);
-            ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);
-        } else {
-            if (a_tma)
-                ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
-                                        static_cast<uint16_t>(r * kp.dh));
-            ptx::tma_load_2d(b_dst, tm_b, bar, kb * BK, n0);
-        }
+        else
+            ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+                                    static_cast<uint16_t>(r * kp.dh));
+    }
+    __device__ __forceinline__ void load_b(const CUtensorMap* tm_b, uint8_t* b_dst, uint64_t* bar) const
+    {
+        if constexpr (LOADER == LOADER_BOX) ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);  // KC k-blocks
+        else ptx::tma_load_2d(b_dst, tm_b, bar, kb * BK, n0);
     }
     // The same reads as L2 prefetches (nothing lands in shared memory).
     __device__ __forceinline__ void prefetch(const CUtensorMap* tm_a, const CUtensorMap* tm_b,
@@ -350,7 +374,13 @@ __device__ void prefetch_first_stages(const CUtensorMap* tm_a, const CUtensorMap
     }
 }
 
-template <int BM, int BN, int LOADER>
+// TMA producer (one thread).  OPS selects what it loads: PROD_A the
+// activation tiles, PROD_B the weight tiles, PROD_AB both (gather loaders'
+// warp 0, which loads the weight tiles and, for the hybrid loader, the even
+// stages' activations).
+enum ProducerOps : int { PROD_A = 1, PROD_B = 2, PROD_AB = 3 };
+
+template <int BM, int BN, int LOADER, int OPS>
 __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
                                  const SmemView& sm)
 {
@@ -361,37 +391,97 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
     const uint32_t a_bytes = LOADER == LOADER_BOX ? static_cast<uint32_t>(KC * kp.px * BK * 2) : A_STAGE_BYTES;
     int it = 0;  // stages issued so far (all segments)
     bool ok = true;
-    uint64_t wait_cycles = 0;
+    uint64_t wait_cycles = 0, issue_cycles = 0;
     (void)wait_cycles;
+    (void)issue_cycles;
     SegmentWalker walk(kp);
     Segment sg;
     while (ok && walk.next(kp, sg)) {
         LoadCursor<BM, BN, LOADER> cur(kp, sg);
         for (; cur.kb < sg.kb_end; cur.advance(kp), ++it) {
             const int stage = it % STAGES;
-            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
-            if (*sm.abort_flag) { ok = false; break; }
             SGB_CYCLES_BEGIN(tw);
-            if (!ptx::mbar_wait(&sm.empty[stage], parity ^ 1u, kp.wait_limit_ns)) {
+            if (*sm.abort_flag) { ok = false; break; }
+            if (!ptx::mbar_wait(&sm.empty[stage], (static_cast<uint32_t>(it / STAGES) & 1u) ^ 1u, kp.wait_limit_ns)) {
                 record_timeout(kp, sm.abort_flag);
                 ok = false;
                 break;
             }
             SGB_CYCLES_END(wait_cycles, tw);
-            const bool a_tma = a_by_tma<LOADER>(it);
-            ptx::mbar_arrive_expect_tx(&sm.full[stage], (a_tma ? a_bytes : 0) + Cfg::B_STAGE_BYTES);
-            cur.load(tm_a, tm_b, kp, sm.a + stage * A_STAGE_BYTES, sm.b + stage * Cfg::B_STAGE_BYTES,
-                     &sm.full[stage], a_tma);
+            SGB_CYCLES_BEGIN(ti);
+            const bool a_tma = (OPS & PROD_A) && a_by_tma<LOADER>(it);
+            const uint32_t bytes = (a_tma ? a_bytes : 0u) + ((OPS & PROD_B) ? Cfg::B_STAGE_BYTES : 0u);
+            ptx::mbar_arrive_expect_tx(&sm.full[stage], bytes);
+            if (a_tma) cur.load_a(tm_a, kp, sm.a + stage * A_STAGE_BYTES, &sm.full[stage]);
+            if (OPS & PROD_B) cur.load_b(tm_b, sm.b + stage * Cfg::B_STAGE_BYTES, &sm.full[stage]);
+            SGB_STAGE_MARK(kp, it, (OPS & PROD_A) ? 0 : 1);
+            SGB_CYCLES_END(issue_cycles, ti);
         }
     }
-    SGB_TRACE(kp, true, 3);
-    SGB_TRACE_VALUE(kp, true, 2, wait_cycles);
-    // Drain: the last load of each stage must have landed before the CTA can exit.
+    SGB_TRACE(kp, (OPS & PROD_A) != 0, 3);
+    SGB_TRACE_VALUE(kp, (OPS & PROD_A) != 0, 2, wait_cycles);
+    SGB_TRACE_VALUE(kp, (OPS & PROD_A) != 0, 18, issue_cycles);
+    SGB_TRACE_VALUE(kp, OPS == PROD_B, 19, wait_cycles | (issue_cycles << 32));
+    // Drain: this producer's last load of each slot must have landed before the CTA can exit.
     for (int i = it > STAGES ? it - STAGES : 0; i < it; ++i)
         ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
 }
 
-// ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
+// ---------------------------------------------------------------- stage waiter (warp 10)
+// Waits (bounded) for each ring stage's data in the MMA's order and releases
+// the MMA warp through the stage's named barrier.  The MMA warp never touches
+// shared memory between its MMAs: the tensor pipe queues little work, and a
+// shared-memory access issued after a group of tcgen05.mma instructions
+// returns only once they have drained, leaving the pipe idle for ~200 cycles
+// per stage.
+//
+// Named-barrier generations must pair one waiter arrival with one MMA-warp
+// sync, so the waiter may arrive for use u of a stage only after the MMA warp
+// has passed that stage's use u - 1.  Normally the data guarantees it: use u
+// was loaded after the MMA released use u - 1.  After a timeout the waiter
+// stops waiting for data and waits instead for that release on the stage's
+// empty barrier (the MMA warp commits every stage, issuing or not), so the MMA
+// warp still runs to its end; its MMAs may then read stale data, and the
+// epilogue stores nothing once the abort flag is set.
+template <int BM, int BN, int LOADER>
+__device__ void run_stage_waiter(const ConvKernelParams& kp, const SmemView& sm)
+{
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    constexpr int STAGES = Cfg::STAGES;
+    const int lane = threadIdx.x & 31;
+    bool waiting = true;
+    int it = 0;
+    uint64_t full_cycles = 0;
+    (void)full_cycles;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            const int stage = it % STAGES;
+            const uint32_t use = static_cast<uint32_t>(it / STAGES);
+            if (lane == 0) {
+                SGB_CYCLES_BEGIN(tf);
+                if (waiting && (*sm.abort_flag || !ptx::mbar_wait(&sm.full[stage], use & 1u, kp.wait_limit_ns))) {
+                    record_timeout(kp, sm.abort_flag);
+                    waiting = false;
+                }
+                // The MMA warp always gets this far (its only other waits are bounded),
+                // so the release comes; the retry cap only bounds the loop.
+                if (!waiting && use > 0)
+                    for (int t = 0; t < 16 && !ptx::mbar_wait(&sm.empty[stage], (use - 1u) & 1u, kp.wait_limit_ns); ++t) {
+                    }
+                SGB_CYCLES_END(full_cycles, tf);
+                SGB_STAGE_MARK(kp, it, 2);
+            }
+            __syncwarp();
+            ptx::named_bar_arrive(STAGE_BAR0 + stage, 64);
+        }
+    }
+    SGB_TRACE_VALUE(kp, lane == 0, 4, full_cycles);
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 1)
+// The whole warp walks the stages (named barriers count warps); lane 0 issues.
 template <int BM, int BN, int LOADER>
 __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, uint32_t tmem_base)
 {
@@ -399,82 +489,76 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     constexpr int STAGES = Cfg::STAGES;
     constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(MMA_M, BN);
+    const int lane = threadIdx.x & 31;
     const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
     const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
     const uint32_t a_chunk16 = LOADER == LOADER_BOX ? static_cast<uint32_t>(kp.px * 8) : 0u;
     int it = 0, seg_idx = 0;
-    bool ok = true;
-    uint64_t full_cycles = 0, acc_cycles = 0;
-    (void)full_cycles;
+    bool issue = true;  // false once a wait has run out: keep pace with the waiter, issue nothing
+    uint64_t acc_cycles = 0;
     (void)acc_cycles;
     SegmentWalker walk(kp);
     Segment sg;
-    while (ok && walk.next(kp, sg)) {
+    while (walk.next(kp, sg)) {
         const int buf = seg_idx % Cfg::NUM_ACC;
         const uint32_t use = static_cast<uint32_t>(seg_idx / Cfg::NUM_ACC) & 1u;
         // The epilogue must have drained this accumulator's previous segment.
-        SGB_CYCLES_BEGIN(ta);
-        if (!ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
-            record_timeout(kp, sm.abort_flag);
-            break;
+        if (lane == 0 && issue) {
+            SGB_CYCLES_BEGIN(ta);
+            if (*sm.abort_flag || !ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
+                record_timeout(kp, sm.abort_flag);
+                issue = false;
+            }
+            SGB_CYCLES_END(acc_cycles, ta);
         }
-        SGB_CYCLES_END(acc_cycles, ta);
+        __syncwarp();
         ptx::tc_fence_after();
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * Cfg::ACC_COLS);
         for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
             const int stage = it % STAGES;
-            const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
-            if (*sm.abort_flag) { ok = false; break; }
-            SGB_CYCLES_BEGIN(tf);
-            if (!ptx::mbar_wait(&sm.full[stage], parity, kp.wait_limit_ns)) {
-                record_timeout(kp, sm.abort_flag);
-                ok = false;
-                break;
-            }
-            SGB_CYCLES_END(full_cycles, tf);
+            ptx::named_bar_sync(STAGE_BAR0 + stage, 64);
             ptx::tc_fence_after();
-            // Gathered tiles were written through the generic proxy (cp.async);
-            // order them before the tensor cores read the stage.
-            if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) ptx::fence_proxy_async_smem();
-            // The MMA issue stalls until the tensor pipe takes the instruction, so
-            // all descriptors of the stage are formed before the first MMA and the
-            // MMAs then go out back to back.  Descriptor start addresses are
-            // address >> 4 in the low bits (no carry: shared addresses < 256 KB), so
-            // an offset is added to the descriptor itself; advancing along K inside
-            // a 128-B swizzled row moves the start address by 32 B.
-            // A stage with KC k-blocks holds them as KC chunks, a_chunk16 apart (in 16-B units).
-            const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
-            constexpr int KSTEPS = Cfg::KC * BK / UMMA_K;
-            uint64_t adk[KSTEPS][Cfg::M_SUB], bdk[KSTEPS];
+            if (lane == 0) SGB_STAGE_MARK(kp, it, 3);
+            if (lane == 0 && issue) {
+                // Gathered tiles were written through the generic proxy (cp.async);
+                // order them before the tensor cores read the stage.
+                if (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) ptx::fence_proxy_async_smem();
+                // Descriptor start addresses are address >> 4 in the low bits (no
+                // carry: shared addresses < 256 KB), so an offset is added to the
+                // descriptor itself; advancing along K inside a 128-B swizzled row
+                // moves the start address by 32 B.  A stage with KC k-blocks holds
+                // them as KC chunks, a_chunk16 apart (in 16-B units).
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
+                constexpr int KSTEPS = Cfg::KC * BK / UMMA_K;
+                const uint32_t acc0 = kb > sg.kb_begin ? 1u : 0u;
 #pragma unroll
-            for (int k = 0; k < KSTEPS; ++k) {
-                const int chunk = k / (BK / UMMA_K), kin = k % (BK / UMMA_K);
-                bdk[k] = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * UMMA_K * 2) >> 4);
+                for (int k = 0; k < KSTEPS; ++k) {
+                    const int chunk = k / (BK / UMMA_K), kin = k % (BK / UMMA_K);
+                    const uint64_t bdk = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * UMMA_K * 2) >> 4);
 #pragma unroll
-                for (int sub = 0; sub < Cfg::M_SUB; ++sub)
-                    adk[k][sub] = ad + static_cast<uint64_t>(chunk) * a_chunk16 +
-                                  static_cast<uint64_t>((sub * MMA_M * 128 + kin * UMMA_K * 2) >> 4);
+                    for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
+                        ptx::mma_bf16(tmem_d + sub * BN,
+                                      ad + static_cast<uint64_t>(chunk) * a_chunk16 +
+                                          static_cast<uint64_t>((sub * MMA_M * 128 + kin * UMMA_K * 2) >> 4),
+                                      bdk, IDESC, k > 0 ? 1u : acc0);
+                }
             }
-            const uint32_t acc0 = kb > sg.kb_begin ? 1u : 0u;
-#pragma unroll
-            for (int k = 0; k < KSTEPS; ++k) {
-#pragma unroll
-                for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
-                    ptx::mma_bf16(tmem_d + sub * BN, adk[k][sub], bdk[k], IDESC, k > 0 ? 1u : acc0);
-            }
-            ptx::mma_commit(&sm.empty[stage]);
+            if (lane == 0) ptx::mma_commit(&sm.empty[stage]);  // every stage, issuing or not
+            __syncwarp();
         }
-        if (!ok) break;
-        ptx::mma_commit(&sm.acc_full[buf]);
+        if (lane == 0) ptx::mma_commit(&sm.acc_full[buf]);  // also when not issuing: the epilogue must not wait out
+        __syncwarp();
         ++seg_idx;
     }
-    SGB_TRACE(kp, true, 5);
-    SGB_TRACE_VALUE(kp, true, 4, full_cycles);
-    SGB_TRACE_VALUE(kp, true, 6, acc_cycles);
+    SGB_TRACE(kp, lane == 0, 5);
+    SGB_TRACE_VALUE(kp, lane == 0, 6, acc_cycles);
     // No MMA may be in flight when the CTA reaches its teardown.
-    ptx::mma_commit(sm.mma_done);
-    ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
+    if (lane == 0) {
+        ptx::mma_commit(sm.mma_done);
+        ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- gather producers (warps 6..9)
@@ -760,8 +844,11 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                 bias4[j] = __ldg(reinterpret_cast<const float4*>(kp.bias + cbase + chunk * 4));
             if (add_bias && !kp.vec_store && cbase + lane < kp.K) bias_r[j] = __ldg(kp.bias + cbase + lane);
         }
+        // One thread polls the accumulator barrier; the others wait at the named
+        // barrier below (polling shared memory from every warp would steal issue
+        // slots from the MMA warp).
         SGB_CYCLES_BEGIN(t_acc);
-        if (!ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) record_timeout(kp, sm.abort_flag);
+        if (et == 0 && !ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) record_timeout(kp, sm.abort_flag);
         SGB_CYCLES_END(c_acc, t_acc);
         // One thread decides for all (including, for a later split, waiting for
         // split 0 or for its turn), so that every epilogue warp takes the same path.
@@ -938,7 +1025,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         // arrive per thread (issued by its copies); scalar gather: one per warp.
         constexpr uint32_t GATHER_WARPS = GATHER_THREADS / 32;
         const uint32_t full_count =
-            (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 1u
+            (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 2u  // the activation and the weight producer
                                                            : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
         for (int i = 0; i < Cfg::STAGES; ++i) {
             ptx::mbar_init(&sm.full[i], full_count);
@@ -976,11 +1063,20 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
-        if (lane == 0 && LOADER != LOADER_SCALAR) run_tma_producer<BM, BN, LOADER>(&tm_a, &tm_b, kp, sm);
+        if constexpr (Cfg::TMA_A) {
+            if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_A>(&tm_a, &tm_b, kp, sm);
+        } else if constexpr (LOADER != LOADER_SCALAR) {
+            if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_AB>(&tm_a, &tm_b, kp, sm);
+        }
     } else if (warp == 1) {
-        if (lane == 0) run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
+        run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
     } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
         run_epilogue<BM, BN, LOADER>(kp, sm, tmem_base);
+    } else if (warp == WAITER_WARP) {
+        run_stage_waiter<BM, BN, LOADER>(kp, sm);
+    } else if (warp > WAITER_WARP) {
+        if constexpr (Cfg::TMA_A)  // warp 11: the weight tiles
+            if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_B>(&tm_a, &tm_b, kp, sm);
     } else {
         if constexpr (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BM, BN, LOADER>(kp, sm);
         if constexpr (LOADER == LOADER_SCALAR) run_gather_scalar<BM, BN, LOADER>(kp, sm);

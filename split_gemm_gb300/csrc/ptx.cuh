@@ -70,6 +70,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // about `limit_ns` nanoseconds (counted in SM cycles) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
@@ -264,6 +278,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Marks this warp's arrival at named barrier `id` without waiting; the warps
+// that wait there with bar.sync are released once `count` threads have come.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch

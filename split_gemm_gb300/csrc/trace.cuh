@@ -23,7 +23,18 @@
     do {                                                                                        \
         if ((kp).trace && (cond)) (kp).trace[static_cast<size_t>(blockIdx.x) * 32 + (slot)] = (value); \
     } while (0)
+// Per-stage timeline of CTA 0 (stages < 256): role r of stage i at
+// trace[8192 + 4*i + r] (0 activation issue, 1 weight issue, 2 data landed
+// (waiter), 3 MMA start).
+#define SGB_STAGE_MARK(kp, i, r)                                                                \
+    do {                                                                                        \
+        if ((kp).trace && blockIdx.x == 0 && (i) < 256)                                        \
+            (kp).trace[8192 + 4 * static_cast<size_t>(i) + (r)] = ::sgb::ptx::globaltimer();    \
+    } while (0)
 #else
+#define SGB_STAGE_MARK(kp, i, r) \
+    do {                         \
+    } while (0)
 #define SGB_TRACE(kp, cond, slot) \
     do {                          \
     } while (0)
