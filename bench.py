@@ -501,7 +501,7 @@ def parse_args(argv=None):
     ap.add_argument("--splits", type=int, default=0, help="force the split-K factor")
     ap.add_argument("--reduction", type=int, default=0,
                     help="force the in-place reduction of cut tiles (1 ordered, 2 concurrent)")
-    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box)")
+    ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box, 7 halo)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
     args = ap.parse_args(argv)

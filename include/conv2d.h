@@ -81,10 +81,17 @@ typedef enum {
     CONV2D_LOADER_ROW_WINDOW = 5, /* few channels: staged input rows read in place by the MMA as overlapping
                                      16-byte-pitch windows; needs dil_w == 1, stride_w in {1,2,4,8},
                                      C <= 8 / stride_w, K <= 256 (one tile of output channels), no split */
-    CONV2D_LOADER_TMA_BOX = 6     /* tiles are rectangles of output pixels; each tiled TMA box carries two
+    CONV2D_LOADER_TMA_BOX = 6,    /* tiles are rectangles of output pixels; each tiled TMA box carries two
                                      64-channel chunks of one filter tap (and a 3-D box two weight k-blocks);
                                      needs C % 128 == 0, strides <= 8, a rectangle whose pixel count is a
                                      multiple of 8, and block_n <= 128 with 256-pixel tiles */
+    CONV2D_LOADER_HALO = 7        /* stride 1 only: a tile is 128 consecutive pixels of an image seen with the
+                                     padded row pitch W + 2*pad_w (pixels past Q are computed and discarded);
+                                     per 64-channel chunk one tiled TMA box of whole padded input rows serves
+                                     every filter tap, which the MMA reads in place at the tap's row offset.
+                                     Needs C % 64 == 0, W + 2*pad_w <= 256, 128-pixel tiles, and the two halo
+                                     buffers plus the weight ring within shared memory (block_n is narrowed
+                                     to fit unless forced) */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".

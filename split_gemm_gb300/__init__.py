@@ -21,7 +21,7 @@ from . import _build
 
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
-    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "REDUCTION_AUTO", "REDUCTION_ORDERED",
+    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "REDUCTION_AUTO", "REDUCTION_ORDERED",
     "REDUCTION_CONCURRENT",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
@@ -30,6 +30,7 @@ __all__ = [
 
 LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR, LOADER_HYBRID, LOADER_ROW_WINDOW = 0, 1, 2, 3, 4, 5
 LOADER_TMA_BOX = 6
+LOADER_HALO = 7
 REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
 DEBUG_SKIP_SIGNAL = 1
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",

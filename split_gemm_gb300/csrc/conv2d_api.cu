@@ -292,6 +292,49 @@ bool rowwin_config(const Shape& s, int bn_force, RowWinCfg* o)
 }
 
 // ------------------------------------------------------------------ heuristic
+// ------------------------------------------------------------------ halo loader (stride 1)
+// Each image is a grid of virtual pixels with the padded row pitch wv = W + 2*pw;
+// a tile is 128 consecutive virtual pixels of one image and, per 64-channel
+// chunk, one tiled TMA box of hr whole padded input rows holds every filter
+// tap's operand (the kernel header describes the layout).
+struct HaloGeom {
+    int wv, vp, tpi, hr, halo_bytes;
+    int64_t m_tiles;
+};
+
+// Halo geometry for output-channel tile width bn, or false when the shape does
+// not allow the halo loader: stride 1, C % 64 == 0, a padded row of at most 256
+// pixels (a TMA box dimension), and the ring plus two halo buffers within the
+// per-block shared memory.
+bool halo_geometry(const Shape& s, int bn, HaloGeom* g)
+{
+    if (s.sh != 1 || s.sw != 1 || s.c % BK != 0) return false;
+    const int64_t wv = s.w + 2 * s.pw;
+    if (wv > 256 || s.p < 1) return false;
+    const int64_t vp = s.p * wv;
+    // Highest halo row any tap of any tile reads: the tile may start up to wv - 1
+    // pixels into its first padded row.
+    const int64_t max_row = (wv - 1) + (s.r - 1) * s.dh * wv + (s.s - 1) * s.dw + (kMinTileM - 1);
+    const int64_t hr = max_row / wv + 1;
+    if (hr > 256) return false;
+    const int64_t halo_bytes = (hr * wv * 128 + 1023) / 1024 * 1024;
+    int fixed;
+    if (bn == 64) fixed = sgb::conv2d_tc_smem_bytes<128, 64, sgb::LOADER_HALO>(0);
+    else if (bn == 128) fixed = sgb::conv2d_tc_smem_bytes<128, 128, sgb::LOADER_HALO>(0);
+    else if (bn == 256) fixed = sgb::conv2d_tc_smem_bytes<128, 256, sgb::LOADER_HALO>(0);
+    else return false;
+    if (fixed + 2 * halo_bytes > sgb::kMaxSmemBytes) return false;
+    const int64_t tpi = cdiv(vp, kMinTileM);
+    if (s.n * tpi > 2147483647ll / 1024) return false;
+    g->wv = static_cast<int>(wv);
+    g->vp = static_cast<int>(vp);
+    g->tpi = static_cast<int>(tpi);
+    g->hr = static_cast<int>(hr);
+    g->halo_bytes = static_cast<int>(halo_bytes);
+    g->m_tiles = s.n * tpi;
+    return true;
+}
+
 struct Plan {
     int block_m;
     int block_n;
@@ -301,6 +344,7 @@ struct Plan {
     int grid;         // CTAs launched
     long long units;  // (tile, stage) work units
     BoxGeom box;      // box loader only
+    HaloGeom halo;    // halo loader only
 };
 
 // Semaphores the workspace holds: one per tile of the smallest tiles any plan
@@ -311,6 +355,8 @@ int64_t semaphore_capacity(const Shape& s)
     int64_t m_tiles = cdiv(s.m, kMinTileM);
     BoxGeom g;
     if (box_geometry(s, 128, &g) && g.m_tiles > m_tiles) m_tiles = g.m_tiles;
+    HaloGeom h;
+    if (halo_geometry(s, 64, &h) && h.m_tiles > m_tiles) m_tiles = h.m_tiles;
     return m_tiles * cdiv(s.k, 64);
 }
 
@@ -325,6 +371,10 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     int loader = force ? force->loader : 0;
     RowWinCfg rw;
     if (loader == CONV2D_LOADER_AUTO) {
+        // The halo loader (CONV2D_LOADER_HALO) moves fewer bytes and issues fewer
+        // TMA operations, but measured slower than the im2col loader on every
+        // stride-1 benchmark shape (its per-stage weight loads see a longer ring
+        // round trip), so the heuristic does not pick it; callers may force it.
         if (tma_im2col_eligible(s)) loader = CONV2D_LOADER_TMA_IM2COL;
         else if (s.c % 8 == 0) loader = CONV2D_LOADER_CPASYNC;
         else if (rowwin_config(s, force ? force->block_n : 0, &rw)) loader = CONV2D_LOADER_ROW_WINDOW;
@@ -340,6 +390,9 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     } else if (loader == CONV2D_LOADER_TMA_BOX) {
         BoxGeom g;
         if (!box_geometry(s, 128, &g) && !box_geometry(s, 256, &g)) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader == CONV2D_LOADER_HALO) {
+        HaloGeom g;
+        if (!halo_geometry(s, 64, &g)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
@@ -383,7 +436,11 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         return CONV2D_ERR_UNSUPPORTED;
     BoxGeom geom{};
     if (loader == CONV2D_LOADER_TMA_BOX && !box_geometry(s, bm, &geom)) return CONV2D_ERR_UNSUPPORTED;
-    const int64_t m_tiles = loader == CONV2D_LOADER_TMA_BOX ? geom.m_tiles : cdiv(s.m, bm);
+    HaloGeom hgeom{};
+    if (loader == CONV2D_LOADER_HALO && !halo_geometry(s, 64, &hgeom)) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t m_tiles = loader == CONV2D_LOADER_TMA_BOX ? geom.m_tiles
+                            : loader == CONV2D_LOADER_HALO  ? hgeom.m_tiles
+                                                            : cdiv(s.m, bm);
     const int64_t num_kb = loader == CONV2D_LOADER_TMA_BOX ? s.crs / (kBoxChunks * BK) : cdiv(s.crs, BK);
     const int64_t forced_splits = force ? force->splits : 0;
     const int64_t forced_grid = force ? force->grid : 0;
@@ -403,6 +460,13 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     }
     if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
     if (loader == CONV2D_LOADER_TMA_BOX && bm == 256 && bn > 128) return CONV2D_ERR_UNSUPPORTED;
+    if (loader == CONV2D_LOADER_HALO) {
+        // The widest tile whose ring and halo buffers fit the shared memory.
+        while (!halo_geometry(s, bn, &hgeom)) {
+            if (bn == 64 || (force && force->block_n)) return CONV2D_ERR_UNSUPPORTED;
+            bn /= 2;
+        }
+    }
     const int64_t n_tiles = cdiv(s.k, bn);
     const int64_t tiles = m_tiles * n_tiles;
     const int64_t units = tiles * num_kb;
@@ -436,6 +500,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     if (((units % grid) != 0 || (units / grid) % num_kb != 0) && tiles > semaphore_capacity(s))
         return CONV2D_ERR_UNSUPPORTED;
     plan->box = geom;
+    plan->halo = hgeom;
     plan->block_m = bm;
     plan->block_n = bn;
     plan->splits = static_cast<int>(splits);
@@ -473,6 +538,20 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
                                       strides, lower, upper, BK, static_cast<cuuint32_t>(plan.block_m), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    }
+    if (plan.loader == CONV2D_LOADER_HALO) {
+        // x as {C, W, H, N}; a box is one 64-channel chunk of hr whole padded
+        // rows (wv columns from -pad_w), landing pixel-major in 128-byte rows.
+        const HaloGeom& g = plan.halo;
+        const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                       (cuuint64_t)(s.h * s.w * s.c * 2)};
+        const cuuint32_t box[4] = {(cuuint32_t)BK, (cuuint32_t)g.wv, (cuuint32_t)g.hr, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult rc = g_encode_tiled(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     }
     if (plan.loader == CONV2D_LOADER_TMA_BOX) {
@@ -517,6 +596,13 @@ cudaError_t dispatch(int bm, int bn, int loader, const CUtensorMap& a, const CUt
                      const sgb::ConvKernelParams& kp, int grid, cudaStream_t st)
 {
     using namespace sgb;
+    if (loader == CONV2D_LOADER_HALO) {
+        if (bm != 128) return cudaErrorInvalidValue;
+        if (bn == 64) return launch_conv2d_tc<128, 64, LOADER_HALO>(a, b, kp, grid, st);
+        if (bn == 128) return launch_conv2d_tc<128, 128, LOADER_HALO>(a, b, kp, grid, st);
+        if (bn == 256) return launch_conv2d_tc<128, 256, LOADER_HALO>(a, b, kp, grid, st);
+        return cudaErrorInvalidValue;
+    }
     if (loader == CONV2D_LOADER_TMA_BOX) {
         if (bm == 256) {
             if (bn == 64) return launch_conv2d_tc<256, 64, LOADER_BOX>(a, b, kp, grid, st);
@@ -669,6 +755,12 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.px = plan.box.px;
     kp.q_blocks = plan.box.q_blocks;
     kp.p_blocks = plan.box.p_blocks;
+    kp.wv = plan.halo.wv;
+    kp.vp = plan.halo.vp;
+    kp.tpi = plan.halo.tpi;
+    kp.halo_rows = plan.halo.hr;
+    kp.halo_bytes = plan.loader == CONV2D_LOADER_HALO ? plan.halo.halo_bytes : 0;
+    kp.halo_tx = plan.halo.hr * plan.halo.wv * 128;
     kp.debug_flags = algo ? algo->debug_flags : 0;
     kp.reduce_concurrent = (algo && algo->reduction == CONV2D_REDUCTION_ORDERED) ? 0 : 1;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;

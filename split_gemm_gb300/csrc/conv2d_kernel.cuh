@@ -63,7 +63,9 @@
 //   warps 6..9  (cp.async and scalar loaders only) im2col gather into the ring;
 //   warp 10     stage waiter: waits for each stage's full barrier, releases the
 //               MMA warp by the stage's named barrier;
-//   warp 11     (TMA loaders) TMA producer of the weight tiles.
+//   warp 11     (TMA loaders) TMA producer of the weight tiles; with the halo
+//               loader warps 0, 11, 12 and 13 share the weight tiles by ring
+//               slot and warp 0 also loads the halos.
 // The ring replaces block-wide syncs between load and MMA (burn PR #2545's
 // sync-placement discussion; ROCm/rocMLIR PR #1511 "Double buffering
 // improvements" splits loads and MMAs into overlapping stages the same way).
@@ -95,8 +97,11 @@ constexpr int GATHER_THREADS = 128;
 constexpr int EPI_SLOT_BYTES = 32 * 32 * 4;  // one warp's 32 rows x 32 fp32 columns
 constexpr int EPI_SLOTS = 1;                 // staging slots per epilogue warp
 constexpr uint32_t STATUS_TIMEOUT = 6;  // same value as CONV2D_ERR_TIMEOUT
+constexpr int kMaxSmemBytes = 232448;   // opt-in dynamic shared memory per block (227 KB)
 
-enum LoaderKind : int { LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6 };
+enum LoaderKind : int {
+    LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6, LOADER_HALO = 7
+};
 
 // Which engine brings in the im2col tile of the CTA's k-block number `it`:
 // the TMA unit (im2col mode) or the gather warps (cp.async).  The hybrid
@@ -129,6 +134,11 @@ struct ConvKernelParams {
     // Box loader only: the tile rectangle (bn_img images x bh rows x bw columns,
     // px of its pixels) and the tile grid over (images, rows, columns).
     int bw, bh, bn_img, px, q_blocks, p_blocks;
+    // Halo loader only (stride 1): virtual row pitch wv = W + 2*pw, virtual
+    // pixels per image vp = P*wv, 128-pixel tiles per image tpi, halo rows hr
+    // and bytes per halo buffer (64 channels x wv x hr, 1024-B multiple).
+    int wv, vp, tpi, halo_rows, halo_bytes;
+    int halo_tx;  // bytes one halo box delivers: 128 * wv * halo_rows (halo_bytes rounds it up to 1024)
     int debug_flags;
     int reduce_concurrent;    // 1: later splits add concurrently after split 0; 0: strict turns
     unsigned long long wait_limit_ns;
@@ -145,23 +155,27 @@ struct TileConfig {
     static_assert(BM == 128 || BM == 256, "BM must be 128 or 256");
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
     static_assert(BM == 128 || LOADER == LOADER_TMA || LOADER == LOADER_BOX, "256-pixel tiles need a TMA loader");
+    static constexpr bool HALO = LOADER == LOADER_HALO;
     static constexpr int M_SUB = BM / MMA_M;  // 128-row MMA blocks per tile
     static constexpr int KC = LOADER == LOADER_BOX ? 2 : 1;  // k-blocks per pipeline stage
-    static constexpr int A_STAGE_BYTES = KC * BM * BK * 2;
+    // The halo loader keeps its activations in two halo buffers outside the ring.
+    static constexpr int A_STAGE_BYTES = HALO ? 0 : KC * BM * BK * 2;
     static constexpr int B_STAGE_BYTES = KC * BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int STAGES =
-        LOADER == LOADER_BOX ? (196608 / STAGE_BYTES > 8 ? 8 : 196608 / STAGE_BYTES)
+        HALO ? (BN == 64 ? 8 : 4)
+        : LOADER == LOADER_BOX ? (196608 / STAGE_BYTES > 8 ? 8 : 196608 / STAGE_BYTES)
         : BM == 128 ? (BN == 256 ? 4 : (BN == 128 ? 6 : 8)) : (BN == 256 ? 3 : 4);
     static_assert(STAGES >= 2, "the ring needs at least two stages");
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int BAR_BYTES = (2 * STAGES + 9) * 8 + 16;
     // With a TMA loader the gather warps' places go to the epilogue: 8 warps, two
     // per TMEM lane quadrant, each writing half of the tile's columns.
-    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 8 : 4;
+    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO) ? 8 : 4;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOTS * EPI_SLOT_BYTES;
+    // Without the halo loader's two halo buffers (2 * kp.halo_bytes, placed after the ring).
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
-    static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared-memory limit");
+    static_assert(SMEM_BYTES <= kMaxSmemBytes, "exceeds the per-block shared-memory limit");
     static constexpr int ACC_COLS = M_SUB * BN;                   // TMEM columns of one accumulator set
     static constexpr int NUM_ACC = 2 * ACC_COLS <= 512 ? 2 : 1;   // double-buffered when TMEM allows
     static constexpr uint32_t TMEM_COLS = NUM_ACC * ACC_COLS;
@@ -173,8 +187,12 @@ struct TileConfig {
     // thus has one issuer, loading its uses in order, and a slot's parity waits
     // never run more than one phase ahead of the MMA's releases.  (Gather
     // loaders: warp 0 issues the weight tiles.)
-    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX;
-    static constexpr int NPROD = TMA_A ? 2 : 1;
+    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO;
+    // The halo loader's only per-stage load is the weight tile: four threads
+    // (warps 0, 11, 12, 13) share them, ring slot s going to producer s % 4.
+    static constexpr int HALO_NB = 4;
+    static_assert(!HALO || (BM == 128 && STAGES % HALO_NB == 0), "halo loader: 128-pixel tiles, a ring of 4k slots");
+    static constexpr int NPROD = HALO ? HALO_NB : TMA_A ? 2 : 1;
     static_assert(STAGES <= 8, "one named barrier per stage: ids 2 .. 9");
     static constexpr int THREADS = (WAITER_WARP + NPROD) * 32;
 };
@@ -188,6 +206,9 @@ struct SmemView {
     uint64_t* acc_full;  // 2: accumulator ready for the epilogue
     uint64_t* acc_empty; // 2: accumulator drained by the epilogue
     uint64_t* mma_done;  // teardown drain of the MMA pipe
+    uint8_t* halo;          // halo loader: 2 halo buffers
+    uint64_t* halo_full;    // 2: halo landed
+    uint64_t* halo_empty;   // 2: halo no longer read by any MMA
     uint32_t* tmem_slot;
     volatile uint32_t* abort_flag;
     volatile uint32_t* epi_go;  // epilogue decision, written by one thread between two barriers
@@ -266,13 +287,54 @@ __device__ __forceinline__ void box_origin(const ConvKernelParams& kp, int m_til
     q0 = qb * kp.bw;
 }
 
+// Halo loader.  Each image is seen as a grid of virtual pixels with the
+// padded row pitch wv = W + 2*pw (stride 1): virtual pixel j = p*wv + v of an
+// image is output pixel (p, v) when v < Q, and the input value of filter tap
+// (r, s) for it sits at padded linear index j + r*dh*wv + s*dw, on padded row
+// (j + r*dh*wv + s*dw) / wv.  A tile is 128 consecutive virtual pixels of one
+// image, so for each 64-channel chunk one tiled TMA box of whole padded input
+// rows (zero fill outside the image gives the padding) holds every tap's A
+// operand: tap (r, s) is the 128 rows starting r*dh*wv + s*dw rows further on.
+// The reduction runs chunk-major, then over the R*S taps.
+__device__ __forceinline__ void halo_kb(const ConvKernelParams& kp, int kb, int& chunk, int& tap)
+{
+    const int rs = kp.R * kp.S;
+    chunk = kb / rs;
+    tap = kb - chunk * rs;
+}
+
+// A halo use starts at a chunk's first tap or a segment's first stage, and
+// ends at the chunk's last tap or the segment's last stage.
+__device__ __forceinline__ bool halo_starts(const Segment& sg, int kb, int tap) { return kb == sg.kb_begin || tap == 0; }
+__device__ __forceinline__ bool halo_ends(const ConvKernelParams& kp, const Segment& sg, int kb, int tap)
+{
+    return kb + 1 == sg.kb_end || tap + 1 == kp.R * kp.S;
+}
+
+// Image, first virtual pixel and first padded input row of tile row-block m_tile.
+__device__ __forceinline__ void halo_origin(const ConvKernelParams& kp, int m_tile, int& n_img, int& j0, int& prow0)
+{
+    n_img = m_tile / kp.tpi;
+    j0 = (m_tile - n_img * kp.tpi) * MMA_M;
+    prow0 = j0 / kp.wv;
+}
+
 // GEMM row (output pixel index) of row `row` of tile row-block m_tile, or -1
 // when the row lies past the output.  (n0, p0, q0) is the box origin (box
 // loader only).
 template <int BM, int LOADER>
 __device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile, int row, int n0, int p0, int q0)
 {
-    if constexpr (LOADER == LOADER_BOX) {
+    if constexpr (LOADER == LOADER_HALO) {
+        (void)n0; (void)p0; (void)q0;
+        const int n = m_tile / kp.tpi;
+        const int j = (m_tile - n * kp.tpi) * MMA_M + row;
+        if (j >= kp.vp) return -1;
+        const int p = j / kp.wv;
+        const int q = j - p * kp.wv;
+        if (q >= kp.Q) return -1;
+        return (n * kp.P + p) * kp.Q + q;
+    } else if constexpr (LOADER == LOADER_BOX) {
         if (row >= kp.px) return -1;
         const int q = q0 + row % kp.bw;
         const int t = row / kp.bw;
@@ -367,6 +429,19 @@ __device__ void prefetch_first_stages(const CUtensorMap* tm_a, const CUtensorMap
     SegmentWalker walk(kp);
     Segment sg;
     if (!walk.next(kp, sg)) return;
+    if constexpr (LOADER == LOADER_HALO) {
+        const int m_tile = sg.tile / kp.n_tiles;
+        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int n_img, j0, prow0, chunk, tap;
+        halo_origin(kp, m_tile, n_img, j0, prow0);
+        halo_kb(kp, sg.kb_begin, chunk, tap);
+        ptx::tma_prefetch_4d(tm_a, chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
+        for (int kb = sg.kb_begin; kb < sg.kb_end && kb < sg.kb_begin + TileConfig<BM, BN, LOADER>::STAGES; ++kb) {
+            halo_kb(kp, kb, chunk, tap);
+            ptx::tma_prefetch_2d(tm_b, tap * kp.C + chunk * BK, n0);
+        }
+        return;
+    }
     LoadCursor<BM, BN, LOADER> cur(kp, sg);
     for (int i = 0; i < TileConfig<BM, BN, LOADER>::STAGES && cur.kb < sg.kb_end; ++i) {
         cur.prefetch(tm_a, tm_b, kp);
@@ -427,6 +502,66 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
         ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
 }
 
+// ---------------------------------------------------------------- halo producers (warps 0, 11, 12, 13)
+// Producer `role` loads the weight tiles of the ring slots s % HALO_NB == role;
+// role 0 (warp 0) also issues the halo of each (segment, chunk).  Each ring
+// slot and each halo buffer thus has one issuer, loading its uses in order.
+template <int BM, int BN, int LOADER>
+__device__ void run_halo_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
+                                  const SmemView& sm, int role)
+{
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int NB = Cfg::HALO_NB;
+    int it = 0;  // stages walked (all segments)
+    int h = 0;   // halo uses issued (role 0)
+    bool ok = true;
+    SegmentWalker walk(kp);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        const int m_tile = sg.tile / kp.n_tiles;
+        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int n_img, j0, prow0;
+        halo_origin(kp, m_tile, n_img, j0, prow0);
+        for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
+            int chunk, tap;
+            halo_kb(kp, kb, chunk, tap);
+            if (*sm.abort_flag) { ok = false; break; }
+            if (role == 0 && halo_starts(sg, kb, tap)) {
+                const int slot = h & 1;
+                if (!ptx::mbar_wait(&sm.halo_empty[slot], (static_cast<uint32_t>(h >> 1) & 1u) ^ 1u,
+                                    kp.wait_limit_ns)) {
+                    record_timeout(kp, sm.abort_flag);
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(&sm.halo_full[slot], static_cast<uint32_t>(kp.halo_tx));
+                ptx::tma_load_4d(sm.halo + slot * kp.halo_bytes, tm_a, &sm.halo_full[slot], chunk * BK, -kp.pw,
+                                 prow0 - kp.ph, n_img);
+                SGB_STAGE_MARK(kp, it, 0);
+                ++h;
+            }
+            const int stage = it % STAGES;
+            if (stage % NB != role) continue;
+            if (!ptx::mbar_wait(&sm.empty[stage], (static_cast<uint32_t>(it / STAGES) & 1u) ^ 1u, kp.wait_limit_ns)) {
+                record_timeout(kp, sm.abort_flag);
+                ok = false;
+                break;
+            }
+            ptx::mbar_arrive_expect_tx(&sm.full[stage], Cfg::B_STAGE_BYTES);
+            ptx::tma_load_2d(sm.b + stage * Cfg::B_STAGE_BYTES, tm_b, &sm.full[stage], tap * kp.C + chunk * BK, n0);
+            SGB_STAGE_MARK(kp, it, 1);
+        }
+    }
+    // Drain: this thread's last halo of each buffer and last load of each of its slots must have landed.
+    if (role == 0)
+        for (int i = h > 2 ? h - 2 : 0; i < h; ++i)
+            ptx::mbar_wait(&sm.halo_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, kp.wait_limit_ns);
+    for (int i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+        if ((i % STAGES) % NB == role)
+            ptx::mbar_wait(&sm.full[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
+}
+
 // ---------------------------------------------------------------- stage waiter (warp 10)
 // Waits (bounded) for each ring stage's data in the MMA's order and releases
 // the MMA warp through the stage's named barrier.  The MMA warp never touches
@@ -451,6 +586,7 @@ __device__ void run_stage_waiter(const ConvKernelParams& kp, const SmemView& sm)
     const int lane = threadIdx.x & 31;
     bool waiting = true;
     int it = 0;
+    int h = 0;  // halo uses (halo loader)
     uint64_t full_cycles = 0;
     (void)full_cycles;
     SegmentWalker walk(kp);
@@ -459,6 +595,18 @@ __device__ void run_stage_waiter(const ConvKernelParams& kp, const SmemView& sm)
         for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
             const int stage = it % STAGES;
             const uint32_t use = static_cast<uint32_t>(it / STAGES);
+            if constexpr (Cfg::HALO) {
+                int chunk, tap;
+                halo_kb(kp, kb, chunk, tap);
+                if (halo_starts(sg, kb, tap)) {
+                    if (lane == 0 && waiting &&
+                        !ptx::mbar_wait(&sm.halo_full[h & 1], static_cast<uint32_t>(h >> 1) & 1u, kp.wait_limit_ns)) {
+                        record_timeout(kp, sm.abort_flag);
+                        waiting = false;
+                    }
+                    ++h;
+                }
+            }
             if (lane == 0) {
                 SGB_CYCLES_BEGIN(tf);
                 if (waiting && (*sm.abort_flag || !ptx::mbar_wait(&sm.full[stage], use & 1u, kp.wait_limit_ns))) {
@@ -493,6 +641,8 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
     const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
     const uint32_t a_chunk16 = LOADER == LOADER_BOX ? static_cast<uint32_t>(kp.px * 8) : 0u;
+    const uint64_t halo_desc0 = Cfg::HALO ? ptx::sw128_kmajor_desc(ptx::smem_addr(sm.halo)) : 0ull;
+    int h = 0;  // halo uses (halo loader)
     int it = 0, seg_idx = 0;
     bool issue = true;  // false once a wait has run out: keep pace with the waiter, issue nothing
     uint64_t acc_cycles = 0;
@@ -514,8 +664,35 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
         __syncwarp();
         ptx::tc_fence_after();
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * Cfg::ACC_COLS);
+        // Halo loader: buffer row of the tile's first virtual pixel, and the
+        // filter tap (tap = r*S + fs) of the stage, stepped without divisions.
+        int a_row0 = 0, tap = 0, fr = 0, fs = 0;
+        if constexpr (Cfg::HALO) {
+            int n_img, j0, prow0, chunk;
+            halo_origin(kp, sg.tile / kp.n_tiles, n_img, j0, prow0);
+            a_row0 = j0 - prow0 * kp.wv;
+            halo_kb(kp, sg.kb_begin, chunk, tap);
+            fr = tap / kp.S;
+            fs = tap - fr * kp.S;
+        }
         for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
             const int stage = it % STAGES;
+            int halo_slot = 0;
+            bool halo_last = false;
+            uint64_t halo_ad = 0;
+            if constexpr (Cfg::HALO) {
+                if (kb == sg.kb_begin || tap == 0) ++h;
+                halo_slot = (h - 1) & 1;
+                halo_last = kb + 1 == sg.kb_end || tap + 1 == kp.R * kp.S;
+                const int a_row = a_row0 + fr * kp.dh * kp.wv + fs * kp.dw;
+                halo_ad = halo_desc0 + static_cast<uint64_t>((halo_slot * kp.halo_bytes + a_row * 128) >> 4);
+                ++tap;
+                if (++fs == kp.S) {
+                    fs = 0;
+                    ++fr;
+                }
+                if (tap == kp.R * kp.S) tap = fr = 0;
+            }
             ptx::named_bar_sync(STAGE_BAR0 + stage, 64);
             ptx::tc_fence_after();
             if (lane == 0) SGB_STAGE_MARK(kp, it, 3);
@@ -528,7 +705,8 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
                 // descriptor itself; advancing along K inside a 128-B swizzled row
                 // moves the start address by 32 B.  A stage with KC k-blocks holds
                 // them as KC chunks, a_chunk16 apart (in 16-B units).
-                const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
+                const uint64_t ad =
+                    Cfg::HALO ? halo_ad : a_desc0 + static_cast<uint64_t>((stage * A_STAGE_BYTES) >> 4);
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
                 constexpr int KSTEPS = Cfg::KC * BK / UMMA_K;
                 const uint32_t acc0 = kb > sg.kb_begin ? 1u : 0u;
@@ -544,7 +722,10 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
                                       bdk, IDESC, k > 0 ? 1u : acc0);
                 }
             }
-            if (lane == 0) ptx::mma_commit(&sm.empty[stage]);  // every stage, issuing or not
+            if (lane == 0) {
+                ptx::mma_commit(&sm.empty[stage]);  // every stage, issuing or not
+                if (Cfg::HALO && halo_last) ptx::mma_commit(&sm.halo_empty[halo_slot]);
+            }
             __syncwarp();
         }
         if (lane == 0) ptx::mma_commit(&sm.acc_full[buf]);  // also when not issuing: the epilogue must not wait out
@@ -1006,13 +1187,17 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     SmemView sm;
     sm.a = smem;
     sm.b = smem + Cfg::STAGES * Cfg::A_STAGE_BYTES;
-    sm.epi = smem + Cfg::RING_BYTES;
-    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + Cfg::EPI_BYTES);
+    sm.halo = smem + Cfg::RING_BYTES;  // halo loader: 2 buffers of kp.halo_bytes (1024-B multiples)
+    const int halo_total = Cfg::HALO ? 2 * kp.halo_bytes : 0;
+    sm.epi = smem + Cfg::RING_BYTES + halo_total;
+    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING_BYTES + halo_total + Cfg::EPI_BYTES);
     sm.empty = sm.full + Cfg::STAGES;
     sm.acc_full = sm.empty + Cfg::STAGES;
     sm.acc_empty = sm.acc_full + 2;
     sm.mma_done = sm.acc_empty + 2;
-    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
+    sm.halo_full = sm.mma_done + 1;
+    sm.halo_empty = sm.halo_full + 2;
+    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.halo_empty + 2);
     sm.abort_flag = sm.tmem_slot + 1;
     sm.epi_go = sm.tmem_slot + 2;
 
@@ -1024,8 +1209,10 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         // TMA producer: one arrive (with the byte count); cp.async gather: one
         // arrive per thread (issued by its copies); scalar gather: one per warp.
         constexpr uint32_t GATHER_WARPS = GATHER_THREADS / 32;
+        // Halo loader: one arrive (the weight tile's producer).
         const uint32_t full_count =
-            (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 2u  // the activation and the weight producer
+            Cfg::HALO ? 1u
+            : (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 2u  // the activation and the weight producer
                                                            : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
         for (int i = 0; i < Cfg::STAGES; ++i) {
             ptx::mbar_init(&sm.full[i], full_count);
@@ -1036,14 +1223,18 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
             ptx::mbar_init(&sm.acc_empty[i], Cfg::EPI_WARPS * 32);
         }
         ptx::mbar_init(sm.mma_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sm.halo_full[i], 1);
+            ptx::mbar_init(&sm.halo_empty[i], 1);
+        }
         *sm.abort_flag = 0u;
         *sm.epi_go = 0u;
         ptx::mbar_init_fence();
     }
     if (warp == 0 && lane == 0) {
-        if (LOADER == LOADER_TMA || LOADER == LOADER_HYBRID || LOADER == LOADER_BOX) ptx::prefetch_tensormap(&tm_a);
+        if (Cfg::TMA_A || LOADER == LOADER_HYBRID) ptx::prefetch_tensormap(&tm_a);
         if (LOADER != LOADER_SCALAR) ptx::prefetch_tensormap(&tm_b);
-        if constexpr (LOADER == LOADER_TMA || LOADER == LOADER_BOX) prefetch_first_stages<BM, BN, LOADER>(&tm_a, &tm_b, kp);
+        if constexpr (Cfg::TMA_A) prefetch_first_stages<BM, BN, LOADER>(&tm_a, &tm_b, kp);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sm.tmem_slot, Cfg::TMEM_COLS);
@@ -1063,7 +1254,9 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
-        if constexpr (Cfg::TMA_A) {
+        if constexpr (Cfg::HALO) {
+            if (lane == 0) run_halo_producer<BM, BN, LOADER>(&tm_a, &tm_b, kp, sm, 0);
+        } else if constexpr (Cfg::TMA_A) {
             if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_A>(&tm_a, &tm_b, kp, sm);
         } else if constexpr (LOADER != LOADER_SCALAR) {
             if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_AB>(&tm_a, &tm_b, kp, sm);
@@ -1075,8 +1268,11 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     } else if (warp == WAITER_WARP) {
         run_stage_waiter<BM, BN, LOADER>(kp, sm);
     } else if (warp > WAITER_WARP) {
-        if constexpr (Cfg::TMA_A)  // warp 11: the weight tiles
+        if constexpr (Cfg::HALO) {  // warps 11 .. 13: weight tiles of ring slots 1 .. 3 (mod 4)
+            if (lane == 0) run_halo_producer<BM, BN, LOADER>(&tm_a, &tm_b, kp, sm, warp - WAITER_WARP);
+        } else if constexpr (Cfg::TMA_A) {  // warp 11: the weight tiles
             if (lane == 0) run_tma_producer<BM, BN, LOADER, PROD_B>(&tm_a, &tm_b, kp, sm);
+        }
     } else {
         if constexpr (LOADER == LOADER_CPASYNC || LOADER == LOADER_HYBRID) run_gather_cpasync<BM, BN, LOADER>(kp, sm);
         if constexpr (LOADER == LOADER_SCALAR) run_gather_scalar<BM, BN, LOADER>(kp, sm);
@@ -1103,6 +1299,15 @@ inline bool pdl_enabled()
     return on;
 }
 
+// Dynamic shared memory of one CTA: the configuration's fixed part plus, for
+// the halo loader, its two halo buffers.
+template <int BM, int BN, int LOADER>
+inline int conv2d_tc_smem_bytes(int halo_bytes)
+{
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    return Cfg::SMEM_BYTES + (Cfg::HALO ? 2 * halo_bytes : 0);
+}
+
 // Host-side launcher for one instantiation; explicitly instantiated in one
 // translation unit per tile width so that the variants compile in parallel.
 template <int BM, int BN, int LOADER>
@@ -1110,6 +1315,8 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
                              cudaStream_t stream)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
+    const int smem_bytes = conv2d_tc_smem_bytes<BM, BN, LOADER>(kp.halo_bytes);
+    if (smem_bytes > kMaxSmemBytes) return cudaErrorInvalidValue;
     auto kern = conv2d_fwd_tc_kernel<BM, BN, LOADER>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -1118,7 +1325,8 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     static unsigned long long configured = 0ull;
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
     if (!bit || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Cfg::HALO ? kMaxSmemBytes : Cfg::SMEM_BYTES);
         if (err != cudaSuccess) return err;
         if (bit) __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
     }
@@ -1128,7 +1336,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(Cfg::THREADS);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1142,7 +1350,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     cudaError_t launch_conv2d_tc<BM_, BN_, L_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, \
                                                int, cudaStream_t)
 
-// Every loader with 128-pixel tiles, the TMA loader with 256-pixel tiles, and
+// Every loader with 128-pixel tiles (the halo loader's only size), the TMA loader with 256-pixel tiles, and
 // the box loader with 256-pixel tiles where two k-blocks of both operands fit
 // a stage twice (BN <= 128).
 #define SGB_INSTANTIATE_CONV2D(BN_)                    \
@@ -1151,6 +1359,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
     template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_INSTANTIATE_CONV2D_BOX256(BN_) template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 
@@ -1161,6 +1370,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_SCALAR);  \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
     extern template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_DECLARE_CONV2D_BOX256(BN_) extern template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 

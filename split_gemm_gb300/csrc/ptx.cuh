@@ -125,6 +125,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, uint64_t* bar, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_5d(void* dst, const void* map, uint64_t* bar, int32_t c0, int32_t c1,
                                             int32_t c2, int32_t c3, int32_t c4)
 {
@@ -148,6 +158,13 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t c0, int
 {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const void* map, int32_t c0, int32_t c1, int32_t c2, int32_t c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                  : "memory");
 }
 

@@ -61,8 +61,10 @@ def test_invalid_params_rejected(kw, code):
 
 def test_workspace_and_staging_sizes():
     p = _params()
-    # status block + one semaphore per 128 x 64 tile
-    assert sg.workspace_bytes(p) == 256 + 98 * 1 * 4
+    # status block + one semaphore per 128 x 64 tile of the finest tiling any loader can be forced to
+    # use: the halo loader's 128-pixel tiles of each image seen with the padded row pitch 58 (26 per
+    # image, 4 images)
+    assert sg.workspace_bytes(p) == 256 + 4 * 26 * 1 * 4
     assert sg.host_staging_bytes(p) >= (4 * 56 * 56 * 64 * 2 + 64 * 576 * 2 + 12544 * 64 * 4)
 
 
