@@ -150,10 +150,12 @@ struct BoxGeom {
 };
 
 // Rectangle of at most bm output pixels for the box loader, or false when the
-// shape does not allow one: the chunks of a box must stay 1024-byte aligned in
-// shared memory (px % 8 == 0), a box spans at most 256 elements per dimension
+// shape does not allow one: a box spans at most 256 elements per dimension
 // (bw * stride_w, bh * stride_h), the traversal strides are at most 8, and two
-// 64-channel chunks must divide C.
+// 64-channel chunks must divide C.  The pixel count px needs no rounding: the
+// second chunk of a box lands px 128-byte rows after the first, and the
+// 128-byte swizzle of both the TMA write and the MMA read follows absolute
+// shared-memory addresses, so a chunk may start at any row.
 bool box_geometry(const Shape& s, int bm, BoxGeom* g)
 {
     if (s.c % (kBoxChunks * BK) != 0 || s.sw > 8 || s.sh > 8) return false;
@@ -166,26 +168,22 @@ bool box_geometry(const Shape& s, int bm, BoxGeom* g)
         bw = (cdiv(s.q, qb) + 7) / 8 * 8;
         if (bw > cap) bw = cap / 8 * 8;
     } else if (s.p * s.q > bm) {
-        // Whole rows: as many as fit, balanced over the row blocks, with a pixel count that is a multiple of 8.
+        // Whole rows: as many as fit, balanced over the row blocks.
         bw = s.q;
         int64_t rows = bm / s.q;
         if (rows > hmax) rows = hmax;
         const int64_t pb = cdiv(s.p, rows);
         bh = cdiv(s.p, pb);
-        while (bh > 1 && (bw * bh) % 8 != 0) --bh;
-        if ((bw * bh) % 8 != 0) bh = rows;
-        while (bh > 1 && (bw * bh) % 8 != 0) --bh;
     } else {
         // Whole images.
         bw = s.q;
         bh = s.p;
         bn = bm / (s.p * s.q);
         if (bn > s.n) bn = s.n;
-        while (bn > 1 && (bw * bh * bn) % 8 != 0) --bn;
     }
     if (bw < 1 || bh < 1 || bn < 1) return false;
     const int64_t px = bw * bh * bn;
-    if (px % 8 != 0 || px > bm || bw > wmax || bh > hmax) return false;
+    if (px > bm || bw > wmax || bh > hmax) return false;
     g->bw = static_cast<int>(bw);
     g->bh = static_cast<int>(bh);
     g->bn_img = static_cast<int>(bn);

@@ -43,9 +43,10 @@
 // image gives the padding).  One box brings KC = 2 consecutive 64-channel
 // chunks, and one 3-D box of the weight viewed as {64, K, C*R*S/64} brings the
 // matching two k-blocks of B, so a pipeline stage holds two k-blocks.  Chunk j
-// of A lands px rows after chunk j-1 (px is a multiple of 8, keeping the
-// 128-byte swizzle atoms aligned); the MMA reads 128 rows from each chunk start
-// and the rows past px are ignored by the epilogue.
+// of A lands px rows after chunk j-1 (any px: the 128-byte swizzle of the TMA
+// write and of the MMA read follows absolute shared-memory addresses); the MMA
+// reads 128 rows from each chunk start and the rows past px are ignored by the
+// epilogue.
 //
 // Warp roles:
 //   warp 0      TMA producer (one thread): the im2col activation tiles

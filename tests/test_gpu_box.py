@@ -74,6 +74,15 @@ def test_box_geometries(sg, geom):
     _check(sg, wl, x, w, b, make_algo(sg, loader=BOX, wait_limit_ns=WAIT), wl.describe())
 
 
+@pytest.mark.parametrize("bm", [128, 256])
+def test_box_pixel_count_not_a_multiple_of_8(sg, bm):
+    # 7 x 7 images: boxes of 2 (bm 128) or 5 (bm 256) whole images hold 98 or 245 pixels, so the
+    # second channel chunk of every box starts mid-way through a 1024-byte swizzle atom.
+    wl, x, w, b = _case(6, 7, 7, 256, 128, 3, 3, pad=1, seed=20)
+    _check(sg, wl, x, w, b, make_algo(sg, loader=BOX, block_m=bm, block_n=128, wait_limit_ns=WAIT),
+           f"box 7x7 BM={bm}")
+
+
 @pytest.mark.parametrize("reduction", [1, 2])
 @pytest.mark.parametrize("splits", [2, 3])
 def test_box_split_k(sg, splits, reduction):
