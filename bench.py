@@ -55,7 +55,7 @@ def shape_of(wl):
 
 def flops_per_step(wl):
     p, q = shape_of(wl)
-    return 2.0 * wl.n * p * q * wl.k * wl.c * wl.r * wl.s
+    return 2.0 * wl.n * p * q * wl.k * (wl.c // wl.groups) * wl.r * wl.s
 
 
 def _touched(extent_in, extent_out, stride, pad, dil, ker):
@@ -74,7 +74,7 @@ def algorithmic_bytes(wl):
     th = _touched(wl.h, p, wl.stride_h, wl.pad_h, wl.dil_h, wl.r)
     tw = _touched(wl.w, q, wl.stride_w, wl.pad_w, wl.dil_w, wl.s)
     x_b = wl.n * th * tw * wl.c * 2
-    w_b = wl.k * wl.r * wl.s * wl.c * 2
+    w_b = wl.k * wl.r * wl.s * (wl.c // wl.groups) * 2
     y_b = wl.n * p * q * wl.k * 4
     b_b = wl.k * 4 if wl.bias is not None else 0
     return float(x_b + w_b + y_b + b_b)
@@ -266,9 +266,9 @@ class OracleSampler:
         ki = rng.integers(0, wl.k, size=npts)
         t0 = time.perf_counter()
         oracle.conv2d_fwd_points_f64(self.xd, self.wd, self.b, self.opts["stride"], self.opts["padding"],
-                                     self.opts["dilation"], mi, ki, lib=self.lib)
+                                     self.opts["dilation"], mi, ki, lib=self.lib, groups=self.opts["groups"])
         done = time.perf_counter() - t0
-        flops = 2.0 * wl.c * wl.r * wl.s * npts
+        flops = 2.0 * (wl.c // wl.groups) * wl.r * wl.s * npts
         return flops / done / 1e12, 1, f"{npts} random output elements, 1 thread", done
 
 

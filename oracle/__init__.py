@@ -119,16 +119,19 @@ def _bias_f32(b) -> Optional[np.ndarray]:
     return np.ascontiguousarray(b.detach().cpu().to(dtype=__import__("torch").float32).numpy())
 
 
-def _dims_opts(xshape, wshape, stride, padding, dilation):
+def _dims_opts(xshape, wshape, stride, padding, dilation, groups=1):
     n, h, w, c = (int(v) for v in xshape)
-    k, r, s, c2 = (int(v) for v in wshape)
-    if c2 != c:
-        raise ValueError(f"channel mismatch: input C={c}, weight C={c2}")
+    k, r, s, cg = (int(v) for v in wshape)
+    groups = int(groups)
+    if groups < 1 or c % groups or k % groups:
+        raise ValueError(f"groups={groups} must divide C={c} and K={k}")
+    if cg * groups != c:
+        raise ValueError(f"channel mismatch: input C={c}, weight C/groups={cg}, groups={groups}")
     sh, sw = _pair(stride)
     ph, pw = _pair(padding)
     dh, dw = _pair(dilation)
     dims = (ctypes.c_int64 * 7)(n, h, w, c, k, r, s)
-    opts = (ctypes.c_int64 * 6)(sh, sw, ph, pw, dh, dw)
+    opts = (ctypes.c_int64 * 7)(sh, sw, ph, pw, dh, dw, groups)
     return (n, h, w, c, k, r, s), (sh, sw, ph, pw, dh, dw), dims, opts
 
 
@@ -137,10 +140,10 @@ def _ptr(a: Optional[np.ndarray]):
 
 
 def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, threads: Optional[int] = None,
-               lib=None) -> np.ndarray:
+               lib=None, groups=1) -> np.ndarray:
     """Direct convolution over bf16 inputs in fp64.
 
-    x: [N,H,W,C] bf16 (torch tensor or uint16 bit array); w: [K,R,S,C] bf16;
+    x: [N,H,W,C] bf16 (torch tensor or uint16 bit array); w: [K,R,S,C/groups] bf16;
     bias: [K] fp32 or None.  Returns y: [N,P,Q,K] float64 (NHWC).
     """
     lib = lib or load()
@@ -148,7 +151,7 @@ def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, threads: Option
     ws = _bf16_bits(w)
     b = _bias_f32(bias)
     (n, h, wd, c, k, r, s), (sh, sw, ph, pw, dh, dw), dims, opts = _dims_opts(xs.shape, ws.shape, stride,
-                                                                              padding, dilation)
+                                                                              padding, dilation, groups)
     p = out_extent(h, ph, dh, r, sh, lib)
     q = out_extent(wd, pw, dw, s, sw, lib)
     y = np.zeros((n, p, q, k), dtype=np.float64)
@@ -160,14 +163,14 @@ def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, threads: Option
 
 
 def conv2d_fwd_f64(x: np.ndarray, w: np.ndarray, bias=None, stride=1, padding=0, dilation=1,
-                   threads: Optional[int] = None, lib=None) -> np.ndarray:
+                   threads: Optional[int] = None, lib=None, groups=1) -> np.ndarray:
     """Direct convolution over float64 inputs (no bf16 widening), for exact pins."""
     lib = lib or load()
     xs = np.ascontiguousarray(x, dtype=np.float64)
     ws = np.ascontiguousarray(w, dtype=np.float64)
     b = _bias_f32(bias)
     (n, h, wd, c, k, r, s), (sh, sw, ph, pw, dh, dw), dims, opts = _dims_opts(xs.shape, ws.shape, stride,
-                                                                              padding, dilation)
+                                                                              padding, dilation, groups)
     p = out_extent(h, ph, dh, r, sh, lib)
     q = out_extent(wd, pw, dw, s, sw, lib)
     y = np.zeros((n, p, q, k), dtype=np.float64)
@@ -179,13 +182,13 @@ def conv2d_fwd_f64(x: np.ndarray, w: np.ndarray, bias=None, stride=1, padding=0,
 
 
 def conv2d_fwd_points(x, w, bias, stride, padding, dilation, m_idx: Sequence[int],
-                      k_idx: Sequence[int], lib=None) -> np.ndarray:
+                      k_idx: Sequence[int], lib=None, groups=1) -> np.ndarray:
     """Selected outputs y[m][k] of the [N*P*Q, K] view of the NHWC output, in float64."""
     lib = lib or load()
     xs = _bf16_bits(x)
     ws = _bf16_bits(w)
     b = _bias_f32(bias)
-    _, _, dims, opts = _dims_opts(xs.shape, ws.shape, stride, padding, dilation)
+    _, _, dims, opts = _dims_opts(xs.shape, ws.shape, stride, padding, dilation, groups)
     mi = np.ascontiguousarray(m_idx, dtype=np.int64)
     ki = np.ascontiguousarray(k_idx, dtype=np.int64)
     if mi.shape != ki.shape:
@@ -199,13 +202,13 @@ def conv2d_fwd_points(x, w, bias, stride, padding, dilation, m_idx: Sequence[int
 
 
 def conv2d_fwd_points_f64(x: np.ndarray, w: np.ndarray, bias, stride, padding, dilation, m_idx, k_idx,
-                          lib=None) -> np.ndarray:
+                          lib=None, groups=1) -> np.ndarray:
     """As conv2d_fwd_points over float64 inputs (widen once, sample many times)."""
     lib = lib or load()
     xs = np.ascontiguousarray(x, dtype=np.float64)
     ws = np.ascontiguousarray(w, dtype=np.float64)
     b = _bias_f32(bias)
-    _, _, dims, opts = _dims_opts(xs.shape, ws.shape, stride, padding, dilation)
+    _, _, dims, opts = _dims_opts(xs.shape, ws.shape, stride, padding, dilation, groups)
     mi = np.ascontiguousarray(m_idx, dtype=np.int64)
     ki = np.ascontiguousarray(k_idx, dtype=np.int64)
     if mi.shape != ki.shape:
@@ -225,5 +228,7 @@ def widen_bf16(t) -> np.ndarray:
 
 
 def tolerance(c: int, r: int, s: int) -> Tuple[float, float]:
-    """(rtol, atol) of the parity bar: |gpu - ref| <= 1e-5*|ref| + 1e-4*sqrt(C*R*S)."""
+    """(rtol, atol) of the parity bar: |gpu - ref| <= 1e-5*|ref| + 1e-4*sqrt(C*R*S).
+
+    For a grouped convolution pass the channels one output sums over, C/groups."""
     return 1e-5, 1e-4 * float(np.sqrt(c * r * s))

@@ -16,9 +16,18 @@
  *                 + sum_{r,s,c} x[n][p*sh - ph + r*dh][q*sw - pw + s*dw][c] * w[k][r][s][c]
  *
  * with out-of-image input positions contributing zero (symmetric zero padding),
- * cross-correlation (no filter flip), groups = 1, NHWC input, KRSC weight and
- * the bias added once per output channel ("The bias added to each channel",
- * conv_forward's doc comment on the same page).  Output extents:
+ * cross-correlation (no filter flip), NHWC input, KRSC weight and the bias
+ * added once per output channel ("The bias added to each channel",
+ * conv_forward's doc comment on the same page).  With `groups` = G (the
+ * ConvOptions field of the same page; burn's conv_forward_nhwc sends G != 1 to
+ * the direct strategy) the channels split into G equal consecutive groups:
+ * output channel k belongs to group g = k / (K/G) and sums only over the input
+ * channels g*C/G .. (g+1)*C/G - 1, its weight row holding C/G channels per tap
+ * (weight [K][R][S][C/G]):
+ *
+ *   y[n][p][q][k] = bias[k] + sum_{r,s,c < C/G} x[n][ih][iw][g*C/G + c] * w[k][r][s][c]
+ *
+ * G = 1 is the formula above.  Output extents:
  *
  *   P = floor((H + 2*ph - dh*(R-1) - 1) / sh) + 1   (0 if the window does not fit)
  *
@@ -34,6 +43,7 @@
 typedef struct {
     int64_t n, h, w, c, k, r, s;
     int64_t sh, sw, ph, pw, dh, dw;
+    int64_t g;       /* groups */
     int64_t p, q;
 } oracle_shape;
 
@@ -59,6 +69,8 @@ static double bf16_to_double(uint16_t b)
 static double conv_point(const oracle_shape* sp, const double* x, const double* w,
                          const float* bias, int64_t n, int64_t p, int64_t q, int64_t k)
 {
+    const int64_t cg = sp->c / sp->g;          /* input channels per group */
+    const int64_t group = k / (sp->k / sp->g); /* the group of output channel k */
     double acc = bias ? (double)bias[k] : 0.0;
     for (int64_t r = 0; r < sp->r; ++r) {
         int64_t ih = p * sp->sh - sp->ph + r * sp->dh;
@@ -66,9 +78,9 @@ static double conv_point(const oracle_shape* sp, const double* x, const double* 
         for (int64_t s = 0; s < sp->s; ++s) {
             int64_t iw = q * sp->sw - sp->pw + s * sp->dw;
             if (iw < 0 || iw >= sp->w) continue;
-            const double* xv = x + ((n * sp->h + ih) * sp->w + iw) * sp->c;
-            const double* wv = w + ((k * sp->r + r) * sp->s + s) * sp->c;
-            for (int64_t c = 0; c < sp->c; ++c) acc += xv[c] * wv[c];
+            const double* xv = x + ((n * sp->h + ih) * sp->w + iw) * sp->c + group * cg;
+            const double* wv = w + ((k * sp->r + r) * sp->s + s) * cg;
+            for (int64_t c = 0; c < cg; ++c) acc += xv[c] * wv[c];
         }
     }
     return acc;
@@ -98,15 +110,16 @@ static void* conv_rows(void* arg)
     return NULL;
 }
 
-static int make_shape(oracle_shape* sp, const int64_t dims[7], const int64_t opts[6])
+static int make_shape(oracle_shape* sp, const int64_t dims[7], const int64_t opts[7])
 {
     sp->n = dims[0]; sp->h = dims[1]; sp->w = dims[2]; sp->c = dims[3];
     sp->k = dims[4]; sp->r = dims[5]; sp->s = dims[6];
     sp->sh = opts[0]; sp->sw = opts[1]; sp->ph = opts[2]; sp->pw = opts[3];
-    sp->dh = opts[4]; sp->dw = opts[5];
+    sp->dh = opts[4]; sp->dw = opts[5]; sp->g = opts[6];
     for (int i = 0; i < 7; ++i) if (dims[i] < 0) return 1;
     if (sp->sh < 1 || sp->sw < 1 || sp->dh < 1 || sp->dw < 1 || sp->ph < 0 || sp->pw < 0) return 1;
     if (sp->r < 1 || sp->s < 1) return 1;
+    if (sp->g < 1 || sp->c % sp->g != 0 || sp->k % sp->g != 0) return 1;
     sp->p = oracle_out_extent(sp->h, sp->ph, sp->dh, sp->r, sp->sh);
     sp->q = oracle_out_extent(sp->w, sp->pw, sp->dw, sp->s, sp->sw);
     return 0;
@@ -114,13 +127,13 @@ static int make_shape(oracle_shape* sp, const int64_t dims[7], const int64_t opt
 
 /*
  * Full convolution over double inputs.
- *   dims = {N, H, W, C, K, R, S}; opts = {stride_h, stride_w, pad_h, pad_w, dil_h, dil_w}
- *   x: N*H*W*C doubles (NHWC); w: K*R*S*C doubles (KRSC); bias: K floats or NULL
+ *   dims = {N, H, W, C, K, R, S}; opts = {stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, groups}
+ *   x: N*H*W*C doubles (NHWC); w: K*R*S*(C/groups) doubles (KRSC); bias: K floats or NULL
  *   y: N*P*Q*K doubles (NHWC), P and Q from oracle_out_extent.
  * Rows (n, p) are split statically over `threads` POSIX threads.
  * Returns 0 on success, 1 on invalid arguments, 2 if a thread could not start.
  */
-int oracle_conv2d_f64(const int64_t dims[7], const int64_t opts[6], const double* x,
+int oracle_conv2d_f64(const int64_t dims[7], const int64_t opts[7], const double* x,
                       const double* w, const float* bias, double* y, int threads)
 {
     oracle_shape sp;
@@ -162,11 +175,12 @@ static double* widen_bf16(const uint16_t* v, int64_t count)
 }
 
 /* Same as oracle_conv2d_f64 with bf16 (bit pattern) input and weight. */
-int oracle_conv2d_bf16(const int64_t dims[7], const int64_t opts[6], const uint16_t* x,
+int oracle_conv2d_bf16(const int64_t dims[7], const int64_t opts[7], const uint16_t* x,
                        const uint16_t* w, const float* bias, double* y, int threads)
 {
+    if (opts[6] < 1 || dims[3] % opts[6] != 0) return 1;
     int64_t nx = dims[0] * dims[1] * dims[2] * dims[3];
-    int64_t nw = dims[4] * dims[5] * dims[6] * dims[3];
+    int64_t nw = dims[4] * dims[5] * dims[6] * (dims[3] / opts[6]);
     double* xd = widen_bf16(x, nx);
     double* wd = widen_bf16(w, nw);
     int rc = 2;
@@ -202,14 +216,14 @@ static int check_points(const oracle_shape* sp, const int64_t* m_idx, const int6
  * m = (n*P + p)*Q + q is the row of the NHWC output viewed as [N*P*Q][K].
  * Returns 0, 1 on invalid arguments / out-of-range indices, 2 on allocation failure.
  */
-int oracle_conv2d_points_bf16(const int64_t dims[7], const int64_t opts[6], const uint16_t* x,
+int oracle_conv2d_points_bf16(const int64_t dims[7], const int64_t opts[7], const uint16_t* x,
                               const uint16_t* w, const float* bias, const int64_t* m_idx,
                               const int64_t* k_idx, int64_t npts, double* out)
 {
     oracle_shape sp;
     if (make_shape(&sp, dims, opts) || check_points(&sp, m_idx, k_idx, npts)) return 1;
     double* xd = widen_bf16(x, sp.n * sp.h * sp.w * sp.c);
-    double* wd = widen_bf16(w, sp.k * sp.r * sp.s * sp.c);
+    double* wd = widen_bf16(w, sp.k * sp.r * sp.s * (sp.c / sp.g));
     if (!xd || !wd) { free(xd); free(wd); return 2; }
     points_f64(&sp, xd, wd, bias, m_idx, k_idx, npts, out);
     free(xd);
@@ -218,7 +232,7 @@ int oracle_conv2d_points_bf16(const int64_t dims[7], const int64_t opts[6], cons
 }
 
 /* As oracle_conv2d_points_bf16 over double inputs (for repeated sampling of one problem). */
-int oracle_conv2d_points_f64(const int64_t dims[7], const int64_t opts[6], const double* x,
+int oracle_conv2d_points_f64(const int64_t dims[7], const int64_t opts[7], const double* x,
                              const double* w, const float* bias, const int64_t* m_idx,
                              const int64_t* k_idx, int64_t npts, double* out)
 {

@@ -140,8 +140,8 @@ def _pair(v) -> Tuple[int, int]:
 def make_params(x_shape, w_shape, stride=1, padding=0, dilation=1, groups=1) -> Params:
     n, h, w, c = (int(v) for v in x_shape)
     k, r, s, c2 = (int(v) for v in w_shape)
-    if groups == 1 and c2 != c:
-        raise ValueError(f"channel mismatch: input C={c}, weight C={c2}")
+    if int(groups) >= 1 and c2 * int(groups) != c:
+        raise ValueError(f"channel mismatch: input C={c}, weight C/groups={c2}, groups={groups}")
     sh, sw = _pair(stride)
     ph, pw = _pair(padding)
     dh, dw = _pair(dilation)

@@ -15,7 +15,10 @@ The pins (none re-types the oracle's formula):
   naive GEMM, on integer-valued inputs so that every sum is exact in fp64;
 * invariants: linearity in the input, the bias shift, zero input gives the bias,
   output extents on edge cases, thread-count independence, the point-query
-  entry agreeing with the full output, bf16 widening matching float64 input.
+  entry agreeing with the full output, bf16 widening matching float64 input;
+* grouped convolution: per group, the same brute force on the group's slice of
+  input channels, filters and bias (channels split into consecutive groups),
+  and a depthwise case (groups = C = K) written as its own loop.
 Only numpy is used here, so the battery runs quickly in a subprocess.
 """
 from __future__ import annotations
@@ -290,8 +293,56 @@ def pin_points_and_bf16(lib):
     assert got.item() == ((widened[0] + widened[1]) + widened[2]) + widened[3]
 
 
+GROUP_CASES = [
+    # (n, h, w, c, k, r, s, groups, stride, pad, dil)
+    (2, 5, 6, 4, 6, 3, 3, 2, (1, 1), (1, 1), (1, 1)),
+    (1, 7, 5, 6, 9, 3, 2, 3, (2, 1), (1, 0), (1, 2)),
+    (2, 6, 6, 8, 4, 1, 1, 4, (1, 1), (0, 0), (1, 1)),
+    (1, 6, 7, 6, 12, 2, 3, 6, (1, 2), (1, 1), (2, 1)),
+]
+
+
+def pin_groups(lib):
+    rng = np.random.default_rng(7)
+    for case in GROUP_CASES:
+        n, h, wd, c, k, r, s, g, st, pd, dl = case
+        cg, kg = c // g, k // g
+        x = rng.integers(-3, 4, size=(n, h, wd, c)).astype(np.float64)
+        w = rng.integers(-3, 4, size=(k, r, s, cg)).astype(np.float64)
+        b = rng.integers(-8, 9, size=(k,)).astype(np.float32)
+        # consecutive groups: group i takes input channels i*cg.. and filters i*kg..
+        expect = np.concatenate(
+            [im2col_gemm(x[..., i * cg:(i + 1) * cg], w[i * kg:(i + 1) * kg], b[i * kg:(i + 1) * kg], st, pd, dl)
+             for i in range(g)], axis=-1)
+        y = oracle.conv2d_fwd_f64(x, w, b, st, pd, dl, lib=lib, groups=g)
+        assert y.shape == expect.shape, (case, y.shape, expect.shape)
+        assert np.array_equal(y, expect), case
+        xb, wb = bf16_bits_of_ints(x), bf16_bits_of_ints(w)
+        assert np.array_equal(oracle.conv2d_fwd(xb, wb, b, st, pd, dl, lib=lib, groups=g), expect), case
+        flat = expect.reshape(-1, k)
+        mi = rng.integers(0, flat.shape[0], size=32)
+        ki = rng.integers(0, k, size=32)
+        pts = oracle.conv2d_fwd_points(xb, wb, b, st, pd, dl, mi, ki, lib=lib, groups=g)
+        assert np.array_equal(pts, flat[mi, ki]), case
+    # depthwise: every channel filtered by its own R x S kernel, written as its own loop
+    x = rng.integers(-3, 4, size=(1, 5, 4, 3)).astype(np.float64)
+    w = rng.integers(-3, 4, size=(3, 3, 3, 1)).astype(np.float64)
+    expect = np.zeros((1, 5, 4, 3))
+    for ch in range(3):
+        for pi in range(5):
+            for qi in range(4):
+                acc = 0.0
+                for ri in range(3):
+                    for si in range(3):
+                        ih, iw = pi - 1 + ri, qi - 1 + si
+                        if 0 <= ih < 5 and 0 <= iw < 4:
+                            acc += x[0, ih, iw, ch] * w[ch, ri, si, 0]
+                expect[0, pi, qi, ch] = acc
+    assert np.array_equal(oracle.conv2d_fwd_f64(x, w, None, 1, 1, 1, lib=lib, groups=3), expect)
+
+
 ALL_PINS = [pin_golden, pin_delta_identity, pin_shifted_delta, pin_1x1_matmul, pin_bruteforce_im2col,
-            pin_invariants, pin_extents, pin_points_and_bf16]
+            pin_invariants, pin_extents, pin_points_and_bf16, pin_groups]
 
 
 def run_all(lib):

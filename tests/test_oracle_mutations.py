@@ -27,7 +27,10 @@ MUTANTS = {
     "input_hw_swapped": ("((n * sp->h + ih) * sp->w + iw)", "((n * sp->w + iw) * sp->h + ih)"),
     "bias_dropped": ("bias ? (double)bias[k] : 0.0", "0.0"),
     "bias_wrong_channel": ("bias ? (double)bias[k] : 0.0", "bias ? (double)bias[0] : 0.0"),
-    "first_channel_dropped": ("for (int64_t c = 0; c < sp->c; ++c)", "for (int64_t c = 1; c < sp->c; ++c)"),
+    "first_channel_dropped": ("for (int64_t c = 0; c < cg; ++c)", "for (int64_t c = 1; c < cg; ++c)"),
+    "group_channel_offset_dropped": ("* sp->c + group * cg;", "* sp->c;"),
+    "group_weight_row_stride_full_c": ("* sp->s + s) * cg;", "* sp->s + s) * sp->c;"),
+    "groups_interleaved": ("k / (sp->k / sp->g)", "k % sp->g"),
     "border_off_by_one": ("if (ih < 0 || ih >= sp->h) continue;", "if (ih <= 0 || ih >= sp->h) continue;"),
     "extent_missing_plus_one": ("return room / stride + 1;", "return room / stride;"),
     "extent_span_wrong": ("int64_t span = dil * (ker - 1) + 1;", "int64_t span = dil * ker;"),

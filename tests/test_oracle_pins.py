@@ -13,13 +13,32 @@ def test_pin(pin, oracle_lib):
     pin(oracle_lib)
 
 
-def _torch_conv(x, w, b, stride, pad, dil):
+def _torch_conv(x, w, b, stride, pad, dil, groups=1):
     # Library cross-check: torch's own CPU convolution in float64 on NCHW/KCRS views.
     xt = torch.from_numpy(x).permute(0, 3, 1, 2)
     wt = torch.from_numpy(w).permute(0, 3, 1, 2)
     bt = None if b is None else torch.from_numpy(np.asarray(b, dtype=np.float64))
-    y = torch.nn.functional.conv2d(xt, wt, bt, stride=stride, padding=pad, dilation=dil)
+    y = torch.nn.functional.conv2d(xt, wt, bt, stride=stride, padding=pad, dilation=dil, groups=groups)
     return y.permute(0, 2, 3, 1).contiguous().numpy()
+
+
+@pytest.mark.parametrize("geom", [
+    dict(n=2, h=9, w=8, c=8, k=12, r=3, s=3, groups=2, stride_h=1, stride_w=1, pad_h=1, pad_w=1),
+    dict(n=1, h=11, w=7, c=12, k=6, r=3, s=2, groups=3, stride_h=2, stride_w=1, pad_h=1, pad_w=0, dil_w=2),
+    dict(n=2, h=6, w=6, c=16, k=16, r=3, s=3, groups=16, stride_h=1, stride_w=1, pad_h=1, pad_w=1),
+    dict(n=1, h=8, w=9, c=128, k=64, r=1, s=3, groups=2, stride_h=1, stride_w=2, pad_h=0, pad_w=1),
+])
+def test_library_grouped_conv_crosscheck(geom, oracle_lib):
+    kw = dict(geom)
+    wl = workloads.Workload("grp", kw.pop("n"), kw.pop("h"), kw.pop("w"), kw.pop("c"), kw.pop("k"), kw.pop("r"),
+                            kw.pop("s"), bias="normal:0.1", seed=3, **kw)
+    x, w, b = workloads.make_inputs(wl)
+    assert w.shape == (wl.k, wl.r, wl.s, wl.c // wl.groups)
+    ours = oracle.conv2d_fwd(x, w, b, **wl.options(), lib=oracle_lib)
+    ref = _torch_conv(x.to(torch.float64).numpy(), w.to(torch.float64).numpy(), b.numpy(),
+                      (wl.stride_h, wl.stride_w), (wl.pad_h, wl.pad_w), (wl.dil_h, wl.dil_w), wl.groups)
+    assert ours.shape == ref.shape
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
 
 
 @pytest.mark.parametrize("seed", range(12))

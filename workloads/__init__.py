@@ -56,14 +56,16 @@ class Workload:
     bias: Optional[str] = None  # None | "zero" | "uniform" | "normal:<variance>" | "int:<lo>:<hi>"
     seed: int = 0
     note: str = ""
+    groups: int = 1  # channels split into consecutive groups; weight [K][R][S][C/groups]
 
     def options(self) -> dict:
         return dict(stride=(self.stride_h, self.stride_w), padding=(self.pad_h, self.pad_w),
-                    dilation=(self.dil_h, self.dil_w))
+                    dilation=(self.dil_h, self.dil_w), groups=self.groups)
 
     def describe(self) -> str:
         return (f"N{self.n} H{self.h} W{self.w} C{self.c} K{self.k} {self.r}x{self.s} "
-                f"s{self.stride_h}x{self.stride_w} p{self.pad_h}x{self.pad_w} d{self.dil_h}x{self.dil_w}")
+                f"s{self.stride_h}x{self.stride_w} p{self.pad_h}x{self.pad_w} d{self.dil_h}x{self.dil_w}"
+                + (f" g{self.groups}" if self.groups != 1 else ""))
 
 
 # The seven workloads of the build's benchmark list.  Shapes and distributions
@@ -123,12 +125,13 @@ def _draw(gen: torch.Generator, shape, dist: str, fan_in: int) -> torch.Tensor:
 
 
 def make_inputs(wl: Workload, seed: Optional[int] = None):
-    """Return (x, w, bias) on the CPU: x [N,H,W,C] bf16, w [K,R,S,C] bf16, bias [K] fp32 or None."""
+    """Return (x, w, bias) on the CPU: x [N,H,W,C] bf16, w [K,R,S,C/groups] bf16, bias [K] fp32 or None."""
     gen = torch.Generator("cpu")
     gen.manual_seed(wl.seed if seed is None else seed)
-    fan_in = wl.c * wl.r * wl.s
+    cg = wl.c // wl.groups
+    fan_in = cg * wl.r * wl.s
     x = _draw(gen, (wl.n, wl.h, wl.w, wl.c), wl.x_dist, fan_in).to(torch.bfloat16).contiguous()
-    w = _draw(gen, (wl.k, wl.r, wl.s, wl.c), wl.w_dist, fan_in).to(torch.bfloat16).contiguous()
+    w = _draw(gen, (wl.k, wl.r, wl.s, cg), wl.w_dist, fan_in).to(torch.bfloat16).contiguous()
     b = None
     if wl.bias is not None:
         b = _draw(gen, (wl.k,), wl.bias, fan_in).contiguous()
