@@ -17,8 +17,13 @@
  *     matmul is slow even for few partitions" (Eliminating the workspace, and the
  *     comment on aliasing the output buffer).
  *
- * Math (cross-correlation, zero padding, groups = 1):
- *   y[n][p][q][k] = bias[k] + sum_{r,s,c} x[n][p*sh-ph+r*dh][q*sw-pw+s*dw][c] * w[k][r][s][c]
+ * Math (cross-correlation, zero padding):
+ *   y[n][p][q][k] = bias[k] + sum_{r,s,c} x[n][p*sh-ph+r*dh][q*sw-pw+s*dw][g*Cg + c] * w[k][r][s][c]
+ *   with G = groups, Cg = C/G, Kg = K/G, g = k / Kg and c over 0 .. Cg-1: the
+ *   channels split into G equal consecutive groups, each output channel summing
+ *   over its own group's input channels (burn's ConvOptions carry `groups`; its
+ *   implicit GEMM sends G != 1 to the direct strategy, burn-cubecl base.rs
+ *   conv_forward_nhwc).  G = 1 is the ordinary convolution.
  *   P = floor((H + 2*ph - dh*(R-1) - 1)/sh) + 1,  Q likewise.
  * Inputs are bf16, products are exact in fp32, accumulation is fp32 (tensor
  * cores, TMEM), the output is fp32.
@@ -28,8 +33,8 @@
  *   - Pointers named *_dev are device pointers owned by the caller; pointers
  *     named *_host are host pointers owned by the caller.  The library never
  *     frees or retains them beyond the call.
- *   - Tensors are dense and contiguous: x is [N][H][W][C] bf16, w is [K][R][S][C]
- *     bf16, bias is [K] fp32, y is [N][P][Q][K] fp32.
+ *   - Tensors are dense and contiguous: x is [N][H][W][C] bf16, w is
+ *     [K][R][S][C/groups] bf16, bias is [K] fp32, y is [N][P][Q][K] fp32.
  *   - Device pointers must be 16-byte aligned, or the call returns
  *     CONV2D_ERR_ALIGNMENT.
  *   - Device work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -57,13 +62,13 @@ typedef struct {
     int32_t stride_h, stride_w;
     int32_t pad_h, pad_w;
     int32_t dil_h, dil_w;
-    int32_t groups;      /* must be 1 */
+    int32_t groups;      /* >= 1, dividing both c and k (CONV2D_ERR_INVALID otherwise) */
 } conv2d_params;
 
 typedef enum {
     CONV2D_OK = 0,
     CONV2D_ERR_INVALID = 1,     /* bad sizes/options, NULL pointer, empty window */
-    CONV2D_ERR_UNSUPPORTED = 2, /* groups != 1, sizes beyond 32-bit index range, or a forced algo that cannot run */
+    CONV2D_ERR_UNSUPPORTED = 2, /* sizes beyond 32-bit index range, or a forced algo that cannot run */
     CONV2D_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned */
     CONV2D_ERR_WORKSPACE = 4,   /* workspace missing or smaller than conv2d_fwd_workspace_bytes() */
     CONV2D_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
@@ -74,22 +79,22 @@ typedef enum {
 /* Loader kinds for the im2col (activation) operand. */
 typedef enum {
     CONV2D_LOADER_AUTO = 0,
-    CONV2D_LOADER_TMA_IM2COL = 1, /* TMA im2col-mode descriptor; needs C % 64 == 0 */
-    CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C % 8 == 0 */
+    CONV2D_LOADER_TMA_IM2COL = 1, /* TMA im2col-mode descriptor; needs C/groups % 64 == 0 */
+    CONV2D_LOADER_CPASYNC = 2,    /* 16-byte cp.async gather; needs C/groups % 8 == 0 */
     CONV2D_LOADER_SCALAR = 3,     /* element gather; any C (also gathers the weight) */
-    CONV2D_LOADER_HYBRID = 4,     /* TMA im2col and cp.async gather on alternate k-blocks; needs C % 64 == 0 */
+    CONV2D_LOADER_HYBRID = 4,     /* TMA im2col and cp.async gather on alternate k-blocks; needs C/groups % 64 == 0 */
     CONV2D_LOADER_ROW_WINDOW = 5, /* few channels: staged input rows read in place by the MMA as overlapping
-                                     16-byte-pitch windows; needs dil_w == 1, stride_w in {1,2,4,8},
+                                     16-byte-pitch windows; needs groups == 1, dil_w == 1, stride_w in {1,2,4,8},
                                      C <= 8 / stride_w, K <= 256 (one tile of output channels), no split */
     CONV2D_LOADER_TMA_BOX = 6,    /* tiles are rectangles of output pixels; each tiled TMA box carries two
                                      64-channel chunks of one filter tap (and a 3-D box two weight k-blocks);
-                                     needs C % 128 == 0, strides <= 8, a rectangle whose pixel count is a
-                                     multiple of 8, and block_n <= 128 with 256-pixel tiles */
+                                     needs groups == 1, C % 128 == 0, strides <= 8, and block_n <= 128
+                                     with 256-pixel tiles */
     CONV2D_LOADER_HALO = 7        /* stride 1 only: a tile is 128 consecutive pixels of an image seen with the
                                      padded row pitch W + 2*pad_w (pixels past Q are computed and discarded);
                                      per 64-channel chunk one tiled TMA box of whole padded input rows serves
                                      every filter tap, which the MMA reads in place at the tap's row offset.
-                                     Needs C % 64 == 0, W + 2*pad_w <= 256, 128-pixel tiles, and the two halo
+                                     Needs groups == 1, C % 64 == 0, W + 2*pad_w <= 256, 128-pixel tiles, and the two halo
                                      buffers plus the weight ring within shared memory (block_n is narrowed
                                      to fit unless forced) */
 } conv2d_loader;

@@ -140,7 +140,9 @@ def _pair(v) -> Tuple[int, int]:
 def make_params(x_shape, w_shape, stride=1, padding=0, dilation=1, groups=1) -> Params:
     n, h, w, c = (int(v) for v in x_shape)
     k, r, s, c2 = (int(v) for v in w_shape)
-    if int(groups) >= 1 and c2 * int(groups) != c:
+    # The weight holds C/groups channels per tap; whether `groups` itself is valid
+    # (>= 1, dividing C and K) is the C ABI's call.
+    if int(groups) >= 1 and c % int(groups) == 0 and c2 * int(groups) != c:
         raise ValueError(f"channel mismatch: input C={c}, weight C/groups={c2}, groups={groups}")
     sh, sw = _pair(stride)
     ph, pw = _pair(padding)

@@ -45,7 +45,8 @@ unsigned long long* g_trace = nullptr;  // profiling builds only: per-CTA phase 
 struct Shape {
     int64_t n, h, w, c, k, r, s;
     int64_t sh, sw, ph, pw, dh, dw;
-    int64_t p, q, m, crs;
+    int64_t g, cg, kg;  // groups; input and output channels per group
+    int64_t p, q, m, crs;  // crs = R*S*Cg: the reduction length of one output channel
 };
 
 int64_t out_extent(int64_t in, int64_t pad, int64_t dil, int64_t ker, int64_t stride)
@@ -59,9 +60,10 @@ int64_t out_extent(int64_t in, int64_t pad, int64_t dil, int64_t ker, int64_t st
 int make_shape(const conv2d_params* prm, Shape* sh)
 {
     if (!prm) return CONV2D_ERR_INVALID;
-    if (prm->groups != 1) return prm->groups < 1 ? CONV2D_ERR_INVALID : CONV2D_ERR_UNSUPPORTED;
     if (prm->n < 0 || prm->k < 0 || prm->h < 1 || prm->w < 1 || prm->c < 1 || prm->r < 1 || prm->s < 1)
         return CONV2D_ERR_INVALID;
+    // Groups split the channels into equal consecutive groups (both C and K).
+    if (prm->groups < 1 || prm->c % prm->groups != 0 || prm->k % prm->groups != 0) return CONV2D_ERR_INVALID;
     if (prm->stride_h < 1 || prm->stride_w < 1 || prm->dil_h < 1 || prm->dil_w < 1 || prm->pad_h < 0 ||
         prm->pad_w < 0)
         return CONV2D_ERR_INVALID;
@@ -70,6 +72,9 @@ int make_shape(const conv2d_params* prm, Shape* sh)
     sh->sh = prm->stride_h; sh->sw = prm->stride_w;
     sh->ph = prm->pad_h; sh->pw = prm->pad_w;
     sh->dh = prm->dil_h; sh->dw = prm->dil_w;
+    sh->g = prm->groups;
+    sh->cg = sh->c / sh->g;
+    sh->kg = sh->k / sh->g;
     // Guard the extent arithmetic itself against overflow before using it.
     if (sh->h > kIndexLimit || sh->w > kIndexLimit || sh->r > kIndexLimit || sh->s > kIndexLimit ||
         sh->c > kIndexLimit || sh->n > kIndexLimit || sh->k > kIndexLimit)
@@ -77,7 +82,7 @@ int make_shape(const conv2d_params* prm, Shape* sh)
     sh->p = out_extent(sh->h, sh->ph, sh->dh, sh->r, sh->sh);
     sh->q = out_extent(sh->w, sh->pw, sh->dw, sh->s, sh->sw);
     if (sh->p < 1 || sh->q < 1) return CONV2D_ERR_INVALID;
-    sh->crs = sh->c * sh->r * sh->s;
+    sh->crs = sh->cg * sh->r * sh->s;
     sh->m = sh->n * sh->p * sh->q;
     // 32-bit device indexing: every element count must fit in int32.
     if (sh->crs > kIndexLimit || sh->n * sh->h * sh->w * sh->c > kIndexLimit || sh->m > kIndexLimit ||
@@ -130,7 +135,7 @@ bool load_encoders()
 // per-tap offsets that fit the instruction's offset field, traversal strides <= 8.
 bool tma_im2col_eligible(const Shape& s)
 {
-    if (s.c % BK != 0) return false;
+    if (s.cg % BK != 0) return false;  // each 64-channel box stays inside one group
     const int64_t lo_w = -s.pw, lo_h = -s.ph;
     const int64_t up_w = s.pw - (s.s - 1) * s.dw, up_h = s.ph - (s.r - 1) * s.dh;
     auto in8 = [](int64_t v) { return v >= -128 && v <= 127; };
@@ -158,7 +163,7 @@ struct BoxGeom {
 // shared-memory addresses, so a chunk may start at any row.
 bool box_geometry(const Shape& s, int bm, BoxGeom* g)
 {
-    if (s.c % (kBoxChunks * BK) != 0 || s.sw > 8 || s.sh > 8) return false;
+    if (s.g != 1 || s.c % (kBoxChunks * BK) != 0 || s.sw > 8 || s.sh > 8) return false;
     const int64_t wmax = 256 / s.sw, hmax = 256 / s.sh;
     int64_t bw, bh = 1, bn = 1;
     if (s.q >= bm || s.q > wmax) {
@@ -214,7 +219,7 @@ struct RowWinCfg {
 // dil_h > 1 or stride_h > 8, and further down while shared memory is short.
 bool rowwin_config(const Shape& s, int bn_force, RowWinCfg* o)
 {
-    if (s.dw != 1 || s.r > 64 || s.s > 64 || s.dh > 64) return false;
+    if (s.g != 1 || s.dw != 1 || s.r > 64 || s.s > 64 || s.dh > 64) return false;
     int cp_log2;
     switch (s.sw) {
         case 1: cp_log2 = 3; break;
@@ -306,7 +311,7 @@ struct HaloGeom {
 // per-block shared memory.
 bool halo_geometry(const Shape& s, int bn, HaloGeom* g)
 {
-    if (s.sh != 1 || s.sw != 1 || s.c % BK != 0) return false;
+    if (s.g != 1 || s.sh != 1 || s.sw != 1 || s.c % BK != 0) return false;
     const int64_t wv = s.w + 2 * s.pw;
     if (wv > 256 || s.p < 1) return false;
     const int64_t vp = s.p * wv;
@@ -355,7 +360,7 @@ int64_t semaphore_capacity(const Shape& s)
     if (box_geometry(s, 128, &g) && g.m_tiles > m_tiles) m_tiles = g.m_tiles;
     HaloGeom h;
     if (halo_geometry(s, 64, &h) && h.m_tiles > m_tiles) m_tiles = h.m_tiles;
-    return m_tiles * cdiv(s.k, 64);
+    return m_tiles * s.g * cdiv(s.kg, 64);
 }
 
 
@@ -374,7 +379,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         // stride-1 benchmark shape (its per-stage weight loads see a longer ring
         // round trip), so the heuristic does not pick it; callers may force it.
         if (tma_im2col_eligible(s)) loader = CONV2D_LOADER_TMA_IM2COL;
-        else if (s.c % 8 == 0) loader = CONV2D_LOADER_CPASYNC;
+        else if (s.cg % 8 == 0) loader = CONV2D_LOADER_CPASYNC;
         else if (rowwin_config(s, force ? force->block_n : 0, &rw)) loader = CONV2D_LOADER_ROW_WINDOW;
         else loader = CONV2D_LOADER_SCALAR;
     } else if (loader == CONV2D_LOADER_ROW_WINDOW) {
@@ -382,7 +387,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     } else if (loader == CONV2D_LOADER_TMA_IM2COL) {
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_CPASYNC) {
-        if (s.c % 8 != 0) return CONV2D_ERR_UNSUPPORTED;
+        if (s.cg % 8 != 0) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_HYBRID) {
         if (!tma_im2col_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_TMA_BOX) {
@@ -417,11 +422,11 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
         // is per operation); worth it when the output channels are few (<= 128,
         // so the MMA per k-block is short) and the tiles still cover the SMs.
         bm = 128;
-        const int64_t bn_guess = (force && force->block_n) ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+        const int64_t bn_guess = (force && force->block_n) ? force->block_n : (s.kg <= 64 ? 64 : (s.kg <= 128 ? 128 : 256));
         const int64_t cover = (sms > 0 ? sms : 1) * 4;
         BoxGeom g256;
         if (loader == CONV2D_LOADER_TMA_IM2COL && bn_guess <= 128 && (!force || force->splits == 0) &&
-            cdiv(s.m, 256) * cdiv(s.k, bn_guess) * 5 >= cover)
+            cdiv(s.m, 256) * s.g * cdiv(s.kg, bn_guess) * 5 >= cover)
             bm = 256;
         if (loader == CONV2D_LOADER_TMA_BOX && bn_guess <= 128 && (!force || force->splits == 0) &&
             box_geometry(s, 256, &g256) && g256.px * 4 >= 256 * 3 && g256.m_tiles * cdiv(s.k, bn_guess) * 5 >= cover)
@@ -449,9 +454,9 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     // need more than kMaxSplitsPerTile in-place turns per tile.
     int bn = force ? force->block_n : 0;
     if (bn == 0) {
-        bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+        bn = s.kg <= 64 ? 64 : (s.kg <= 128 ? 128 : 256);
         while (bn > 64 && forced_splits == 0 && forced_grid == 0) {
-            const int64_t tiles = m_tiles * cdiv(s.k, bn);
+            const int64_t tiles = m_tiles * s.g * cdiv(s.kg, bn);
             if (tiles * 2 > nsm || num_kb < 8 || nsm / tiles <= kMaxSplitsPerTile) break;
             bn /= 2;
         }
@@ -465,7 +470,8 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
             bn /= 2;
         }
     }
-    const int64_t n_tiles = cdiv(s.k, bn);
+    // Column blocks never straddle a group: ntpg blocks per group.
+    const int64_t n_tiles = s.g * cdiv(s.kg, bn);
     const int64_t tiles = m_tiles * n_tiles;
     const int64_t units = tiles * num_kb;
     int64_t splits = forced_splits;
@@ -660,7 +666,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     const bool cuts_tiles = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
     if (cuts_tiles && !have_ws) return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
-    const bool vec_store = (s.k % 4) == 0;  // 16-byte vector writes of y rows
+    const bool vec_store = (s.k % 4) == 0 && (s.kg % 4) == 0;  // 16-byte vector writes inside one group's columns
     if (plan.loader == CONV2D_LOADER_ROW_WINDOW) {
         RowWinCfg rw;
         if (!rowwin_config(s, plan.block_n, &rw)) return CONV2D_ERR_UNSUPPORTED;
@@ -741,6 +747,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.sh = (int)s.sh; kp.sw = (int)s.sw; kp.ph = (int)s.ph; kp.pw = (int)s.pw; kp.dh = (int)s.dh; kp.dw = (int)s.dw;
     kp.M = (int)s.m;
     kp.CRS = (int)s.crs;
+    kp.G = (int)s.g;
+    kp.Cg = (int)s.cg;
+    kp.Kg = (int)s.kg;
+    kp.ntpg = (int)(plan.n_tiles / s.g);
     kp.num_kb = plan.num_kb;
     kp.m_tiles = plan.m_tiles;
     kp.n_tiles = plan.n_tiles;
@@ -901,7 +911,7 @@ const char* conv2d_strerror(int status)
     switch (status) {
         case CONV2D_OK: return "ok";
         case CONV2D_ERR_INVALID: return "invalid argument (sizes, options or pointers)";
-        case CONV2D_ERR_UNSUPPORTED: return "unsupported (groups != 1, sizes beyond 32-bit indexing, or forced algo)";
+        case CONV2D_ERR_UNSUPPORTED: return "unsupported (sizes beyond 32-bit indexing, or a forced algo that cannot run)";
         case CONV2D_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
         case CONV2D_ERR_WORKSPACE: return "workspace missing or too small";
         case CONV2D_ERR_CUDA: return "CUDA runtime or driver error";

@@ -127,7 +127,10 @@ struct ConvKernelParams {
     uint32_t* sems;     // one per output tile (needed whenever a tile is split)
     int N, H, W, C, K, R, S, P, Q;
     int sh, sw, ph, pw, dh, dw;
-    int M, CRS, num_kb;       // num_kb: pipeline stages per tile (KC k-blocks each)
+    int M, CRS, num_kb;       // CRS = R*S*Cg: reduction length of one output channel; num_kb: stages per tile
+    // Groups: G groups of Cg input and Kg output channels; a tile's column block
+    // lies inside one group (ntpg column blocks per group).  G = 1: Cg = C, Kg = K.
+    int G, Cg, Kg, ntpg;
     int m_tiles, n_tiles;
     int grid;                 // G: CTAs sharing the unit range
     long long units;          // U = m_tiles * n_tiles * num_kb
@@ -277,6 +280,20 @@ __device__ __forceinline__ void decode_pixel(const ConvKernelParams& kp, int m, 
     q = rem - p * kp.Q;
 }
 
+// Output-channel range [n0, n_end) of a tile's column block and the first input
+// channel of its group (grouped convolution: output channel n sums over the
+// input channels of group n / Kg only).
+template <int BN>
+__device__ __forceinline__ void tile_columns(const ConvKernelParams& kp, int tile, int m_tile, int& n0, int& n_end,
+                                             int& c_base)
+{
+    const int nt = tile - m_tile * kp.n_tiles;
+    const int g = nt / kp.ntpg;
+    n0 = g * kp.Kg + (nt - g * kp.ntpg) * BN;
+    n_end = (g + 1) * kp.Kg;
+    c_base = g * kp.Cg;
+}
+
 // Box loader: first image, row and column of the rectangle of tile row-block m_tile.
 __device__ __forceinline__ void box_origin(const ConvKernelParams& kp, int m_tile, int& n0, int& p0, int& q0)
 {
@@ -357,12 +374,13 @@ __device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile
 template <int BM, int BN, int LOADER>
 struct LoadCursor {
     static constexpr int KC = TileConfig<BM, BN, LOADER>::KC;
-    int n_img, w_org, h_org, c, r, s, n0, kb;
+    int n_img, w_org, h_org, c, r, s, n0, kb, c_base;  // c: channel within the group
     LoadCursor() = default;
     __device__ __forceinline__ LoadCursor(const ConvKernelParams& kp, const Segment& sg)
     {
         const int m_tile = sg.tile / kp.n_tiles;
-        n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int n_end;
+        tile_columns<BN>(kp, sg.tile, m_tile, n0, n_end, c_base);
         int p0, q0;
         if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, n_img, p0, q0);
         else decode_pixel(kp, m_tile * BM, n_img, p0, q0);
@@ -370,8 +388,8 @@ struct LoadCursor {
         h_org = p0 * kp.sh - kp.ph;
         kb = sg.kb_begin;
         const int kk0 = kb * KC * BK;
-        const int rs0 = kk0 / kp.C;
-        c = kk0 - rs0 * kp.C;
+        const int rs0 = kk0 / kp.Cg;
+        c = kk0 - rs0 * kp.Cg;
         r = rs0 / kp.S;
         s = rs0 - r * kp.S;
     }
@@ -379,7 +397,7 @@ struct LoadCursor {
     {
         ++kb;
         c += KC * BK;
-        if (c >= kp.C) {  // the im2col loaders need C % 64 == 0, the box loader C % 128 == 0
+        if (c >= kp.Cg) {  // the im2col loaders need Cg % 64 == 0, the box loader C % 128 == 0
             c = 0;
             if (++s == kp.S) {
                 s = 0;
@@ -395,10 +413,10 @@ struct LoadCursor {
                                            uint64_t* bar) const
     {
         if constexpr (LOADER == LOADER_BOX)  // KC channel chunks of the rectangle's windows at tap (r, s)
-            ptx::tma_load_5d(a_dst, tm_a, bar, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, c / BK);
+            ptx::tma_load_5d(a_dst, tm_a, bar, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, (c_base + c) / BK);
         else
-            ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
-                                    static_cast<uint16_t>(r * kp.dh));
+            ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c_base + c, w_org, h_org, n_img,
+                                    static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
     }
     __device__ __forceinline__ void load_b(const CUtensorMap* tm_b, uint8_t* b_dst, uint64_t* bar) const
     {
@@ -410,10 +428,10 @@ struct LoadCursor {
                                              const ConvKernelParams& kp) const
     {
         if constexpr (LOADER == LOADER_BOX) {
-            ptx::tma_prefetch_5d(tm_a, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, c / BK);
+            ptx::tma_prefetch_5d(tm_a, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, (c_base + c) / BK);
             ptx::tma_prefetch_3d(tm_b, 0, n0, kb * KC);
         } else {
-            ptx::tma_prefetch_im2col_4d(tm_a, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+            ptx::tma_prefetch_im2col_4d(tm_a, c_base + c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
                                         static_cast<uint16_t>(r * kp.dh));
             ptx::tma_prefetch_2d(tm_b, kb * BK, n0);
         }
@@ -770,6 +788,8 @@ __device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& s
     Segment sg;
     while (ok && walk.next(kp, sg)) {
         const int m_base = (sg.tile / kp.n_tiles) * BM;
+        int gn0, gn_end, c_base;
+        tile_columns<BN>(kp, sg.tile, sg.tile / kp.n_tiles, gn0, gn_end, c_base);
         int ih0[ROWS], iw0[ROWS], img[ROWS];
 #pragma unroll
         for (int i = 0; i < ROWS; ++i) {
@@ -803,8 +823,8 @@ __device__ void run_gather_cpasync(const ConvKernelParams& kp, const SmemView& s
                 const bool col_ok = kk < kp.CRS;
                 int dih = 0, diw = 0, c = 0;
                 if (col_ok) {
-                    const int rs = kk / kp.C;
-                    c = kk - rs * kp.C;
+                    const int rs = kk / kp.Cg;
+                    c = c_base + (kk - rs * kp.Cg);
                     const int r = rs / kp.S;
                     dih = r * kp.dh;
                     diw = (rs - r * kp.S) * kp.dw;
@@ -845,14 +865,15 @@ __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm
     Segment sg;
     while (ok && walk.next(kp, sg)) {
         const int m_tile = sg.tile / kp.n_tiles;
-        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int n0, n_end, c_base;
+        tile_columns<BN>(kp, sg.tile, m_tile, n0, n_end, c_base);
         const int m = m_tile * BM + row;
         const bool row_ok = m < kp.M;
         int n_img = 0, p = 0, q = 0;
         if (row_ok) decode_pixel(kp, m, n_img, p, q);
         const int ih0 = p * kp.sh - kp.ph;
         const int iw0 = q * kp.sw - kp.pw;
-        const uint16_t* xb = kp.x + static_cast<int64_t>(n_img) * kp.H * kp.W * kp.C;
+        const uint16_t* xb = kp.x + static_cast<int64_t>(n_img) * kp.H * kp.W * kp.C + c_base;
         for (int kb = sg.kb_begin; kb < sg.kb_end; ++kb, ++it) {
             const int stage = it % STAGES;
             const uint32_t parity = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -868,8 +889,8 @@ __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm
             const int kk0 = kb * BK;
             // A row: walk (r, s, c) incrementally from kk0.
             {
-                const int rs0 = kk0 / kp.C;
-                int c = kk0 - rs0 * kp.C;
+                const int rs0 = kk0 / kp.Cg;
+                int c = kk0 - rs0 * kp.Cg;
                 int r = rs0 / kp.S;
                 int s = rs0 - r * kp.S;
                 const uint32_t base = ptx::smem_addr(sm.a + stage * A_STAGE_BYTES);
@@ -890,7 +911,7 @@ __device__ void run_gather_scalar(const ConvKernelParams& kp, const SmemView& sm
                         }
                         if (e & 1) packed[e >> 1] |= v << 16;
                         else packed[e >> 1] = v;
-                        if (++c == kp.C) {
+                        if (++c == kp.Cg) {
                             c = 0;
                             if (++s == kp.S) {
                                 s = 0;
@@ -1008,7 +1029,8 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         const int buf = seg_idx % Cfg::NUM_ACC;
         const uint32_t use = static_cast<uint32_t>(seg_idx / Cfg::NUM_ACC) & 1u;
         const int m_tile = sg.tile / kp.n_tiles;
-        const int n0 = (sg.tile - m_tile * kp.n_tiles) * BN;
+        int n0, n_end, c_base_unused;
+        tile_columns<BN>(kp, sg.tile, m_tile, n0, n_end, c_base_unused);
         int bx_n = 0, bx_p = 0, bx_q = 0;
         if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, bx_n, bx_p, bx_q);
         const bool add_bias = kp.bias != nullptr && sg.split == 0;
@@ -1022,9 +1044,9 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
             const int cbase = n0 + (jbeg + j) * 32;
             bias4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             bias_r[j] = 0.f;
-            if (add_bias && kp.vec_store && cbase + chunk * 4 < kp.K)
+            if (add_bias && kp.vec_store && cbase + chunk * 4 < n_end)
                 bias4[j] = __ldg(reinterpret_cast<const float4*>(kp.bias + cbase + chunk * 4));
-            if (add_bias && !kp.vec_store && cbase + lane < kp.K) bias_r[j] = __ldg(kp.bias + cbase + lane);
+            if (add_bias && !kp.vec_store && cbase + lane < n_end) bias_r[j] = __ldg(kp.bias + cbase + lane);
         }
         // One thread polls the accumulator barrier; the others wait at the named
         // barrier below (polling shared memory from every warp would steal issue
@@ -1099,7 +1121,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                             val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
                             val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
                         }
-                        if (m >= 0 && col < kp.K) {
+                        if (m >= 0 && col < n_end) {
                             float* dst = kp.y + static_cast<int64_t>(m) * kp.K + col;
                             if (sg.split == 0) *reinterpret_cast<uint4*>(dst) = val;
                             else ptx::red_add_v4_f32(dst, val);
@@ -1133,12 +1155,12 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                     float old[32];
                     if (accumulate && !kp.reduce_concurrent) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) old[e] = nb + e < kp.K ? yrow[nb + e] : 0.0f;
+                        for (int e = 0; e < 32; ++e) old[e] = nb + e < n_end ? yrow[nb + e] : 0.0f;
                     }
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int n = nb + e;
-                        if (n >= kp.K) break;
+                        if (n >= n_end) break;
                         float o = __uint_as_float(v[e]);
                         if (accumulate && kp.reduce_concurrent) {
                             atomicAdd(yrow + n, o);

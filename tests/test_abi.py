@@ -43,10 +43,14 @@ def test_output_shape_host_only():
     assert sg.output_shape(_params(x_shape=(32, 224, 224, 3), w_shape=(64, 7, 7, 3), stride=2, padding=3)) == (112, 112)
     assert sg.output_shape(_params(x_shape=(8, 64, 64, 128), w_shape=(128, 3, 3, 128), padding=2, dilation=2)) == (64, 64)
     assert sg.output_shape(_params(x_shape=(32, 56, 56, 256), w_shape=(512, 1, 1, 256), stride=2, padding=0)) == (28, 28)
+    # grouped: the weight holds C/groups channels per tap
+    assert sg.output_shape(_params(w_shape=(64, 3, 3, 16), groups=4)) == (56, 56)
+    with pytest.raises(ValueError):
+        _params(w_shape=(64, 3, 3, 64), groups=4)
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(groups=2), 2),                                          # grouped conv: unsupported, no fallback
+    (dict(groups=3), 1),                                          # groups must divide C (64) and K
     (dict(groups=0), 1),
     (dict(x_shape=(1, 2, 2, 3), w_shape=(4, 5, 5, 3), padding=0), 1),  # window does not fit
     (dict(stride=0), 1),

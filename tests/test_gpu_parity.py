@@ -144,9 +144,14 @@ def test_misaligned_pointer_rejected_before_launch(sg):
     assert e.value.code == 3
 
 
-def test_groups_rejected(sg):
-    x = torch.zeros((1, 8, 8, 16), dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros((16, 3, 3, 8), dtype=torch.bfloat16, device="cuda")
+def test_groups_that_do_not_divide_rejected(sg):
+    # groups must divide both C and K (CONV2D_ERR_INVALID); a dividing value runs.
+    x = torch.zeros((1, 8, 8, 18), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((16, 3, 3, 6), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(sg.Conv2dError) as e:
-        sg.conv2d_fwd(x, w, None, padding=1, groups=2)
-    assert e.value.code == 2
+        sg.conv2d_fwd(x, w, None, padding=1, groups=3)  # C = 18 divides, K = 16 does not
+    assert e.value.code == 1
+    y = sg.conv2d_fwd(x[..., :16].contiguous(), torch.zeros((16, 3, 3, 8), dtype=torch.bfloat16, device="cuda"),
+                      None, padding=1, groups=2)
+    torch.cuda.synchronize()
+    assert y.shape == (1, 8, 8, 16) and not bool(y.abs().sum())
