@@ -99,3 +99,10 @@ def test_box_halo_and_row_window_refuse_groups(sg):
     for loader in (5, 6, 7):
         with pytest.raises(m.Conv2dError):
             gpu_conv(sg, x, w, b, wl.options(), algo=make_algo(sg, loader=loader))
+
+
+@pytest.mark.parametrize("name", sorted(workloads.GROUPED))
+def test_grouped_workload_full_size(sg, name):
+    wl = workloads.get(name)
+    x, w, b = workloads.make_inputs(wl)
+    _check(sg, wl, x, w, b, None, name)

@@ -97,6 +97,20 @@ WORKLOADS = {
     ]
 }
 
+# Grouped convolutions (beyond the benchmark list): a ResNeXt-style 3x3 layer with
+# 32 groups of 8 channels, and one with 8 groups of 64 channels.
+GROUPED = {
+    wl.name: wl for wl in [
+        Workload("resnext_28x28_c256_g32", 16, 28, 28, 256, 256, 3, 3, 1, 1, 1, 1, 1, 1,
+                 x_dist="normal", w_dist="he", bias="normal:0.1", groups=32,
+                 note="32 groups of 8 channels: 32 GEMMs 12544x8x72"),
+        Workload("grouped_28x28_c512_g8", 16, 28, 28, 512, 512, 3, 3, 1, 1, 1, 1, 1, 1,
+                 x_dist="normal", w_dist="he", bias="normal:0.1", groups=8,
+                 note="8 groups of 64 channels: 8 GEMMs 12544x64x576"),
+    ]
+}
+WORKLOADS.update(GROUPED)
+
 # Order in which the benchmark list names them.
 ORDER = ["tiny_8x8_c16", "resnet_56x56_c64", "resnet_28x28_c256", "splitk_7x7_c2048",
          "stem_224_c3_7x7s2", "proj_56_c256_1x1s2", "dil2_64_c128"]
