@@ -68,14 +68,15 @@ def _touched(extent_in, extent_out, stride, pad, dil, ker):
     return len(rows)
 
 
-def algorithmic_bytes(wl):
-    """Input pixels some window touches (bf16) + weight (bf16) + output (fp32) + bias (fp32)."""
+def algorithmic_bytes(wl, out_bytes=4):
+    """Input pixels some window touches (bf16) + weight (bf16) + output (fp32, or bf16 with
+    the fused bf16-output epilogue) + bias (fp32)."""
     p, q = shape_of(wl)
     th = _touched(wl.h, p, wl.stride_h, wl.pad_h, wl.dil_h, wl.r)
     tw = _touched(wl.w, q, wl.stride_w, wl.pad_w, wl.dil_w, wl.s)
     x_b = wl.n * th * tw * wl.c * 2
     w_b = wl.k * wl.r * wl.s * (wl.c // wl.groups) * 2
-    y_b = wl.n * p * q * wl.k * 4
+    y_b = wl.n * p * q * wl.k * out_bytes
     b_b = wl.k * 4 if wl.bias is not None else 0
     return float(x_b + w_b + y_b + b_b)
 
@@ -294,24 +295,27 @@ def run_ours(args, wl, world, rank, local):
         forced = sg.Algo()
         forced.block_n, forced.splits, forced.loader, forced.grid = args.block_n, args.splits, args.loader, args.grid
         forced.block_m, forced.reduction = args.block_m, args.reduction
-    algo = sg.query_algo(params)
+    relu, out_bf16 = args.epilogue in ("relu", "relu_bf16"), args.epilogue in ("bf16", "relu_bf16")
+    y_dtype, y_bytes = (torch.bfloat16, 2) if out_bf16 else (torch.float32, 4)
+    algo = sg.query_algo(params, relu=relu, out_bf16=out_bf16)
     if forced is not None:
         algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, forced.loader or algo.loader,
                        forced.grid or (0 if forced.splits else algo.grid), 0, forced.block_m or algo.block_m, 0,
                        forced.reduction or algo.reduction)
-    set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * 4 + (0 if b is None else b.numel() * 4)
+    set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * y_bytes + (0 if b is None else b.numel() * 4)
     n_sets = _sets_for(wl, set_bytes)
     sets = []
     for _ in range(n_sets):
         sets.append((x.to(dev), w.to(dev), None if b is None else b.to(dev),
-                     torch.empty((wl.n, p, q, wl.k), dtype=torch.float32, device=dev)))
-    ws = torch.zeros(max(4096, sg.workspace_bytes(params)), dtype=torch.uint8, device=dev)
+                     torch.empty((wl.n, p, q, wl.k), dtype=y_dtype, device=dev)))
+    ws_need = sg.epi_workspace_bytes(params, forced, relu, out_bf16) if (relu or out_bf16) else sg.workspace_bytes(params)
+    ws = torch.zeros(max(4096, ws_need), dtype=torch.uint8, device=dev)
     opts = wl.options()
     stream = torch.cuda.Stream(dev)
 
     def step(i):
         xd, wd, bd, yd = sets[i % n_sets]
-        sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws, algo=forced)
+        sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws, algo=forced, relu=relu)
 
     K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
@@ -362,7 +366,7 @@ def run_ours(args, wl, world, rank, local):
     job_s, job_flops = aggregate(dist_mod, elapsed, flops * K, dev)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.epilogue == "none":
         e2e = run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, min(K, args.e2e_steps), dist_mod)
     return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
                 clocks=clocks.summary(t_host0, t_host1), status=status, e2e=e2e, dist=dist_mod,
@@ -423,10 +427,10 @@ def config_of(wl, extra=None):
     return cfg
 
 
-def roofline(wl, t_step_s, peaks, peak_src):
-    flops, nbytes = flops_per_step(wl), algorithmic_bytes(wl)
+def roofline(wl, t_step_s, peaks, peak_src, out_bytes=4):
+    flops, nbytes = flops_per_step(wl), algorithmic_bytes(wl, out_bytes)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = recorded_traffic(wl.name)
+    traffic = recorded_traffic(wl.name) if out_bytes == 4 else None
     if flops / nbytes >= ridge:
         achieved = flops / t_step_s / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -462,10 +466,14 @@ def main_ours(args):
         "dtype": "bf16", "data": "synthetic",
         "config": config_of(wl, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                  "algo": res["algo"], "accumulate": "fp32 (TMEM)",
+                                 "epilogue": {"none": "bias, fp32 y", "relu": "bias, ReLU, fp32 y",
+                                              "bf16": "bias, bf16 y", "relu_bf16": "bias, ReLU, bf16 y"}[args.epilogue],
+                                 **({"layout": "x NHWC bf16, w KRSC bf16, bias fp32, y NHWC bf16"}
+                                    if args.epilogue in ("bf16", "relu_bf16") else {}),
                                  "l2": f"{res['n_sets']} rotating input/output buffer sets (> 2x L2) per step",
                                  "timing": f"CUDA events around CUDA-graph replays ({res['graph_chunk']} launches "
                                            "per graph), max over ranks"}),
-        "roofline": roofline(wl, t_step, peaks, peak_src),
+        "roofline": roofline(wl, t_step, peaks, peak_src, 2 if args.epilogue in ("bf16", "relu_bf16") else 4),
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "gpu_launches": K,
@@ -523,6 +531,8 @@ def parse_args(argv=None):
     ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box, 7 halo)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
+    ap.add_argument("--epilogue", default="none", choices=["none", "relu", "bf16", "relu_bf16"],
+                    help="fused epilogue variant (ReLU after the bias, bf16 output); the e2e leg runs only for none")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")

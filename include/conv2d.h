@@ -186,6 +186,65 @@ int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void*
  * thread enqueued (1 for every algorithm; 0 before any call and for empty problems). */
 int conv2d_last_launch_count(void);
 
+/* Fused epilogue.  After the bias, the epilogue may apply an activation and
+ * may store y in bf16 instead of fp32:
+ *   y[n][p][q][k] = round_out(act(acc + bias[k]))
+ * with act = identity or ReLU (max(v, 0), applied to the fp32 value) and
+ * round_out = identity (fp32 y) or fp32 -> bf16 round to nearest even.
+ * A bf16 output cannot hold the partial sums of a tile cut between CTAs (the
+ * in-place reduction needs the fp32 accumulator type in y; NVIDIA/Fuser issue
+ * #1316 "Split-K matmul is slow even for few partitions", the comment on
+ * aliasing the output as the reduction work buffer, notes the same for a
+ * half-precision output), and ReLU needs the finished sum.  So under a fused
+ * epilogue the splits of a cut tile add their partial sums into a separate
+ * fp32 [M][K] buffer in the workspace (atomic adds in L2, no waiting), and the
+ * CTA that arrives last at the tile's counter reads the complete sum back, adds
+ * the bias, applies the activation, converts, stores y and zeroes its part of
+ * the buffer again.  The heuristic still splits few-tile, long-reduction
+ * problems (classic split-K); where it would cut tiles stream-K style over many
+ * tiles it gives each CTA whole tiles instead.  conv2d_fwd_epi_workspace_bytes
+ * gives the workspace a fused call needs. */
+typedef enum {
+    CONV2D_ACT_NONE = 0,
+    CONV2D_ACT_RELU = 1
+} conv2d_activation;
+
+typedef enum {
+    CONV2D_OUT_F32 = 0,   /* y is float[N][P][Q][K] */
+    CONV2D_OUT_BF16 = 1   /* y is bf16 (uint16 bit patterns) [N][P][Q][K] */
+} conv2d_out_dtype;
+
+typedef struct {
+    int32_t activation;  /* conv2d_activation */
+    int32_t out_dtype;   /* conv2d_out_dtype */
+} conv2d_epilogue;
+
+/* conv2d_fwd_ex with a fused epilogue.  y_dev points to N*P*Q*K values of the
+ * type `epi->out_dtype` names (16-byte aligned, caller-owned, fully
+ * overwritten).  algo may be NULL (heuristic); epi may be NULL, which is the
+ * plain fp32 epilogue and then this call is conv2d_fwd_ex itself.  Returns
+ * CONV2D_ERR_INVALID for an unknown activation or output type, and
+ * CONV2D_ERR_WORKSPACE when the plan cuts tiles and the workspace is smaller
+ * than conv2d_fwd_epi_workspace_bytes(params, algo, epi).  The workspace
+ * follows the rules of conv2d_fwd's (zero before first use; left zero by every
+ * successful call, partial-sum buffer included). */
+int conv2d_fwd_epi(const conv2d_params* params, const void* x_dev, const void* w_dev,
+                   const float* bias_dev, void* y_dev, void* workspace_dev,
+                   size_t workspace_bytes, conv2d_stream_t stream, const conv2d_algo* algo,
+                   const conv2d_epilogue* epi);
+
+/* Bytes of workspace conv2d_fwd_epi needs with this configuration (algo NULL:
+ * the heuristic's) and epilogue: conv2d_fwd_workspace_bytes, plus
+ * 256-byte-aligned room for an fp32 [M][K] partial-sum buffer when a fused
+ * epilogue's plan cuts tiles.  Uses the current device's SM count, as the
+ * heuristic does; 0 for invalid params. */
+size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_algo* algo,
+                                      const conv2d_epilogue* epi);
+
+/* What the heuristic picks for conv2d_fwd_epi with this epilogue (NULL: as
+ * conv2d_fwd_query_algo).  A fused epilogue's plan gives every tile to one CTA. */
+int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue* epi, conv2d_algo* out);
+
 /* Size of the library's built-in device scratch array used by conv2d_fwd_noalloc. */
 #define CONV2D_NOALLOC_SCRATCH_BYTES 65536
 

@@ -9,6 +9,9 @@ loaded, every call raises.
     y = conv2d_fwd(x, w, bias, stride=1, padding=0, dilation=1)
       x: [N,H,W,C] bf16 CUDA tensor (NHWC), w: [K,R,S,C] bf16 (KRSC),
       bias: [K] fp32 or None  ->  y: [N,P,Q,K] fp32 (NHWC)
+
+    y = conv2d_fwd(x, w, bias, relu=True, out_dtype=torch.bfloat16)
+      the fused epilogue: ReLU after the bias, y stored as bf16 (whole-tile plans)
 """
 from __future__ import annotations
 
@@ -22,9 +25,9 @@ from . import _build
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
     "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "REDUCTION_AUTO", "REDUCTION_ORDERED",
-    "REDUCTION_CONCURRENT",
+    "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
-    "query_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
+    "query_algo", "epi_workspace_bytes", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
     "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
 ]
 
@@ -32,6 +35,8 @@ LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR, LOADER_HYBRID, LO
 LOADER_TMA_BOX = 6
 LOADER_HALO = 7
 REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
+ACT_NONE, ACT_RELU = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
 DEBUG_SKIP_SIGNAL = 1
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
                 4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT",
@@ -40,7 +45,8 @@ STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPOR
 EXPORTED_SYMBOLS = [
     "conv2d_fwd_output_shape", "conv2d_fwd_workspace_bytes", "conv2d_fwd", "conv2d_fwd_ex",
     "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
-    "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc",
+    "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc", "conv2d_fwd_epi",
+    "conv2d_fwd_query_algo_epi", "conv2d_fwd_epi_workspace_bytes",
 ]
 
 
@@ -68,6 +74,10 @@ class Algo(ctypes.Structure):
                     grid=self.grid, reduction=self.reduction)
 
 
+class Epilogue(ctypes.Structure):
+    _fields_ = [("activation", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -88,6 +98,12 @@ def _bind(lib):
     lib.conv2d_fwd.restype = ctypes.c_int
     lib.conv2d_fwd_ex.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, A]
     lib.conv2d_fwd_ex.restype = ctypes.c_int
+    lib.conv2d_fwd_epi.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, A, ctypes.POINTER(Epilogue)]
+    lib.conv2d_fwd_epi.restype = ctypes.c_int
+    lib.conv2d_fwd_epi_workspace_bytes.argtypes = [P, A, ctypes.POINTER(Epilogue)]
+    lib.conv2d_fwd_epi_workspace_bytes.restype = sz
+    lib.conv2d_fwd_query_algo_epi.argtypes = [P, ctypes.POINTER(Epilogue), A]
+    lib.conv2d_fwd_query_algo_epi.restype = ctypes.c_int
     lib.conv2d_fwd_query_algo.argtypes = [P, A]
     lib.conv2d_fwd_query_algo.restype = ctypes.c_int
     lib.conv2d_fwd_status.argtypes = [vp, sz, vp]
@@ -162,13 +178,26 @@ def workspace_bytes(params: Params) -> int:
     return int(load_library().conv2d_fwd_workspace_bytes(ctypes.byref(params)))
 
 
+def epi_workspace_bytes(params: Params, algo: Optional[Algo] = None, relu: bool = False,
+                        out_bf16: bool = False) -> int:
+    """Workspace bytes a fused-epilogue call needs with this configuration (None: the heuristic's)."""
+    epi = Epilogue(ACT_RELU if relu else ACT_NONE, OUT_BF16 if out_bf16 else OUT_F32)
+    return int(load_library().conv2d_fwd_epi_workspace_bytes(
+        ctypes.byref(params), None if algo is None else ctypes.byref(algo), ctypes.byref(epi)))
+
+
 def host_staging_bytes(params: Params) -> int:
     return int(load_library().conv2d_fwd_host_staging_bytes(ctypes.byref(params)))
 
 
-def query_algo(params: Params) -> Algo:
+def query_algo(params: Params, relu: bool = False, out_bf16: bool = False) -> Algo:
+    """The heuristic's configuration; with ``relu``/``out_bf16`` that of the fused epilogue's call."""
     out = Algo()
-    rc = load_library().conv2d_fwd_query_algo(ctypes.byref(params), ctypes.byref(out))
+    if relu or out_bf16:
+        epi = Epilogue(ACT_RELU if relu else ACT_NONE, OUT_BF16 if out_bf16 else OUT_F32)
+        rc = load_library().conv2d_fwd_query_algo_epi(ctypes.byref(params), ctypes.byref(epi), ctypes.byref(out))
+    else:
+        rc = load_library().conv2d_fwd_query_algo(ctypes.byref(params), ctypes.byref(out))
     if rc:
         raise Conv2dError(rc, "conv2d_fwd_query_algo")
     return out
@@ -208,36 +237,53 @@ def _check_tensor(t, name, dtype, ndim):
 
 
 def conv2d_fwd_into(y, x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
-                    algo: Optional[Algo] = None, stream=None) -> None:
-    """Writes conv2d(x, w) + bias into the preallocated fp32 NHWC tensor ``y`` (asynchronous)."""
+                    algo: Optional[Algo] = None, stream=None, relu: bool = False) -> None:
+    """Writes conv2d(x, w) + bias into the preallocated NHWC tensor ``y`` (asynchronous).
+
+    ``y`` is fp32, or bf16 for the fused bf16-output epilogue; ``relu`` applies
+    max(v, 0) after the bias.  Under either fused option a tile cut between CTAs is
+    summed in an fp32 buffer in the workspace and finished by its last CTA.
+    """
     import torch
     _check_tensor(x, "x", torch.bfloat16, 4)
     _check_tensor(w, "w", torch.bfloat16, 4)
-    _check_tensor(y, "y", torch.float32, 4)
+    _check_tensor(y, "y", torch.bfloat16 if y.dtype == torch.bfloat16 else torch.float32, 4)
     if bias is not None:
         _check_tensor(bias, "bias", torch.float32, 1)
     params = make_params(x.shape, w.shape, stride, padding, dilation, groups)
     lib = load_library()
+    fused = relu or y.dtype == torch.bfloat16
     if workspace is None:
-        workspace = _default_workspace(workspace_bytes(params), x.device)
+        need = epi_workspace_bytes(params, algo, relu, y.dtype == torch.bfloat16) if fused else workspace_bytes(params)
+        workspace = _default_workspace(need, x.device)
     ws_ptr, ws_len = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     args = (ctypes.byref(params), x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
             y.data_ptr(), ws_ptr, ws_len, st.cuda_stream)
-    rc = lib.conv2d_fwd(*args) if algo is None else lib.conv2d_fwd_ex(*args, ctypes.byref(algo))
+    if fused:
+        epi = Epilogue(ACT_RELU if relu else ACT_NONE, OUT_BF16 if y.dtype == torch.bfloat16 else OUT_F32)
+        rc = lib.conv2d_fwd_epi(*args, None if algo is None else ctypes.byref(algo), ctypes.byref(epi))
+    else:
+        rc = lib.conv2d_fwd(*args) if algo is None else lib.conv2d_fwd_ex(*args, ctypes.byref(algo))
     if rc:
         raise Conv2dError(rc, "conv2d_fwd")
 
 
 def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
-               algo: Optional[Algo] = None, stream=None):
-    """Returns y = conv2d(x, w) + bias as a new fp32 NHWC CUDA tensor (asynchronous)."""
+               algo: Optional[Algo] = None, stream=None, relu: bool = False, out_dtype=None):
+    """Returns y = conv2d(x, w) + bias as a new NHWC CUDA tensor (asynchronous).
+
+    ``out_dtype``: torch.float32 (default) or torch.bfloat16; ``relu``: see conv2d_fwd_into.
+    """
     import torch
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"out_dtype must be torch.float32 or torch.bfloat16, got {out_dtype}")
     params = make_params(x.shape, w.shape, stride, padding, dilation, groups)
     p, q = output_shape(params)
-    y = torch.empty((params.n, p, q, params.k), dtype=torch.float32, device=x.device)
+    y = torch.empty((params.n, p, q, params.k), dtype=out_dtype, device=x.device)
     conv2d_fwd_into(y, x, w, bias, stride, padding, dilation, groups, workspace=workspace, algo=algo,
-                    stream=stream)
+                    stream=stream, relu=relu)
     return y
 
 

@@ -367,7 +367,10 @@ int64_t semaphore_capacity(const Shape& s)
 constexpr int kMinUnitsPerCta = 4;     // no split gets fewer k-blocks than this
 constexpr int kMaxSplitsPerTile = 6;   // longest serial in-place reduction chain the heuristic builds
 
-int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
+// whole_tiles: where the heuristic would divide many tiles stream-K style over
+// the SMs, give every CTA whole tiles instead.  A fused epilogue (bf16 output,
+// activation) asks for it: its cut tiles take a detour through an fp32 buffer.
+int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles = false)
 {
     const int sms = sm_count_current();
     // Loader.
@@ -476,7 +479,17 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     const int64_t units = tiles * num_kb;
     int64_t splits = forced_splits;
     int64_t grid = forced_grid;
-    if (splits == 0 && grid == 0) {
+    if (splits == 0 && grid == 0 && whole_tiles && tiles >= nsm) {
+        // Each CTA takes whole tiles: the smallest whole-tile share per CTA that
+        // fits the SMs in one wave and divides the tiles evenly, else one tile per CTA.
+        grid = tiles;
+        const int64_t per_cta = cdiv(tiles, nsm);
+        for (int64_t d = per_cta; d <= 2 * per_cta; ++d)
+            if (tiles % d == 0) {
+                grid = tiles / d;
+                break;
+            }
+    } else if (splits == 0 && grid == 0) {
         if (tiles >= nsm) {
             // Persistent: every SM takes the same number of whole tiles where that
             // divides out, otherwise an even share of (tile, k-block) units.
@@ -501,7 +514,7 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     }
     if (grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
     // A plan that cuts tiles needs one semaphore per tile.
-    if (((units % grid) != 0 || (units / grid) % num_kb != 0) && tiles > semaphore_capacity(s))
+    if (num_kb > 1 && ((units % grid) != 0 || (units / grid) % num_kb != 0) && tiles > semaphore_capacity(s))
         return CONV2D_ERR_UNSUPPORTED;
     plan->box = geom;
     plan->halo = hgeom;
@@ -517,10 +530,31 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan)
     return CONV2D_OK;
 }
 
+// CTA b takes units [b*units/grid, (b+1)*units/grid): a tile is cut when a
+// boundary falls inside its num_kb units.  With one unit per tile no boundary
+// can; otherwise equal shares that are whole multiples of num_kb cut nothing,
+// and every other division is treated as cutting (it may spare some tiles).
+bool plan_cuts_tiles(const Plan& p)
+{
+    if (p.num_kb <= 1) return false;
+    return (p.units % p.grid) != 0 || (p.units / p.grid) % p.num_kb != 0;
+}
+
 size_t workspace_bytes_for(const Shape& s)
 {
     // Enough semaphores for the narrowest tile width.
     return kStatusBytes + static_cast<size_t>(semaphore_capacity(s)) * sizeof(uint32_t);
+}
+
+// Where the fused epilogue's fp32 partial-sum buffer starts in the workspace.
+size_t part_offset(const Shape& s) { return (workspace_bytes_for(s) + 255) & ~size_t(255); }
+
+// Workspace one call needs: status and semaphores, plus under a fused epilogue
+// an fp32 [M][K] partial-sum buffer when the plan cuts tiles.
+size_t workspace_bytes_for_plan(const Shape& s, const Plan& plan, bool fused)
+{
+    if (fused && plan_cuts_tiles(plan)) return part_offset(s) + static_cast<size_t>(s.m * s.k) * sizeof(float);
+    return workspace_bytes_for(s);
 }
 
 // ------------------------------------------------------------------ descriptors
@@ -643,7 +677,8 @@ bool log_enabled()
 }
 
 int run_conv(const conv2d_params* params, const void* x, const void* w, const float* bias, float* y,
-             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo,
+             const conv2d_epilogue* epi = nullptr)
 {
     g_last_launches = 0;
     Shape s;
@@ -658,13 +693,21 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
                  algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
                  algo->reduction > CONV2D_REDUCTION_CONCURRENT))
         return CONV2D_ERR_INVALID;
+    if (epi && (epi->activation < CONV2D_ACT_NONE || epi->activation > CONV2D_ACT_RELU ||
+                epi->out_dtype < CONV2D_OUT_F32 || epi->out_dtype > CONV2D_OUT_BF16))
+        return CONV2D_ERR_INVALID;
+    const bool relu = epi && epi->activation == CONV2D_ACT_RELU;
+    const bool out_bf16 = epi && epi->out_dtype == CONV2D_OUT_BF16;
+    const bool fused = relu || out_bf16;
     Plan plan;
-    rc = choose_plan(s, algo, &plan);
+    rc = choose_plan(s, algo, &plan, fused);
     if (rc != CONV2D_OK) return rc;
     const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(s);
-    // Any tile cut between CTAs needs the semaphores.
-    const bool cuts_tiles = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
-    if (cuts_tiles && !have_ws) return CONV2D_ERR_WORKSPACE;
+    // Any tile cut between CTAs needs the semaphores (and, under a fused
+    // epilogue, the partial-sum buffer).
+    const bool cuts_tiles = plan_cuts_tiles(plan);
+    if (cuts_tiles && (!workspace || workspace_bytes < workspace_bytes_for_plan(s, plan, fused)))
+        return CONV2D_ERR_WORKSPACE;
     if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
     const bool vec_store = (s.k % 4) == 0 && (s.kg % 4) == 0;  // 16-byte vector writes inside one group's columns
     if (plan.loader == CONV2D_LOADER_ROW_WINDOW) {
@@ -701,6 +744,8 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
         rp.grid = plan.grid;
         rp.tmem_cols = rw.tmem_cols;
         rp.vec_store = vec_store ? 1 : 0;
+        rp.relu = relu ? 1 : 0;
+        rp.out_bf16 = out_bf16 ? 1 : 0;
         rp.x_bytes = s.n * s.h * s.w * s.c * 2;
         rp.w_bytes = s.k * s.crs * 2;
         rp.off_rows = rw.lay.off_rows;
@@ -757,6 +802,9 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.grid = plan.grid;
     kp.units = plan.units;
     kp.vec_store = vec_store ? 1 : 0;
+    kp.relu = relu ? 1 : 0;
+    kp.out_bf16 = out_bf16 ? 1 : 0;
+    kp.part = fused && cuts_tiles ? reinterpret_cast<float*>(static_cast<char*>(workspace) + part_offset(s)) : nullptr;
     kp.bw = plan.box.bw;
     kp.bh = plan.box.bh;
     kp.bn_img = plan.box.bn_img;
@@ -819,6 +867,14 @@ int conv2d_fwd_ex(const conv2d_params* params, const void* x_dev, const void* w_
                     reinterpret_cast<cudaStream_t>(stream), algo);
 }
 
+int conv2d_fwd_epi(const conv2d_params* params, const void* x_dev, const void* w_dev, const float* bias_dev,
+                   void* y_dev, void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream,
+                   const conv2d_algo* algo, const conv2d_epilogue* epi)
+{
+    return run_conv(params, x_dev, w_dev, bias_dev, static_cast<float*>(y_dev), workspace_dev, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream), algo, epi);
+}
+
 int conv2d_fwd(const conv2d_params* params, const void* x_dev, const void* w_dev, const float* bias_dev,
                float* y_dev, void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream)
 {
@@ -826,14 +882,18 @@ int conv2d_fwd(const conv2d_params* params, const void* x_dev, const void* w_dev
                     reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
-int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
+int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue* epi, conv2d_algo* out)
 {
     if (!out) return CONV2D_ERR_INVALID;
+    if (epi && (epi->activation < CONV2D_ACT_NONE || epi->activation > CONV2D_ACT_RELU ||
+                epi->out_dtype < CONV2D_OUT_F32 || epi->out_dtype > CONV2D_OUT_BF16))
+        return CONV2D_ERR_INVALID;
+    const bool fused = epi && (epi->activation != CONV2D_ACT_NONE || epi->out_dtype != CONV2D_OUT_F32);
     Shape s;
     int rc = make_shape(params, &s);
     if (rc != CONV2D_OK) return rc;
     Plan plan;
-    rc = choose_plan(s, nullptr, &plan);
+    rc = choose_plan(s, nullptr, &plan, fused);
     if (rc != CONV2D_OK) return rc;
     std::memset(out, 0, sizeof(*out));
     out->block_m = plan.block_m;
@@ -841,9 +901,26 @@ int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
     out->splits = plan.splits;
     out->loader = plan.loader;
     out->grid = plan.grid;
-    const bool cuts = (plan.units % plan.grid) != 0 || (plan.units / plan.grid) % plan.num_kb != 0;
+    const bool cuts = plan_cuts_tiles(plan);
     out->reduction = cuts ? CONV2D_REDUCTION_CONCURRENT : CONV2D_REDUCTION_AUTO;
     return CONV2D_OK;
+}
+
+size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_algo* algo,
+                                      const conv2d_epilogue* epi)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    const bool fused = epi && (epi->activation != CONV2D_ACT_NONE || epi->out_dtype != CONV2D_OUT_F32);
+    if (!fused) return workspace_bytes_for(s);
+    Plan plan;
+    if (s.m == 0 || s.k == 0 || choose_plan(s, algo, &plan, true) != CONV2D_OK) return workspace_bytes_for(s);
+    return workspace_bytes_for_plan(s, plan, true);
+}
+
+int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
+{
+    return conv2d_fwd_query_algo_epi(params, nullptr, out);
 }
 
 int conv2d_fwd_status(void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream)

@@ -145,6 +145,12 @@ struct ConvKernelParams {
     int halo_tx;  // bytes one halo box delivers: 128 * wv * halo_rows (halo_bytes rounds it up to 1024)
     int debug_flags;
     int reduce_concurrent;    // 1: later splits add concurrently after split 0; 0: strict turns
+    // Fused epilogue: ReLU after the bias, and y stored as bf16 (round to nearest
+    // even) instead of fp32.  A tile cut between CTAs cannot be reduced in y then:
+    // its splits add their partial sums into `part` (fp32 [M][K], zero outside a
+    // call) and the CTA that arrives last at the tile's counter finishes it.
+    int relu, out_bf16;
+    float* part;
     unsigned long long wait_limit_ns;
     unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
 };
@@ -1003,6 +1009,86 @@ __device__ __forceinline__ void pass_turn(const ConvKernelParams& kp, const Segm
     ptx::st_release_gpu(kp.sems + sg.tile, next);
 }
 
+// Finishing pass of a cut tile under the fused epilogue: the tile's complete sum
+// from kp.part (read through L2), + bias, activation, conversion, store in y,
+// and the part buffer reset to zero.  Same thread-to-element mapping as the
+// accumulator stores.
+template <int BM, int BN, int LOADER>
+__device__ __forceinline__ void finish_from_part(const ConvKernelParams& kp, int m_tile, int n0, int n_end, int jbeg,
+                                                 int bx_n, int bx_p, int bx_q)
+{
+    using Cfg = TileConfig<BM, BN, LOADER>;
+    constexpr int SLABS = BN / 32 / (Cfg::EPI_WARPS / 4);
+    const int lane = threadIdx.x & 31;
+    const int quad = (threadIdx.x >> 5) & 3;
+    const int rsub = lane >> 3;
+    const int chunk = lane & 7;
+    uint16_t* yb = reinterpret_cast<uint16_t*>(kp.y);
+    // All loads of a slab are issued before any is used: one L2 round trip per
+    // slab rather than one per row.
+#pragma unroll 1
+    for (int sub = 0; sub < Cfg::M_SUB; ++sub) {
+        const int trow0 = sub * MMA_M;
+        if (kp.vec_store) {
+            int mrow[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mrow[i] = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + quad * 32 + 4 * i + rsub, bx_n, bx_p, bx_q);
+#pragma unroll
+            for (int j = 0; j < SLABS; ++j) {
+                const int col = n0 + (jbeg + j) * 32 + chunk * 4;
+                if (col >= n_end) continue;
+                const float4 b4 = kp.bias ? __ldg(reinterpret_cast<const float4*>(kp.bias + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < 8; h += 4) {  // four rows' loads in flight at a time
+                    float4 v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v[i] = mrow[h + i] >= 0
+                                   ? __ldcg(reinterpret_cast<const float4*>(kp.part + static_cast<int64_t>(mrow[h + i]) * kp.K + col))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (mrow[h + i] < 0) continue;
+                        const int64_t at = static_cast<int64_t>(mrow[h + i]) * kp.K + col;
+                        __stcg(reinterpret_cast<float4*>(kp.part + at), make_float4(0.f, 0.f, 0.f, 0.f));
+                        uint4 val = make_uint4(__float_as_uint(v[i].x + b4.x), __float_as_uint(v[i].y + b4.y),
+                                               __float_as_uint(v[i].z + b4.z), __float_as_uint(v[i].w + b4.w));
+                        if (kp.relu) val = ptx::relu4(val);
+                        if (kp.out_bf16) *reinterpret_cast<uint2*>(yb + at) = ptx::pack_bf16x4(val);
+                        else *reinterpret_cast<uint4*>(kp.y + at) = val;
+                    }
+                }
+            }
+        } else {
+            const int m = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + quad * 32 + lane, bx_n, bx_p, bx_q);
+#pragma unroll
+            for (int j = 0; j < SLABS; ++j) {
+                const int nb = n0 + (jbeg + j) * 32;
+                const int64_t at0 = static_cast<int64_t>(m < 0 ? 0 : m) * kp.K + nb;
+                const float bias_l = (kp.bias && nb + lane < n_end) ? __ldg(kp.bias + nb + lane) : 0.0f;
+#pragma unroll
+                for (int h = 0; h < 32; h += 16) {  // sixteen loads in flight at a time
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        v[e] = (m >= 0 && nb + h + e < n_end) ? __ldcg(kp.part + at0 + h + e) : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float bias = __shfl_sync(0xffffffffu, bias_l, h + e);
+                        if (m < 0 || nb + h + e >= n_end) continue;
+                        __stcg(kp.part + at0 + h + e, 0.0f);
+                        float o = v[e] + bias;
+                        if (kp.relu) o = fmaxf(o, 0.0f);
+                        if (kp.out_bf16) yb[at0 + h + e] = ptx::bf16_bits(o);
+                        else kp.y[at0 + h + e] = o;
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <int BM, int BN, int LOADER>
 __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                              uint32_t tmem_base)
@@ -1033,7 +1119,10 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         tile_columns<BN>(kp, sg.tile, m_tile, n0, n_end, c_base_unused);
         int bx_n = 0, bx_p = 0, bx_q = 0;
         if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, bx_n, bx_p, bx_q);
-        const bool add_bias = kp.bias != nullptr && sg.split == 0;
+        // Fused epilogue of a cut tile: partial sums go to kp.part, and the bias,
+        // the activation and the output conversion wait for the finishing pass.
+        const bool via_part = (kp.relu | kp.out_bf16) != 0 && sg.nsplits > 1;
+        const bool add_bias = kp.bias != nullptr && sg.split == 0 && !via_part;
         // Bias of this warp's slabs, fetched before the accumulator wait so that
         // its latency is hidden.  Vector stores: lane holds the four columns of its
         // 16-byte chunk; row stores: lane l holds column 32*j + l.
@@ -1060,7 +1149,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         ptx::named_bar_sync(1, EPI_T);
         if (et == 0) {
             bool go = *sm.abort_flag == 0u;
-            if (go && sg.split > 0)
+            if (go && sg.split > 0 && !via_part)
                 go = kp.reduce_concurrent ? wait_base(kp, sg.tile, sm.abort_flag)
                                           : wait_turn(kp, sg.tile, sg.split, sm.abort_flag);
             *sm.epi_go = go ? 1u : 0u;
@@ -1121,10 +1210,14 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                             val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
                             val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
                         }
+                        if (kp.relu && !via_part) val = ptx::relu4(val);
                         if (m >= 0 && col < n_end) {
-                            float* dst = kp.y + static_cast<int64_t>(m) * kp.K + col;
-                            if (sg.split == 0) *reinterpret_cast<uint4*>(dst) = val;
-                            else ptx::red_add_v4_f32(dst, val);
+                            const int64_t at = static_cast<int64_t>(m) * kp.K + col;
+                            if (via_part) ptx::red_add_v4_f32(kp.part + at, val);
+                            else if (kp.out_bf16)
+                                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
+                            else if (sg.split == 0) *reinterpret_cast<uint4*>(kp.y + at) = val;
+                            else ptx::red_add_v4_f32(kp.y + at, val);
                         }
                     }
                     SGB_CYCLES_END(c_slot, t_slot);
@@ -1152,6 +1245,13 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                     }
                     if (!row_ok) continue;
                     const int nb = n0 + (jbeg + j) * 32;
+                    if (via_part) {
+                        float* prow = kp.part + static_cast<int64_t>(m) * kp.K;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (nb + e < n_end) atomicAdd(prow + nb + e, __uint_as_float(v[e]));
+                        continue;
+                    }
                     float old[32];
                     if (accumulate && !kp.reduce_concurrent) {
 #pragma unroll
@@ -1162,6 +1262,11 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                         const int n = nb + e;
                         if (n >= n_end) break;
                         float o = __uint_as_float(v[e]);
+                        if (kp.relu) o = fmaxf(o, 0.0f);
+                        if (kp.out_bf16) {  // fused epilogue: whole tiles only
+                            reinterpret_cast<uint16_t*>(kp.y)[static_cast<int64_t>(m) * kp.K + n] = ptx::bf16_bits(o);
+                            continue;
+                        }
                         if (accumulate && kp.reduce_concurrent) {
                             atomicAdd(yrow + n, o);
                             continue;
@@ -1173,7 +1278,25 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
             }
         }
 
-        if (sg.nsplits > 1) {
+        if (via_part) {
+            // Every thread fences its adds, then one thread counts the CTA in; the
+            // CTA that completes the count (all splits' adds are then in L2) reads
+            // the sums back, finishes the tile and zeroes its part of the buffer.
+            __threadfence();
+            ptx::named_bar_sync(1, EPI_T);
+            if (et == 0) {
+                const uint32_t before = atomicAdd(kp.sems + sg.tile, 1u);
+                const bool last = before + 1u == static_cast<uint32_t>(sg.nsplits);
+                if (last) {
+                    atomicExch(kp.sems + sg.tile, 0u);
+                    __threadfence();
+                }
+                *sm.epi_go = last ? 2u : 1u;
+            }
+            ptx::named_bar_sync(1, EPI_T);
+            if (*sm.epi_go == 2u)
+                finish_from_part<BM, BN, LOADER>(kp, m_tile, n0, n_end, jbeg, bx_n, bx_p, bx_q);
+        } else if (sg.nsplits > 1) {
             SGB_CYCLES_BEGIN(t_done);
             // Before the next split may read or add: split 0's stores (both modes)
             // and every split's writes in the ordered mode must be complete and

@@ -96,6 +96,8 @@ struct RowWinParams {
     int tiles;         // N * qblocks * pblocks
     int grid;
     int vec_store;     // K % 4 == 0: 16-byte vector writes of y
+    int relu;          // fused epilogue: ReLU after the bias
+    int out_bf16;      // fused epilogue: y stored as bf16 (round to nearest even)
     uint32_t tmem_cols;  // power of two >= 2 * T * BN
     long long x_bytes;   // copies never read at or past these sizes
     long long w_bytes;
@@ -657,9 +659,16 @@ __device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t t
                     for (int i = 0; i < 8; ++i) {
                         const int rr = 4 * i + rsub;  // row within the warp's 32 rows
                         const int row = quad * 32 + rr;
-                        const uint4 val =
+                        uint4 val =
                             ptx::ld_shared_v4(saddr + static_cast<uint32_t>(rr * 128 + ((chunk ^ (rr & 7)) << 4)));
-                        if (row < nv && col < kp.K) *reinterpret_cast<uint4*>(kp.y + (m0 + row) * kp.K + col) = val;
+                        if (kp.relu) val = ptx::relu4(val);
+                        if (row < nv && col < kp.K) {
+                            if (kp.out_bf16)
+                                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + (m0 + row) * kp.K + col) =
+                                    ptx::pack_bf16x4(val);
+                            else
+                                *reinterpret_cast<uint4*>(kp.y + (m0 + row) * kp.K + col) = val;
+                        }
                     }
                     SGB_CYCLES_END(c_st, t_st);
                 }
@@ -685,7 +694,13 @@ __device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t t
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int n = j * 32 + e;
-                        if (n < kp.K) yrow[n] = __uint_as_float(v[e]);
+                        if (n >= kp.K) break;
+                        float o = __uint_as_float(v[e]);
+                        if (kp.relu) o = fmaxf(o, 0.0f);
+                        if (kp.out_bf16)
+                            reinterpret_cast<uint16_t*>(kp.y)[(m0 + row) * kp.K + n] = ptx::bf16_bits(o);
+                        else
+                            yrow[n] = o;
                     }
                 }
             }

@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 namespace sgb {
 namespace ptx {
 
@@ -270,6 +272,31 @@ __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
     uint16_t v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// Fused epilogue step: optional ReLU on four fp32 values.
+__device__ __forceinline__ uint4 relu4(uint4 v)
+{
+    v.x = __float_as_uint(fmaxf(__uint_as_float(v.x), 0.0f));
+    v.y = __float_as_uint(fmaxf(__uint_as_float(v.y), 0.0f));
+    v.z = __float_as_uint(fmaxf(__uint_as_float(v.z), 0.0f));
+    v.w = __float_as_uint(fmaxf(__uint_as_float(v.w), 0.0f));
+    return v;
+}
+
+// Four fp32 values rounded to bf16 (round to nearest even, CUDA's conversion
+// intrinsic), packed low half first.
+__device__ __forceinline__ uint2 pack_bf16x4(uint4 v)
+{
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(__uint_as_float(v.x), __uint_as_float(v.y));
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(__uint_as_float(v.z), __uint_as_float(v.w));
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float f)
+{
+    const __nv_bfloat16 b = __float2bfloat16_rn(f);
+    return *reinterpret_cast<const uint16_t*>(&b);
 }
 
 // Vector fp32 atomic add to global memory (no return value).

@@ -76,3 +76,15 @@ def test_strerror_covers_codes():
     for code in range(8):
         assert sg.strerror(code)
     assert sg.strerror(99) == "unknown status"
+
+
+@pytest.mark.parametrize("act,dtype", [(2, 0), (-1, 0), (0, 2), (1, -3)])
+def test_unknown_epilogue_rejected_before_any_device_work(act, dtype):
+    """An unknown activation or output type is CONV2D_ERR_INVALID; the check runs on the host
+    before anything touches the (here fake, never dereferenced) device pointers."""
+    lib = sg.load_library()
+    p = _params()
+    fake = 1 << 20  # 16-byte aligned, non-null
+    rc = lib.conv2d_fwd_epi(ctypes.byref(p), fake, fake, None, fake, None, 0, None, None,
+                            ctypes.byref(sg.Epilogue(act, dtype)))
+    assert rc == 1
