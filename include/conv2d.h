@@ -245,6 +245,34 @@ size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_
  * conv2d_fwd_query_algo).  A fused epilogue's plan gives every tile to one CTA. */
 int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue* epi, conv2d_algo* out);
 
+/* Weight gradient: the backward pass of the convolution with regard to the
+ * weight (docs.rs burn-cubecl 0.20.0, burn_cubecl/kernel/conv/base.rs,
+ * conv_weight_backward: the input feature map and the output gradient, both
+ * NHWC, give a weight gradient of the weight's shape in KRSC order):
+ *
+ *   dw[k][r][s][c] = sum_{n,p,q} dy[n][p][q][k] * x[n][p*sh - ph + r*dh][q*sw - pw + s*dw][c]
+ *
+ * out-of-image positions contributing zero.  params describe the forward
+ * convolution (x [N][H][W][C], weight [K][R][S][C]); x_dev: bf16 NHWC input;
+ * dy_dev: bf16 [N][P][Q][K] output gradient; dw_dev: fp32 [K][R][S][C], fully
+ * overwritten (zero for an empty batch).  Computed as an implicit GEMM on the
+ * forward kernel's pipeline: rows are output channels, columns (tap, channel)
+ * pairs, the reduction runs over the N*P*Q output pixels (split over CTAs and
+ * reduced in place in dw like a split forward tile; the workspace follows the
+ * rules of conv2d_fwd's).  Supported: groups == 1, C % 64 == 0 (im2col TMA
+ * boxes of 64 channels) and K % 8 == 0 (16-byte rows of dy); otherwise
+ * CONV2D_ERR_UNSUPPORTED.  algo may be NULL; block_n 64/128/256 is the channel
+ * width of a column block, splits/grid/reduction as for conv2d_fwd_ex;
+ * block_m must be 0 or 128 and loader 0 or CONV2D_LOADER_TMA_IM2COL. */
+size_t conv2d_bwd_weight_workspace_bytes(const conv2d_params* params);
+
+int conv2d_bwd_weight(const conv2d_params* params, const void* x_dev, const void* dy_dev, float* dw_dev,
+                      void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream,
+                      const conv2d_algo* algo);
+
+/* What the heuristic picks for conv2d_bwd_weight (no launch; current device's SM count). */
+int conv2d_bwd_weight_query_algo(const conv2d_params* params, conv2d_algo* out);
+
 /* Size of the library's built-in device scratch array used by conv2d_fwd_noalloc. */
 #define CONV2D_NOALLOC_SCRATCH_BYTES 65536
 

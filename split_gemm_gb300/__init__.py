@@ -27,7 +27,8 @@ __all__ = [
     "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "REDUCTION_AUTO", "REDUCTION_ORDERED",
     "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
-    "query_algo", "epi_workspace_bytes", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
+    "query_algo", "epi_workspace_bytes", "conv2d_bwd_weight", "conv2d_bwd_weight_into",
+    "wgrad_workspace_bytes", "query_wgrad_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
     "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
 ]
 
@@ -46,7 +47,8 @@ EXPORTED_SYMBOLS = [
     "conv2d_fwd_output_shape", "conv2d_fwd_workspace_bytes", "conv2d_fwd", "conv2d_fwd_ex",
     "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
     "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc", "conv2d_fwd_epi",
-    "conv2d_fwd_query_algo_epi", "conv2d_fwd_epi_workspace_bytes",
+    "conv2d_fwd_query_algo_epi", "conv2d_fwd_epi_workspace_bytes", "conv2d_bwd_weight_workspace_bytes",
+    "conv2d_bwd_weight", "conv2d_bwd_weight_query_algo",
 ]
 
 
@@ -104,6 +106,12 @@ def _bind(lib):
     lib.conv2d_fwd_epi_workspace_bytes.restype = sz
     lib.conv2d_fwd_query_algo_epi.argtypes = [P, ctypes.POINTER(Epilogue), A]
     lib.conv2d_fwd_query_algo_epi.restype = ctypes.c_int
+    lib.conv2d_bwd_weight_workspace_bytes.argtypes = [P]
+    lib.conv2d_bwd_weight_workspace_bytes.restype = sz
+    lib.conv2d_bwd_weight.argtypes = [P, vp, vp, vp, vp, sz, vp, A]
+    lib.conv2d_bwd_weight.restype = ctypes.c_int
+    lib.conv2d_bwd_weight_query_algo.argtypes = [P, A]
+    lib.conv2d_bwd_weight_query_algo.restype = ctypes.c_int
     lib.conv2d_fwd_query_algo.argtypes = [P, A]
     lib.conv2d_fwd_query_algo.restype = ctypes.c_int
     lib.conv2d_fwd_status.argtypes = [vp, sz, vp]
@@ -285,6 +293,52 @@ def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, wo
     conv2d_fwd_into(y, x, w, bias, stride, padding, dilation, groups, workspace=workspace, algo=algo,
                     stream=stream, relu=relu)
     return y
+
+
+def wgrad_workspace_bytes(params: Params) -> int:
+    return int(load_library().conv2d_bwd_weight_workspace_bytes(ctypes.byref(params)))
+
+
+def query_wgrad_algo(params: Params) -> Algo:
+    """The heuristic's configuration for the weight gradient of this convolution."""
+    out = Algo()
+    rc = load_library().conv2d_bwd_weight_query_algo(ctypes.byref(params), ctypes.byref(out))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd_weight_query_algo")
+    return out
+
+
+def conv2d_bwd_weight_into(dw, x, dy, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+                           algo: Optional[Algo] = None, stream=None) -> None:
+    """Writes the weight gradient of conv2d(x, w) for output gradient ``dy`` into the fp32
+    tensor ``dw`` [K,R,S,C] (asynchronous).  x [N,H,W,C] and dy [N,P,Q,K] are bf16 CUDA tensors."""
+    import torch
+    _check_tensor(x, "x", torch.bfloat16, 4)
+    _check_tensor(dy, "dy", torch.bfloat16, 4)
+    _check_tensor(dw, "dw", torch.float32, 4)
+    params = make_params(x.shape, dw.shape, stride, padding, dilation, groups)
+    p, q = output_shape(params)
+    if tuple(dy.shape) != (params.n, p, q, params.k):
+        raise ValueError(f"dy must be [{params.n}, {p}, {q}, {params.k}], got {list(dy.shape)}")
+    lib = load_library()
+    if workspace is None:
+        workspace = _default_workspace(wgrad_workspace_bytes(params), x.device)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    rc = lib.conv2d_bwd_weight(ctypes.byref(params), x.data_ptr(), dy.data_ptr(), dw.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), st.cuda_stream,
+                               None if algo is None else ctypes.byref(algo))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd_weight")
+
+
+def conv2d_bwd_weight(x, dy, w_shape, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+                      algo: Optional[Algo] = None, stream=None):
+    """Returns the weight gradient [K,R,S,C/groups] fp32 as a new CUDA tensor (asynchronous)."""
+    import torch
+    dw = torch.empty(tuple(int(v) for v in w_shape), dtype=torch.float32, device=x.device)
+    conv2d_bwd_weight_into(dw, x, dy, stride, padding, dilation, groups, workspace=workspace, algo=algo,
+                           stream=stream)
+    return dw
 
 
 def conv2d_fwd_host(x_host, w_host, bias_host, y_host, params: Params, staging, stream=None) -> None:

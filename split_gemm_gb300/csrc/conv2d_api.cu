@@ -785,6 +785,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     kp.w = static_cast<const uint16_t*>(w);
     kp.bias = bias;
     kp.y = y;
+    kp.ldy = (int)s.k;
     kp.status = have_ws ? static_cast<uint32_t*>(workspace) : nullptr;
     kp.sems = have_ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kStatusBytes) : nullptr;
     kp.N = (int)s.n; kp.H = (int)s.h; kp.W = (int)s.w; kp.C = (int)s.c;
@@ -837,6 +838,178 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
 }
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------ weight gradient
+// dw[k][(r*S + s)*C + c] = sum over output pixels l of dy[l][k] * im2col(x)[l][(r, s, c)]:
+// GEMM rows are output channels (128 per tile), columns are (tap, channel block)
+// pairs inside one tap, and the reduction runs over the N*P*Q output pixels in
+// 64-pixel k-blocks.  The kernel is the forward kernel's pipeline with the
+// LOADER_WGRAD loads: dy by tiled TMA, x by 64-pixel im2col TMA boxes.
+bool wgrad_eligible(const Shape& s) { return s.g == 1 && s.c % BK == 0 && s.k % 8 == 0; }
+
+int64_t wgrad_sem_capacity(const Shape& s) { return cdiv(s.k, 128) * s.r * s.s * cdiv(s.c, 64); }
+
+size_t wgrad_workspace_bytes_for(const Shape& s)
+{
+    return kStatusBytes + static_cast<size_t>(wgrad_sem_capacity(s)) * sizeof(uint32_t);
+}
+
+struct WgradPlan {
+    int block_n, splits, grid, m_tiles, n_tiles, ntpt, num_kb;
+    int64_t units;
+};
+
+int choose_wgrad_plan(const Shape& s, const conv2d_algo* force, WgradPlan* pl)
+{
+    const int64_t nsm = sm_count_current() > 0 ? sm_count_current() : 1;
+    if (force && force->block_m != 0 && force->block_m != 128) return CONV2D_ERR_UNSUPPORTED;
+    if (force && force->loader != CONV2D_LOADER_AUTO && force->loader != CONV2D_LOADER_TMA_IM2COL)
+        return CONV2D_ERR_UNSUPPORTED;
+    const int bn = (force && force->block_n) ? force->block_n : (s.c % 128 == 0 ? 128 : 64);
+    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    const int64_t m_tiles = cdiv(s.k, 128);
+    const int64_t ntpt = cdiv(s.c, bn);
+    const int64_t n_tiles = s.r * s.s * ntpt;
+    const int64_t tiles = m_tiles * n_tiles;
+    const int64_t num_kb = cdiv(s.m, BK);
+    const int64_t units = tiles * num_kb;
+    int64_t splits = force ? force->splits : 0;
+    int64_t grid = force ? force->grid : 0;
+    if (splits < 0 || grid < 0 || (splits > 0 && grid > 0)) return CONV2D_ERR_INVALID;
+    if (splits == 0 && grid == 0) {
+        if (tiles >= nsm) {
+            const int64_t per_cta = cdiv(tiles, nsm);
+            grid = cdiv(tiles, per_cta);
+        } else {
+            // Few tiles, a long reduction over the output pixels: every SM takes an
+            // even share of the (tile, k-block) units, at least kMinUnitsPerCta.
+            grid = units / kMinUnitsPerCta < nsm ? units / kMinUnitsPerCta : nsm;
+            if (grid < tiles) grid = tiles;
+        }
+    }
+    if (splits > 0) {
+        if (splits > num_kb) return CONV2D_ERR_UNSUPPORTED;
+        grid = tiles * splits;
+    } else if (grid > units) {
+        return CONV2D_ERR_UNSUPPORTED;
+    }
+    if (grid > 2147483647ll || units > (int64_t(1) << 62)) return CONV2D_ERR_UNSUPPORTED;
+    pl->block_n = bn;
+    pl->splits = static_cast<int>(splits);
+    pl->grid = static_cast<int>(grid);
+    pl->m_tiles = static_cast<int>(m_tiles);
+    pl->n_tiles = static_cast<int>(n_tiles);
+    pl->ntpt = static_cast<int>(ntpt);
+    pl->num_kb = static_cast<int>(num_kb);
+    pl->units = units;
+    return CONV2D_OK;
+}
+
+bool wgrad_cuts_tiles(const WgradPlan& p)
+{
+    if (p.num_kb <= 1) return false;
+    return (p.units % p.grid) != 0 || (p.units / p.grid) % p.num_kb != 0;
+}
+
+int run_wgrad(const conv2d_params* params, const void* x, const void* dy, float* dw, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.k == 0) return CONV2D_OK;  // no filters: nothing to write
+    if (!dw || (s.m > 0 && (!x || !dy))) return CONV2D_ERR_INVALID;
+    if (!aligned16(dw) || (x && !aligned16(x)) || (dy && !aligned16(dy)) || (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_ALIGNMENT;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
+                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
+                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
+        return CONV2D_ERR_INVALID;
+    if (!wgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    if (s.m == 0) {  // empty batch: the gradient is zero
+        if (cudaMemsetAsync(dw, 0, static_cast<size_t>(s.k * s.crs) * sizeof(float), stream) != cudaSuccess)
+            return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
+    WgradPlan plan;
+    rc = choose_wgrad_plan(s, algo, &plan);
+    if (rc != CONV2D_OK) return rc;
+    const bool have_ws = workspace && workspace_bytes >= wgrad_workspace_bytes_for(s);
+    const bool cuts = wgrad_cuts_tiles(plan);
+    if (cuts && !have_ws) return CONV2D_ERR_WORKSPACE;
+    if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
+    if (!load_encoders()) return CONV2D_ERR_CUDA;
+
+    CUtensorMap tm_a, tm_b;
+    std::memset(&tm_a, 0, sizeof(tm_a));
+    std::memset(&tm_b, 0, sizeof(tm_b));
+    {   // dy as [N*P*Q][K]: boxes of 64 channels x 64 output pixels, 128-byte swizzle
+        const cuuint64_t dims[2] = {(cuuint64_t)s.k, (cuuint64_t)s.m};
+        const cuuint64_t strides[1] = {(cuuint64_t)(s.k * 2)};
+        const cuuint32_t box[2] = {64, (cuuint32_t)BK};
+        const cuuint32_t estr[2] = {1, 1};
+        if (g_encode_tiled(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(dy), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+    {   // x as im2col boxes of 64 output pixels x 64 channels (the forward map with 64-pixel columns)
+        const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                       (cuuint64_t)(s.h * s.w * s.c * 2)};
+        const int lower[2] = {(int)-s.pw, (int)-s.ph};
+        const int upper[2] = {(int)(s.pw - (s.s - 1) * s.dw), (int)(s.ph - (s.r - 1) * s.dh)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1};
+        if (g_encode_im2col(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, lower,
+                            upper, BK, BK, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+
+    sgb::ConvKernelParams kp{};
+    kp.x = static_cast<const uint16_t*>(x);
+    kp.w = nullptr;
+    kp.bias = nullptr;
+    kp.y = dw;
+    kp.ldy = static_cast<int>(s.crs);
+    kp.status = have_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+    kp.sems = have_ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kStatusBytes) : nullptr;
+    kp.N = (int)s.n; kp.H = (int)s.h; kp.W = (int)s.w; kp.C = (int)s.c;
+    kp.K = (int)s.k; kp.R = (int)s.r; kp.S = (int)s.s; kp.P = (int)s.p; kp.Q = (int)s.q;
+    kp.sh = (int)s.sh; kp.sw = (int)s.sw; kp.ph = (int)s.ph; kp.pw = (int)s.pw; kp.dh = (int)s.dh; kp.dw = (int)s.dw;
+    kp.M = (int)s.k;        // GEMM rows: output channels
+    kp.CRS = (int)s.m;      // reduction length: output pixels
+    kp.G = (int)(s.r * s.s);  // column blocks never straddle a tap: R*S "groups" of C columns
+    kp.Cg = (int)s.c;
+    kp.Kg = (int)s.c;
+    kp.ntpg = plan.ntpt;
+    kp.num_kb = plan.num_kb;
+    kp.m_tiles = plan.m_tiles;
+    kp.n_tiles = plan.n_tiles;
+    kp.grid = plan.grid;
+    kp.units = plan.units;
+    kp.vec_store = 1;  // C % 64 == 0: every row and column block is 16-byte aligned
+    kp.debug_flags = algo ? algo->debug_flags : 0;
+    kp.reduce_concurrent = (algo && algo->reduction == CONV2D_REDUCTION_ORDERED) ? 0 : 1;
+    kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+    kp.trace = nullptr;
+#ifdef SGB_TRACE_ENABLED
+    kp.trace = g_trace;
+#endif
+    if (log_enabled())
+        std::fprintf(stderr, "[conv2d wgrad] K=%lld RSC=%lld NPQ=%lld -> BN=%d splits=%d grid=%d kb=%d tiles=%d\n",
+                     (long long)s.k, (long long)s.crs, (long long)s.m, plan.block_n, plan.splits, plan.grid,
+                     plan.num_kb, plan.m_tiles * plan.n_tiles);
+    cudaError_t err;
+    if (plan.block_n == 64) err = sgb::launch_conv2d_tc<128, 64, sgb::LOADER_WGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    else if (plan.block_n == 128) err = sgb::launch_conv2d_tc<128, 128, sgb::LOADER_WGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    else err = sgb::launch_conv2d_tc<128, 256, sgb::LOADER_WGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    if (err != cudaSuccess) return CONV2D_ERR_CUDA;
+    g_last_launches = 1;
+    return CONV2D_OK;
+}
+
 
 }  // namespace
 
@@ -921,6 +1094,40 @@ size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_
 int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
 {
     return conv2d_fwd_query_algo_epi(params, nullptr, out);
+}
+
+size_t conv2d_bwd_weight_workspace_bytes(const conv2d_params* params)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    return wgrad_workspace_bytes_for(s);
+}
+
+int conv2d_bwd_weight(const conv2d_params* params, const void* x_dev, const void* dy_dev, float* dw_dev,
+                      void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream, const conv2d_algo* algo)
+{
+    return run_wgrad(params, x_dev, dy_dev, dw_dev, workspace_dev, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), algo);
+}
+
+int conv2d_bwd_weight_query_algo(const conv2d_params* params, conv2d_algo* out)
+{
+    if (!out) return CONV2D_ERR_INVALID;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (!wgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    WgradPlan plan;
+    rc = choose_wgrad_plan(s, nullptr, &plan);
+    if (rc != CONV2D_OK) return rc;
+    std::memset(out, 0, sizeof(*out));
+    out->block_m = 128;
+    out->block_n = plan.block_n;
+    out->splits = plan.splits;
+    out->loader = CONV2D_LOADER_TMA_IM2COL;
+    out->grid = plan.grid;
+    out->reduction = wgrad_cuts_tiles(plan) ? CONV2D_REDUCTION_CONCURRENT : CONV2D_REDUCTION_AUTO;
+    return CONV2D_OK;
 }
 
 int conv2d_fwd_status(void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream)

@@ -101,7 +101,10 @@ constexpr uint32_t STATUS_TIMEOUT = 6;  // same value as CONV2D_ERR_TIMEOUT
 constexpr int kMaxSmemBytes = 232448;   // opt-in dynamic shared memory per block (227 KB)
 
 enum LoaderKind : int {
-    LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6, LOADER_HALO = 7
+    LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6, LOADER_HALO = 7,
+    // Weight gradient: the same pipeline with the GEMM dw[k][(r,s,c)] = sum_l dy[l][k] * im2col(x)[l][(r,s,c)]
+    // over the output pixels l, both operands MN-major in shared memory.
+    LOADER_WGRAD = 8
 };
 
 // Which engine brings in the im2col tile of the CTA's k-block number `it`:
@@ -110,7 +113,8 @@ enum LoaderKind : int {
 template <int LOADER>
 __device__ __forceinline__ bool a_by_tma(int it)
 {
-    return LOADER == LOADER_TMA || LOADER == LOADER_BOX || (LOADER == LOADER_HYBRID && (it & 1) == 0);
+    return LOADER == LOADER_TMA || LOADER == LOADER_BOX || LOADER == LOADER_WGRAD ||
+           (LOADER == LOADER_HYBRID && (it & 1) == 0);
 }
 template <int LOADER>
 __device__ __forceinline__ bool a_by_gather(int it)
@@ -122,7 +126,8 @@ struct ConvKernelParams {
     const uint16_t* x;  // bf16 NHWC
     const uint16_t* w;  // bf16 KRSC
     const float* bias;  // [K] or nullptr
-    float* y;           // fp32 NHWC = [M][K]
+    float* y;           // fp32 NHWC = [M][K] (weight gradient: dw [K][R*S*C])
+    int ldy;            // elements between consecutive rows of y: K (weight gradient: R*S*C)
     uint32_t* status;   // device status word or nullptr
     uint32_t* sems;     // one per output tile (needed whenever a tile is split)
     int N, H, W, C, K, R, S, P, Q;
@@ -166,6 +171,7 @@ struct TileConfig {
     static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
     static_assert(BM == 128 || LOADER == LOADER_TMA || LOADER == LOADER_BOX, "256-pixel tiles need a TMA loader");
     static constexpr bool HALO = LOADER == LOADER_HALO;
+    static constexpr bool WGRAD = LOADER == LOADER_WGRAD;
     static constexpr int M_SUB = BM / MMA_M;  // 128-row MMA blocks per tile
     static constexpr int KC = LOADER == LOADER_BOX ? 2 : 1;  // k-blocks per pipeline stage
     // The halo loader keeps its activations in two halo buffers outside the ring.
@@ -181,7 +187,7 @@ struct TileConfig {
     static constexpr int BAR_BYTES = (2 * STAGES + 9) * 8 + 16;
     // With a TMA loader the gather warps' places go to the epilogue: 8 warps, two
     // per TMEM lane quadrant, each writing half of the tile's columns.
-    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO) ? 8 : 4;
+    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD) ? 8 : 4;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOTS * EPI_SLOT_BYTES;
     // Without the halo loader's two halo buffers (2 * kp.halo_bytes, placed after the ring).
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
@@ -197,7 +203,7 @@ struct TileConfig {
     // thus has one issuer, loading its uses in order, and a slot's parity waits
     // never run more than one phase ahead of the MMA's releases.  (Gather
     // loaders: warp 0 issues the weight tiles.)
-    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO;
+    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD;
     // The halo loader's only per-stage load is the weight tile: four threads
     // (warps 0, 11, 12, 13) share them, ring slot s going to producer s % 4.
     static constexpr int HALO_NB = 4;
@@ -381,12 +387,24 @@ template <int BM, int BN, int LOADER>
 struct LoadCursor {
     static constexpr int KC = TileConfig<BM, BN, LOADER>::KC;
     int n_img, w_org, h_org, c, r, s, n0, kb, c_base;  // c: channel within the group
+    int k0;  // weight gradient: first output channel of the tile (its dy columns)
     LoadCursor() = default;
     __device__ __forceinline__ LoadCursor(const ConvKernelParams& kp, const Segment& sg)
     {
         const int m_tile = sg.tile / kp.n_tiles;
         int n_end;
         tile_columns<BN>(kp, sg.tile, m_tile, n0, n_end, c_base);
+        if constexpr (LOADER == LOADER_WGRAD) {
+            // Column block (tap, channel block): G = R*S taps of Kg = C columns each.
+            const int tap = c_base / kp.Cg;
+            r = tap / kp.S;
+            s = tap - r * kp.S;
+            c = n0 - tap * kp.C;
+            k0 = m_tile * BM;
+            kb = sg.kb_begin;
+            set_pixel_origin(kp);
+            return;
+        }
         int p0, q0;
         if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, n_img, p0, q0);
         else decode_pixel(kp, m_tile * BM, n_img, p0, q0);
@@ -399,9 +417,21 @@ struct LoadCursor {
         r = rs0 / kp.S;
         s = rs0 - r * kp.S;
     }
+    // Weight gradient: window origin of output pixel kb*BK (the stage's first reduction index).
+    __device__ __forceinline__ void set_pixel_origin(const ConvKernelParams& kp)
+    {
+        int p0, q0;
+        decode_pixel(kp, kb * BK, n_img, p0, q0);
+        w_org = q0 * kp.sw - kp.pw;
+        h_org = p0 * kp.sh - kp.ph;
+    }
     __device__ __forceinline__ void advance(const ConvKernelParams& kp)
     {
         ++kb;
+        if constexpr (LOADER == LOADER_WGRAD) {
+            set_pixel_origin(kp);
+            return;
+        }
         c += KC * BK;
         if (c >= kp.Cg) {  // the im2col loaders need Cg % 64 == 0, the box loader C % 128 == 0
             c = 0;
@@ -418,22 +448,41 @@ struct LoadCursor {
     __device__ __forceinline__ void load_a(const CUtensorMap* tm_a, const ConvKernelParams& kp, uint8_t* a_dst,
                                            uint64_t* bar) const
     {
-        if constexpr (LOADER == LOADER_BOX)  // KC channel chunks of the rectangle's windows at tap (r, s)
+        if constexpr (LOADER == LOADER_WGRAD) {
+            // dy rows kb*BK .. +63 (output pixels), output channels k0 .. k0+127 as two
+            // 64-column boxes: 128-byte rows of 64 channels, 8 KB apart.
+            ptx::tma_load_2d(a_dst, tm_a, bar, k0, kb * BK);
+            ptx::tma_load_2d(a_dst + BK * 128, tm_a, bar, k0 + 64, kb * BK);
+        } else if constexpr (LOADER == LOADER_BOX)  // KC channel chunks of the rectangle's windows at tap (r, s)
             ptx::tma_load_5d(a_dst, tm_a, bar, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, (c_base + c) / BK);
         else
             ptx::tma_load_im2col_4d(a_dst, tm_a, bar, c_base + c, w_org, h_org, n_img,
                                     static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
     }
-    __device__ __forceinline__ void load_b(const CUtensorMap* tm_b, uint8_t* b_dst, uint64_t* bar) const
+    __device__ __forceinline__ void load_b(const CUtensorMap* tm_b, const ConvKernelParams& kp, uint8_t* b_dst,
+                                           uint64_t* bar) const
     {
-        if constexpr (LOADER == LOADER_BOX) ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);  // KC k-blocks
+        if constexpr (LOADER == LOADER_WGRAD) {
+            // im2col boxes of the stage's 64 output pixels at tap (r, s): BN / 64 boxes of
+            // 64 channels, each 64 pixel rows of 128 bytes, 8 KB apart.
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+                ptx::tma_load_im2col_4d(b_dst + i * BK * 128, tm_b, bar, c + 64 * i, w_org, h_org, n_img,
+                                        static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
+        } else if constexpr (LOADER == LOADER_BOX) ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);  // KC k-blocks
         else ptx::tma_load_2d(b_dst, tm_b, bar, kb * BK, n0);
     }
     // The same reads as L2 prefetches (nothing lands in shared memory).
     __device__ __forceinline__ void prefetch(const CUtensorMap* tm_a, const CUtensorMap* tm_b,
                                              const ConvKernelParams& kp) const
     {
-        if constexpr (LOADER == LOADER_BOX) {
+        if constexpr (LOADER == LOADER_WGRAD) {
+            ptx::tma_prefetch_2d(tm_a, k0, kb * BK);
+            ptx::tma_prefetch_2d(tm_a, k0 + 64, kb * BK);
+            for (int i = 0; i < BN / 64; ++i)
+                ptx::tma_prefetch_im2col_4d(tm_b, c + 64 * i, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+                                            static_cast<uint16_t>(r * kp.dh));
+        } else if constexpr (LOADER == LOADER_BOX) {
             ptx::tma_prefetch_5d(tm_a, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, (c_base + c) / BK);
             ptx::tma_prefetch_3d(tm_b, 0, n0, kb * KC);
         } else {
@@ -513,7 +562,7 @@ __device__ void run_tma_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_
             const uint32_t bytes = (a_tma ? a_bytes : 0u) + ((OPS & PROD_B) ? Cfg::B_STAGE_BYTES : 0u);
             ptx::mbar_arrive_expect_tx(&sm.full[stage], bytes);
             if (a_tma) cur.load_a(tm_a, kp, sm.a + stage * A_STAGE_BYTES, &sm.full[stage]);
-            if (OPS & PROD_B) cur.load_b(tm_b, sm.b + stage * Cfg::B_STAGE_BYTES, &sm.full[stage]);
+            if (OPS & PROD_B) cur.load_b(tm_b, kp, sm.b + stage * Cfg::B_STAGE_BYTES, &sm.full[stage]);
             SGB_STAGE_MARK(kp, it, (OPS & PROD_A) ? 0 : 1);
             SGB_CYCLES_END(issue_cycles, ti);
         }
@@ -661,10 +710,17 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(MMA_M, BN);
+    constexpr uint32_t IDESC = Cfg::WGRAD ? ptx::idesc_bf16_f32_mn(MMA_M, BN) : ptx::idesc_bf16_f32(MMA_M, BN);
     const int lane = threadIdx.x & 31;
-    const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
-    const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    // Weight gradient: MN-major operands, 64-element blocks along M/N 8 KB apart
+    // (one 64-row TMA box each), groups of 8 reduction rows 1024 B apart.
+    const uint64_t a_desc0 = Cfg::WGRAD ? ptx::sw128_mnmajor_desc(ptx::smem_addr(sm.a), BK * 128, 1024)
+                                        : ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
+    const uint64_t b_desc0 = Cfg::WGRAD ? ptx::sw128_mnmajor_desc(ptx::smem_addr(sm.b), BK * 128, 1024)
+                                        : ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    // Reduction step of one MMA (16 elements): 32 B along a K-major row, 16 rows of
+    // 128 B in an MN-major tile.
+    constexpr int KSTEP_BYTES = Cfg::WGRAD ? UMMA_K * 128 : UMMA_K * 2;
     const uint32_t a_chunk16 = LOADER == LOADER_BOX ? static_cast<uint32_t>(kp.px * 8) : 0u;
     const uint64_t halo_desc0 = Cfg::HALO ? ptx::sw128_kmajor_desc(ptx::smem_addr(sm.halo)) : 0ull;
     int h = 0;  // halo uses (halo loader)
@@ -738,12 +794,12 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
 #pragma unroll
                 for (int k = 0; k < KSTEPS; ++k) {
                     const int chunk = k / (BK / UMMA_K), kin = k % (BK / UMMA_K);
-                    const uint64_t bdk = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * UMMA_K * 2) >> 4);
+                    const uint64_t bdk = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * KSTEP_BYTES) >> 4);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
                         ptx::mma_bf16(tmem_d + sub * BN,
                                       ad + static_cast<uint64_t>(chunk) * a_chunk16 +
-                                          static_cast<uint64_t>((sub * MMA_M * 128 + kin * UMMA_K * 2) >> 4),
+                                          static_cast<uint64_t>((sub * MMA_M * 128 + kin * KSTEP_BYTES) >> 4),
                                       bdk, IDESC, k > 0 ? 1u : acc0);
                 }
             }
@@ -1045,12 +1101,12 @@ __device__ __forceinline__ void finish_from_part(const ConvKernelParams& kp, int
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         v[i] = mrow[h + i] >= 0
-                                   ? __ldcg(reinterpret_cast<const float4*>(kp.part + static_cast<int64_t>(mrow[h + i]) * kp.K + col))
+                                   ? __ldcg(reinterpret_cast<const float4*>(kp.part + static_cast<int64_t>(mrow[h + i]) * kp.ldy + col))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if (mrow[h + i] < 0) continue;
-                        const int64_t at = static_cast<int64_t>(mrow[h + i]) * kp.K + col;
+                        const int64_t at = static_cast<int64_t>(mrow[h + i]) * kp.ldy + col;
                         __stcg(reinterpret_cast<float4*>(kp.part + at), make_float4(0.f, 0.f, 0.f, 0.f));
                         uint4 val = make_uint4(__float_as_uint(v[i].x + b4.x), __float_as_uint(v[i].y + b4.y),
                                                __float_as_uint(v[i].z + b4.z), __float_as_uint(v[i].w + b4.w));
@@ -1065,7 +1121,7 @@ __device__ __forceinline__ void finish_from_part(const ConvKernelParams& kp, int
 #pragma unroll
             for (int j = 0; j < SLABS; ++j) {
                 const int nb = n0 + (jbeg + j) * 32;
-                const int64_t at0 = static_cast<int64_t>(m < 0 ? 0 : m) * kp.K + nb;
+                const int64_t at0 = static_cast<int64_t>(m < 0 ? 0 : m) * kp.ldy + nb;
                 const float bias_l = (kp.bias && nb + lane < n_end) ? __ldg(kp.bias + nb + lane) : 0.0f;
 #pragma unroll
                 for (int h = 0; h < 32; h += 16) {  // sixteen loads in flight at a time
@@ -1212,7 +1268,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                         }
                         if (kp.relu && !via_part) val = ptx::relu4(val);
                         if (m >= 0 && col < n_end) {
-                            const int64_t at = static_cast<int64_t>(m) * kp.K + col;
+                            const int64_t at = static_cast<int64_t>(m) * kp.ldy + col;
                             if (via_part) ptx::red_add_v4_f32(kp.part + at, val);
                             else if (kp.out_bf16)
                                 *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
@@ -1228,7 +1284,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                 const int m = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + row, bx_n, bx_p, bx_q);
                 const bool row_ok = m >= 0;
                 const bool accumulate = sg.split > 0;
-                float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.K;
+                float* yrow = kp.y + static_cast<int64_t>(row_ok ? m : 0) * kp.ldy;
 #pragma unroll
                 for (int j = 0; j < SLABS; ++j) {
                     uint32_t v[32];
@@ -1246,7 +1302,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                     if (!row_ok) continue;
                     const int nb = n0 + (jbeg + j) * 32;
                     if (via_part) {
-                        float* prow = kp.part + static_cast<int64_t>(m) * kp.K;
+                        float* prow = kp.part + static_cast<int64_t>(m) * kp.ldy;
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             if (nb + e < n_end) atomicAdd(prow + nb + e, __uint_as_float(v[e]));
@@ -1264,7 +1320,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                         float o = __uint_as_float(v[e]);
                         if (kp.relu) o = fmaxf(o, 0.0f);
                         if (kp.out_bf16) {  // fused epilogue: whole tiles only
-                            reinterpret_cast<uint16_t*>(kp.y)[static_cast<int64_t>(m) * kp.K + n] = ptx::bf16_bits(o);
+                            reinterpret_cast<uint16_t*>(kp.y)[static_cast<int64_t>(m) * kp.ldy + n] = ptx::bf16_bits(o);
                             continue;
                         }
                         if (accumulate && kp.reduce_concurrent) {
@@ -1358,7 +1414,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         // Halo loader: one arrive (the weight tile's producer).
         const uint32_t full_count =
             Cfg::HALO ? 1u
-            : (LOADER == LOADER_TMA || LOADER == LOADER_BOX) ? 2u  // the activation and the weight producer
+            : Cfg::TMA_A ? 2u  // the activation (or output-gradient) and the weight (or im2col) producer
                                                            : (LOADER == LOADER_SCALAR ? GATHER_WARPS : 1u + GATHER_THREADS);
         for (int i = 0; i < Cfg::STAGES; ++i) {
             ptx::mbar_init(&sm.full[i], full_count);
@@ -1506,6 +1562,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_WGRAD);   \
     template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_INSTANTIATE_CONV2D_BOX256(BN_) template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 
@@ -1517,6 +1574,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HYBRID);  \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_WGRAD);   \
     extern template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_DECLARE_CONV2D_BOX256(BN_) extern template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 

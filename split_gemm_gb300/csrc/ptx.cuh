@@ -410,6 +410,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand with 128-byte
+// swizzling: each 128-byte row holds 64 consecutive M (or N) elements of one
+// reduction index, 8 rows (8 reduction indices) form a 1024-byte swizzle atom;
+// atoms adjacent along the reduction are `sbo` bytes apart and atoms adjacent
+// along M/N (the next 64 elements) `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the unswizzled
 // ("interleaved") layout: core matrices of 8 rows x 16 bytes, the 8 rows 16 B
 // apart; `lbo` is the byte distance between core matrices adjacent along K and
@@ -433,6 +449,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// The same with both operands MN-major (the transpose-A and transpose-B bits).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n)
+{
+    return idesc_bf16_f32(m, n) | (1u << 15) | (1u << 16);
 }
 
 }  // namespace ptx

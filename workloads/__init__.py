@@ -32,7 +32,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "random_small"]
+__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "make_output_grad", "random_small"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -150,6 +150,26 @@ def make_inputs(wl: Workload, seed: Optional[int] = None):
     if wl.bias is not None:
         b = _draw(gen, (wl.k,), wl.bias, fan_in).contiguous()
     return x, w, b
+
+
+def output_extent(in_size: int, pad: int, dil: int, ker: int, stride: int) -> int:
+    """Output size along one axis (the shape of the output gradient only; no arithmetic of the method)."""
+    room = in_size + 2 * pad - (dil * (ker - 1) + 1)
+    return 0 if room < 0 else room // stride + 1
+
+
+def make_output_grad(wl: Workload, seed: Optional[int] = None) -> torch.Tensor:
+    """The output gradient dy [N,P,Q,K] bf16 for a workload's weight gradient: N(0, 2/L) with
+    L = N*P*Q, the reduction length of every weight-gradient element (the He scaling the
+    forward weights use for theirs), drawn in fp32 from its own generator (seed + 7919) and
+    rounded to bf16."""
+    p = output_extent(wl.h, wl.pad_h, wl.dil_h, wl.r, wl.stride_h)
+    q = output_extent(wl.w, wl.pad_w, wl.dil_w, wl.s, wl.stride_w)
+    gen = torch.Generator("cpu")
+    gen.manual_seed((wl.seed if seed is None else seed) + 7919)
+    L = max(1, wl.n * p * q)
+    return (torch.randn((wl.n, p, q, wl.k), generator=gen, dtype=torch.float32) * math.sqrt(2.0 / L)).to(
+        torch.bfloat16).contiguous()
 
 
 def random_small(seed: int, *, max_hw: int = 12, channels=(1, 3, 8, 16, 24, 64),
