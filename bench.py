@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "conv2d fwd TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
+METRIC_WGRAD = "conv2d wgrad TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
 DEFAULT_WORKLOAD = "resnet_56x56_c64"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -79,6 +80,14 @@ def algorithmic_bytes(wl, out_bytes=4):
     y_b = wl.n * p * q * wl.k * out_bytes
     b_b = wl.k * 4 if wl.bias is not None else 0
     return float(x_b + w_b + y_b + b_b)
+
+
+def algorithmic_bytes_wgrad(wl):
+    """Input pixels some window touches (bf16) + output gradient dy (bf16) + weight gradient (fp32)."""
+    p, q = shape_of(wl)
+    th = _touched(wl.h, p, wl.stride_h, wl.pad_h, wl.dil_h, wl.r)
+    tw = _touched(wl.w, q, wl.stride_w, wl.pad_w, wl.dil_w, wl.s)
+    return float(wl.n * th * tw * wl.c * 2 + wl.n * p * q * wl.k * 2 + wl.k * wl.r * wl.s * (wl.c // wl.groups) * 4)
 
 
 def load_peaks():
@@ -273,6 +282,43 @@ class OracleSampler:
         return flops / done / 1e12, 1, f"{npts} random output elements, 1 thread", done
 
 
+class WgradOracleSampler:
+    """Times the weight-gradient oracle on randomly chosen gradient elements (one thread;
+    inputs widened to float64 once): each element is a sum over the N*P*Q output pixels."""
+
+    def __init__(self, wl):
+        import numpy as np
+
+        import oracle
+        from oracle import wgrad as ow
+        self.np, self.ow, self.wl = np, ow, wl
+        x, w, _ = workloads.make_inputs(wl)
+        dy = workloads.make_output_grad(wl)
+        self.w_shape = tuple(w.shape)
+        self.xd, self.dyd = oracle.widen_bf16(x), oracle.widen_bf16(dy)
+        self.o = wl.options()
+        self.lib = ow.load()
+        self.L = dy.shape[0] * dy.shape[1] * dy.shape[2]
+        self.cols = self.w_shape[1] * self.w_shape[2] * self.w_shape[3]
+        t0 = time.perf_counter()
+        self._points(8)
+        self.per_point = max(1e-7, (time.perf_counter() - t0) / 8)
+
+    def _points(self, npts):
+        rng = self.np.random.default_rng(npts)
+        kk = rng.integers(0, self.wl.k, size=npts)
+        jj = rng.integers(0, self.cols, size=npts)
+        self.ow.conv2d_wgrad_points_f64(self.xd, self.dyd, self.w_shape, self.o["stride"], self.o["padding"],
+                                        self.o["dilation"], kk, jj, lib=self.lib)
+
+    def run(self, budget_s: float):
+        npts = max(8, int(budget_s / self.per_point))
+        t0 = time.perf_counter()
+        self._points(npts)
+        done = time.perf_counter() - t0
+        return 2.0 * self.L * npts / done / 1e12, 1, f"{npts} random weight-gradient elements, 1 thread", done
+
+
 # ----------------------------------------------------------------------------- the GPU arm
 def _sets_for(wl, set_bytes):
     return max(1, min(64, math.ceil(2 * L2_BYTES / max(1, set_bytes))))
@@ -290,6 +336,8 @@ def run_ours(args, wl, world, rank, local):
     x, w, b = workloads.make_inputs(wl)
     params = sg.make_params(x.shape, w.shape, **wl.options())
     p, q = sg.output_shape(params)
+    if args.op == "wgrad":
+        return run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params)
     forced = None
     if args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction:
         forced = sg.Algo()
@@ -373,6 +421,90 @@ def run_ours(args, wl, world, rank, local):
                 graph_chunk=chunk)
 
 
+def _forced_algo(sg, args):
+    if not (args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction):
+        return None
+    a = sg.Algo()
+    a.block_n, a.splits, a.loader, a.grid = args.block_n, args.splits, args.loader, args.grid
+    a.block_m, a.reduction = args.block_m, args.reduction
+    return a
+
+
+def _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check):
+    """W warm-up steps, then K steps replayed from CUDA graphs between two events: (seconds, clocks, chunk)."""
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    stream.synchronize()
+    check()
+    chunk = min(K, 512)
+    chunk = max(n_sets, (chunk // n_sets) * n_sets) if K >= n_sets else K
+    full, rem = divmod(K, chunk)
+    graphs = []
+    for length in ([chunk] if full else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(length):
+                step(i)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    stream.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist_mod, dev)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graphs[0].replay()
+        if rem:
+            graphs[-1].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(dist_mod, dev)
+    clocks.stop()
+    return start.elapsed_time(end) / 1e3, clocks.summary(t0, t1), chunk
+
+
+def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
+    """The weight gradient of the workload: conv2d_bwd_weight over rotating buffer sets."""
+    dy = workloads.make_output_grad(wl)
+    forced = _forced_algo(sg, args)
+    algo = sg.query_wgrad_algo(params)
+    if forced is not None:
+        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, algo.loader,
+                       forced.grid or (0 if forced.splits else algo.grid), 0, 128, 0, forced.reduction or algo.reduction)
+    set_bytes = x.numel() * 2 + dy.numel() * 2 + w.numel() * 4
+    n_sets = _sets_for(wl, set_bytes)
+    sets = [(x.to(dev), dy.to(dev), torch.empty(tuple(w.shape), dtype=torch.float32, device=dev))
+            for _ in range(n_sets)]
+    ws = torch.zeros(max(4096, sg.wgrad_workspace_bytes(params)), dtype=torch.uint8, device=dev)
+    o = wl.options()
+    opts = dict(stride=o["stride"], padding=o["padding"], dilation=o["dilation"])
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        xd, dyd, dwd = sets[i % n_sets]
+        sg.conv2d_bwd_weight_into(dwd, xd, dyd, **opts, workspace=ws, algo=forced)
+
+    def check():
+        if sg.status(ws, stream) != 0:
+            raise RuntimeError("device status reported a timeout during warm-up")
+
+    elapsed, clocks, chunk = _time_graphs(torch, stream, step, args.steps, args.warmup, n_sets, dev, dist_mod, check)
+    status = sg.status(ws, stream)
+    flops = flops_per_step(wl)
+    job_s, job_flops = aggregate(dist_mod, elapsed, flops * args.steps, dev)
+    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
+                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
+
+
 def run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, steps, dist_mod):
     """Same metric through the host-buffer entry point: H2D of x, w, bias + kernel + D2H of y, every step.
 
@@ -427,10 +559,11 @@ def config_of(wl, extra=None):
     return cfg
 
 
-def roofline(wl, t_step_s, peaks, peak_src, out_bytes=4):
-    flops, nbytes = flops_per_step(wl), algorithmic_bytes(wl, out_bytes)
+def roofline(wl, t_step_s, peaks, peak_src, out_bytes=4, op="fwd"):
+    flops = flops_per_step(wl)
+    nbytes = algorithmic_bytes_wgrad(wl) if op == "wgrad" else algorithmic_bytes(wl, out_bytes)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = recorded_traffic(wl.name) if out_bytes == 4 else None
+    traffic = recorded_traffic(wl.name if op == "fwd" else f"{wl.name}:wgrad") if out_bytes == 4 else None
     if flops / nbytes >= ridge:
         achieved = flops / t_step_s / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -452,7 +585,8 @@ def main_ours(args):
     t_step = res["elapsed"] / K
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, cores, desc, secs = OracleSampler(wl).run(args.cpu_budget)
+        sampler = WgradOracleSampler(wl) if args.op == "wgrad" else OracleSampler(wl)
+        v, cores, desc, secs = sampler.run(args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
                "seconds": round(secs, 2)}
     if res["dist"] is not None:
@@ -461,7 +595,8 @@ def main_ours(args):
         return 0
     value = res["job_flops"] / res["job_s"] / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "metric": METRIC_WGRAD if args.op == "wgrad" else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup,
         "ms_per_step": res["job_s"] / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": config_of(wl, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -470,10 +605,14 @@ def main_ours(args):
                                               "bf16": "bias, bf16 y", "relu_bf16": "bias, ReLU, bf16 y"}[args.epilogue],
                                  **({"layout": "x NHWC bf16, w KRSC bf16, bias fp32, y NHWC bf16"}
                                     if args.epilogue in ("bf16", "relu_bf16") else {}),
+                                 **({"op": "weight gradient", "epilogue": "fp32 dw",
+                                     "layout": "x NHWC bf16, dy NPQK bf16 ~N(0, 2/(N*P*Q)), dw KRSC fp32",
+                                     "gemm_mnk": [wl.k, wl.r * wl.s * wl.c, wl.n * shape_of(wl)[0] * shape_of(wl)[1]]}
+                                    if args.op == "wgrad" else {}),
                                  "l2": f"{res['n_sets']} rotating input/output buffer sets (> 2x L2) per step",
                                  "timing": f"CUDA events around CUDA-graph replays ({res['graph_chunk']} launches "
                                            "per graph), max over ranks"}),
-        "roofline": roofline(wl, t_step, peaks, peak_src, 2 if args.epilogue in ("bf16", "relu_bf16") else 4),
+        "roofline": roofline(wl, t_step, peaks, peak_src, 2 if args.epilogue in ("bf16", "relu_bf16") else 4, args.op),
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "gpu_launches": K,
@@ -531,6 +670,8 @@ def parse_args(argv=None):
     ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box, 7 halo)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "wgrad"],
+                    help="fwd: the forward convolution (the headline); wgrad: its weight gradient")
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "bf16", "relu_bf16"],
                     help="fused epilogue variant (ReLU after the bias, bf16 output); the e2e leg runs only for none")
     args = ap.parse_args(argv)
