@@ -273,6 +273,36 @@ int conv2d_bwd_weight(const conv2d_params* params, const void* x_dev, const void
 /* What the heuristic picks for conv2d_bwd_weight (no launch; current device's SM count). */
 int conv2d_bwd_weight_query_algo(const conv2d_params* params, conv2d_algo* out);
 
+/* Data gradient: the backward pass of the convolution with regard to the input
+ * (docs.rs burn-cubecl 0.20.0, burn_cubecl/kernel/conv/base.rs,
+ * conv_data_backward: output gradient and weights, NHWC / KRSC, give an input
+ * gradient NHWC):
+ *
+ *   dx[n][h][w][c] = sum_{r,s,k} dy[n][p][q][k] * w[k][r][s][c]
+ *       over the taps with h + ph - r*dh = p*sh, w + pw - s*dw = q*sw, 0 <= p < P, 0 <= q < Q.
+ *
+ * It is also conv_transpose2d: conv_transpose2d of an input [N][Hi][Wi][Cin]
+ * with weights [Cin][R][S][Cout] (padding p, dilation d, stride 1) is this call
+ * with params {n = N, h = Hi - 2p + d(R-1), w = Wi - 2p + d(S-1), c = Cout,
+ * k = Cin, r = R, s = S, pad p, dil d, stride 1} and dy = the input.
+ * params describe the forward convolution (x [N][H][W][C], weight
+ * [K][R][S][C]); dy_dev: bf16 [N][P][Q][K]; w_dev: bf16 [K][R][S][C]; dx_dev:
+ * fp32 [N][H][W][C], fully overwritten.  Computed at stride 1 as the forward
+ * convolution of dy with the flipped, transposed weight w'[c][r][s][k] =
+ * w[k][R-1-r][S-1-s][c] and padding dil*(R-1) - pad, which the kernel reads
+ * from w directly (no transformed copy).  Supported, as burn's implicit GEMM:
+ * stride 1, groups == 1; and K % 64 == 0 (im2col TMA boxes of dy), C % 8 == 0,
+ * pad <= dil*(R-1) per axis; otherwise CONV2D_ERR_UNSUPPORTED.  algo as for
+ * conv2d_fwd_ex (block_m 0/128, loader 0 or CONV2D_LOADER_TMA_IM2COL). */
+size_t conv2d_bwd_data_workspace_bytes(const conv2d_params* params);
+
+int conv2d_bwd_data(const conv2d_params* params, const void* dy_dev, const void* w_dev, float* dx_dev,
+                    void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream,
+                    const conv2d_algo* algo);
+
+/* What the heuristic picks for conv2d_bwd_data (no launch; current device's SM count). */
+int conv2d_bwd_data_query_algo(const conv2d_params* params, conv2d_algo* out);
+
 /* Size of the library's built-in device scratch array used by conv2d_fwd_noalloc. */
 #define CONV2D_NOALLOC_SCRATCH_BYTES 65536
 

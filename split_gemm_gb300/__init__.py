@@ -28,7 +28,8 @@ __all__ = [
     "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "epi_workspace_bytes", "conv2d_bwd_weight", "conv2d_bwd_weight_into",
-    "wgrad_workspace_bytes", "query_wgrad_algo", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
+    "wgrad_workspace_bytes", "query_wgrad_algo", "conv2d_bwd_data", "conv2d_bwd_data_into", "dgrad_workspace_bytes",
+    "query_dgrad_algo", "conv_transpose2d", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
     "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
 ]
 
@@ -48,7 +49,8 @@ EXPORTED_SYMBOLS = [
     "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
     "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc", "conv2d_fwd_epi",
     "conv2d_fwd_query_algo_epi", "conv2d_fwd_epi_workspace_bytes", "conv2d_bwd_weight_workspace_bytes",
-    "conv2d_bwd_weight", "conv2d_bwd_weight_query_algo",
+    "conv2d_bwd_weight", "conv2d_bwd_weight_query_algo", "conv2d_bwd_data_workspace_bytes", "conv2d_bwd_data",
+    "conv2d_bwd_data_query_algo",
 ]
 
 
@@ -106,6 +108,12 @@ def _bind(lib):
     lib.conv2d_fwd_epi_workspace_bytes.restype = sz
     lib.conv2d_fwd_query_algo_epi.argtypes = [P, ctypes.POINTER(Epilogue), A]
     lib.conv2d_fwd_query_algo_epi.restype = ctypes.c_int
+    lib.conv2d_bwd_data_workspace_bytes.argtypes = [P]
+    lib.conv2d_bwd_data_workspace_bytes.restype = sz
+    lib.conv2d_bwd_data.argtypes = [P, vp, vp, vp, vp, sz, vp, A]
+    lib.conv2d_bwd_data.restype = ctypes.c_int
+    lib.conv2d_bwd_data_query_algo.argtypes = [P, A]
+    lib.conv2d_bwd_data_query_algo.restype = ctypes.c_int
     lib.conv2d_bwd_weight_workspace_bytes.argtypes = [P]
     lib.conv2d_bwd_weight_workspace_bytes.restype = sz
     lib.conv2d_bwd_weight.argtypes = [P, vp, vp, vp, vp, sz, vp, A]
@@ -339,6 +347,64 @@ def conv2d_bwd_weight(x, dy, w_shape, stride=1, padding=0, dilation=1, groups=1,
     conv2d_bwd_weight_into(dw, x, dy, stride, padding, dilation, groups, workspace=workspace, algo=algo,
                            stream=stream)
     return dw
+
+
+def dgrad_workspace_bytes(params: Params) -> int:
+    return int(load_library().conv2d_bwd_data_workspace_bytes(ctypes.byref(params)))
+
+
+def query_dgrad_algo(params: Params) -> Algo:
+    """The heuristic's configuration for the data gradient of this convolution."""
+    out = Algo()
+    rc = load_library().conv2d_bwd_data_query_algo(ctypes.byref(params), ctypes.byref(out))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd_data_query_algo")
+    return out
+
+
+def conv2d_bwd_data_into(dx, dy, w, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+                         algo: Optional[Algo] = None, stream=None) -> None:
+    """Writes the input gradient of conv2d(x, w) for output gradient ``dy`` into the fp32
+    tensor ``dx`` [N,H,W,C] (asynchronous).  dy [N,P,Q,K] and w [K,R,S,C] are bf16 CUDA tensors."""
+    import torch
+    _check_tensor(dy, "dy", torch.bfloat16, 4)
+    _check_tensor(w, "w", torch.bfloat16, 4)
+    _check_tensor(dx, "dx", torch.float32, 4)
+    params = make_params(dx.shape, w.shape, stride, padding, dilation, groups)
+    p, q = output_shape(params)
+    if tuple(dy.shape) != (params.n, p, q, params.k):
+        raise ValueError(f"dy must be [{params.n}, {p}, {q}, {params.k}], got {list(dy.shape)}")
+    lib = load_library()
+    if workspace is None:
+        workspace = _default_workspace(dgrad_workspace_bytes(params), dy.device)
+    st = torch.cuda.current_stream(dy.device) if stream is None else stream
+    rc = lib.conv2d_bwd_data(ctypes.byref(params), dy.data_ptr(), w.data_ptr(), dx.data_ptr(), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), st.cuda_stream,
+                             None if algo is None else ctypes.byref(algo))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd_data")
+
+
+def conv2d_bwd_data(dy, w, x_shape, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
+                    algo: Optional[Algo] = None, stream=None):
+    """Returns the input gradient [N,H,W,C] fp32 for a forward input of shape ``x_shape``."""
+    import torch
+    dx = torch.empty(tuple(int(v) for v in x_shape), dtype=torch.float32, device=dy.device)
+    conv2d_bwd_data_into(dx, dy, w, stride, padding, dilation, groups, workspace=workspace, algo=algo, stream=stream)
+    return dx
+
+
+def conv_transpose2d(x, w, padding=0, dilation=1, *, workspace=None, algo: Optional[Algo] = None, stream=None):
+    """conv_transpose2d at stride 1: x [N,Hi,Wi,Cin] bf16, w [Cin,R,S,Cout] bf16 ->
+    y [N,Hi-2p+d(R-1), Wi-2p+d(S-1), Cout] fp32, through the data-gradient kernel (dy = x)."""
+    ph, pw = _pair(padding)
+    dh, dw = _pair(dilation)
+    n, hi, wi, cin = (int(v) for v in x.shape)
+    cin_w, r, s, cout = (int(v) for v in w.shape)
+    if cin_w != cin:
+        raise ValueError(f"weight has {cin_w} input channels, x has {cin}")
+    return conv2d_bwd_data(x, w, (n, hi - 2 * ph + dh * (r - 1), wi - 2 * pw + dw * (s - 1), cout), 1, (ph, pw),
+                           (dh, dw), workspace=workspace, algo=algo, stream=stream)
 
 
 def conv2d_fwd_host(x_host, w_host, bias_host, y_host, params: Params, staging, stream=None) -> None:

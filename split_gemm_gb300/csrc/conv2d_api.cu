@@ -913,6 +913,143 @@ bool wgrad_cuts_tiles(const WgradPlan& p)
     return (p.units % p.grid) != 0 || (p.units / p.grid) % p.num_kb != 0;
 }
 
+// ------------------------------------------------------------------ data gradient (stride 1)
+// dx = conv(dy, w') with w'[c][r][s][k] = w[k][R-1-r][S-1-s][c], stride 1, the same
+// dilation and padding dil*(R-1) - pad: a forward convolution of the output
+// gradient, whose weight operand the kernel reads from w itself (LOADER_DGRAD).
+bool dgrad_eligible(const Shape& s)
+{
+    return s.g == 1 && s.sh == 1 && s.sw == 1 && s.k % BK == 0 && s.c % 8 == 0 && s.ph <= s.dh * (s.r - 1) &&
+           s.pw <= s.dw * (s.s - 1);
+}
+
+// The forward problem the data gradient is: input dy [N][P][Q][K], output dx [N][H][W][C].
+Shape dgrad_forward_shape(const Shape& s)
+{
+    Shape t = s;
+    t.h = s.p; t.w = s.q; t.c = s.k; t.k = s.c;
+    t.sh = 1; t.sw = 1;
+    t.ph = s.dh * (s.r - 1) - s.ph;
+    t.pw = s.dw * (s.s - 1) - s.pw;
+    t.g = 1; t.cg = t.c; t.kg = t.k;
+    t.p = s.h; t.q = s.w;
+    t.m = s.n * s.h * s.w;
+    t.crs = t.c * t.r * t.s;
+    return t;
+}
+
+int dgrad_plan(const Shape& t, const conv2d_algo* algo, Plan* plan)
+{
+    if (algo && algo->loader != CONV2D_LOADER_AUTO && algo->loader != CONV2D_LOADER_TMA_IM2COL)
+        return CONV2D_ERR_UNSUPPORTED;
+    if (algo && algo->block_m != 0 && algo->block_m != 128) return CONV2D_ERR_UNSUPPORTED;
+    conv2d_algo f{};
+    if (algo) f = *algo;
+    f.loader = CONV2D_LOADER_TMA_IM2COL;
+    f.block_m = 128;
+    return choose_plan(t, &f, plan);
+}
+
+int run_dgrad(const conv2d_params* params, const void* dy, const void* w, float* dx, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.n == 0 || s.c == 0) return CONV2D_OK;  // empty input gradient
+    if (!dx || (s.k > 0 && (!dy || !w))) return CONV2D_ERR_INVALID;
+    if (!aligned16(dx) || (dy && !aligned16(dy)) || (w && !aligned16(w)) || (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_ALIGNMENT;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
+                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
+                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
+        return CONV2D_ERR_INVALID;
+    if (s.k == 0) {  // no filters: the gradient is zero
+        if (cudaMemsetAsync(dx, 0, static_cast<size_t>(s.n * s.h * s.w * s.c) * sizeof(float), stream) != cudaSuccess)
+            return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
+    if (!dgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    const Shape t = dgrad_forward_shape(s);
+    Plan plan;
+    rc = dgrad_plan(t, algo, &plan);
+    if (rc != CONV2D_OK) return rc;
+    const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(t);
+    const bool cuts = plan_cuts_tiles(plan);
+    if (cuts && !have_ws) return CONV2D_ERR_WORKSPACE;
+    if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
+    if (!load_encoders()) return CONV2D_ERR_CUDA;
+
+    CUtensorMap tm_a, tm_b;
+    std::memset(&tm_a, 0, sizeof(tm_a));
+    std::memset(&tm_b, 0, sizeof(tm_b));
+    {   // dy through the forward im2col map of problem t (128-pixel columns, 64 channels)
+        const cuuint64_t dims[4] = {(cuuint64_t)t.c, (cuuint64_t)t.w, (cuuint64_t)t.h, (cuuint64_t)t.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(t.c * 2), (cuuint64_t)(t.w * t.c * 2),
+                                       (cuuint64_t)(t.h * t.w * t.c * 2)};
+        const int lower[2] = {(int)-t.pw, (int)-t.ph};
+        const int upper[2] = {(int)(t.pw - (t.s - 1) * t.dw), (int)(t.ph - (t.r - 1) * t.dh)};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode_im2col(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, lower,
+                            upper, BK, static_cast<cuuint32_t>(plan.block_m), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+    {   // w as {C, R*S, K}: boxes of 64 channels x one tap x 64 filters (rows), 128-byte swizzle
+        const cuuint64_t dims[3] = {(cuuint64_t)s.c, (cuuint64_t)(s.r * s.s), (cuuint64_t)s.k};
+        const cuuint64_t strides[2] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.r * s.s * s.c * 2)};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)BK};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode_tiled(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return CONV2D_ERR_CUDA;
+    }
+
+    sgb::ConvKernelParams kp{};
+    kp.x = static_cast<const uint16_t*>(dy);
+    kp.w = static_cast<const uint16_t*>(w);
+    kp.bias = nullptr;
+    kp.y = dx;
+    kp.ldy = (int)t.k;
+    kp.status = have_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+    kp.sems = have_ws ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + kStatusBytes) : nullptr;
+    kp.N = (int)t.n; kp.H = (int)t.h; kp.W = (int)t.w; kp.C = (int)t.c;
+    kp.K = (int)t.k; kp.R = (int)t.r; kp.S = (int)t.s; kp.P = (int)t.p; kp.Q = (int)t.q;
+    kp.sh = 1; kp.sw = 1; kp.ph = (int)t.ph; kp.pw = (int)t.pw; kp.dh = (int)t.dh; kp.dw = (int)t.dw;
+    kp.M = (int)t.m;
+    kp.CRS = (int)t.crs;
+    kp.G = 1;
+    kp.Cg = (int)t.c;
+    kp.Kg = (int)t.k;
+    kp.ntpg = plan.n_tiles;
+    kp.num_kb = plan.num_kb;
+    kp.m_tiles = plan.m_tiles;
+    kp.n_tiles = plan.n_tiles;
+    kp.grid = plan.grid;
+    kp.units = plan.units;
+    kp.vec_store = (t.k % 4) == 0 ? 1 : 0;
+    kp.debug_flags = algo ? algo->debug_flags : 0;
+    kp.reduce_concurrent = (algo && algo->reduction == CONV2D_REDUCTION_ORDERED) ? 0 : 1;
+    kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+    kp.trace = nullptr;
+#ifdef SGB_TRACE_ENABLED
+    kp.trace = g_trace;
+#endif
+    if (log_enabled())
+        std::fprintf(stderr, "[conv2d dgrad] M=%lld C=%lld KRS=%lld -> BN=%d splits=%d grid=%d\n", (long long)t.m,
+                     (long long)t.k, (long long)t.crs, plan.block_n, plan.splits, plan.grid);
+    cudaError_t err;
+    if (plan.block_n == 64) err = sgb::launch_conv2d_tc<128, 64, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    else if (plan.block_n == 128) err = sgb::launch_conv2d_tc<128, 128, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    else err = sgb::launch_conv2d_tc<128, 256, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
+    if (err != cudaSuccess) return CONV2D_ERR_CUDA;
+    g_last_launches = 1;
+    return CONV2D_OK;
+}
+
 int run_wgrad(const conv2d_params* params, const void* x, const void* dy, float* dw, void* workspace,
               size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
 {
@@ -1096,6 +1233,40 @@ size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_
 int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)
 {
     return conv2d_fwd_query_algo_epi(params, nullptr, out);
+}
+
+size_t conv2d_bwd_data_workspace_bytes(const conv2d_params* params)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    return workspace_bytes_for(dgrad_forward_shape(s));
+}
+
+int conv2d_bwd_data(const conv2d_params* params, const void* dy_dev, const void* w_dev, float* dx_dev,
+                    void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream, const conv2d_algo* algo)
+{
+    return run_dgrad(params, dy_dev, w_dev, dx_dev, workspace_dev, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), algo);
+}
+
+int conv2d_bwd_data_query_algo(const conv2d_params* params, conv2d_algo* out)
+{
+    if (!out) return CONV2D_ERR_INVALID;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (!dgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    Plan plan;
+    rc = dgrad_plan(dgrad_forward_shape(s), nullptr, &plan);
+    if (rc != CONV2D_OK) return rc;
+    std::memset(out, 0, sizeof(*out));
+    out->block_m = plan.block_m;
+    out->block_n = plan.block_n;
+    out->splits = plan.splits;
+    out->loader = plan.loader;
+    out->grid = plan.grid;
+    out->reduction = plan_cuts_tiles(plan) ? CONV2D_REDUCTION_CONCURRENT : CONV2D_REDUCTION_AUTO;
+    return CONV2D_OK;
 }
 
 size_t conv2d_bwd_weight_workspace_bytes(const conv2d_params* params)

@@ -104,7 +104,11 @@ enum LoaderKind : int {
     LOADER_TMA = 1, LOADER_CPASYNC = 2, LOADER_SCALAR = 3, LOADER_HYBRID = 4, LOADER_BOX = 6, LOADER_HALO = 7,
     // Weight gradient: the same pipeline with the GEMM dw[k][(r,s,c)] = sum_l dy[l][k] * im2col(x)[l][(r,s,c)]
     // over the output pixels l, both operands MN-major in shared memory.
-    LOADER_WGRAD = 8
+    LOADER_WGRAD = 8,
+    // Data gradient at stride 1: the forward convolution of dy with the weight
+    // w'[c][r][s][k] = w[k][R-1-r][S-1-s][c], read straight from w by TMA as an
+    // MN-major operand (channels c contiguous), the taps flipped by coordinate.
+    LOADER_DGRAD = 9
 };
 
 // Which engine brings in the im2col tile of the CTA's k-block number `it`:
@@ -113,7 +117,7 @@ enum LoaderKind : int {
 template <int LOADER>
 __device__ __forceinline__ bool a_by_tma(int it)
 {
-    return LOADER == LOADER_TMA || LOADER == LOADER_BOX || LOADER == LOADER_WGRAD ||
+    return LOADER == LOADER_TMA || LOADER == LOADER_BOX || LOADER == LOADER_WGRAD || LOADER == LOADER_DGRAD ||
            (LOADER == LOADER_HYBRID && (it & 1) == 0);
 }
 template <int LOADER>
@@ -172,6 +176,7 @@ struct TileConfig {
     static_assert(BM == 128 || LOADER == LOADER_TMA || LOADER == LOADER_BOX, "256-pixel tiles need a TMA loader");
     static constexpr bool HALO = LOADER == LOADER_HALO;
     static constexpr bool WGRAD = LOADER == LOADER_WGRAD;
+    static constexpr bool DGRAD = LOADER == LOADER_DGRAD;
     static constexpr int M_SUB = BM / MMA_M;  // 128-row MMA blocks per tile
     static constexpr int KC = LOADER == LOADER_BOX ? 2 : 1;  // k-blocks per pipeline stage
     // The halo loader keeps its activations in two halo buffers outside the ring.
@@ -187,7 +192,7 @@ struct TileConfig {
     static constexpr int BAR_BYTES = (2 * STAGES + 9) * 8 + 16;
     // With a TMA loader the gather warps' places go to the epilogue: 8 warps, two
     // per TMEM lane quadrant, each writing half of the tile's columns.
-    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD) ? 8 : 4;
+    static constexpr int EPI_WARPS = (LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD || DGRAD) ? 8 : 4;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOTS * EPI_SLOT_BYTES;
     // Without the halo loader's two halo buffers (2 * kp.halo_bytes, placed after the ring).
     static constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
@@ -203,7 +208,7 @@ struct TileConfig {
     // thus has one issuer, loading its uses in order, and a slot's parity waits
     // never run more than one phase ahead of the MMA's releases.  (Gather
     // loaders: warp 0 issues the weight tiles.)
-    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD;
+    static constexpr bool TMA_A = LOADER == LOADER_TMA || LOADER == LOADER_BOX || HALO || WGRAD || DGRAD;
     // The halo loader's only per-stage load is the weight tile: four threads
     // (warps 0, 11, 12, 13) share them, ring slot s going to producer s % 4.
     static constexpr int HALO_NB = 4;
@@ -469,6 +474,12 @@ struct LoadCursor {
             for (int i = 0; i < BN / 64; ++i)
                 ptx::tma_load_im2col_4d(b_dst + i * BK * 128, tm_b, bar, c + 64 * i, w_org, h_org, n_img,
                                         static_cast<uint16_t>(s * kp.dw), static_cast<uint16_t>(r * kp.dh));
+        } else if constexpr (LOADER == LOADER_DGRAD) {
+            // w as {C, R*S, K}: for the flipped tap, output channels n0 + 64i .. +63 (contiguous)
+            // x dy channels c .. c+63 (rows): BN / 64 boxes of 64 rows of 128 bytes, 8 KB apart.
+            const int tap = (kp.R - 1 - r) * kp.S + (kp.S - 1 - s);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) ptx::tma_load_3d(b_dst + i * BK * 128, tm_b, bar, n0 + 64 * i, tap, c);
         } else if constexpr (LOADER == LOADER_BOX) ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);  // KC k-blocks
         else ptx::tma_load_2d(b_dst, tm_b, bar, kb * BK, n0);
     }
@@ -485,6 +496,11 @@ struct LoadCursor {
         } else if constexpr (LOADER == LOADER_BOX) {
             ptx::tma_prefetch_5d(tm_a, 0, w_org + s * kp.dw, h_org + r * kp.dh, n_img, (c_base + c) / BK);
             ptx::tma_prefetch_3d(tm_b, 0, n0, kb * KC);
+        } else if constexpr (LOADER == LOADER_DGRAD) {
+            ptx::tma_prefetch_im2col_4d(tm_a, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
+                                        static_cast<uint16_t>(r * kp.dh));
+            const int tap = (kp.R - 1 - r) * kp.S + (kp.S - 1 - s);
+            for (int i = 0; i < BN / 64; ++i) ptx::tma_prefetch_3d(tm_b, n0 + 64 * i, tap, c);
         } else {
             ptx::tma_prefetch_im2col_4d(tm_a, c_base + c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
                                         static_cast<uint16_t>(r * kp.dh));
@@ -710,17 +726,20 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
     using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int A_STAGE_BYTES = Cfg::A_STAGE_BYTES;
-    constexpr uint32_t IDESC = Cfg::WGRAD ? ptx::idesc_bf16_f32_mn(MMA_M, BN) : ptx::idesc_bf16_f32(MMA_M, BN);
+    constexpr uint32_t IDESC = Cfg::WGRAD   ? ptx::idesc_bf16_f32_mn(MMA_M, BN)
+                               : Cfg::DGRAD ? ptx::idesc_bf16_f32_bmn(MMA_M, BN)
+                                            : ptx::idesc_bf16_f32(MMA_M, BN);
     const int lane = threadIdx.x & 31;
     // Weight gradient: MN-major operands, 64-element blocks along M/N 8 KB apart
     // (one 64-row TMA box each), groups of 8 reduction rows 1024 B apart.
     const uint64_t a_desc0 = Cfg::WGRAD ? ptx::sw128_mnmajor_desc(ptx::smem_addr(sm.a), BK * 128, 1024)
                                         : ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
-    const uint64_t b_desc0 = Cfg::WGRAD ? ptx::sw128_mnmajor_desc(ptx::smem_addr(sm.b), BK * 128, 1024)
-                                        : ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    const uint64_t b_desc0 = (Cfg::WGRAD || Cfg::DGRAD) ? ptx::sw128_mnmajor_desc(ptx::smem_addr(sm.b), BK * 128, 1024)
+                                                        : ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
     // Reduction step of one MMA (16 elements): 32 B along a K-major row, 16 rows of
     // 128 B in an MN-major tile.
-    constexpr int KSTEP_BYTES = Cfg::WGRAD ? UMMA_K * 128 : UMMA_K * 2;
+    constexpr int KSTEP_A = Cfg::WGRAD ? UMMA_K * 128 : UMMA_K * 2;
+    constexpr int KSTEP_B = (Cfg::WGRAD || Cfg::DGRAD) ? UMMA_K * 128 : UMMA_K * 2;
     const uint32_t a_chunk16 = LOADER == LOADER_BOX ? static_cast<uint32_t>(kp.px * 8) : 0u;
     const uint64_t halo_desc0 = Cfg::HALO ? ptx::sw128_kmajor_desc(ptx::smem_addr(sm.halo)) : 0ull;
     int h = 0;  // halo uses (halo loader)
@@ -794,12 +813,12 @@ __device__ void run_mma_issuer(const ConvKernelParams& kp, const SmemView& sm, u
 #pragma unroll
                 for (int k = 0; k < KSTEPS; ++k) {
                     const int chunk = k / (BK / UMMA_K), kin = k % (BK / UMMA_K);
-                    const uint64_t bdk = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * KSTEP_BYTES) >> 4);
+                    const uint64_t bdk = bd + static_cast<uint64_t>((chunk * BN * 128 + kin * KSTEP_B) >> 4);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::M_SUB; ++sub)  // 128-row blocks share the B tile
                         ptx::mma_bf16(tmem_d + sub * BN,
                                       ad + static_cast<uint64_t>(chunk) * a_chunk16 +
-                                          static_cast<uint64_t>((sub * MMA_M * 128 + kin * KSTEP_BYTES) >> 4),
+                                          static_cast<uint64_t>((sub * MMA_M * 128 + kin * KSTEP_A) >> 4),
                                       bdk, IDESC, k > 0 ? 1u : acc0);
                 }
             }
@@ -1563,6 +1582,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
     template SGB_LAUNCH_SIG(128, BN_, LOADER_WGRAD);   \
+    template SGB_LAUNCH_SIG(128, BN_, LOADER_DGRAD);   \
     template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_INSTANTIATE_CONV2D_BOX256(BN_) template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 
@@ -1575,6 +1595,7 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_BOX);     \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_HALO);    \
     extern template SGB_LAUNCH_SIG(128, BN_, LOADER_WGRAD);   \
+    extern template SGB_LAUNCH_SIG(128, BN_, LOADER_DGRAD);   \
     extern template SGB_LAUNCH_SIG(256, BN_, LOADER_TMA);
 #define SGB_DECLARE_CONV2D_BOX256(BN_) extern template SGB_LAUNCH_SIG(256, BN_, LOADER_BOX);
 

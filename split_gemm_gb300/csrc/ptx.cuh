@@ -457,5 +457,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n)
     return idesc_bf16_f32(m, n) | (1u << 15) | (1u << 16);
 }
 
+// The same with A K-major and B MN-major (the transpose-B bit only).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int m, int n)
+{
+    return idesc_bf16_f32(m, n) | (1u << 16);
+}
+
 }  // namespace ptx
 }  // namespace sgb

@@ -158,17 +158,19 @@ def output_extent(in_size: int, pad: int, dil: int, ker: int, stride: int) -> in
     return 0 if room < 0 else room // stride + 1
 
 
-def make_output_grad(wl: Workload, seed: Optional[int] = None) -> torch.Tensor:
-    """The output gradient dy [N,P,Q,K] bf16 for a workload's weight gradient: N(0, 2/L) with
-    L = N*P*Q, the reduction length of every weight-gradient element (the He scaling the
-    forward weights use for theirs), drawn in fp32 from its own generator (seed + 7919) and
-    rounded to bf16."""
+def make_output_grad(wl: Workload, seed: Optional[int] = None, variance: Optional[float] = None) -> torch.Tensor:
+    """An output gradient dy [N,P,Q,K] bf16 for a workload's backward passes, drawn in fp32
+    from its own generator (seed + 7919) and rounded to bf16.
+
+    Default variance 2/L with L = N*P*Q, the reduction length of every weight-gradient
+    element (the He scaling the forward weights use for theirs); the data gradient, whose
+    reduction runs over K*R*S against the He-init weights, takes ``variance=1.0``."""
     p = output_extent(wl.h, wl.pad_h, wl.dil_h, wl.r, wl.stride_h)
     q = output_extent(wl.w, wl.pad_w, wl.dil_w, wl.s, wl.stride_w)
     gen = torch.Generator("cpu")
     gen.manual_seed((wl.seed if seed is None else seed) + 7919)
-    L = max(1, wl.n * p * q)
-    return (torch.randn((wl.n, p, q, wl.k), generator=gen, dtype=torch.float32) * math.sqrt(2.0 / L)).to(
+    var = 2.0 / max(1, wl.n * p * q) if variance is None else float(variance)
+    return (torch.randn((wl.n, p, q, wl.k), generator=gen, dtype=torch.float32) * math.sqrt(var)).to(
         torch.bfloat16).contiguous()
 
 
