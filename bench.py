@@ -36,6 +36,7 @@ import workloads  # noqa: E402
 
 METRIC = "conv2d fwd TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
 METRIC_WGRAD = "conv2d wgrad TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
+METRIC_DGRAD = "conv2d dgrad TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
 DEFAULT_WORKLOAD = "resnet_56x56_c64"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -88,6 +89,12 @@ def algorithmic_bytes_wgrad(wl):
     th = _touched(wl.h, p, wl.stride_h, wl.pad_h, wl.dil_h, wl.r)
     tw = _touched(wl.w, q, wl.stride_w, wl.pad_w, wl.dil_w, wl.s)
     return float(wl.n * th * tw * wl.c * 2 + wl.n * p * q * wl.k * 2 + wl.k * wl.r * wl.s * (wl.c // wl.groups) * 4)
+
+
+def algorithmic_bytes_dgrad(wl):
+    """Output gradient dy (bf16) + weights (bf16) + input gradient dx (fp32)."""
+    p, q = shape_of(wl)
+    return float(wl.n * p * q * wl.k * 2 + wl.k * wl.r * wl.s * wl.c * 2 + wl.n * wl.h * wl.w * wl.c * 4)
 
 
 def load_peaks():
@@ -319,6 +326,42 @@ class WgradOracleSampler:
         return 2.0 * self.L * npts / done / 1e12, 1, f"{npts} random weight-gradient elements, 1 thread", done
 
 
+class DgradOracleSampler:
+    """Times the data-gradient oracle on randomly chosen gradient elements (one thread)."""
+
+    def __init__(self, wl):
+        import numpy as np
+
+        import oracle
+        from oracle import dgrad as od
+        self.np, self.od, self.wl = np, od, wl
+        _, w, _ = workloads.make_inputs(wl)
+        dy = workloads.make_output_grad(wl, variance=1.0)
+        self.wd, self.dyd = oracle.widen_bf16(w), oracle.widen_bf16(dy)
+        self.o = wl.options()
+        self.lib = od.load()
+        self.xs = (wl.n, wl.h, wl.w, wl.c)
+        t0 = time.perf_counter()
+        self._points(64)
+        self.per_point = max(1e-7, (time.perf_counter() - t0) / 64)
+
+    def _points(self, npts):
+        rng = self.np.random.default_rng(npts)
+        mi = rng.integers(0, self.wl.n * self.wl.h * self.wl.w, size=npts)
+        ci = rng.integers(0, self.wl.c, size=npts)
+        self.od.conv2d_dgrad_points_f64(self.dyd, self.wd, self.xs, self.o["stride"], self.o["padding"],
+                                        self.o["dilation"], mi, ci, lib=self.lib)
+
+    def run(self, budget_s: float):
+        npts = max(64, int(budget_s / self.per_point))
+        t0 = time.perf_counter()
+        self._points(npts)
+        done = time.perf_counter() - t0
+        # Same FLOP count per step as the forward convolution, spread over N*H*W*C elements.
+        flops = flops_per_step(self.wl) * npts / (self.wl.n * self.wl.h * self.wl.w * self.wl.c)
+        return flops / done / 1e12, 1, f"{npts} random input-gradient elements, 1 thread", done
+
+
 # ----------------------------------------------------------------------------- the GPU arm
 def _sets_for(wl, set_bytes):
     return max(1, min(64, math.ceil(2 * L2_BYTES / max(1, set_bytes))))
@@ -338,6 +381,8 @@ def run_ours(args, wl, world, rank, local):
     p, q = sg.output_shape(params)
     if args.op == "wgrad":
         return run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params)
+    if args.op == "dgrad":
+        return run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params)
     forced = None
     if args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction:
         forced = sg.Algo()
@@ -505,6 +550,38 @@ def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
                 clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
 
 
+def run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params):
+    """The data gradient of the workload: conv2d_bwd_data over rotating buffer sets."""
+    dy = workloads.make_output_grad(wl, variance=1.0)
+    forced = _forced_algo(sg, args)
+    algo = sg.query_dgrad_algo(params)
+    if forced is not None:
+        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, algo.loader,
+                       forced.grid or (0 if forced.splits else algo.grid), 0, 128, 0, forced.reduction or algo.reduction)
+    xs = (wl.n, wl.h, wl.w, wl.c)
+    set_bytes = dy.numel() * 2 + w.numel() * 2 + wl.n * wl.h * wl.w * wl.c * 4
+    n_sets = _sets_for(wl, set_bytes)
+    sets = [(dy.to(dev), w.to(dev), torch.empty(xs, dtype=torch.float32, device=dev)) for _ in range(n_sets)]
+    ws = torch.zeros(max(4096, sg.dgrad_workspace_bytes(params)), dtype=torch.uint8, device=dev)
+    o = wl.options()
+    opts = dict(stride=o["stride"], padding=o["padding"], dilation=o["dilation"])
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        dyd, wd, dxd = sets[i % n_sets]
+        sg.conv2d_bwd_data_into(dxd, dyd, wd, **opts, workspace=ws, algo=forced)
+
+    def check():
+        if sg.status(ws, stream) != 0:
+            raise RuntimeError("device status reported a timeout during warm-up")
+
+    elapsed, clocks, chunk = _time_graphs(torch, stream, step, args.steps, args.warmup, n_sets, dev, dist_mod, check)
+    status = sg.status(ws, stream)
+    job_s, job_flops = aggregate(dist_mod, elapsed, flops_per_step(wl) * args.steps, dev)
+    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
+                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
+
+
 def run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, steps, dist_mod):
     """Same metric through the host-buffer entry point: H2D of x, w, bias + kernel + D2H of y, every step.
 
@@ -561,9 +638,10 @@ def config_of(wl, extra=None):
 
 def roofline(wl, t_step_s, peaks, peak_src, out_bytes=4, op="fwd"):
     flops = flops_per_step(wl)
-    nbytes = algorithmic_bytes_wgrad(wl) if op == "wgrad" else algorithmic_bytes(wl, out_bytes)
+    nbytes = (algorithmic_bytes_wgrad(wl) if op == "wgrad" else algorithmic_bytes_dgrad(wl) if op == "dgrad"
+              else algorithmic_bytes(wl, out_bytes))
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = recorded_traffic(wl.name if op == "fwd" else f"{wl.name}:wgrad") if out_bytes == 4 else None
+    traffic = recorded_traffic(wl.name if op == "fwd" else f"{wl.name}:{op}") if out_bytes == 4 else None
     if flops / nbytes >= ridge:
         achieved = flops / t_step_s / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -585,7 +663,7 @@ def main_ours(args):
     t_step = res["elapsed"] / K
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        sampler = WgradOracleSampler(wl) if args.op == "wgrad" else OracleSampler(wl)
+        sampler = {"wgrad": WgradOracleSampler, "dgrad": DgradOracleSampler}.get(args.op, OracleSampler)(wl)
         v, cores, desc, secs = sampler.run(args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
                "seconds": round(secs, 2)}
@@ -595,7 +673,7 @@ def main_ours(args):
         return 0
     value = res["job_flops"] / res["job_s"] / 1e12
     line = {
-        "metric": METRIC_WGRAD if args.op == "wgrad" else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": {"wgrad": METRIC_WGRAD, "dgrad": METRIC_DGRAD}.get(args.op, METRIC), "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup,
         "ms_per_step": res["job_s"] / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
@@ -609,6 +687,10 @@ def main_ours(args):
                                      "layout": "x NHWC bf16, dy NPQK bf16 ~N(0, 2/(N*P*Q)), dw KRSC fp32",
                                      "gemm_mnk": [wl.k, wl.r * wl.s * wl.c, wl.n * shape_of(wl)[0] * shape_of(wl)[1]]}
                                     if args.op == "wgrad" else {}),
+                                 **({"op": "data gradient", "epilogue": "fp32 dx",
+                                     "layout": "dy NPQK bf16 ~N(0, 1), w KRSC bf16, dx NHWC fp32",
+                                     "gemm_mnk": [wl.n * wl.h * wl.w, wl.c, wl.k * wl.r * wl.s]}
+                                    if args.op == "dgrad" else {}),
                                  "l2": f"{res['n_sets']} rotating input/output buffer sets (> 2x L2) per step",
                                  "timing": f"CUDA events around CUDA-graph replays ({res['graph_chunk']} launches "
                                            "per graph), max over ranks"}),
@@ -670,8 +752,8 @@ def parse_args(argv=None):
     ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box, 7 halo)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "wgrad"],
-                    help="fwd: the forward convolution (the headline); wgrad: its weight gradient")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "wgrad", "dgrad"],
+                    help="fwd: the forward convolution (the headline); wgrad / dgrad: its weight / input gradient")
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "bf16", "relu_bf16"],
                     help="fused epilogue variant (ReLU after the bias, bf16 output); the e2e leg runs only for none")
     args = ap.parse_args(argv)

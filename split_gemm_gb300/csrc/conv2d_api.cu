@@ -865,9 +865,12 @@ int choose_wgrad_plan(const Shape& s, const conv2d_algo* force, WgradPlan* pl)
     if (force && force->block_m != 0 && force->block_m != 128) return CONV2D_ERR_UNSUPPORTED;
     if (force && force->loader != CONV2D_LOADER_AUTO && force->loader != CONV2D_LOADER_TMA_IM2COL)
         return CONV2D_ERR_UNSUPPORTED;
-    // The widest column block the channels fill: each 64-pixel stage's dy tile then
-    // feeds the most MMA work (measured: 256 beats 128 by 8-25% where C allows it).
-    const int bn = (force && force->block_n) ? force->block_n : (s.c % 256 == 0 ? 256 : s.c % 128 == 0 ? 128 : 64);
+    // The widest column block the channels fill, so that each 64-pixel stage's dy tile
+    // feeds the most MMA work (measured: 256 beats 128 by 8-25% where C allows it),
+    // unless that leaves fewer than 16 tiles to share the reduction (a 1x1 layer with
+    // C = 256 and K = 512 measured 8% slower at 256 wide).
+    int bn = (force && force->block_n) ? force->block_n : (s.c % 256 == 0 ? 256 : s.c % 128 == 0 ? 128 : 64);
+    if (!(force && force->block_n) && bn == 256 && cdiv(s.k, 128) * s.r * s.s * (s.c / 256) < 16) bn = 128;
     if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
     const int64_t m_tiles = cdiv(s.k, 128);
     const int64_t ntpt = cdiv(s.c, bn);
