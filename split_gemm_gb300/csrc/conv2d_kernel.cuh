@@ -1164,9 +1164,10 @@ __device__ __forceinline__ void finish_from_part(const ConvKernelParams& kp, int
     }
 }
 
-template <int BM, int BN, int LOADER>
-__device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
-                             uint32_t tmem_base)
+// FUSED: the fused epilogue (ReLU, bf16 output, cut tiles through kp.part)
+// compiled in; the plain instantiation carries none of its code.
+template <int BM, int BN, int LOADER, bool FUSED>
+__device__ void run_epilogue_impl(const ConvKernelParams& kp, const SmemView& sm, uint32_t tmem_base)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
     constexpr int EPI_T = Cfg::EPI_WARPS * 32;
@@ -1196,7 +1197,7 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
         if constexpr (LOADER == LOADER_BOX) box_origin(kp, m_tile, bx_n, bx_p, bx_q);
         // Fused epilogue of a cut tile: partial sums go to kp.part, and the bias,
         // the activation and the output conversion wait for the finishing pass.
-        const bool via_part = (kp.relu | kp.out_bf16) != 0 && sg.nsplits > 1;
+        const bool via_part = FUSED && sg.nsplits > 1;
         const bool add_bias = kp.bias != nullptr && sg.split == 0 && !via_part;
         // Bias of this warp's slabs, fetched before the accumulator wait so that
         // its latency is hidden.  Vector stores: lane holds the four columns of its
@@ -1285,11 +1286,11 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                             val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
                             val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
                         }
-                        if (kp.relu && !via_part) val = ptx::relu4(val);
+                        if (FUSED && kp.relu && !via_part) val = ptx::relu4(val);
                         if (m >= 0 && col < n_end) {
                             const int64_t at = static_cast<int64_t>(m) * kp.ldy + col;
                             if (via_part) ptx::red_add_v4_f32(kp.part + at, val);
-                            else if (kp.out_bf16)
+                            else if (FUSED && kp.out_bf16)
                                 *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
                             else if (sg.split == 0) *reinterpret_cast<uint4*>(kp.y + at) = val;
                             else ptx::red_add_v4_f32(kp.y + at, val);
@@ -1337,8 +1338,8 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                         const int n = nb + e;
                         if (n >= n_end) break;
                         float o = __uint_as_float(v[e]);
-                        if (kp.relu) o = fmaxf(o, 0.0f);
-                        if (kp.out_bf16) {  // fused epilogue: whole tiles only
+                        if (FUSED && kp.relu) o = fmaxf(o, 0.0f);
+                        if (FUSED && kp.out_bf16) {  // fused epilogue: whole tiles (cut ones go through kp.part)
                             reinterpret_cast<uint16_t*>(kp.y)[static_cast<int64_t>(m) * kp.ldy + n] = ptx::bf16_bits(o);
                             continue;
                         }
@@ -1369,8 +1370,9 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
                 *sm.epi_go = last ? 2u : 1u;
             }
             ptx::named_bar_sync(1, EPI_T);
-            if (*sm.epi_go == 2u)
-                finish_from_part<BM, BN, LOADER>(kp, m_tile, n0, n_end, jbeg, bx_n, bx_p, bx_q);
+            if constexpr (FUSED) {
+                if (*sm.epi_go == 2u) finish_from_part<BM, BN, LOADER>(kp, m_tile, n0, n_end, jbeg, bx_n, bx_p, bx_q);
+            }
         } else if (sg.nsplits > 1) {
             SGB_CYCLES_BEGIN(t_done);
             // Before the next split may read or add: split 0's stores (both modes)
@@ -1397,7 +1399,10 @@ __device__ void run_epilogue(const ConvKernelParams& kp, const SmemView& sm,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int BM, int BN, int LOADER>
+// FUSED selects the instantiation with the fused epilogue (ReLU, bf16 output),
+// so that the plain one's code and register allocation are exactly those of a
+// kernel without it.
+template <int BM, int BN, int LOADER, bool FUSED>
 __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     conv2d_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const ConvKernelParams kp)
@@ -1485,7 +1490,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     } else if (warp == 1) {
         run_mma_issuer<BM, BN, LOADER>(kp, sm, tmem_base);
     } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
-        run_epilogue<BM, BN, LOADER>(kp, sm, tmem_base);
+        run_epilogue_impl<BM, BN, LOADER, FUSED>(kp, sm, tmem_base);
     } else if (warp == WAITER_WARP) {
         run_stage_waiter<BM, BN, LOADER>(kp, sm);
     } else if (warp > WAITER_WARP) {
@@ -1538,18 +1543,21 @@ cudaError_t launch_conv2d_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, c
     using Cfg = TileConfig<BM, BN, LOADER>;
     const int smem_bytes = conv2d_tc_smem_bytes<BM, BN, LOADER>(kp.halo_bytes);
     if (smem_bytes > kMaxSmemBytes) return cudaErrorInvalidValue;
-    auto kern = conv2d_fwd_tc_kernel<BM, BN, LOADER>;
+    // The gradients have no fused epilogue: one instantiation.
+    constexpr bool kHasFused = LOADER != LOADER_WGRAD && LOADER != LOADER_DGRAD;
+    const bool fused = kHasFused && (kp.relu | kp.out_bf16) != 0;
+    auto kern = fused ? conv2d_fwd_tc_kernel<BM, BN, LOADER, kHasFused> : conv2d_fwd_tc_kernel<BM, BN, LOADER, false>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    // The dynamic shared-memory opt-in is per device; remember which devices have it.
-    static unsigned long long configured = 0ull;
+    // The dynamic shared-memory opt-in is per device and instantiation; remember which have it.
+    static unsigned long long configured[2] = {0ull, 0ull};
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    if (!bit || !(__atomic_load_n(&configured[fused], __ATOMIC_ACQUIRE) & bit)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    Cfg::HALO ? kMaxSmemBytes : Cfg::SMEM_BYTES);
         if (err != cudaSuccess) return err;
-        if (bit) __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+        if (bit) __atomic_fetch_or(&configured[fused], bit, __ATOMIC_RELEASE);
     }
     // Programmatic stream serialization: this launch may start while the
     // previous kernel in the stream drains; the kernel waits for it (see

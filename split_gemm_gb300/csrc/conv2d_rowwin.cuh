@@ -565,8 +565,10 @@ __device__ void rw_mma(const RowWinParams& kp, const RwSmem& sm, uint32_t tmem_b
 }
 
 // ---------------------------------------------------------------- epilogue (warps 9..12)
-template <int BN>
-__device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t tmem_base, int t_lo, int t_hi)
+// FUSED: the fused epilogue (ReLU, bf16 output) compiled in; the plain
+// instantiation carries none of its code.
+template <int BN, bool FUSED>
+__device__ void rw_epilogue_impl(const RowWinParams& kp, const RwSmem& sm, uint32_t tmem_base, int t_lo, int t_hi)
 {
     const int et = threadIdx.x - RW_EPI_WARP0 * 32;  // 0..127
     const int lane = threadIdx.x & 31;
@@ -661,9 +663,9 @@ __device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t t
                         const int row = quad * 32 + rr;
                         uint4 val =
                             ptx::ld_shared_v4(saddr + static_cast<uint32_t>(rr * 128 + ((chunk ^ (rr & 7)) << 4)));
-                        if (kp.relu) val = ptx::relu4(val);
+                        if (FUSED && kp.relu) val = ptx::relu4(val);
                         if (row < nv && col < kp.K) {
-                            if (kp.out_bf16)
+                            if (FUSED && kp.out_bf16)
                                 *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + (m0 + row) * kp.K + col) =
                                     ptx::pack_bf16x4(val);
                             else
@@ -696,8 +698,8 @@ __device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t t
                         const int n = j * 32 + e;
                         if (n >= kp.K) break;
                         float o = __uint_as_float(v[e]);
-                        if (kp.relu) o = fmaxf(o, 0.0f);
-                        if (kp.out_bf16)
+                        if (FUSED && kp.relu) o = fmaxf(o, 0.0f);
+                        if (FUSED && kp.out_bf16)
                             reinterpret_cast<uint16_t*>(kp.y)[(m0 + row) * kp.K + n] = ptx::bf16_bits(o);
                         else
                             yrow[n] = o;
@@ -713,7 +715,9 @@ __device__ void rw_epilogue(const RowWinParams& kp, const RwSmem& sm, uint32_t t
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int BN>
+// FUSED selects the kernel instantiation with the fused epilogue, so that the
+// plain one's register allocation is not shaped by code it never runs.
+template <int BN, bool FUSED>
 __global__ void __launch_bounds__(RW_THREADS, 1) conv2d_rowwin_kernel(const __grid_constant__ RowWinParams kp)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -774,7 +778,7 @@ __global__ void __launch_bounds__(RW_THREADS, 1) conv2d_rowwin_kernel(const __gr
     } else if (warp == RW_MMA_WARP) {
         if (lane == 0) rw_mma<BN>(kp, sm, tmem_base, t_lo, t_hi);
     } else {
-        rw_epilogue<BN>(kp, sm, tmem_base, t_lo, t_hi);
+        rw_epilogue_impl<BN, FUSED>(kp, sm, tmem_base, t_lo, t_hi);
     }
 
     ptx::tc_fence_before();
@@ -790,17 +794,18 @@ __global__ void __launch_bounds__(RW_THREADS, 1) conv2d_rowwin_kernel(const __gr
 template <int BN>
 cudaError_t launch_conv2d_rowwin(const RowWinParams& kp, int smem_bytes, bool pdl, cudaStream_t stream)
 {
-    auto kern = conv2d_rowwin_kernel<BN>;
+    const bool fused = (kp.relu | kp.out_bf16) != 0;
+    auto kern = fused ? conv2d_rowwin_kernel<BN, true> : conv2d_rowwin_kernel<BN, false>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    // Opt in once per device to the largest dynamic shared memory any launch asks for.
-    static unsigned long long configured = 0ull;
+    // Opt in once per device and instantiation to the largest dynamic shared memory any launch asks for.
+    static unsigned long long configured[2] = {0ull, 0ull};
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+    if (!bit || !(__atomic_load_n(&configured[fused], __ATOMIC_ACQUIRE) & bit)) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (err != cudaSuccess) return err;
-        if (bit) __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+        if (bit) __atomic_fetch_or(&configured[fused], bit, __ATOMIC_RELEASE);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(kp.grid));
