@@ -711,7 +711,7 @@ def main_reference(args):
     if rank != 0:
         return 0
     wl = workloads.get(args.workload)
-    sampler = OracleSampler(wl)
+    sampler = {"wgrad": WgradOracleSampler, "dgrad": DgradOracleSampler}.get(args.op, OracleSampler)(wl)
     per_step = max(0.001, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         sampler.run(per_step)
@@ -722,7 +722,8 @@ def main_reference(args):
         total += secs
     value = sum(vals) / len(vals) if vals else 0.0
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "impl": "reference", "metric": {"wgrad": METRIC_WGRAD, "dgrad": METRIC_DGRAD}.get(args.op, METRIC),
+        "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / max(1, args.steps) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl, {"parallelism": "CPU oracle, rank 0 only"}),
