@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 def test_aggregate_takes_max_time_and_sum_of_work():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of a multi-threaded process
         out = mgr.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
