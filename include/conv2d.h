@@ -90,13 +90,19 @@ typedef enum {
                                      64-channel chunks of one filter tap (and a 3-D box two weight k-blocks);
                                      needs groups == 1, C % 128 == 0, strides <= 8, and block_n <= 128
                                      with 256-pixel tiles */
-    CONV2D_LOADER_HALO = 7        /* stride 1 only: a tile is 128 consecutive pixels of an image seen with the
+    CONV2D_LOADER_HALO = 7,       /* stride 1 only: a tile is 128 consecutive pixels of an image seen with the
                                      padded row pitch W + 2*pad_w (pixels past Q are computed and discarded);
                                      per 64-channel chunk one tiled TMA box of whole padded input rows serves
                                      every filter tap, which the MMA reads in place at the tap's row offset.
                                      Needs groups == 1, C % 64 == 0, W + 2*pad_w <= 256, 128-pixel tiles, and the two halo
                                      buffers plus the weight ring within shared memory (block_n is narrowed
                                      to fit unless forced) */
+    CONV2D_LOADER_DIRECT = 8      /* not an implicit GEMM: a CUDA-core direct convolution for groups of few
+                                     channels, one thread per (output pixel, group) in fp32 FMAs, the group
+                                     weights in shared memory.  Needs groups > 1 and C/groups == K/groups in
+                                     {1, 2, 4, 8, 16} (depthwise: 1), the weights (K*R*S*C/groups fp32) within
+                                     shared memory.  The heuristic takes it for such shapes when nothing else
+                                     is forced; block_n, block_m and splits do not apply */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "conv2d.h"
+#include "conv2d_direct.cuh"
 #include "conv2d_kernel.cuh"
 #include "conv2d_rowwin.cuh"
 
@@ -24,6 +25,11 @@ SGB_DECLARE_CONV2D_BOX256(128)
 extern template SGB_ROWWIN_SIG(64);
 extern template SGB_ROWWIN_SIG(128);
 extern template SGB_ROWWIN_SIG(256);
+extern template SGB_DIRECT_SIG(1);
+extern template SGB_DIRECT_SIG(2);
+extern template SGB_DIRECT_SIG(4);
+extern template SGB_DIRECT_SIG(8);
+extern template SGB_DIRECT_SIG(16);
 }  // namespace sgb
 
 namespace {
@@ -34,6 +40,7 @@ constexpr int64_t kMinTileM = 128;  // the narrowest tile height (sizes the sema
 constexpr int64_t kIndexLimit = (int64_t(1) << 31) - 1;
 constexpr size_t kStatusBytes = 256;  // status word, padded so the semaphores start 256-B aligned
 constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // 1 s
+constexpr long long kSmemDirectLimit = 232448;  // dynamic shared memory one CTA may opt in to
 
 thread_local int g_last_launches = 0;
 
@@ -367,6 +374,23 @@ int64_t semaphore_capacity(const Shape& s)
 constexpr int kMinUnitsPerCta = 4;     // no split gets fewer k-blocks than this
 constexpr int kMaxSplitsPerTile = 6;   // longest serial in-place reduction chain the heuristic builds
 
+// ------------------------------------------------------------------ direct kernel (groups of few channels)
+// C/groups == K/groups in {1, 2, 4, 8, 16} with groups > 1: the implicit GEMM would
+// fill CG of each 64-wide column block, so a CUDA-core kernel takes these shapes.
+bool direct_eligible(const Shape& s)
+{
+    if (s.g < 2 || s.cg != s.kg) return false;
+    if (s.cg != 1 && s.cg != 2 && s.cg != 4 && s.cg != 8 && s.cg != 16) return false;
+    return sgb::conv2d_direct_smem_bytes((int)s.k, (int)s.r, (int)s.s, (int)s.cg) <= kSmemDirectLimit;
+}
+
+// Nothing forced but what every path accepts (wait bound, reduction, test hooks).
+bool nothing_forced(const conv2d_algo* a)
+{
+    return !a || (a->loader == CONV2D_LOADER_AUTO && a->splits == 0 && a->grid == 0 && a->block_n == 0 &&
+                  a->block_m == 0);
+}
+
 // whole_tiles: where the heuristic would divide many tiles stream-K style over
 // the SMs, give every CTA whole tiles instead.  A fused epilogue (bf16 output,
 // activation) asks for it: its cut tiles take a detour through an fp32 buffer.
@@ -676,6 +700,48 @@ bool log_enabled()
     return on;
 }
 
+int run_direct(const Shape& s, const void* x, const void* w, const float* bias, float* y, cudaStream_t stream,
+               const conv2d_algo* algo, bool relu, bool out_bf16)
+{
+    sgb::DirectParams dp{};
+    dp.x = static_cast<const uint16_t*>(x);
+    dp.w = static_cast<const uint16_t*>(w);
+    dp.bias = bias;
+    dp.y = y;
+    dp.N = (int)s.n; dp.H = (int)s.h; dp.W = (int)s.w; dp.C = (int)s.c;
+    dp.K = (int)s.k; dp.R = (int)s.r; dp.S = (int)s.s; dp.P = (int)s.p; dp.Q = (int)s.q;
+    dp.sh = (int)s.sh; dp.sw = (int)s.sw; dp.ph = (int)s.ph; dp.pw = (int)s.pw; dp.dh = (int)s.dh; dp.dw = (int)s.dw;
+    dp.G = (int)s.g;
+    dp.relu = relu ? 1 : 0;
+    dp.out_bf16 = out_bf16 ? 1 : 0;
+    dp.total = s.m * s.g;
+    // Every CTA stages the whole group-weight array: as many CTAs per SM as shared
+    // memory and the 2048-thread limit allow, enough to cover the work once.
+    const long long smem = sgb::conv2d_direct_smem_bytes(dp.K, dp.R, dp.S, (int)s.cg);
+    const long long nsm = sm_count_current() > 0 ? sm_count_current() : 1;
+    long long per_sm = smem > 0 ? kSmemDirectLimit / smem : 8;
+    if (per_sm > 2048 / sgb::DIRECT_THREADS) per_sm = 2048 / sgb::DIRECT_THREADS;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = cdiv(dp.total, sgb::DIRECT_THREADS);
+    if (grid > nsm * per_sm) grid = nsm * per_sm;
+    if (algo && algo->grid > 0) grid = algo->grid;
+    if (grid < 1 || grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
+    if (log_enabled())
+        std::fprintf(stderr, "[conv2d] M=%lld K=%lld groups=%lld -> direct CG=%lld grid=%lld smem=%lld\n",
+                     (long long)s.m, (long long)s.k, (long long)s.g, (long long)s.cg, grid, smem);
+    cudaError_t err;
+    switch (s.cg) {
+        case 1: err = sgb::launch_conv2d_direct<1>(dp, (int)grid, stream); break;
+        case 2: err = sgb::launch_conv2d_direct<2>(dp, (int)grid, stream); break;
+        case 4: err = sgb::launch_conv2d_direct<4>(dp, (int)grid, stream); break;
+        case 8: err = sgb::launch_conv2d_direct<8>(dp, (int)grid, stream); break;
+        default: err = sgb::launch_conv2d_direct<16>(dp, (int)grid, stream); break;
+    }
+    if (err != cudaSuccess) return CONV2D_ERR_CUDA;
+    g_last_launches = 1;
+    return CONV2D_OK;
+}
+
 int run_conv(const conv2d_params* params, const void* x, const void* w, const float* bias, float* y,
              void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo,
              const conv2d_epilogue* epi = nullptr)
@@ -699,6 +765,12 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     const bool relu = epi && epi->activation == CONV2D_ACT_RELU;
     const bool out_bf16 = epi && epi->out_dtype == CONV2D_OUT_BF16;
     const bool fused = relu || out_bf16;
+    const bool force_direct = algo && algo->loader == CONV2D_LOADER_DIRECT;
+    if (force_direct || (nothing_forced(algo) && direct_eligible(s))) {
+        if (!direct_eligible(s) || (algo && (algo->splits > 1 || algo->block_m != 0)))
+            return CONV2D_ERR_UNSUPPORTED;
+        return run_direct(s, x, w, bias, y, stream, algo, relu, out_bf16);
+    }
     Plan plan;
     rc = choose_plan(s, algo, &plan, fused);
     if (rc != CONV2D_OK) return rc;
@@ -1207,6 +1279,19 @@ int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue
     Shape s;
     int rc = make_shape(params, &s);
     if (rc != CONV2D_OK) return rc;
+    if (direct_eligible(s)) {
+        std::memset(out, 0, sizeof(*out));
+        out->loader = CONV2D_LOADER_DIRECT;
+        const long long smem = sgb::conv2d_direct_smem_bytes((int)s.k, (int)s.r, (int)s.s, (int)s.cg);
+        long long per_sm = smem > 0 ? kSmemDirectLimit / smem : 8;
+        if (per_sm > 2048 / sgb::DIRECT_THREADS) per_sm = 2048 / sgb::DIRECT_THREADS;
+        if (per_sm < 1) per_sm = 1;
+        const long long nsm = sm_count_current() > 0 ? sm_count_current() : 1;
+        long long grid = cdiv(s.m * s.g, sgb::DIRECT_THREADS);
+        if (grid > nsm * per_sm) grid = nsm * per_sm;
+        out->grid = static_cast<int32_t>(grid);
+        return CONV2D_OK;
+    }
     Plan plan;
     rc = choose_plan(s, nullptr, &plan, fused);
     if (rc != CONV2D_OK) return rc;

@@ -98,7 +98,7 @@ WORKLOADS = {
 }
 
 # Grouped convolutions (beyond the benchmark list): a ResNeXt-style 3x3 layer with
-# 32 groups of 8 channels, and one with 8 groups of 64 channels.
+# 32 groups of 8 channels, one with 8 groups of 64 channels, and a depthwise 3x3.
 GROUPED = {
     wl.name: wl for wl in [
         Workload("resnext_28x28_c256_g32", 16, 28, 28, 256, 256, 3, 3, 1, 1, 1, 1, 1, 1,
@@ -107,6 +107,9 @@ GROUPED = {
         Workload("grouped_28x28_c512_g8", 16, 28, 28, 512, 512, 3, 3, 1, 1, 1, 1, 1, 1,
                  x_dist="normal", w_dist="he", bias="normal:0.1", groups=8,
                  note="8 groups of 64 channels: 8 GEMMs 12544x64x576"),
+        Workload("depthwise_56x56_c128", 16, 56, 56, 128, 128, 3, 3, 1, 1, 1, 1, 1, 1,
+                 x_dist="normal", w_dist="he", bias="normal:0.1", groups=128,
+                 note="depthwise 3x3 (one channel per group), MobileNet-style"),
     ]
 }
 WORKLOADS.update(GROUPED)
