@@ -99,9 +99,9 @@ typedef enum {
                                      to fit unless forced) */
     CONV2D_LOADER_DIRECT = 8      /* not an implicit GEMM: a CUDA-core direct convolution for groups of few
                                      channels, one thread per (output pixel, group) in fp32 FMAs, the group
-                                     weights in shared memory.  Needs groups > 1 and C/groups == K/groups in
-                                     {1, 2, 4, 8, 16} (depthwise: 1), the weights (K*R*S*C/groups fp32) within
-                                     shared memory.  The heuristic takes it for such shapes when nothing else
+                                     weights in shared memory.  Needs groups > 1, C/groups == K/groups in
+                                     {1, 2, 4, 8, 16} (depthwise: 1), C % 8 == 0, and the weights
+                                     (K*R*S*C/groups fp32) within shared memory.  The heuristic takes it for such shapes when nothing else
                                      is forced; block_n, block_m and splits do not apply */
 } conv2d_loader;
 

@@ -377,11 +377,36 @@ constexpr int kMaxSplitsPerTile = 6;   // longest serial in-place reduction chai
 // ------------------------------------------------------------------ direct kernel (groups of few channels)
 // C/groups == K/groups in {1, 2, 4, 8, 16} with groups > 1: the implicit GEMM would
 // fill CG of each 64-wide column block, so a CUDA-core kernel takes these shapes.
+int direct_chunk(int64_t cg) { return cg == 16 ? 16 : 8; }   // channels per thread (DirectCfg::CH)
+int direct_px(int64_t cg) { return cg == 16 ? 2 : 4; }       // output pixels per thread (DirectCfg::PX)
+
+// Threads of the direct kernel: one per (image, output row, block of PX pixels, channel chunk).
+int64_t direct_items(const Shape& s)
+{
+    return s.n * s.p * cdiv(s.q, direct_px(s.cg)) * (s.c / direct_chunk(s.cg));
+}
+
 bool direct_eligible(const Shape& s)
 {
     if (s.g < 2 || s.cg != s.kg) return false;
     if (s.cg != 1 && s.cg != 2 && s.cg != 4 && s.cg != 8 && s.cg != 16) return false;
+    if (s.c % direct_chunk(s.cg) != 0) return false;  // whole 16-byte chunks of whole groups
+    if (direct_items(s) > 2147483647ll) return false;
     return sgb::conv2d_direct_smem_bytes((int)s.k, (int)s.r, (int)s.s, (int)s.cg) <= kSmemDirectLimit;
+}
+
+// CTAs of the direct kernel: as many per SM as shared memory and the thread limit
+// allow (each stages every group weight), enough to cover the items once.
+int64_t direct_grid(const Shape& s)
+{
+    const long long smem = sgb::conv2d_direct_smem_bytes((int)s.k, (int)s.r, (int)s.s, (int)s.cg);
+    const long long nsm = sm_count_current() > 0 ? sm_count_current() : 1;
+    long long per_sm = smem > 0 ? kSmemDirectLimit / smem : 8;
+    if (per_sm > 2048 / sgb::DIRECT_THREADS) per_sm = 2048 / sgb::DIRECT_THREADS;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = cdiv(direct_items(s), sgb::DIRECT_THREADS);
+    if (grid > nsm * per_sm) grid = nsm * per_sm;
+    return grid < 1 ? 1 : grid;
 }
 
 // Nothing forced but what every path accepts (wait bound, reduction, test hooks).
@@ -714,16 +739,11 @@ int run_direct(const Shape& s, const void* x, const void* w, const float* bias, 
     dp.G = (int)s.g;
     dp.relu = relu ? 1 : 0;
     dp.out_bf16 = out_bf16 ? 1 : 0;
-    dp.total = s.m * s.g;
-    // Every CTA stages the whole group-weight array: as many CTAs per SM as shared
-    // memory and the 2048-thread limit allow, enough to cover the work once.
+    dp.nchunk = (int)(s.c / direct_chunk(s.cg));
+    dp.qblocks = (int)cdiv(s.q, direct_px(s.cg));
+    dp.items = (int)direct_items(s);
     const long long smem = sgb::conv2d_direct_smem_bytes(dp.K, dp.R, dp.S, (int)s.cg);
-    const long long nsm = sm_count_current() > 0 ? sm_count_current() : 1;
-    long long per_sm = smem > 0 ? kSmemDirectLimit / smem : 8;
-    if (per_sm > 2048 / sgb::DIRECT_THREADS) per_sm = 2048 / sgb::DIRECT_THREADS;
-    if (per_sm < 1) per_sm = 1;
-    long long grid = cdiv(dp.total, sgb::DIRECT_THREADS);
-    if (grid > nsm * per_sm) grid = nsm * per_sm;
+    long long grid = direct_grid(s);
     if (algo && algo->grid > 0) grid = algo->grid;
     if (grid < 1 || grid > 2147483647ll) return CONV2D_ERR_UNSUPPORTED;
     if (log_enabled())
@@ -1282,14 +1302,7 @@ int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue
     if (direct_eligible(s)) {
         std::memset(out, 0, sizeof(*out));
         out->loader = CONV2D_LOADER_DIRECT;
-        const long long smem = sgb::conv2d_direct_smem_bytes((int)s.k, (int)s.r, (int)s.s, (int)s.cg);
-        long long per_sm = smem > 0 ? kSmemDirectLimit / smem : 8;
-        if (per_sm > 2048 / sgb::DIRECT_THREADS) per_sm = 2048 / sgb::DIRECT_THREADS;
-        if (per_sm < 1) per_sm = 1;
-        const long long nsm = sm_count_current() > 0 ? sm_count_current() : 1;
-        long long grid = cdiv(s.m * s.g, sgb::DIRECT_THREADS);
-        if (grid > nsm * per_sm) grid = nsm * per_sm;
-        out->grid = static_cast<int32_t>(grid);
+        out->grid = static_cast<int32_t>(direct_grid(s));
         return CONV2D_OK;
     }
     Plan plan;

@@ -3,15 +3,17 @@
 //
 // With so few channels per group the implicit GEMM wastes the tensor cores: a
 // 64-wide column block would hold CG useful columns and each tile's reduction
-// is only R*S*CG long.  Here one thread computes the CG outputs of one (output
-// pixel, group) pair in fp32 FMAs: per filter tap it loads its group's CG
-// input channels (one 2..32-byte vector load) and multiplies them with the
-// group's weights, which the block keeps in shared memory as fp32, laid out
-// [tap][c][kk][group] so that the lanes of a warp (consecutive groups of one
-// pixel, or consecutive pixels of a group) read consecutive or identical words.
-// Consecutive threads take consecutive groups, then pixels, so a warp's input
-// loads and output stores cover contiguous NHWC spans.  The bias, the fused
-// ReLU and the bf16 output conversion happen in registers before the store.
+// is only R*S*CG long.  Here each thread owns one 16-byte chunk of channels
+// (CH = 8 channels: 8/CG whole groups; CH = 16 for CG = 16) of PX consecutive
+// output pixels of one output row, and accumulates their CH x PX outputs in
+// fp32 FMAs.  Per filter tap it loads its chunk at the PX input positions (one
+// vector load each) and reads each weight of its groups once from shared
+// memory, for PX FMAs.  The block keeps all group weights in shared memory as
+// fp32, laid out [tap][c][kk][group-in-chunk][chunk] so that the lanes of a
+// warp (consecutive chunks of the same pixels) read consecutive words.
+// Consecutive threads take consecutive chunks, so a warp's loads and stores
+// cover contiguous NHWC spans.  The bias, the fused ReLU and the bf16 output
+// conversion happen in registers before the store.
 #pragma once
 
 #include <cstdint>
@@ -31,102 +33,123 @@ struct DirectParams {
     int sh, sw, ph, pw, dh, dw;
     int G;              // groups
     int relu, out_bf16;
-    long long total;    // N * P * Q * G (one thread per output pixel and group)
+    int nchunk;         // C / CH channel chunks per pixel
+    int qblocks;        // ceil(Q / PX) pixel blocks per output row
+    int items;          // N * P * qblocks * nchunk (one thread each); < 2^31
+};
+
+template <int CG>
+struct DirectCfg {
+    static constexpr int CH = CG == 16 ? 16 : 8;  // channels per thread (one or two 16-byte loads)
+    static constexpr int GB = CH / CG;             // groups per thread
+    static constexpr int PX = CG == 16 ? 2 : 4;    // output pixels per thread
 };
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// The CG channels of one group at one input position, widened to fp32.
-template <int CG>
-__device__ __forceinline__ void load_group(const uint16_t* p, float (&v)[CG])
+// CH consecutive bf16 channels (16-byte aligned) widened to fp32.
+template <int CH>
+__device__ __forceinline__ void load_chunk(const uint16_t* p, float (&v)[CH])
 {
-    if constexpr (CG % 8 == 0) {
 #pragma unroll
-        for (int i = 0; i < CG / 8; ++i) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + i);
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    for (int i = 0; i < CH / 8; ++i) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + i);
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[8 * i + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
-                v[8 * i + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
-            }
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = bf16_bits_to_float(u[j] & 0xFFFFu);
+            v[8 * i + 2 * j + 1] = bf16_bits_to_float(u[j] >> 16);
         }
-    } else if constexpr (CG == 4) {
-        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
-        v[0] = bf16_bits_to_float(q.x & 0xFFFFu);
-        v[1] = bf16_bits_to_float(q.x >> 16);
-        v[2] = bf16_bits_to_float(q.y & 0xFFFFu);
-        v[3] = bf16_bits_to_float(q.y >> 16);
-    } else if constexpr (CG == 2) {
-        const uint32_t q = __ldg(reinterpret_cast<const unsigned int*>(p));
-        v[0] = bf16_bits_to_float(q & 0xFFFFu);
-        v[1] = bf16_bits_to_float(q >> 16);
-    } else {
-        v[0] = bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(p)));
     }
 }
 
 template <int CG>
 __global__ void __launch_bounds__(DIRECT_THREADS) conv2d_direct_kernel(const __grid_constant__ DirectParams kp)
 {
-    extern __shared__ float wsm[];  // [R*S][CG][CG][G] fp32
+    using Cfg = DirectCfg<CG>;
+    constexpr int CH = Cfg::CH, GB = Cfg::GB, PX = Cfg::PX;
+    extern __shared__ float wsm[];  // [tap][c][kk][gi][chunk] fp32
     const int taps = kp.R * kp.S;
-    const int G = kp.G;
-    const int wcount = kp.K * taps * CG;
-    for (int i = threadIdx.x; i < wcount; i += blockDim.x) {
-        // w[k][tap][c] with k = g*CG + kk
-        const int c = i % CG;
-        const int t = i / CG;
-        const int tap = t % taps;
-        const int k = t / taps;
-        const int g = k / CG;
-        const int kk = k - g * CG;
-        wsm[((tap * CG + c) * CG + kk) * G + g] = bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(kp.w) + i));
+    const int nchunk = kp.nchunk;
+    // Stage: one (filter k, tap) pair per iteration, its CG weights in one pass.
+    for (int e = threadIdx.x; e < kp.K * taps; e += blockDim.x) {
+        const int k = e / taps;
+        const int tap = e - k * taps;
+        const int g = k / CG, kk = k - (k / CG) * CG;
+        const int cb = g / GB, gi = g - (g / GB) * GB;
+        const uint16_t* src = kp.w + static_cast<long long>(e) * CG;
+#pragma unroll
+        for (int c = 0; c < CG; ++c)
+            wsm[(((tap * CG + c) * CG + kk) * GB + gi) * nchunk + cb] =
+                bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(src) + c));
     }
     __syncthreads();
 
-    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < kp.total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int g = static_cast<int>(idx % G);
-        const long long pix = idx / G;
-        const int q = static_cast<int>(pix % kp.Q);
-        const long long np = pix / kp.Q;
-        const int p = static_cast<int>(np % kp.P);
-        const int n = static_cast<int>(np / kp.P);
-        float acc[CG];
+    for (int item = blockIdx.x * blockDim.x + threadIdx.x; item < kp.items; item += gridDim.x * blockDim.x) {
+        const int cb = item % nchunk;
+        int rest = item / nchunk;
+        const int qb = rest % kp.qblocks;
+        rest /= kp.qblocks;
+        const int p = rest % kp.P;
+        const int n = rest / kp.P;
+        const int q0 = qb * PX;
+        float acc[PX][CH];
 #pragma unroll
-        for (int kk = 0; kk < CG; ++kk) acc[kk] = kp.bias ? __ldg(kp.bias + g * CG + kk) : 0.0f;
+        for (int i = 0; i < CH; ++i) {
+            const float b = kp.bias ? __ldg(kp.bias + cb * CH + i) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < PX; ++j) acc[j][i] = b;
+        }
         for (int r = 0; r < kp.R; ++r) {
             const int ih = p * kp.sh - kp.ph + r * kp.dh;
             if (ih < 0 || ih >= kp.H) continue;
+            const uint16_t* xrow = kp.x + (static_cast<long long>(n) * kp.H + ih) * kp.W * kp.C + cb * CH;
             for (int s = 0; s < kp.S; ++s) {
-                const int iw = q * kp.sw - kp.pw + s * kp.dw;
-                if (iw < 0 || iw >= kp.W) continue;
-                float xv[CG];
-                load_group<CG>(kp.x + ((static_cast<long long>(n) * kp.H + ih) * kp.W + iw) * kp.C + g * CG, xv);
-                const float* wp = wsm + ((r * kp.S + s) * CG * CG) * G + g;
+                float xv[PX][CH];
 #pragma unroll
-                for (int c = 0; c < CG; ++c)
+                for (int j = 0; j < PX; ++j) {
+                    const int iw = (q0 + j) * kp.sw - kp.pw + s * kp.dw;
+                    if (q0 + j < kp.Q && iw >= 0 && iw < kp.W) {
+                        load_chunk<CH>(xrow + static_cast<long long>(iw) * kp.C, xv[j]);
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < CG; ++kk) acc[kk] = fmaf(xv[c], wp[(c * CG + kk) * G], acc[kk]);
+                        for (int i = 0; i < CH; ++i) xv[j][i] = 0.0f;
+                    }
+                }
+                const float* wt = wsm + (r * kp.S + s) * CG * CG * GB * nchunk + cb;
+#pragma unroll
+                for (int gi = 0; gi < GB; ++gi)
+#pragma unroll
+                    for (int c = 0; c < CG; ++c)
+#pragma unroll
+                        for (int kk = 0; kk < CG; ++kk) {
+                            const float wv = wt[((c * CG + kk) * GB + gi) * nchunk];
+#pragma unroll
+                            for (int j = 0; j < PX; ++j)
+                                acc[j][gi * CG + kk] = fmaf(xv[j][gi * CG + c], wv, acc[j][gi * CG + kk]);
+                        }
             }
         }
-        if (kp.relu) {
 #pragma unroll
-            for (int kk = 0; kk < CG; ++kk) acc[kk] = fmaxf(acc[kk], 0.0f);
-        }
-        const long long at = pix * kp.K + g * CG;
-        if (kp.out_bf16) {
-            uint16_t* yb = reinterpret_cast<uint16_t*>(kp.y) + at;
+        for (int j = 0; j < PX; ++j) {
+            if (q0 + j >= kp.Q) break;
+            const long long at = ((static_cast<long long>(n) * kp.P + p) * kp.Q + q0 + j) * kp.K + cb * CH;
+            if (kp.relu) {
 #pragma unroll
-            for (int kk = 0; kk < CG; ++kk) yb[kk] = ptx::bf16_bits(acc[kk]);
-        } else if constexpr (CG % 4 == 0) {
+                for (int i = 0; i < CH; ++i) acc[j][i] = fmaxf(acc[j][i], 0.0f);
+            }
+            if (kp.out_bf16) {
 #pragma unroll
-            for (int i = 0; i < CG / 4; ++i)
-                reinterpret_cast<float4*>(kp.y + at)[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-        } else {
+                for (int i = 0; i < CH / 4; ++i)
+                    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at)[i] = ptx::pack_bf16x4(make_uint4(
+                        __float_as_uint(acc[j][4 * i]), __float_as_uint(acc[j][4 * i + 1]),
+                        __float_as_uint(acc[j][4 * i + 2]), __float_as_uint(acc[j][4 * i + 3])));
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < CG; ++kk) kp.y[at + kk] = acc[kk];
+                for (int i = 0; i < CH / 4; ++i)
+                    reinterpret_cast<float4*>(kp.y + at)[i] =
+                        make_float4(acc[j][4 * i], acc[j][4 * i + 1], acc[j][4 * i + 2], acc[j][4 * i + 3]);
+            }
         }
     }
 }

@@ -100,7 +100,9 @@ def test_direct_refuses_ineligible_shapes(sg, shape, groups):
     x = torch.zeros(xs, dtype=torch.bfloat16)
     w = torch.zeros(ws, dtype=torch.bfloat16)
     params = sg.make_params(xs, ws, 1, 1, 1, groups)
-    eligible = ws[0] // groups == xs[3] // groups and xs[3] // groups in (1, 2, 4, 8, 16) and groups > 1
+    cg = xs[3] // groups
+    eligible = (ws[0] // groups == cg and cg in (1, 2, 4, 8, 16) and groups > 1
+                and xs[3] % (16 if cg == 16 else 8) == 0)
     if eligible:
         got = gpu_conv(sg, x, w, None, dict(stride=1, padding=1, dilation=1, groups=groups),
                        algo=make_algo(sg, loader=sg.LOADER_DIRECT))
