@@ -6,6 +6,8 @@ planted mistakes.
 
 What pins it:
 
+* hand-worked fixtures (tests/golden/backward/, each with its derivation), one
+  with stride 2 and padding;
 * adjoint identity: the data gradient is the adjoint of the forward
   convolution in the input, so for every input-shaped U,
   sum(dx * U) == sum(dy * conv(U, w)); the forward convolution is the
@@ -31,6 +33,35 @@ if ROOT not in sys.path:
 
 import oracle  # noqa: E402
 from oracle import dgrad as od  # noqa: E402
+
+GOLDEN_BACKWARD = os.path.join(HERE, "golden", "backward")
+
+
+def read_backward_fixtures(op):
+    """The hand-worked fixtures of tests/golden/backward for `op` ("wgrad" or "dgrad")."""
+    out = []
+    for name in sorted(os.listdir(GOLDEN_BACKWARD)):
+        if not name.endswith(".txt"):
+            continue
+        d = {}
+        for line in open(os.path.join(GOLDEN_BACKWARD, name)):
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, val = line.split(":", 1)
+                d[key.strip()] = val.split()
+        if d["op"] != [op]:
+            continue
+        shape = lambda k: tuple(int(v) for v in d[k])  # noqa: E731
+        arr = lambda k, s: np.array([float(v) for v in d[k]]).reshape(shape(s))  # noqa: E731
+        f = dict(name=name, shape_x=shape("shape_x"), shape_w=shape("shape_w"), stride=shape("stride"),
+                 pad=shape("pad"), dil=shape("dil"), dy=arr("dy", "shape_dy"))
+        for key, s in (("x", "shape_x"), ("w", "shape_w"), ("dw", "shape_w"), ("dx", "shape_x")):
+            if key in d:
+                f[key] = arr(key, s)
+        out.append(f)
+    assert out, f"no {op} fixtures"
+    return out
+
 
 GEOMS = [  # (N, H, W, C, K, R, S, stride, pad, dil, groups)
     (2, 5, 6, 3, 4, 3, 3, (1, 1), (1, 1), (1, 1), 1),
@@ -159,7 +190,13 @@ def pin_zero_cases(lib):
     assert dx0.shape == (0, 4, 4, 3)
 
 
-ALL_PINS = [pin_adjoint, pin_bruteforce_ints, pin_1x1_matmul, pin_library_gradient, pin_points_mass_bf16,
+def pin_golden(lib):
+    for f in read_backward_fixtures("dgrad"):
+        got = od.conv2d_dgrad_f64(f["dy"], f["w"], f["shape_x"], f["stride"], f["pad"], f["dil"], lib=lib)
+        assert np.array_equal(got, f["dx"]), f"{f['name']}: {got.reshape(-1)} vs {f['dx'].reshape(-1)}"
+
+
+ALL_PINS = [pin_golden, pin_adjoint, pin_bruteforce_ints, pin_1x1_matmul, pin_library_gradient, pin_points_mass_bf16,
             pin_zero_cases]
 
 

@@ -6,6 +6,8 @@ a library path (``python tests/oracle_wgrad_pins.py path/to/lib.so``; exit statu
 
 What pins it:
 
+* hand-worked fixtures (tests/golden/backward/, each with its derivation), one
+  with stride 2 and padding;
 * adjoint identity: the weight gradient is the adjoint of the forward
   convolution in the weight, so for every weight-shaped V,
   sum(dw * V) == sum(dy * conv(x, V)); the forward convolution is the separately
@@ -32,6 +34,35 @@ if ROOT not in sys.path:
 
 import oracle  # noqa: E402
 from oracle import wgrad as ow  # noqa: E402
+
+GOLDEN_BACKWARD = os.path.join(HERE, "golden", "backward")
+
+
+def read_backward_fixtures(op):
+    """The hand-worked fixtures of tests/golden/backward for `op` ("wgrad" or "dgrad")."""
+    out = []
+    for name in sorted(os.listdir(GOLDEN_BACKWARD)):
+        if not name.endswith(".txt"):
+            continue
+        d = {}
+        for line in open(os.path.join(GOLDEN_BACKWARD, name)):
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, val = line.split(":", 1)
+                d[key.strip()] = val.split()
+        if d["op"] != [op]:
+            continue
+        shape = lambda k: tuple(int(v) for v in d[k])  # noqa: E731
+        arr = lambda k, s: np.array([float(v) for v in d[k]]).reshape(shape(s))  # noqa: E731
+        f = dict(name=name, shape_x=shape("shape_x"), shape_w=shape("shape_w"), stride=shape("stride"),
+                 pad=shape("pad"), dil=shape("dil"), dy=arr("dy", "shape_dy"))
+        for key, s in (("x", "shape_x"), ("w", "shape_w"), ("dw", "shape_w"), ("dx", "shape_x")):
+            if key in d:
+                f[key] = arr(key, s)
+        out.append(f)
+    assert out, f"no {op} fixtures"
+    return out
+
 
 GEOMS = [  # (N, H, W, C, K, R, S, stride, pad, dil, groups)
     (2, 5, 6, 3, 4, 3, 3, (1, 1), (1, 1), (1, 1), 1),
@@ -176,7 +207,13 @@ def pin_zero_cases(lib):
     assert dw0.shape == (5, 3, 3, 3) and np.array_equal(dw0, np.zeros_like(dw0))
 
 
-ALL_PINS = [pin_adjoint, pin_bruteforce_ints, pin_1x1_matmul, pin_library_gradient, pin_points_mass_bf16,
+def pin_golden(lib):
+    for f in read_backward_fixtures("wgrad"):
+        got = ow.conv2d_wgrad_f64(f["x"], f["dy"], f["shape_w"], f["stride"], f["pad"], f["dil"], lib=lib)
+        assert np.array_equal(got, f["dw"]), f"{f['name']}: {got.reshape(-1)} vs {f['dw'].reshape(-1)}"
+
+
+ALL_PINS = [pin_golden, pin_adjoint, pin_bruteforce_ints, pin_1x1_matmul, pin_library_gradient, pin_points_mass_bf16,
             pin_zero_cases]
 
 
