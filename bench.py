@@ -392,9 +392,7 @@ def run_ours(args, wl, world, rank, local):
     y_dtype, y_bytes = (torch.bfloat16, 2) if out_bf16 else (torch.float32, 4)
     algo = sg.query_algo(params, relu=relu, out_bf16=out_bf16)
     if forced is not None:
-        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, forced.loader or algo.loader,
-                       forced.grid or (0 if forced.splits else algo.grid), 0, forced.block_m or algo.block_m, 0,
-                       forced.reduction or algo.reduction)
+        algo = _algo_report(algo, forced)
     set_bytes = x.numel() * 2 + w.numel() * 2 + wl.n * p * q * wl.k * y_bytes + (0 if b is None else b.numel() * 4)
     n_sets = _sets_for(wl, set_bytes)
     sets = []
@@ -461,9 +459,17 @@ def run_ours(args, wl, world, rank, local):
     e2e = None
     if not args.no_e2e and args.epilogue == "none":
         e2e = run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, min(K, args.e2e_steps), dist_mod)
-    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
+    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
                 clocks=clocks.summary(t_host0, t_host1), status=status, e2e=e2e, dist=dist_mod,
                 graph_chunk=chunk)
+
+
+def _algo_report(heuristic, forced):
+    """The configuration a line ran: the heuristic's, or the forced fields (0 = left to the
+    heuristic) beside the heuristic's own choice, which a forced loader or tile may replace."""
+    if forced is None:
+        return heuristic.as_dict()
+    return {"forced": {k: v for k, v in forced.as_dict().items() if v}, "heuristic": heuristic.as_dict()}
 
 
 def _forced_algo(sg, args):
@@ -523,8 +529,7 @@ def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
     forced = _forced_algo(sg, args)
     algo = sg.query_wgrad_algo(params)
     if forced is not None:
-        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, algo.loader,
-                       forced.grid or (0 if forced.splits else algo.grid), 0, 128, 0, forced.reduction or algo.reduction)
+        algo = _algo_report(algo, forced)
     set_bytes = x.numel() * 2 + dy.numel() * 2 + w.numel() * 4
     n_sets = _sets_for(wl, set_bytes)
     sets = [(x.to(dev), dy.to(dev), torch.empty(tuple(w.shape), dtype=torch.float32, device=dev))
@@ -546,7 +551,7 @@ def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
     status = sg.status(ws, stream)
     flops = flops_per_step(wl)
     job_s, job_flops = aggregate(dist_mod, elapsed, flops * args.steps, dev)
-    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
+    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
                 clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
 
 
@@ -556,8 +561,7 @@ def run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params):
     forced = _forced_algo(sg, args)
     algo = sg.query_dgrad_algo(params)
     if forced is not None:
-        algo = sg.Algo(forced.block_n or algo.block_n, forced.splits, algo.loader,
-                       forced.grid or (0 if forced.splits else algo.grid), 0, 128, 0, forced.reduction or algo.reduction)
+        algo = _algo_report(algo, forced)
     xs = (wl.n, wl.h, wl.w, wl.c)
     set_bytes = dy.numel() * 2 + w.numel() * 2 + wl.n * wl.h * wl.w * wl.c * 4
     n_sets = _sets_for(wl, set_bytes)
@@ -578,7 +582,7 @@ def run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params):
     elapsed, clocks, chunk = _time_graphs(torch, stream, step, args.steps, args.warmup, n_sets, dev, dist_mod, check)
     status = sg.status(ws, stream)
     job_s, job_flops = aggregate(dist_mod, elapsed, flops_per_step(wl) * args.steps, dev)
-    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo.as_dict(), n_sets=n_sets,
+    return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
                 clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
 
 
