@@ -271,7 +271,11 @@ def conv2d_fwd_into(y, x, w, bias=None, stride=1, padding=0, dilation=1, groups=
     lib = load_library()
     fused = relu or y.dtype == torch.bfloat16
     if workspace is None:
-        need = epi_workspace_bytes(params, algo, relu, y.dtype == torch.bfloat16) if fused else workspace_bytes(params)
+        need = workspace_bytes(params)
+        # A fused call whose plan cuts tiles also needs the fp32 partial-sum buffer (the direct
+        # kernel for small groups, which the heuristic picks when nothing is forced, needs none).
+        if fused and not (algo is None and query_algo(params).loader == LOADER_DIRECT):
+            need = epi_workspace_bytes(params, algo, relu, y.dtype == torch.bfloat16)
         workspace = _default_workspace(need, x.device)
     ws_ptr, ws_len = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     st = torch.cuda.current_stream(x.device) if stream is None else stream
