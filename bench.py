@@ -4,14 +4,20 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one forward convolution of the workload (every hot-path stage runs
-inside the one kernel launch).  ``value`` is whole-job TFLOP/s
-(2*N*P*Q*K*C*R*S per step) with inputs resident in HBM, device-timed with CUDA
-events around a CUDA-graph replay of exactly K launches.  Consecutive steps
-rotate through enough independent input/output buffer sets to exceed twice the
-L2 size, so no step reads the previous step's data from L2.  ``e2e`` is the
-same metric through the host-buffer entry point (pinned H2D copies, kernel,
-D2H copy of y, every step).  ``--impl reference`` times the CPU oracle on a
-bounded sample of the same workload instead.
+inside the one kernel launch).  The default workload is the 28x28 C256 ResNet
+layer (GEMM 12544 x 256 x 2304), the largest compute-bound entry of the
+benchmark list and the first one with a tensor-peak target.
+
+``value`` is whole-job TFLOP/s (2*N*P*Q*K*C*R*S per step) with inputs resident
+in HBM, device-timed with CUDA events around CUDA-graph replays of exactly K
+launches.  Consecutive steps rotate through independent input/output buffer
+sets (at least twice the L2 size in total), and the L2 is flushed by a 2 x L2
+scratch write between the warm-up and the timed region, so no timed step finds
+its inputs in L2 ("cold" mode).  ``hot_l2`` is the same K launches back to
+back on one buffer set (inputs and output L2-resident after the first step).
+``e2e`` is the same metric through the host-buffer entry point (pinned H2D
+copies, kernel, D2H copy of y, every step).  ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload instead.
 
 Multi-GPU (torchrun): the convolution does not need an exchange step, so each
 rank runs an independent replica on its own GPU (weak scaling); the job time is
@@ -37,7 +43,7 @@ import workloads  # noqa: E402
 METRIC = "conv2d fwd TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
 METRIC_WGRAD = "conv2d wgrad TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
 METRIC_DGRAD = "conv2d dgrad TFLOP/s (2·NPQ·K·CRS/time) and % of GB300 BF16 tensor peak"
-DEFAULT_WORKLOAD = "resnet_56x56_c64"
+DEFAULT_WORKLOAD = "resnet_28x28_c256"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -383,11 +389,7 @@ def run_ours(args, wl, world, rank, local):
         return run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params)
     if args.op == "dgrad":
         return run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params)
-    forced = None
-    if args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction:
-        forced = sg.Algo()
-        forced.block_n, forced.splits, forced.loader, forced.grid = args.block_n, args.splits, args.loader, args.grid
-        forced.block_m, forced.reduction = args.block_m, args.reduction
+    forced = _forced_algo(sg, args)
     relu, out_bf16 = args.epilogue in ("relu", "relu_bf16"), args.epilogue in ("bf16", "relu_bf16")
     y_dtype, y_bytes = (torch.bfloat16, 2) if out_bf16 else (torch.float32, 4)
     algo = sg.query_algo(params, relu=relu, out_bf16=out_bf16)
@@ -408,60 +410,34 @@ def run_ours(args, wl, world, rank, local):
         xd, wd, bd, yd = sets[i % n_sets]
         sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws, algo=forced, relu=relu)
 
+    def step_hot(i):
+        xd, wd, bd, yd = sets[0]
+        sg.conv2d_fwd_into(yd, xd, wd, bd, **opts, workspace=ws, algo=forced, relu=relu)
+
+    def check():
+        if sg.status(ws, stream) != 0:
+            raise RuntimeError("device status reported a timeout during warm-up")
+
     K, W = args.steps, args.warmup
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            step(i)
-    stream.synchronize()
-    if sg.status(ws, stream) != 0:
-        raise RuntimeError("device status reported a timeout during warm-up")
-
-    # CUDA graphs of back-to-back launches; chunk length is a multiple of the
-    # buffer-set count so the rotation never repeats a set on consecutive steps.
-    chunk = min(K, 512)
-    chunk = max(n_sets, (chunk // n_sets) * n_sets) if K >= n_sets else K
-    full, rem = divmod(K, chunk)
-    graphs = []
-    for length in ([chunk] if full else []) + ([rem] if rem else []):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(length):
-                step(i)
-        graphs.append((g, length))
-    with torch.cuda.stream(stream):  # one untimed replay of each graph (upload)
-        for g, _ in graphs:
-            g.replay()
-    stream.synchronize()
-
-    clocks = ClockSampler(dev.index)
-    clocks.start()
-    time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist_mod, dev)
-    torch.cuda.synchronize()
-    t_host0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(full):
-            graphs[0][0].replay()
-        if rem:
-            graphs[-1][0].replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    barrier(dist_mod, dev)
-    clocks.stop()
-    elapsed = start.elapsed_time(end) / 1e3
+    elapsed, clocks, chunk = _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check)
+    launches = sg.last_launch_count()
     status = sg.status(ws, stream)
     flops = flops_per_step(wl)
     job_s, job_flops = aggregate(dist_mod, elapsed, flops * K, dev)
+    hot = None
+    if not args.no_hot:
+        hot_s, _, _ = _time_graphs(torch, stream, step_hot, K, 0, 1, dev, dist_mod, check, flush=False, roll_s=0.05)
+        hot_job_s, hot_flops = aggregate(dist_mod, hot_s, flops * K, dev)
+        hot = {"value": hot_flops / hot_job_s / 1e12, "unit": "TFLOP/s", "ms_per_step": hot_job_s / K * 1e3,
+               "mode": "hot: one buffer set, back to back (inputs and output L2-resident after the first step)"}
+        status = status or sg.status(ws, stream)
 
     e2e = None
     if not args.no_e2e and args.epilogue == "none":
         e2e = run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, min(K, args.e2e_steps), dist_mod)
     return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
-                clocks=clocks.summary(t_host0, t_host1), status=status, e2e=e2e, dist=dist_mod,
-                graph_chunk=chunk)
+                clocks=clocks, status=status, e2e=e2e, dist=dist_mod, graph_chunk=chunk,
+                l2=_l2_statement(K, n_sets, set_bytes), hot=hot, launches_per_step=launches)
 
 
 def _algo_report(heuristic, forced):
@@ -473,21 +449,19 @@ def _algo_report(heuristic, forced):
 
 
 def _forced_algo(sg, args):
-    if not (args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction):
+    if not (args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction or args.pair_kb):
         return None
     a = sg.Algo()
     a.block_n, a.splits, a.loader, a.grid = args.block_n, args.splits, args.loader, args.grid
     a.block_m, a.reduction = args.block_m, args.reduction
+    a.debug_flags = {1: 2, 2: 4}.get(args.pair_kb, 0)  # CONV2D_DEBUG_PAIR_KB1 / KB2
     return a
 
 
-def _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check):
-    """W warm-up steps, then K steps replayed from CUDA graphs between two events: (seconds, clocks, chunk)."""
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            step(i)
-    stream.synchronize()
-    check()
+def _build_graphs(torch, stream, step, K, n_sets):
+    """CUDA graphs of back-to-back launches covering K steps.  A graph's length is a multiple
+    of the buffer-set count (or K itself when K < n_sets), so replaying one after another
+    continues the rotation: the same set never comes round within n_sets consecutive steps."""
     chunk = min(K, 512)
     chunk = max(n_sets, (chunk // n_sets) * n_sets) if K >= n_sets else K
     full, rem = divmod(K, chunk)
@@ -498,10 +472,40 @@ def _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check):
             for i in range(length):
                 step(i)
         graphs.append(g)
-    with torch.cuda.stream(stream):
+    plan = [graphs[0]] * full + ([graphs[-1]] if rem else [])
+    with torch.cuda.stream(stream):  # one untimed replay of each graph (upload)
         for g in graphs:
             g.replay()
     stream.synchronize()
+    return plan, chunk
+
+
+def _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check, flush=True, roll_s=0.25):
+    """W warm-up steps, then exactly K steps replayed from CUDA graphs between two events.
+
+    The clocks are sampled while the GPU runs these same launches: an untimed pre-roll of
+    about ``roll_s`` seconds, the timed region, and a post-roll, all queued back to back on
+    the stream (a timed region of a few hundred microseconds is far shorter than the
+    sampling period).  With ``flush`` a 2 x L2 scratch write runs between the pre-roll and
+    the timed region, so the timed steps start from an L2 that holds none of their inputs.
+    Returns (seconds, clocks, chunk)."""
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    stream.synchronize()
+    check()
+    plan, chunk = _build_graphs(torch, stream, step, K, n_sets)
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    # Replays of the step graphs that fill about roll_s seconds (estimated from one timed pass).
+    probe0, probe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        probe0.record(stream)
+        for g in plan:
+            g.replay()
+        probe1.record(stream)
+    stream.synchronize()
+    pass_s = max(1e-6, probe0.elapsed_time(probe1) / 1e3)
+    rolls = max(1, min(100000, int(roll_s / pass_s)))
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
@@ -510,17 +514,34 @@ def _time_graphs(torch, stream, step, K, W, n_sets, dev, dist_mod, check):
     torch.cuda.synchronize()
     t0 = time.time()
     with torch.cuda.stream(stream):
+        for _ in range(rolls):
+            for g in plan:
+                g.replay()
+        if scratch is not None:
+            scratch.fill_(1.0)
         start.record(stream)
-        for _ in range(full):
-            graphs[0].replay()
-        if rem:
-            graphs[-1].replay()
+        for g in plan:
+            g.replay()
         end.record(stream)
+        for _ in range(rolls):
+            for g in plan:
+                g.replay()
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(dist_mod, dev)
     clocks.stop()
-    return start.elapsed_time(end) / 1e3, clocks.summary(t0, t1), chunk
+    summary = clocks.summary(t0, t1)
+    summary["window"] = ("pre-roll, timed region and post-roll of the same launches "
+                         f"({rolls} untimed passes on each side)") if summary.get("window") == "during" else summary.get("window")
+    return start.elapsed_time(end) / 1e3, summary, chunk
+
+
+def _l2_statement(K, n_sets, set_bytes, flush=True):
+    touched = min(K, n_sets)
+    return {"mode": "cold: rotating buffer sets" + (", L2 flushed (2 x L2 write) before the timed region" if flush else ""),
+            "buffer_sets": n_sets, "set_bytes": int(set_bytes), "sets_touched_in_timed_region": touched,
+            "bytes_touched_in_timed_region": int(touched * set_bytes),
+            "reuse_distance_bytes": int(n_sets * set_bytes) if K > n_sets else None}
 
 
 def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
@@ -548,11 +569,13 @@ def run_wgrad(args, wl, sg, torch, dev, dist_mod, x, w, params):
             raise RuntimeError("device status reported a timeout during warm-up")
 
     elapsed, clocks, chunk = _time_graphs(torch, stream, step, args.steps, args.warmup, n_sets, dev, dist_mod, check)
+    launches = sg.last_launch_count()
     status = sg.status(ws, stream)
     flops = flops_per_step(wl)
     job_s, job_flops = aggregate(dist_mod, elapsed, flops * args.steps, dev)
     return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
-                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
+                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk,
+                l2=_l2_statement(args.steps, n_sets, set_bytes), hot=None, launches_per_step=launches)
 
 
 def run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params):
@@ -580,10 +603,12 @@ def run_dgrad(args, wl, sg, torch, dev, dist_mod, w, params):
             raise RuntimeError("device status reported a timeout during warm-up")
 
     elapsed, clocks, chunk = _time_graphs(torch, stream, step, args.steps, args.warmup, n_sets, dev, dist_mod, check)
+    launches = sg.last_launch_count()
     status = sg.status(ws, stream)
     job_s, job_flops = aggregate(dist_mod, elapsed, flops_per_step(wl) * args.steps, dev)
     return dict(elapsed=elapsed, job_s=job_s, job_flops=job_flops, algo=algo if isinstance(algo, dict) else algo.as_dict(), n_sets=n_sets,
-                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk)
+                clocks=clocks, status=status, e2e=None, dist=dist_mod, graph_chunk=chunk,
+                l2=_l2_statement(args.steps, n_sets, set_bytes), hot=None, launches_per_step=launches)
 
 
 def run_e2e(sg, torch, dev, stream, wl, x, w, b, params, p, q, steps, dist_mod):
@@ -646,15 +671,20 @@ def roofline(wl, t_step_s, peaks, peak_src, out_bytes=4, op="fwd"):
               else algorithmic_bytes(wl, out_bytes))
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     traffic = recorded_traffic(wl.name if op == "fwd" else f"{wl.name}:{op}") if out_bytes == 4 else None
+    note = ("dram__bytes_read.sum + dram__bytes_write.sum of one launch captured alone under ncu "
+            "(profiles/ncu_traffic.txt): inputs read from DRAM once; an output smaller than L2 is still in L2 "
+            "when the launch ends, so its write-back is not in the figure") if traffic is not None else None
     if flops / nbytes >= ridge:
         achieved = flops / t_step_s / 1e12
         return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                "peak_source": f"{peak_src} (bf16 burst)", "traffic": traffic, "algorithmic_bytes": nbytes,
+                "peak_source": f"{peak_src} (bf16 burst)", "traffic": traffic, "traffic_source": note,
+                "algorithmic_bytes": nbytes,
                 "algorithmic_flops": flops}
     achieved = nbytes / t_step_s / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} (HBM copy)", "traffic": traffic,
+            "traffic_source": note,
             "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
 
 
@@ -695,13 +725,14 @@ def main_ours(args):
                                      "layout": "dy NPQK bf16 ~N(0, 1), w KRSC bf16, dx NHWC fp32",
                                      "gemm_mnk": [wl.n * wl.h * wl.w, wl.c, wl.k * wl.r * wl.s]}
                                     if args.op == "dgrad" else {}),
-                                 "l2": f"{res['n_sets']} rotating input/output buffer sets (> 2x L2) per step",
+                                 "l2": res["l2"],
                                  "timing": f"CUDA events around CUDA-graph replays ({res['graph_chunk']} launches "
                                            "per graph), max over ranks"}),
         "roofline": roofline(wl, t_step, peaks, peak_src, 2 if args.epilogue in ("bf16", "relu_bf16") else 4, args.op),
+        "hot_l2": res["hot"],
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
-        "gpu_launches": K,
+        "gpu_launches": K * max(1, res["launches_per_step"]),
         "clocks": res["clocks"],
         "device_status": res["status"],
     }
@@ -742,12 +773,13 @@ def main_reference(args):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-hot", action="store_true", help="skip the hot-L2 (one buffer set) timing")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time for cpu_baseline")
     ap.add_argument("--block-n", type=int, default=0, help="force the output-channel tile width (64/128/256)")
@@ -757,6 +789,8 @@ def parse_args(argv=None):
     ap.add_argument("--loader", type=int, default=0, help="force the im2col loader (1 TMA, 2 cp.async, 3 scalar, 4 hybrid, 5 row window, 6 TMA box, 7 halo)")
     ap.add_argument("--grid", type=int, default=0, help="force the number of CTAs sharing the work (stream-K)")
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
+    ap.add_argument("--pair-kb", type=int, default=0, choices=[0, 1, 2],
+                    help="CTA-pair loader: force 1 or 2 k-blocks per pipeline stage (0: the heuristic's)")
     ap.add_argument("--op", default="fwd", choices=["fwd", "wgrad", "dgrad"],
                     help="fwd: the forward convolution (the headline); wgrad / dgrad: its weight / input gradient")
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "bf16", "relu_bf16"],

@@ -97,12 +97,19 @@ typedef enum {
                                      Needs groups == 1, C % 64 == 0, W + 2*pad_w <= 256, 128-pixel tiles, and the two halo
                                      buffers plus the weight ring within shared memory (block_n is narrowed
                                      to fit unless forced) */
-    CONV2D_LOADER_DIRECT = 8      /* not an implicit GEMM: a CUDA-core direct convolution for groups of few
+    CONV2D_LOADER_DIRECT = 8,     /* not an implicit GEMM: a CUDA-core direct convolution for groups of few
                                      channels, one thread per (output pixel, group) in fp32 FMAs, the group
                                      weights in shared memory.  Needs groups > 1, C/groups == K/groups in
                                      {1, 2, 4, 8, 16} (depthwise: 1), C % 8 == 0, and the weights
                                      (K*R*S*C/groups fp32) within shared memory.  The heuristic takes it for such shapes when nothing else
                                      is forced; block_n, block_m and splits do not apply */
+    CONV2D_LOADER_TMA_PAIR = 9    /* TMA im2col loads on clusters of two CTAs: a tile is 256 output pixels x
+                                     block_n (64/128/256) channels computed by 2-CTA tensor-core MMAs
+                                     (each CTA loads 128 pixel rows and half the weight rows), two 64-wide
+                                     k-blocks per pipeline stage.  Needs groups == 1, C % 64 == 0,
+                                     K % 4 == 0; block_m is 256 (or 0); grid counts CTA pairs; a fused
+                                     epilogue runs on whole tiles only.  The heuristic takes it for such
+                                     shapes when nothing else is forced */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".
@@ -134,6 +141,10 @@ typedef enum {
 /* Test hook: split 0 of every tile skips its semaphore signal, so later splits'
  * bounded waits run out and the call reports CONV2D_ERR_TIMEOUT. */
 #define CONV2D_DEBUG_SKIP_SIGNAL 1
+/* Measurement hooks of the CTA-pair loader (CONV2D_LOADER_TMA_PAIR): force one
+ * or two 64-wide k-blocks per pipeline stage instead of the heuristic's choice. */
+#define CONV2D_DEBUG_PAIR_KB1 2
+#define CONV2D_DEBUG_PAIR_KB2 4
 
 /* Output extents P and Q (pure host computation).  Returns CONV2D_OK or
  * CONV2D_ERR_INVALID (bad options, or the filter window does not fit). */
@@ -191,6 +202,19 @@ int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void*
 /* Number of kernel launches the last successful conv2d_fwd* call on this host
  * thread enqueued (1 for every algorithm; 0 before any call and for empty problems). */
 int conv2d_last_launch_count(void);
+
+/* Tensor-map cache of the forward entry points (conv2d_fwd, conv2d_fwd_ex,
+ * conv2d_fwd_epi, conv2d_fwd_host, conv2d_fwd_noalloc).  The TMA descriptors a
+ * call needs are encoded on the host; a small process-wide cache (32 entries,
+ * replaced in turn) keyed on the problem (params), the plan's loader and tile
+ * geometry, the x and w pointers and the current device reuses them on
+ * repeated calls, so a call on buffers seen before skips the driver's encoding.
+ * The pages have no counterpart (burn's conv_forward has no descriptors to
+ * encode); it removes per-call host cost of this boundary.  Any change of
+ * pointer, shape or plan encodes afresh.  This reports how many lookups
+ * found an entry (hits) and how many encoded (misses) since the library was
+ * loaded; either pointer may be NULL.  Thread-safe. */
+void conv2d_tensor_map_cache_stats(unsigned long long* hits, unsigned long long* misses);
 
 /* Fused epilogue.  After the bias, the epilogue may apply an activation and
  * may store y in bf16 instead of fp32:
@@ -326,7 +350,10 @@ int conv2d_bwd_data_query_algo(const conv2d_params* params, conv2d_algo* out);
  *     cover 16320 output tiles of 128 pixels x 64 channels).
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current); make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is kept for the life of the
+ *     process: after cudaDeviceReset (or anything else that destroys the
+ *     device's primary context) it no longer names the array, so do not call
+ *     this entry point again on that device in the same process.
  *   - Every call clears the part of the array it uses (cudaMemsetAsync on
  *     `stream`) and then enqueues the kernel.  All calls on one device share
  *     that device's copy of the array, and it keeps the previous call's

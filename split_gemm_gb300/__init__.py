@@ -24,19 +24,20 @@ from . import _build
 
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
-    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "LOADER_DIRECT", "REDUCTION_AUTO", "REDUCTION_ORDERED",
+    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "LOADER_DIRECT", "LOADER_TMA_PAIR", "REDUCTION_AUTO", "REDUCTION_ORDERED",
     "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
     "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "epi_workspace_bytes", "conv2d_bwd_weight", "conv2d_bwd_weight_into",
     "wgrad_workspace_bytes", "query_wgrad_algo", "conv2d_bwd_data", "conv2d_bwd_data_into", "dgrad_workspace_bytes",
     "query_dgrad_algo", "conv_transpose2d", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
-    "last_launch_count", "strerror", "EXPORTED_SYMBOLS",
+    "last_launch_count", "strerror", "EXPORTED_SYMBOLS", "tensor_map_cache_stats",
 ]
 
 LOADER_AUTO, LOADER_TMA_IM2COL, LOADER_CPASYNC, LOADER_SCALAR, LOADER_HYBRID, LOADER_ROW_WINDOW = 0, 1, 2, 3, 4, 5
 LOADER_TMA_BOX = 6
 LOADER_HALO = 7
 LOADER_DIRECT = 8
+LOADER_TMA_PAIR = 9
 REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
 ACT_NONE, ACT_RELU = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
@@ -49,6 +50,7 @@ EXPORTED_SYMBOLS = [
     "conv2d_fwd_output_shape", "conv2d_fwd_workspace_bytes", "conv2d_fwd", "conv2d_fwd_ex",
     "conv2d_fwd_query_algo", "conv2d_fwd_status", "conv2d_fwd_host_staging_bytes", "conv2d_fwd_host",
     "conv2d_last_launch_count", "conv2d_strerror", "conv2d_fwd_noalloc", "conv2d_fwd_epi",
+    "conv2d_tensor_map_cache_stats",
     "conv2d_fwd_query_algo_epi", "conv2d_fwd_epi_workspace_bytes", "conv2d_bwd_weight_workspace_bytes",
     "conv2d_bwd_weight", "conv2d_bwd_weight_query_algo", "conv2d_bwd_data_workspace_bytes", "conv2d_bwd_data",
     "conv2d_bwd_data_query_algo",
@@ -131,6 +133,8 @@ def _bind(lib):
     lib.conv2d_fwd_host.restype = ctypes.c_int
     lib.conv2d_last_launch_count.argtypes = []
     lib.conv2d_last_launch_count.restype = ctypes.c_int
+    lib.conv2d_tensor_map_cache_stats.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_ulonglong)]
+    lib.conv2d_tensor_map_cache_stats.restype = None
     lib.conv2d_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
     lib.conv2d_fwd_noalloc.restype = ctypes.c_int
     lib.conv2d_strerror.argtypes = [ctypes.c_int]
@@ -224,6 +228,13 @@ def last_launch_count() -> int:
     return int(load_library().conv2d_last_launch_count())
 
 
+def tensor_map_cache_stats():
+    """(hits, misses) of the forward calls' tensor-map cache since the library was loaded."""
+    h, m = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    load_library().conv2d_tensor_map_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return int(h.value), int(m.value)
+
+
 # Per-device zero-filled workspaces (the kernels leave them zeroed after each call).
 # They assume one stream at a time per device; pass `workspace=` for concurrent streams.
 _ws_cache = {}
@@ -237,6 +248,14 @@ def _default_workspace(nbytes: int, device):
         buf = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
+
+
+def _mark_used(buf, stream) -> None:
+    """Tells torch's caching allocator that the cached workspace ``buf`` is in use by
+    ``stream``: if a later, larger call replaces it, its memory is not handed out again
+    until the work already queued on that stream has finished."""
+    if stream is not None and buf.device.type == "cuda":
+        buf.record_stream(stream)
 
 
 def _check_tensor(t, name, dtype, ndim):
@@ -270,6 +289,7 @@ def conv2d_fwd_into(y, x, w, bias=None, stride=1, padding=0, dilation=1, groups=
     params = make_params(x.shape, w.shape, stride, padding, dilation, groups)
     lib = load_library()
     fused = relu or y.dtype == torch.bfloat16
+    cached = workspace is None
     if workspace is None:
         need = workspace_bytes(params)
         # A fused call whose plan cuts tiles also needs the fp32 partial-sum buffer (the direct
@@ -288,6 +308,8 @@ def conv2d_fwd_into(y, x, w, bias=None, stride=1, padding=0, dilation=1, groups=
         rc = lib.conv2d_fwd(*args) if algo is None else lib.conv2d_fwd_ex(*args, ctypes.byref(algo))
     if rc:
         raise Conv2dError(rc, "conv2d_fwd")
+    if cached:
+        _mark_used(workspace, st)
 
 
 def conv2d_fwd(x, w, bias=None, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
@@ -334,6 +356,7 @@ def conv2d_bwd_weight_into(dw, x, dy, stride=1, padding=0, dilation=1, groups=1,
     if tuple(dy.shape) != (params.n, p, q, params.k):
         raise ValueError(f"dy must be [{params.n}, {p}, {q}, {params.k}], got {list(dy.shape)}")
     lib = load_library()
+    cached = workspace is None
     if workspace is None:
         workspace = _default_workspace(wgrad_workspace_bytes(params), x.device)
     st = torch.cuda.current_stream(x.device) if stream is None else stream
@@ -342,6 +365,8 @@ def conv2d_bwd_weight_into(dw, x, dy, stride=1, padding=0, dilation=1, groups=1,
                                None if algo is None else ctypes.byref(algo))
     if rc:
         raise Conv2dError(rc, "conv2d_bwd_weight")
+    if cached:
+        _mark_used(workspace, st)
 
 
 def conv2d_bwd_weight(x, dy, w_shape, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,
@@ -380,6 +405,7 @@ def conv2d_bwd_data_into(dx, dy, w, stride=1, padding=0, dilation=1, groups=1, *
     if tuple(dy.shape) != (params.n, p, q, params.k):
         raise ValueError(f"dy must be [{params.n}, {p}, {q}, {params.k}], got {list(dy.shape)}")
     lib = load_library()
+    cached = workspace is None
     if workspace is None:
         workspace = _default_workspace(dgrad_workspace_bytes(params), dy.device)
     st = torch.cuda.current_stream(dy.device) if stream is None else stream
@@ -388,6 +414,8 @@ def conv2d_bwd_data_into(dx, dy, w, stride=1, padding=0, dilation=1, groups=1, *
                              None if algo is None else ctypes.byref(algo))
     if rc:
         raise Conv2dError(rc, "conv2d_bwd_data")
+    if cached:
+        _mark_used(workspace, st)
 
 
 def conv2d_bwd_data(dy, w, x_shape, stride=1, padding=0, dilation=1, groups=1, *, workspace=None,

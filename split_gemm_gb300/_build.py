@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libconv2d.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["conv2d_api.cu", "conv2d_bn64.cu", "conv2d_bn128.cu", "conv2d_bn256.cu", "conv2d_rowwin.cu", "conv2d_direct.cu",
-           "conv2d_noalloc.cu"]
+           "conv2d_noalloc.cu", "conv2d_pair_kb1.cu", "conv2d_pair_kb2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]

@@ -14,6 +14,7 @@
 #include "conv2d.h"
 #include "conv2d_direct.cuh"
 #include "conv2d_kernel.cuh"
+#include "conv2d_pair.cuh"
 #include "conv2d_rowwin.cuh"
 
 namespace sgb {
@@ -30,6 +31,18 @@ extern template SGB_DIRECT_SIG(2);
 extern template SGB_DIRECT_SIG(4);
 extern template SGB_DIRECT_SIG(8);
 extern template SGB_DIRECT_SIG(16);
+extern template SGB_PAIR_SIG(64, 1);
+extern template SGB_PAIR_SIG(128, 1);
+extern template SGB_PAIR_SIG(256, 1);
+extern template SGB_PAIR_SIG(64, 2);
+extern template SGB_PAIR_SIG(128, 2);
+extern template SGB_PAIR_SIG(256, 2);
+extern template SGB_PAIR_RES_SIG(64, 1);
+extern template SGB_PAIR_RES_SIG(128, 1);
+extern template SGB_PAIR_RES_SIG(256, 1);
+extern template SGB_PAIR_RES_SIG(64, 2);
+extern template SGB_PAIR_RES_SIG(128, 2);
+extern template SGB_PAIR_RES_SIG(256, 2);
 }  // namespace sgb
 
 namespace {
@@ -355,6 +368,7 @@ struct Plan {
     long long units;  // (tile, stage) work units
     BoxGeom box;      // box loader only
     HaloGeom halo;    // halo loader only
+    int kbs;          // CTA-pair loader only: 64-wide k-blocks per pipeline stage (1 or 2)
 };
 
 // Semaphores the workspace holds: one per tile of the smallest tiles any plan
@@ -419,6 +433,114 @@ bool nothing_forced(const conv2d_algo* a)
 // whole_tiles: where the heuristic would divide many tiles stream-K style over
 // the SMs, give every CTA whole tiles instead.  A fused epilogue (bf16 output,
 // activation) asks for it: its cut tiles take a detour through an fp32 buffer.
+// ------------------------------------------------------------------ CTA-pair plans
+bool plan_cuts_tiles(const Plan& p);
+
+// The CTA-pair kernel (conv2d_pair.cuh): 256-pixel tiles on clusters of two
+// CTAs, TMA im2col loads of 128 pixels per CTA, 16-byte vector stores.
+bool pair_eligible(const Shape& s) { return s.g == 1 && tma_im2col_eligible(s) && s.k % 4 == 0; }
+
+int pair_max_resident(int bn, int kbs, bool fused)
+{
+    if (kbs == 1) {
+        if (bn == 64) return sgb::conv2d_pair_max_resident<64, 1>(fused);
+        if (bn == 128) return sgb::conv2d_pair_max_resident<128, 1>(fused);
+        if (bn == 256) return sgb::conv2d_pair_max_resident<256, 1>(fused);
+    } else {
+        if (bn == 64) return sgb::conv2d_pair_max_resident<64, 2>(fused);
+        if (bn == 128) return sgb::conv2d_pair_max_resident<128, 2>(fused);
+        if (bn == 256) return sgb::conv2d_pair_max_resident<256, 2>(fused);
+    }
+    return 0;
+}
+
+cudaError_t launch_pair(int bn, int kbs, const CUtensorMap& a, const CUtensorMap& b, const sgb::ConvKernelParams& kp,
+                        int pairs, cudaStream_t st)
+{
+    if (kbs == 1) {
+        if (bn == 64) return sgb::launch_conv2d_pair<64, 1>(a, b, kp, pairs, st);
+        if (bn == 128) return sgb::launch_conv2d_pair<128, 1>(a, b, kp, pairs, st);
+        if (bn == 256) return sgb::launch_conv2d_pair<256, 1>(a, b, kp, pairs, st);
+    } else {
+        if (bn == 64) return sgb::launch_conv2d_pair<64, 2>(a, b, kp, pairs, st);
+        if (bn == 128) return sgb::launch_conv2d_pair<128, 2>(a, b, kp, pairs, st);
+        if (bn == 256) return sgb::launch_conv2d_pair<256, 2>(a, b, kp, pairs, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Stream-K over every resident pair when the reduction gives each pair at least
+// this many two-k-block stages (the cut tiles' in-place adds are then a small
+// share of the work); otherwise whole tiles.
+constexpr int64_t kPairStreamKStages = 8;
+constexpr int64_t PAIR_KBS_NORM = 2;  // units count stages of kbs k-blocks; the threshold counts pairs of k-blocks
+constexpr int64_t PAIR_M_SLACK = 512;  // pixel indices up to one tile past M are decoded
+
+int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
+{
+    if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    if (force && force->block_m != 0 && force->block_m != sgb::PAIR_TILE_M) return CONV2D_ERR_UNSUPPORTED;
+    int bn = force && force->block_n ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    // Stage depth: two k-blocks per stage (three 64 KB stages at block_n = 256, one
+    // producer thread per operand): 1.5 TMA operations per k-block against 2 with one
+    // k-block per stage, and the SM's TMA unit completes about one operation per
+    // ~0.17 us, so the deeper stages measured faster.  A measurement hook forces one.
+    const int dbg = force ? force->debug_flags : 0;
+    const int kbs = (dbg & CONV2D_DEBUG_PAIR_KB1) ? 1 : 2;
+    const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
+    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t tiles = m_tiles * n_tiles;
+    const int64_t stages = cdiv(s.crs / BK, kbs);
+    const int64_t units = tiles * stages;
+    const int64_t resident = pair_max_resident(bn, kbs, whole_tiles);
+    if (resident <= 0) return CONV2D_ERR_CUDA;
+    const int64_t fsplits = force ? force->splits : 0;
+    const int64_t fgrid = force ? force->grid : 0;
+    if (fsplits < 0 || fgrid < 0 || (fsplits > 0 && fgrid > 0)) return CONV2D_ERR_INVALID;
+    int64_t grid;
+    if (fsplits > 0) {
+        if (fsplits > stages) return CONV2D_ERR_UNSUPPORTED;  // every split needs at least one stage
+        grid = tiles * fsplits;
+    } else if (fgrid > 0) {
+        if (fgrid > units) return CONV2D_ERR_UNSUPPORTED;
+        grid = fgrid;
+    } else if (!whole_tiles && units * kbs >= kPairStreamKStages * PAIR_KBS_NORM * resident) {
+        grid = resident;
+    } else {
+        // Whole tiles: the smallest even share of at least tiles/resident tiles per pair.
+        const int64_t per = cdiv(tiles, resident);
+        grid = tiles;
+        for (int64_t d = per; d <= 2 * per; ++d)
+            if (tiles % d == 0) {
+                grid = tiles / d;
+                break;
+            }
+    }
+    // The kernel splits the work with 32-bit arithmetic (FastDiv, n < 2^31).
+    if ((units + 1) * (grid + 1) >= (int64_t(1) << 31) || s.m >= (int64_t(1) << 31) - PAIR_M_SLACK)
+        return CONV2D_ERR_UNSUPPORTED;
+    plan->block_m = sgb::PAIR_TILE_M;
+    plan->block_n = bn;
+    plan->splits = static_cast<int>(fsplits);
+    plan->loader = CONV2D_LOADER_TMA_PAIR;
+    plan->m_tiles = static_cast<int>(m_tiles);
+    plan->n_tiles = static_cast<int>(n_tiles);
+    plan->num_kb = static_cast<int>(stages);
+    plan->grid = static_cast<int>(grid);
+    plan->units = units;
+    plan->box = BoxGeom{};
+    plan->halo = HaloGeom{};
+    plan->kbs = kbs;
+    if (plan_cuts_tiles(*plan)) {
+        // A later split waits for an earlier one: every pair must be resident at once.
+        if (grid > resident) return CONV2D_ERR_UNSUPPORTED;
+        // bf16 output cannot carry partial sums (and ReLU needs the whole sum).
+        if (whole_tiles) return CONV2D_ERR_UNSUPPORTED;
+    }
+    return CONV2D_OK;
+}
+
 int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles = false)
 {
     const int sms = sm_count_current();
@@ -448,6 +570,8 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole
     } else if (loader == CONV2D_LOADER_HALO) {
         HaloGeom g;
         if (!halo_geometry(s, 64, &g)) return CONV2D_ERR_UNSUPPORTED;
+    } else if (loader == CONV2D_LOADER_TMA_PAIR) {
+        return choose_pair_plan(s, force, plan, whole_tiles);
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
@@ -612,6 +736,31 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     std::memset(tm_a, 0, sizeof(*tm_a));
     std::memset(tm_b, 0, sizeof(*tm_b));
     if (!load_encoders()) return CONV2D_ERR_CUDA;
+    if (plan.loader == CONV2D_LOADER_TMA_PAIR) {
+        // A: each CTA's 128 pixels x 64 channels per im2col load (window origins as for the
+        // one-CTA loader).  B: w viewed as {64, K, C*R*S/64}; a box is block_n/2 weight rows x
+        // two consecutive k-blocks, landing k-block-major (a k-block past the end reads zeros).
+        const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                       (cuuint64_t)(s.h * s.w * s.c * 2)};
+        const int lower[2] = {(int)-s.pw, (int)-s.ph};
+        const int upper[2] = {(int)(s.pw - (s.s - 1) * s.dw), (int)(s.ph - (s.r - 1) * s.dh)};
+        const cuuint32_t estr[4] = {1, (cuuint32_t)s.sw, (cuuint32_t)s.sh, 1};
+        CUresult rc = g_encode_im2col(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims,
+                                      strides, lower, upper, BK, static_cast<cuuint32_t>(sgb::PAIR_ROWS), estr,
+                                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        const cuuint64_t wd[3] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.crs / BK)};
+        const cuuint64_t ws[2] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2)};
+        const cuuint32_t wb[3] = {(cuuint32_t)BK, (cuuint32_t)(plan.block_n / 2), (cuuint32_t)plan.kbs};
+        const cuuint32_t we[3] = {1, 1, 1};
+        rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), wd, ws, wb, we,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
     if (plan.loader == CONV2D_LOADER_TMA_IM2COL || plan.loader == CONV2D_LOADER_HYBRID) {
         const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
         const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
@@ -676,6 +825,81 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
     }
+    return CONV2D_OK;
+}
+
+// ------------------------------------------------------------------ tensor-map cache
+// Encoding a tensor map is host work on every call (a driver call per map).
+// Repeated calls on the same problem and the same buffers -- a serving loop,
+// an eager training step -- reuse the maps encoded the first time: a small
+// cache keyed on everything a map depends on (the shape, the loader and tile
+// geometry of the plan, the two base pointers and the device).  A changed
+// pointer, shape or plan is a different key and is encoded afresh.
+struct MapKey {
+    Shape shape;
+    int loader, block_m, block_n, kbs;
+    BoxGeom box;
+    HaloGeom halo;
+    const void* x;
+    const void* w;
+    int device;
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap a, b;
+    bool used;
+};
+
+constexpr int kMapCacheEntries = 32;
+std::mutex g_map_mutex;
+MapEntry g_map_cache[kMapCacheEntries];
+int g_map_next = 0;  // round-robin replacement
+unsigned long long g_map_hits = 0, g_map_misses = 0;
+
+MapKey make_map_key(const Shape& s, const Plan& plan, const void* x, const void* w, int device)
+{
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
+    k.shape = s;
+    k.loader = plan.loader;
+    k.block_m = plan.block_m;
+    k.block_n = plan.block_n;
+    if (plan.loader == CONV2D_LOADER_TMA_PAIR) k.kbs = plan.kbs;
+    if (plan.loader == CONV2D_LOADER_TMA_BOX) k.box = plan.box;
+    if (plan.loader == CONV2D_LOADER_HALO) k.halo = plan.halo;
+    k.x = x;
+    k.w = w;
+    k.device = device;
+    return k;
+}
+
+int encode_maps_cached(const Shape& s, const Plan& plan, const void* x, const void* w, CUtensorMap* tm_a,
+                       CUtensorMap* tm_b)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    const MapKey key = make_map_key(s, plan, x, w, dev);
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (const MapEntry& e : g_map_cache)
+            if (e.used && std::memcmp(&e.key, &key, sizeof(key)) == 0) {
+                *tm_a = e.a;
+                *tm_b = e.b;
+                ++g_map_hits;
+                return CONV2D_OK;
+            }
+    }
+    const int rc = encode_maps(s, plan, x, w, tm_a, tm_b);
+    if (rc != CONV2D_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    MapEntry& e = g_map_cache[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCacheEntries;
+    e.key = key;
+    e.a = *tm_a;
+    e.b = *tm_b;
+    e.used = true;
+    ++g_map_misses;
     return CONV2D_OK;
 }
 
@@ -869,7 +1093,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     }
 
     CUtensorMap tm_a, tm_b;
-    rc = encode_maps(s, plan, x, w, &tm_a, &tm_b);
+    rc = encode_maps_cached(s, plan, x, w, &tm_a, &tm_b);
     if (rc != CONV2D_OK) return rc;
 
     sgb::ConvKernelParams kp{};
@@ -917,13 +1141,27 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
 #ifdef SGB_TRACE_ENABLED
     kp.trace = g_trace;
 #endif
+    if (plan.loader == CONV2D_LOADER_TMA_PAIR) {
+        kp.fd_grid = sgb::FastDiv(static_cast<uint32_t>(plan.grid));
+        kp.fd_units = sgb::FastDiv(static_cast<uint32_t>(plan.units));
+        kp.fd_nkb = sgb::FastDiv(static_cast<uint32_t>(plan.num_kb));
+        kp.fd_ntiles = sgb::FastDiv(static_cast<uint32_t>(plan.n_tiles));
+        kp.fd_pq = sgb::FastDiv(static_cast<uint32_t>(s.p * s.q));
+        kp.fd_q = sgb::FastDiv(static_cast<uint32_t>(s.q));
+        kp.fd_c = sgb::FastDiv(static_cast<uint32_t>(s.c));
+        kp.fd_s = sgb::FastDiv(static_cast<uint32_t>(s.s));
+    }
 
     const int64_t grid = plan.grid;
     if (log_enabled())
         std::fprintf(stderr, "[conv2d] M=%lld K=%lld CRS=%lld -> BM=%d BN=%d splits=%d loader=%d grid=%lld vec_store=%d\n",
                      (long long)s.m, (long long)s.k, (long long)s.crs, plan.block_m, plan.block_n, plan.splits, plan.loader,
                      (long long)grid, (int)vec_store);
-    cudaError_t err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, kp, (int)grid, stream);
+    cudaError_t err;
+    if (plan.loader == CONV2D_LOADER_TMA_PAIR)
+        err = launch_pair(plan.block_n, plan.kbs, tm_a, tm_b, kp, (int)grid, stream);
+    else
+        err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, kp, (int)grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;
     g_last_launches = 1;
     return CONV2D_OK;
@@ -1458,6 +1696,13 @@ int conv2d_fwd_host(const conv2d_params* params, const void* x_host, const void*
 }
 
 int conv2d_last_launch_count(void) { return g_last_launches; }
+
+void conv2d_tensor_map_cache_stats(unsigned long long* hits, unsigned long long* misses)
+{
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    if (hits) *hits = g_map_hits;
+    if (misses) *misses = g_map_misses;
+}
 
 #ifdef SGB_TRACE_ENABLED
 // Profiling builds only: device buffer of grid x 16 timestamps that later launches fill.

@@ -82,6 +82,7 @@
 #include <cstdint>
 #include <cstdlib>
 
+#include "fastdiv.h"
 #include "ptx.cuh"
 #include "trace.cuh"
 
@@ -162,6 +163,9 @@ struct ConvKernelParams {
     float* part;
     unsigned long long wait_limit_ns;
     unsigned long long* trace;  // per-CTA phase timestamps; only written in trace builds
+    // CTA-pair kernel: divisions by the loop-invariant sizes (grid = pairs,
+    // units, stages per tile, column blocks, P*Q, Q, C, S).
+    FastDiv fd_grid, fd_units, fd_nkb, fd_ntiles, fd_pq, fd_q, fd_c, fd_s;
 };
 
 

@@ -10,7 +10,9 @@
 // Every GPU that loads this library holds that array until the process exits.
 // In host code `g_noalloc_scratch` only names a host-side stand-in, so its
 // device address is looked up with cudaGetSymbolAddress once per device (with
-// that device current) on the first call made on that device.
+// that device current) on the first call made on that device and kept for the
+// life of the process.  A device reset unloads the module that holds the array,
+// so the kept address is only valid while the device's primary context lives.
 #include <cuda_runtime.h>
 
 #include <cstddef>

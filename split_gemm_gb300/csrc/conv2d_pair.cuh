@@ -1,0 +1,650 @@
+// Implicit-GEMM 2-D convolution forward on CTA pairs (tcgen05.mma.cta_group::2).
+//
+// The GEMM view is the one-CTA kernel's (burn PR #2287 "Introduce autotuning to
+// conv2d ...", Changes; burn PR #2545 "[Optimization] Implicit gemm rewrite",
+// Changes): rows m = (n*P + p)*Q + q are output pixels, columns are output
+// channels, the reduction index is kk = (r*S + s)*C + c, A is the im2col matrix
+// gathered tile by tile by TMA in im2col mode and B the KRSC weight viewed as
+// [K][C*R*S].
+//
+// A tile is 256 output pixels x BN output channels, computed by a cluster of
+// two CTAs on two SMs.  Each CTA loads into its own shared memory the im2col
+// rows of its 128 pixels and BN/2 of the weight rows; one thread of the even
+// CTA (the leader) issues 256 x BN x 16 MMAs that read A rows 0..127 and the
+// first half of B from the leader and the rest from the same shared-memory
+// addresses in the peer, and accumulate rows 0..127 in the leader's tensor
+// memory and rows 128..255 in the peer's.  Per SM this halves the weight bytes
+// moved per MMA compared with a 128-pixel tile of the same width.
+//
+// A pipeline stage holds two 64-wide k-blocks: per CTA, two im2col loads of
+// 128 pixel rows x 64 channels and one 3-D box of BN/2 weight rows x 2
+// k-blocks, so that one stage carries 1024 MMA cycles of work per SM at
+// BN = 256.  A producer thread spends a roughly fixed ~0.2 us per ring stage
+// (barrier wait, expect, issue) whatever the stage's size, so fewer, larger
+// stages keep the producer ahead of the tensor cores.  Both CTAs' loads of a
+// stage complete on the leader's full barrier (the leader's producer expects the
+// bytes of both); the leader's MMA commit releases the stage in both CTAs at
+// once (multicast), and the accumulator-ready signal likewise.  Each CTA's
+// epilogue drains its own 128 accumulator rows and tells the leader's MMA warp
+// through a remote arrive on the leader's barrier.
+//
+// Work split: units are (tile, stage) pairs numbered tile-major; pair c of G
+// takes units [c*U/G, (c+1)*U/G) (stream-K, as in the one-CTA kernel), so all
+// SM pairs get the same number of MMAs.  A tile cut between pairs is reduced in
+// place in y, each 128-row half with its own semaphore (NVIDIA/Fuser issue #1316
+// "Split-K matmul is slow even for few partitions", Eliminating the workspace):
+// the owner of split 0 zeroes the rows early, then every split adds (see the
+// epilogue).
+//
+// Warp roles, the same in both CTAs (the MMA issuer and the stage waiter are
+// idle in the peer):
+//   warp 0      TMA producer (one thread) of this CTA's im2col rows;
+//   warp 1      tensor-memory allocation for the pair; in the leader the MMA issuer;
+//   warps 2..9  epilogue: TMEM -> registers (+ bias) -> swizzled staging -> 16-byte stores;
+//   warp 10     in the leader, the stage waiter (waits for each stage's full
+//               barrier and releases the MMA warp by named barrier, so the MMA
+//               thread never polls shared memory between its MMAs);
+//   warp 11     TMA producer (one thread) of this CTA's weight rows.
+//
+// Every wait is bounded; a wait that runs out records CONV2D_ERR_TIMEOUT, flags
+// both CTAs of the pair, and the pair runs its loops to the end without
+// issuing or storing.
+#pragma once
+
+#include "conv2d_kernel.cuh"
+
+namespace sgb {
+
+constexpr int PAIR_ROWS = 128;  // output pixels (GEMM rows) each CTA of the pair holds
+constexpr int PAIR_TILE_M = 2 * PAIR_ROWS;
+// 64-wide k-blocks per pipeline stage (KBS): 2 gives three 64 KB stages at BN =
+// 256 with one producer thread per operand; 1 gives six 32 KB stages with two
+// producer threads per operand taking alternate stages.
+constexpr int PAIR_KBS_MAX = 2;
+
+template <int BN, int KBS>
+struct PairConfig {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "pair tiles are 256 pixels x 64, 128 or 256 channels");
+    static_assert(KBS == 1 || KBS == 2, "one or two k-blocks per stage");
+    static constexpr int B_ROWS = BN / 2;                  // weight rows each CTA holds
+    static constexpr int A_KB = PAIR_ROWS * BK * 2;        // one k-block of this CTA's A rows: 16 KB
+    static constexpr int B_KB = B_ROWS * BK * 2;           // one k-block of this CTA's B rows
+    static constexpr int A_STAGE = KBS * A_KB;
+    static constexpr int B_STAGE = KBS * B_KB;
+    static constexpr int NPROD = KBS == 1 ? 2 : 1;  // producer threads per operand
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int STAGES = 196608 / STAGE > 8 ? 8 : 196608 / STAGE;  // 3 (BN 256), 4 (128, 64)
+    static_assert(STAGES >= 3, "the ring needs at least three stages");
+    static_assert(STAGES % NPROD == 0, "each producer owns whole ring slots");
+    static constexpr int RING = STAGES * STAGE;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int EPI_T = EPI_WARPS * 32;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOT_BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int SMEM_BYTES = RING + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= kMaxSmemBytes, "exceeds the per-block shared-memory limit");
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns (128 lanes)
+    static constexpr int THREADS = (WAITER_WARP + 2 * NPROD) * 32;  // warps 0 .. 11 (13 with two producers per operand)
+    // Both operands K-major bf16, fp32 accumulator, M = 256 across the pair.
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR_TILE_M, BN);
+    // Accumulator-empty arrivals: every epilogue warp of both CTAs, once per segment.
+    static constexpr uint32_t ACC_EMPTY_COUNT = 2 * EPI_WARPS;
+};
+
+struct PairSmem {
+    uint8_t* a;          // STAGES x (2 k-blocks x 128 rows x 128 B)
+    uint8_t* b;          // STAGES x (2 k-blocks x BN/2 rows x 128 B)
+    uint8_t* epi;        // EPI_WARPS staging slots
+    uint64_t* full;      // STAGES (used in the leader)
+    uint64_t* empty;     // STAGES (both)
+    uint64_t* acc_full;  // 2 (both)
+    uint64_t* acc_empty; // 2 (leader)
+    uint64_t* mma_done;  // 1 (leader)
+    uint32_t* tmem_slot;
+    volatile uint32_t* abort_flag;
+    volatile uint32_t* epi_go;
+};
+
+// Records a timeout and flags both CTAs of the pair.
+__device__ __forceinline__ void pair_record_timeout(const ConvKernelParams& kp, const PairSmem& sm, uint32_t rank)
+{
+    *sm.abort_flag = 1u;
+    ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t*>(sm.abort_flag)), rank ^ 1u), 1u);
+    if (kp.status) atomicMax(kp.status, STATUS_TIMEOUT);
+}
+
+// This pair's segments, from the end of its unit range to the start.  kp.grid
+// is the number of pairs and kp.num_kb the number of stages per tile.  All
+// arithmetic is 32-bit and every division goes through a FastDiv: the host
+// admits only plans with (units + 1) * (grid + 1) < 2^31.
+struct PairWalker {
+    uint32_t lo, cur, nkb, grid, units;
+    int pair;
+    __device__ __forceinline__ PairWalker(const ConvKernelParams& kp, int pair_idx)
+    {
+        pair = pair_idx;
+        units = static_cast<uint32_t>(kp.units);
+        grid = static_cast<uint32_t>(kp.grid);
+        nkb = static_cast<uint32_t>(kp.num_kb);
+        lo = kp.fd_grid.div(static_cast<uint32_t>(pair) * units);
+        cur = kp.fd_grid.div((static_cast<uint32_t>(pair) + 1u) * units);
+    }
+    // The pair whose unit range holds unit u: the largest c with floor(c*U/G) <= u.
+    __device__ __forceinline__ uint32_t pair_of_unit(const ConvKernelParams& kp, uint32_t u) const
+    {
+        return kp.fd_units.div((u + 1u) * grid + units - 1u) - 1u;
+    }
+    __device__ __forceinline__ bool next(const ConvKernelParams& kp, Segment& sg)
+    {
+        if (cur <= lo) return false;
+        const uint32_t t = kp.fd_nkb.div(cur - 1u);
+        const uint32_t base = t * nkb;
+        const uint32_t seg_lo = lo > base ? lo : base;
+        sg.tile = static_cast<int>(t);
+        sg.kb_begin = static_cast<int>(seg_lo - base);
+        sg.kb_end = static_cast<int>(cur - base);
+        const uint32_t first = pair_of_unit(kp, base);
+        const uint32_t last = pair_of_unit(kp, base + nkb - 1u);
+        sg.split = pair - static_cast<int>(first);
+        sg.nsplits = static_cast<int>(last - first + 1u);
+        cur = seg_lo;
+        return true;
+    }
+};
+
+// Tile row-block and column-block of a tile index.
+__device__ __forceinline__ void pair_tile_coords(const ConvKernelParams& kp, int tile, int& m_tile, int& n_tile)
+{
+    m_tile = static_cast<int>(kp.fd_ntiles.div(static_cast<uint32_t>(tile)));
+    n_tile = tile - m_tile * kp.n_tiles;
+}
+
+// Reduction cursor: filter tap (r, s) and channel c of a 64-wide k-block, stepped without divisions.
+struct PairCursor {
+    int r, s, c;
+    __device__ __forceinline__ void at(const ConvKernelParams& kp, int kb)
+    {
+        const int kk = kb * BK;
+        const int rs = static_cast<int>(kp.fd_c.div(static_cast<uint32_t>(kk)));
+        c = kk - rs * kp.C;
+        r = static_cast<int>(kp.fd_s.div(static_cast<uint32_t>(rs)));
+        s = rs - r * kp.S;
+    }
+    __device__ __forceinline__ void step(const ConvKernelParams& kp)
+    {
+        c += BK;
+        if (c >= kp.C) {
+            c = 0;
+            if (++s == kp.S) {
+                s = 0;
+                ++r;
+            }
+        }
+    }
+};
+
+// Window origin of this CTA's first pixel in tile row-block m_tile (pixels
+// past the output decode to images >= N, which the TMA zero-fills).
+__device__ __forceinline__ void pair_origin(const ConvKernelParams& kp, int m_tile, uint32_t rank, int& n_img,
+                                            int& w_org, int& h_org)
+{
+    const uint32_t m = static_cast<uint32_t>(m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS);
+    n_img = static_cast<int>(kp.fd_pq.div(m));
+    const uint32_t rem = m - static_cast<uint32_t>(n_img) * kp.fd_pq.d;
+    const int p0 = static_cast<int>(kp.fd_q.div(rem));
+    const int q0 = static_cast<int>(rem) - p0 * kp.Q;
+    w_org = q0 * kp.sw - kp.pw;
+    h_org = p0 * kp.sh - kp.ph;
+}
+
+// ---------------------------------------------------------------- producers (warps 0 and 11, one thread each, both CTAs)
+// The TMA unit of an SM takes ~0.1 us per operation and ~0.17 us per ring
+// stage of barrier traffic on the issuing thread, whatever the bytes; the
+// activation loads (two im2col operations) and the weight load (one 3-D box)
+// of a stage are therefore issued by two threads in different warps, each
+// keeping its own pace ahead of the tensor cores.  Each operand of each slot
+// has one issuer, loading its uses in order.
+enum PairOperand : int { PAIR_A = 0, PAIR_B = 1 };
+
+template <int BN, int KBS, int OP>
+__device__ void pair_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
+                              const PairSmem& sm, uint32_t rank, int pair, int role)
+{
+    using Cfg = PairConfig<BN, KBS>;
+    constexpr int STAGES = Cfg::STAGES;
+    const int kb_total = kp.CRS / BK;
+    const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(sm.full), 0u);  // the leader's full[0]
+    int it = 0;  // stages issued (all segments)
+    bool ok = true;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        int n_img = 0, w_org = 0, h_org = 0;
+        if (OP == PAIR_A) pair_origin(kp, m_tile, rank, n_img, w_org, h_org);
+        const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        PairCursor cur;
+        if (OP == PAIR_A) cur.at(kp, sg.kb_begin * KBS);
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            const int nkb = kb_total - st * KBS < KBS ? kb_total - st * KBS : KBS;
+            if (slot % Cfg::NPROD != role) {  // another producer's slot: only keep the cursor in step
+                if (OP == PAIR_A)
+                    for (int j = 0; j < nkb; ++j) cur.step(kp);
+                continue;
+            }
+            if (*sm.abort_flag) { ok = false; break; }
+            if (!ptx::mbar_wait_spin(&sm.empty[slot], (static_cast<uint32_t>(it / STAGES) & 1u) ^ 1u, kp.wait_limit_ns)) {
+                pair_record_timeout(kp, sm, rank);
+                ok = false;
+                break;
+            }
+            const uint32_t bar = full0 + static_cast<uint32_t>(slot) * 8u;
+            if (OP == PAIR_A) {
+                // The leader expects the activation bytes of both CTAs.
+                if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(nkb * Cfg::A_KB));
+                uint8_t* a_dst = sm.a + slot * Cfg::A_STAGE;
+                for (int j = 0; j < nkb; ++j) {
+                    ptx::tma_load_im2col_4d_pair(a_dst + j * Cfg::A_KB, tm_a, bar, cur.c, w_org, h_org, n_img,
+                                                 static_cast<uint16_t>(cur.s * kp.dw), static_cast<uint16_t>(cur.r * kp.dh));
+                    cur.step(kp);
+                }
+                SGB_PAIR_MARK(kp, it, static_cast<int>(rank));
+            } else {
+                // The weight box always counts both k-blocks (one past the reduction is zero-filled).
+                if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(Cfg::B_STAGE));
+                ptx::tma_load_3d_pair(sm.b + slot * Cfg::B_STAGE, tm_b, bar, 0, b_row, st * KBS);
+                SGB_PAIR_MARK(kp, it, 5 + static_cast<int>(rank));
+            }
+        }
+    }
+    // Drain: the last load of each slot has been consumed (so it landed) once the
+    // MMA's release of that use arrives on this CTA's empty barrier.
+    for (int i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+        if ((i % STAGES) % Cfg::NPROD == role)
+            ptx::mbar_wait(&sm.empty[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------- stage waiter (warp 10, leader)
+template <int BN, int KBS>
+__device__ void pair_waiter(const ConvKernelParams& kp, const PairSmem& sm, int pair)
+{
+    using Cfg = PairConfig<BN, KBS>;
+    constexpr int STAGES = Cfg::STAGES;
+    const int lane = threadIdx.x & 31;
+    bool waiting = true;
+    int it = 0;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            const uint32_t use = static_cast<uint32_t>(it / STAGES);
+            if (lane == 0) {
+                if (waiting && (*sm.abort_flag || !ptx::mbar_wait_spin(&sm.full[slot], use & 1u, kp.wait_limit_ns))) {
+                    pair_record_timeout(kp, sm, 0u);
+                    waiting = false;
+                }
+                // After a timeout: pace the MMA warp by its own release of the previous use.
+                if (!waiting && use > 0)
+                    for (int t = 0; t < 16 && !ptx::mbar_wait(&sm.empty[slot], (use - 1u) & 1u, kp.wait_limit_ns); ++t) {
+                    }
+                SGB_PAIR_MARK(kp, it, 2);
+            }
+            __syncwarp();
+            ptx::named_bar_arrive(STAGE_BAR0 + slot, 64);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 1, leader)
+template <int BN, int KBS>
+__device__ void pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, int pair)
+{
+    using Cfg = PairConfig<BN, KBS>;
+    constexpr int STAGES = Cfg::STAGES;
+    const int lane = threadIdx.x & 31;
+    const int kb_total = kp.CRS / BK;
+    const uint64_t a_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.a));
+    const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    int it = 0, seg_idx = 0;
+    bool issue = true;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        const int buf = seg_idx & 1;
+        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        // Both CTAs' epilogues must have drained this accumulator's previous segment.
+        if (lane == 0 && issue) {
+            if (*sm.abort_flag || !ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
+                pair_record_timeout(kp, sm, 0u);
+                issue = false;
+            }
+        }
+        __syncwarp();
+        ptx::tc_fence_after();
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            ptx::named_bar_sync(STAGE_BAR0 + slot, 64);
+            ptx::tc_fence_after();
+            if (lane == 0) SGB_PAIR_MARK(kp, it, 3);
+            if (lane == 0 && issue && !*sm.abort_flag) {
+                const int nkb = kb_total - st * KBS < KBS ? kb_total - st * KBS : KBS;
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((slot * Cfg::A_STAGE) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((slot * Cfg::B_STAGE) >> 4);
+#pragma unroll
+                for (int j = 0; j < KBS; ++j) {
+                    if (j < nkb) {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            ptx::mma_bf16_pair(tmem_d, ad + static_cast<uint64_t>((j * Cfg::A_KB + k * UMMA_K * 2) >> 4),
+                                               bd + static_cast<uint64_t>((j * Cfg::B_KB + k * UMMA_K * 2) >> 4),
+                                               Cfg::IDESC, (st > sg.kb_begin || j > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+            }
+            if (lane == 0) ptx::mma_commit_pair(&sm.empty[slot], 0x3);  // every stage, issuing or not
+            if (lane == 0) SGB_PAIR_MARK(kp, it, 4);
+            __syncwarp();
+        }
+        if (lane == 0) ptx::mma_commit_pair(&sm.acc_full[buf], 0x3);
+        __syncwarp();
+        ++seg_idx;
+    }
+    // No MMA may be in flight when the pair reaches its teardown.
+    if (lane == 0) {
+        ptx::mma_commit_pair(sm.mma_done, 0x1);
+        ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------- epilogue (warps 2..9, both CTAs)
+// Cut tiles are reduced in place in y without any split waiting for another
+// split's stores.  The pair that owns split 0 of a cut tile zeroes its rows of
+// y at the start of the kernel, while its first MMAs run and its store path is
+// otherwise idle, and publishes that on the tile half's semaphore (value 1).
+// Every split -- split 0 with the bias -- then adds its partial sums with
+// vector atomic adds once the semaphore is non-zero and counts itself in
+// (value 1 + splits done); the last one resets the semaphore to 0.  In the
+// ordered mode split j waits for the value j + 1 and publishes j + 2 after a
+// fence (the last resets), so the adds land in k order: bitwise reproducible.
+// (A split that stored first and let the others add would chain one tile
+// half's store -- ~2.5 us for 128 KB at one SM's ~60 GB/s store rate -- in
+// front of the other splits' adds at the end of the kernel.)
+//
+// Semaphore of one 128-row half of a tile: [row half][column block].
+__device__ __forceinline__ int pair_sem_index(const ConvKernelParams& kp, int m_tile, uint32_t rank, int n_tile)
+{
+    return (m_tile * 2 + static_cast<int>(rank)) * kp.n_tiles + n_tile;
+}
+
+__device__ __forceinline__ void pair_pass_turn(const ConvKernelParams& kp, int sem, const Segment& sg)
+{
+    if (kp.reduce_concurrent) {
+        const uint32_t before = atomicAdd(kp.sems + sem, 1u);
+        if (before == static_cast<uint32_t>(sg.nsplits)) atomicExch(kp.sems + sem, 0u);
+        return;
+    }
+    const uint32_t next = (sg.split + 1 == sg.nsplits) ? 0u : static_cast<uint32_t>(sg.split + 2);
+    ptx::st_release_gpu(kp.sems + sem, next);
+}
+
+// Zeroes this CTA's rows of every cut tile whose split 0 this pair owns, then
+// publishes them (all epilogue threads take part; one barrier).
+template <int BN>
+__device__ void pair_zero_cut_tiles(const ConvKernelParams& kp, uint32_t rank, int pair, int et)
+{
+    constexpr int EPI_T = PairConfig<BN, 1>::EPI_T;
+    bool any = false;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        if (sg.nsplits < 2 || sg.split != 0) continue;
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        const int row0 = m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS;
+        if (row0 >= kp.M) continue;
+        const int n0 = n_tile * BN;
+        const int vecs = ((n0 + BN < kp.K ? n0 + BN : kp.K) - n0) / 4;  // float4 per row (K % 4 == 0)
+        const int rows = kp.M - row0 < PAIR_ROWS ? kp.M - row0 : PAIR_ROWS;
+        for (int i = et; i < rows * vecs; i += EPI_T) {
+            const int r = i / vecs;
+            const int v = i - r * vecs;
+            *reinterpret_cast<float4*>(kp.y + static_cast<int64_t>(row0 + r) * kp.ldy + n0 + 4 * v) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        any = true;
+    }
+    if (any) __threadfence();
+    ptx::named_bar_sync(1, EPI_T);
+    if (et == 0 && any && !(kp.debug_flags & 1)) {  // test hook: never signal
+        PairWalker again(kp, pair);
+        while (again.next(kp, sg)) {
+            if (sg.nsplits < 2 || sg.split != 0) continue;
+            int m_tile, n_tile;
+            pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+            if (m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS >= kp.M) continue;
+            ptx::st_release_gpu(kp.sems + pair_sem_index(kp, m_tile, rank, n_tile), 1u);
+        }
+    }
+}
+
+template <int BN, bool FUSED>
+__device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, uint32_t rank,
+                              int pair)
+{
+    using Cfg = PairConfig<BN, 1>;  // the epilogue does not depend on the stage depth
+    constexpr int SLABS = BN / 64;  // 32-column slabs per warp: two warps share each lane quadrant
+    const int et = threadIdx.x - EPI_WARP0 * 32;
+    const int ew = et >> 5;
+    const int lane = threadIdx.x & 31;
+    const int quad = (threadIdx.x >> 5) & 3;  // the TMEM lane quadrant this warp may read
+    const int jbeg = (ew >> 2) * SLABS;
+    const int rsub = lane >> 3;
+    const int chunk = lane & 7;
+    const uint32_t saddr = ptx::smem_addr(sm.epi + ew * EPI_SLOT_BYTES);
+    const uint32_t acc_empty0 = ptx::mapa_shared(ptx::smem_addr(sm.acc_empty), 0u);  // the leader's
+    if (!FUSED) pair_zero_cut_tiles<BN>(kp, rank, pair, et);  // fused plans cut no tiles
+    int seg_idx = 0;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        const int buf = seg_idx & 1;
+        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        const int row0 = m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS;
+        const bool has_rows = row0 < kp.M;  // a half past the output stores nothing and takes no turn
+        const int n0 = n_tile * BN;
+        const int n_end = n0 + BN < kp.K ? n0 + BN : kp.K;
+        const int sem = pair_sem_index(kp, m_tile, rank, n_tile);
+        const bool cut = sg.nsplits > 1;
+        const bool add_bias = kp.bias != nullptr && sg.split == 0;
+        float4 bias4[SLABS];
+#pragma unroll
+        for (int j = 0; j < SLABS; ++j) {
+            const int col = n0 + (jbeg + j) * 32 + chunk * 4;
+            bias4[j] = (add_bias && col < n_end) ? __ldg(reinterpret_cast<const float4*>(kp.bias + col))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (et == 0 && !ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) pair_record_timeout(kp, sm, rank);
+        ptx::named_bar_sync(1, Cfg::EPI_T);
+        if (et == 0) {
+            bool go = *sm.abort_flag == 0u;
+            if (go && has_rows && cut) {  // the rows are zeroed (concurrent) or it is this split's turn (ordered)
+                go = kp.reduce_concurrent ? wait_base(kp, sem, sm.abort_flag)
+                                          : wait_turn(kp, sem, sg.split + 1, sm.abort_flag);
+                if (!go) pair_record_timeout(kp, sm, rank);  // the turn never came: flag the peer too
+            }
+            *sm.epi_go = go ? 1u : 0u;
+        }
+        ptx::named_bar_sync(1, Cfg::EPI_T);
+        SGB_TRACE(kp, et == 0 && seg_idx < 4, 2 + 2 * seg_idx);  // segment: accumulator ready, turn granted
+        const bool store = *sm.epi_go != 0u && has_rows;
+        ptx::tc_fence_after();
+        int mrow[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int m = row0 + quad * 32 + 4 * i + rsub;
+            mrow[i] = m < kp.M ? m : -1;
+        }
+        const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll
+        for (int j = 0; j < SLABS; ++j) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(taddr + (jbeg + j) * 32, v);
+            ptx::tmem_ld_wait();
+            if (j == SLABS - 1) {  // this warp's part of the accumulator is in registers: tell the leader
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(buf) * 8u);
+            }
+            if (!store) continue;
+            // Registers -> this warp's 32 x 32 swizzled slot -> 16-byte global writes
+            // (8 lanes per 128-byte row segment, four rows per instruction).
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            __syncwarp();
+            const int col = n0 + (jbeg + j) * 32 + chunk * 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(4 * i + rsub, chunk));
+                if (add_bias) {
+                    val.x = __float_as_uint(__uint_as_float(val.x) + bias4[j].x);
+                    val.y = __float_as_uint(__uint_as_float(val.y) + bias4[j].y);
+                    val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
+                    val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
+                }
+                if (FUSED && kp.relu) val = ptx::relu4(val);
+                const int m = mrow[i];
+                if (m >= 0 && col < n_end) {
+                    const int64_t at = static_cast<int64_t>(m) * kp.ldy + col;
+                    if (FUSED && kp.out_bf16)
+                        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
+                    else if (!cut)
+                        *reinterpret_cast<uint4*>(kp.y + at) = val;
+                    else
+                        ptx::red_add_v4_f32(kp.y + at, val);
+                }
+            }
+        }
+        if (store && cut) {
+            // Ordered mode: this split's adds must be performed before the next split's.
+            if (!kp.reduce_concurrent) __threadfence();
+            ptx::named_bar_sync(1, Cfg::EPI_T);
+            if (et == 0) pair_pass_turn(kp, sem, sg);
+        }
+        SGB_TRACE(kp, et == 0 && seg_idx < 4, 3 + 2 * seg_idx);  // segment: epilogue done
+        ++seg_idx;
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int BN, int KBS, bool FUSED>
+__global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
+    conv2d_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                           const ConvKernelParams kp)
+{
+    using Cfg = PairConfig<BN, KBS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairSmem sm;
+    sm.a = smem;
+    sm.b = smem + Cfg::STAGES * Cfg::A_STAGE;
+    sm.epi = smem + Cfg::RING;
+    sm.full = reinterpret_cast<uint64_t*>(smem + Cfg::RING + Cfg::EPI_BYTES);
+    sm.empty = sm.full + Cfg::STAGES;
+    sm.acc_full = sm.empty + Cfg::STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.mma_done = sm.acc_empty + 2;
+    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
+    sm.abort_flag = sm.tmem_slot + 1;
+    sm.epi_go = sm.tmem_slot + 2;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int pair = static_cast<int>(ptx::cluster_id_x());
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Cfg::STAGES; ++i) {
+            ptx::mbar_init(&sm.full[i], 2);   // the leader's two producers (expecting both CTAs' bytes)
+            ptx::mbar_init(&sm.empty[i], 1);  // the leader's MMA commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sm.acc_full[i], 1);
+            ptx::mbar_init(&sm.acc_empty[i], Cfg::ACC_EMPTY_COUNT);
+        }
+        ptx::mbar_init(sm.mma_done, 1);
+        *sm.abort_flag = 0u;
+        *sm.epi_go = 0u;
+        ptx::mbar_init_fence();
+    }
+    // Only the descriptors are prefetched: L2 prefetches of the first stages would
+    // queue in the SM's TMA unit ahead of the stages' own loads.
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_a);
+        ptx::prefetch_tensormap(&tm_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(sm.tmem_slot, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // both CTAs' barriers are initialised before any remote arrive or TMA completion
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *sm.tmem_slot;
+    // Everything above touches only shared memory, tensor memory, parameters and
+    // (by prefetches) L2, so it may overlap the previous kernel in the stream.
+    SGB_TRACE(kp, threadIdx.x == 0, 0);
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+    SGB_TRACE(kp, threadIdx.x == 0, 1);
+
+    if (warp == 0) {
+        if (lane == 0) pair_producer<BN, KBS, PAIR_A>(&tm_a, &tm_b, kp, sm, rank, pair, 0);
+    } else if (warp == WAITER_WARP + 1) {
+        if (lane == 0) pair_producer<BN, KBS, PAIR_B>(&tm_a, &tm_b, kp, sm, rank, pair, 0);
+    } else if (Cfg::NPROD > 1 && warp == WAITER_WARP + 2) {
+        if (lane == 0) pair_producer<BN, KBS, PAIR_A>(&tm_a, &tm_b, kp, sm, rank, pair, 1);
+    } else if (Cfg::NPROD > 1 && warp == WAITER_WARP + 3) {
+        if (lane == 0) pair_producer<BN, KBS, PAIR_B>(&tm_a, &tm_b, kp, sm, rank, pair, 1);
+    } else if (warp == 1) {
+        if (rank == 0) pair_mma<BN, KBS>(kp, sm, tmem_base, pair);
+    } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
+        pair_epilogue<BN, FUSED>(kp, sm, tmem_base, rank, pair);
+    } else if (warp == WAITER_WARP) {
+        if (rank == 0) pair_waiter<BN, KBS>(kp, sm, pair);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // neither CTA leaves while the other may still use its shared or tensor memory
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+    SGB_TRACE(kp, threadIdx.x == 0, 10);
+}
+
+// Host-side launcher: `pairs` clusters of two CTAs.
+template <int BN, int KBS>
+cudaError_t launch_conv2d_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const ConvKernelParams& kp, int pairs,
+                               cudaStream_t stream);
+
+// Largest number of CTA pairs of this instantiation that can be resident at once.
+template <int BN, int KBS>
+int conv2d_pair_max_resident(bool fused);
+
+#define SGB_PAIR_SIG(BN_, KBS_)                                                                              \
+    cudaError_t launch_conv2d_pair<BN_, KBS_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, \
+                                              int, cudaStream_t)
+#define SGB_PAIR_RES_SIG(BN_, KBS_) int conv2d_pair_max_resident<BN_, KBS_>(bool)
+
+}  // namespace sgb

@@ -101,6 +101,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// The same wait for a thread on a pipeline's critical path: it first spins on
+// the non-blocking test (no suspension, no clock reads) for `spins` polls, then
+// falls back to the bounded wait above.  A wait that ends within the spin
+// window is noticed a few cycles after the phase completes.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int spins = 2048)
+{
+#pragma unroll 1
+    for (int i = 0; i < spins; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity, limit_ns);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const void* map)
 {
@@ -461,6 +473,123 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n)
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int m, int n)
 {
     return idesc_bf16_f32(m, n) | (1u << 16);
+}
+
+// ---------------------------------------------------------------- clusters and CTA pairs (cta_group::2)
+// Rank of this CTA in its cluster, the cluster's index in the grid and the number of clusters (x only).
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the variable at shared address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 32-bit store into the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// TMA loads of a CTA pair: the data lands in this CTA's shared memory, the
+// completion bytes are counted on the mbarrier at shared::cluster address
+// `bar_cl`, which may be in the peer CTA (the pair's leader holds the barrier
+// that the leader's MMA waits on).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* map, uint32_t bar_cl, int32_t c0, int32_t c1,
+                                                 int32_t c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_im2col_4d_pair(void* dst, const void* map, uint32_t bar_cl, int32_t c,
+                                                        int32_t w, int32_t h, int32_t n, uint16_t w_off,
+                                                        uint16_t h_off)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cl), "r"(c), "r"(w), "r"(h), "r"(n), "h"(w_off), "h"(h_off)
+        : "memory");
+}
+
+// Tensor memory of a CTA pair: one warp of each of the two CTAs allocates (and
+// later frees) the same columns in both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[256 x N] (+)= A[256 x 16] * B[N x 16]^T across the CTA pair, issued by one
+// thread of the leader (even) CTA: A rows 0..127 and B rows 0..N/2-1 come from
+// the leader's shared memory at the descriptors' addresses, A rows 128..255 and
+// B rows N/2..N-1 from the same addresses in the peer CTA; accumulator rows
+// 0..127 live in the leader's tensor memory, rows 128..255 in the peer's.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on the mbarrier at shared offset `bar` in every CTA of `cta_mask`
+// once all pair MMAs this thread issued before have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 }  // namespace ptx

@@ -31,7 +31,17 @@
         if ((kp).trace && blockIdx.x == 0 && (i) < 256)                                        \
             (kp).trace[8192 + 4 * static_cast<size_t>(i) + (r)] = ::sgb::ptx::globaltimer();    \
     } while (0)
+// Per-stage timeline of CTA pair 0 (stages < 256): event r (< 8) of stage i at
+// trace[8192 + 8*i + r].
+#define SGB_PAIR_MARK(kp, i, r)                                                                 \
+    do {                                                                                        \
+        if ((kp).trace && blockIdx.x < 2 && (i) < 256)                                          \
+            (kp).trace[8192 + 8 * static_cast<size_t>(i) + (r)] = ::sgb::ptx::globaltimer();    \
+    } while (0)
 #else
+#define SGB_PAIR_MARK(kp, i, r) \
+    do {                        \
+    } while (0)
 #define SGB_STAGE_MARK(kp, i, r) \
     do {                         \
     } while (0)
