@@ -103,13 +103,21 @@ typedef enum {
                                      {1, 2, 4, 8, 16} (depthwise: 1), C % 8 == 0, and the weights
                                      (K*R*S*C/groups fp32) within shared memory.  The heuristic takes it for such shapes when nothing else
                                      is forced; block_n, block_m and splits do not apply */
-    CONV2D_LOADER_TMA_PAIR = 9    /* TMA im2col loads on clusters of two CTAs: a tile is 256 output pixels x
+    CONV2D_LOADER_TMA_PAIR = 9,   /* TMA im2col loads on clusters of two CTAs: a tile is 256 output pixels x
                                      block_n (64/128/256) channels computed by 2-CTA tensor-core MMAs
                                      (each CTA loads 128 pixel rows and half the weight rows), two 64-wide
                                      k-blocks per pipeline stage.  Needs groups == 1, C % 64 == 0,
                                      K % 4 == 0; block_m is 256 (or 0); grid counts CTA pairs; a fused
                                      epilogue runs on whole tiles only.  The heuristic takes it for such
                                      shapes when nothing else is forced */
+    CONV2D_LOADER_PAIR_HALO = 10  /* stride 1 on clusters of two CTAs: each CTA holds 128 consecutive pixels of
+                                     one image seen with the padded row pitch W + 2*pad_w (pixels past Q are
+                                     computed and discarded), the pair the same pixels of two images; per
+                                     64-channel chunk one tiled TMA box of whole padded input rows serves every
+                                     filter tap, read in place by 2-CTA tensor-core MMAs, and the weights of
+                                     two taps come in one box per stage.  Needs groups == 1, stride 1,
+                                     C % 64 == 0, K % 4 == 0, W + 2*pad_w <= 256 and the two halo buffers within
+                                     shared memory; block_m is 256 (or 0); grid counts CTA pairs */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".

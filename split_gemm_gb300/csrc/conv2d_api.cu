@@ -43,6 +43,12 @@ extern template SGB_PAIR_RES_SIG(256, 1);
 extern template SGB_PAIR_RES_SIG(64, 2);
 extern template SGB_PAIR_RES_SIG(128, 2);
 extern template SGB_PAIR_RES_SIG(256, 2);
+extern template SGB_PAIR_HALO_SIG(64);
+extern template SGB_PAIR_HALO_SIG(128);
+extern template SGB_PAIR_HALO_SIG(256);
+extern template SGB_PAIR_HALO_RES_SIG(64);
+extern template SGB_PAIR_HALO_RES_SIG(128);
+extern template SGB_PAIR_HALO_RES_SIG(256);
 }  // namespace sgb
 
 namespace {
@@ -381,6 +387,11 @@ int64_t semaphore_capacity(const Shape& s)
     if (box_geometry(s, 128, &g) && g.m_tiles > m_tiles) m_tiles = g.m_tiles;
     HaloGeom h;
     if (halo_geometry(s, 64, &h) && h.m_tiles > m_tiles) m_tiles = h.m_tiles;
+    // CTA-pair halo loader: one semaphore per 128-pixel row-block of every image.
+    if (s.sh == 1 && s.sw == 1 && s.w + 2 * s.pw <= 256 && s.p >= 1) {
+        const int64_t rb = s.n * cdiv(s.p * (s.w + 2 * s.pw), kMinTileM);
+        if (rb > m_tiles) m_tiles = rb;
+    }
     return m_tiles * s.g * cdiv(s.kg, 64);
 }
 
@@ -541,6 +552,100 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     return CONV2D_OK;
 }
 
+// The CTA-pair halo loader: geometry (row pitch, row-blocks, halo rows and
+// bytes) for tile width bn, or false when the shape does not allow it.
+bool halo_pair_geometry(const Shape& s, int bn, HaloGeom* g)
+{
+    if (s.g != 1 || s.sh != 1 || s.sw != 1 || s.c % BK != 0 || s.k % 4 != 0 || s.p < 1) return false;
+    const int64_t wv = s.w + 2 * s.pw;
+    if (wv > 256) return false;
+    const int64_t vp = s.p * wv;
+    const int64_t max_row = (wv - 1) + (s.r - 1) * s.dh * wv + (s.s - 1) * s.dw + (sgb::PAIR_ROWS - 1);
+    const int64_t hr = max_row / wv + 1;
+    if (hr > 256) return false;
+    const int64_t halo_bytes = (hr * wv * 128 + 1023) / 1024 * 1024;
+    int smem;
+    if (bn == 64) smem = sgb::conv2d_pair_halo_smem_bytes<64>(static_cast<int>(halo_bytes));
+    else if (bn == 128) smem = sgb::conv2d_pair_halo_smem_bytes<128>(static_cast<int>(halo_bytes));
+    else if (bn == 256) smem = sgb::conv2d_pair_halo_smem_bytes<256>(static_cast<int>(halo_bytes));
+    else return false;
+    if (smem > sgb::kMaxSmemBytes) return false;
+    const int64_t tpi = cdiv(vp, sgb::PAIR_ROWS);
+    if (s.n * tpi > 2147483647ll / 1024) return false;
+    g->wv = static_cast<int>(wv);
+    g->vp = static_cast<int>(vp);
+    g->tpi = static_cast<int>(tpi);
+    g->hr = static_cast<int>(hr);
+    g->halo_bytes = static_cast<int>(halo_bytes);
+    g->m_tiles = cdiv(s.n, 2) * tpi;  // a tile is one row-block of two images
+    return true;
+}
+
+int pair_halo_max_resident(int bn, bool fused, int halo_bytes)
+{
+    if (bn == 64) return sgb::conv2d_pair_halo_max_resident<64>(fused, sgb::conv2d_pair_halo_smem_bytes<64>(halo_bytes));
+    if (bn == 128)
+        return sgb::conv2d_pair_halo_max_resident<128>(fused, sgb::conv2d_pair_halo_smem_bytes<128>(halo_bytes));
+    if (bn == 256)
+        return sgb::conv2d_pair_halo_max_resident<256>(fused, sgb::conv2d_pair_halo_smem_bytes<256>(halo_bytes));
+    return 0;
+}
+
+int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
+{
+    if (force && force->block_m != 0 && force->block_m != sgb::PAIR_TILE_M) return CONV2D_ERR_UNSUPPORTED;
+    int bn = force && force->block_n ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+    if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
+    HaloGeom g;
+    if (!halo_pair_geometry(s, bn, &g)) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t m_tiles = g.m_tiles;
+    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t tiles = m_tiles * n_tiles;
+    const int64_t stages = (s.c / BK) * cdiv(s.r * s.s, 2);  // chunk-major, two taps per stage
+    const int64_t units = tiles * stages;
+    const int64_t resident = pair_halo_max_resident(bn, whole_tiles, g.halo_bytes);
+    if (resident <= 0) return CONV2D_ERR_CUDA;
+    const int64_t fsplits = force ? force->splits : 0;
+    const int64_t fgrid = force ? force->grid : 0;
+    if (fsplits < 0 || fgrid < 0 || (fsplits > 0 && fgrid > 0)) return CONV2D_ERR_INVALID;
+    int64_t grid;
+    if (fsplits > 0) {
+        if (fsplits > stages) return CONV2D_ERR_UNSUPPORTED;
+        grid = tiles * fsplits;
+    } else if (fgrid > 0) {
+        if (fgrid > units) return CONV2D_ERR_UNSUPPORTED;
+        grid = fgrid;
+    } else if (!whole_tiles && units * 2 >= kPairStreamKStages * PAIR_KBS_NORM * resident) {
+        grid = resident;
+    } else {
+        const int64_t per = cdiv(tiles, resident);
+        grid = tiles;
+        for (int64_t d = per; d <= 2 * per; ++d)
+            if (tiles % d == 0) {
+                grid = tiles / d;
+                break;
+            }
+    }
+    if ((units + 1) * (grid + 1) >= (int64_t(1) << 31)) return CONV2D_ERR_UNSUPPORTED;
+    plan->block_m = sgb::PAIR_TILE_M;
+    plan->block_n = bn;
+    plan->splits = static_cast<int>(fsplits);
+    plan->loader = CONV2D_LOADER_PAIR_HALO;
+    plan->m_tiles = static_cast<int>(m_tiles);
+    plan->n_tiles = static_cast<int>(n_tiles);
+    plan->num_kb = static_cast<int>(stages);
+    plan->grid = static_cast<int>(grid);
+    plan->units = units;
+    plan->box = BoxGeom{};
+    plan->halo = g;
+    plan->kbs = 2;
+    if (plan_cuts_tiles(*plan)) {
+        if (grid > resident) return CONV2D_ERR_UNSUPPORTED;
+        if (whole_tiles) return CONV2D_ERR_UNSUPPORTED;
+    }
+    return CONV2D_OK;
+}
+
 int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles = false)
 {
     const int sms = sm_count_current();
@@ -572,6 +677,8 @@ int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole
         if (!halo_geometry(s, 64, &g)) return CONV2D_ERR_UNSUPPORTED;
     } else if (loader == CONV2D_LOADER_TMA_PAIR) {
         return choose_pair_plan(s, force, plan, whole_tiles);
+    } else if (loader == CONV2D_LOADER_PAIR_HALO) {
+        return choose_pair_halo_plan(s, force, plan, whole_tiles);
     } else if (loader != CONV2D_LOADER_SCALAR) {
         return CONV2D_ERR_INVALID;
     }
@@ -736,6 +843,30 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     std::memset(tm_a, 0, sizeof(*tm_a));
     std::memset(tm_b, 0, sizeof(*tm_b));
     if (!load_encoders()) return CONV2D_ERR_CUDA;
+    if (plan.loader == CONV2D_LOADER_PAIR_HALO) {
+        // A: x as {C, W, H, N}; a box is one 64-channel chunk of hr whole padded rows (wv columns
+        // from -pad_w), landing pixel-major in 128-byte rows.  B: w as {64, K, C/64, R*S}; a box
+        // is block_n/2 weight rows of one chunk at two consecutive taps (a tap past R*S reads zeros).
+        const HaloGeom& g = plan.halo;
+        const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
+        const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
+                                       (cuuint64_t)(s.h * s.w * s.c * 2)};
+        const cuuint32_t box[4] = {(cuuint32_t)BK, (cuuint32_t)g.wv, (cuuint32_t)g.hr, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult rc = g_encode_tiled(tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides,
+                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        const cuuint64_t wd[4] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.c / BK), (cuuint64_t)(s.r * s.s)};
+        const cuuint64_t ws[3] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2), (cuuint64_t)(s.c * 2)};
+        const cuuint32_t wb[4] = {(cuuint32_t)BK, (cuuint32_t)(plan.block_n / 2), 1, 2};
+        const cuuint32_t we[4] = {1, 1, 1, 1};
+        rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), wd, ws, wb, we,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
     if (plan.loader == CONV2D_LOADER_TMA_PAIR) {
         // A: each CTA's 128 pixels x 64 channels per im2col load (window origins as for the
         // one-CTA loader).  B: w viewed as {64, K, C*R*S/64}; a box is block_n/2 weight rows x
@@ -867,7 +998,7 @@ MapKey make_map_key(const Shape& s, const Plan& plan, const void* x, const void*
     k.block_n = plan.block_n;
     if (plan.loader == CONV2D_LOADER_TMA_PAIR) k.kbs = plan.kbs;
     if (plan.loader == CONV2D_LOADER_TMA_BOX) k.box = plan.box;
-    if (plan.loader == CONV2D_LOADER_HALO) k.halo = plan.halo;
+    if (plan.loader == CONV2D_LOADER_HALO || plan.loader == CONV2D_LOADER_PAIR_HALO) k.halo = plan.halo;
     k.x = x;
     k.w = w;
     k.device = device;
@@ -1141,7 +1272,18 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
 #ifdef SGB_TRACE_ENABLED
     kp.trace = g_trace;
 #endif
-    if (plan.loader == CONV2D_LOADER_TMA_PAIR) {
+    if (plan.loader == CONV2D_LOADER_PAIR_HALO) {
+        kp.wv = plan.halo.wv;
+        kp.vp = plan.halo.vp;
+        kp.tpi = plan.halo.tpi;
+        kp.halo_rows = plan.halo.hr;
+        kp.halo_bytes = plan.halo.halo_bytes;
+        kp.halo_tx = plan.halo.hr * plan.halo.wv * 128;
+        kp.fd_tpi = sgb::FastDiv(static_cast<uint32_t>(plan.halo.tpi));
+        kp.fd_wv = sgb::FastDiv(static_cast<uint32_t>(plan.halo.wv));
+        kp.fd_tapst = sgb::FastDiv(static_cast<uint32_t>(cdiv(s.r * s.s, 2)));
+    }
+    if (plan.loader == CONV2D_LOADER_TMA_PAIR || plan.loader == CONV2D_LOADER_PAIR_HALO) {
         kp.fd_grid = sgb::FastDiv(static_cast<uint32_t>(plan.grid));
         kp.fd_units = sgb::FastDiv(static_cast<uint32_t>(plan.units));
         kp.fd_nkb = sgb::FastDiv(static_cast<uint32_t>(plan.num_kb));
@@ -1160,6 +1302,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     cudaError_t err;
     if (plan.loader == CONV2D_LOADER_TMA_PAIR)
         err = launch_pair(plan.block_n, plan.kbs, tm_a, tm_b, kp, (int)grid, stream);
+    else if (plan.loader == CONV2D_LOADER_PAIR_HALO)
+        err = plan.block_n == 64    ? sgb::launch_conv2d_pair_halo<64>(tm_a, tm_b, kp, (int)grid, stream)
+              : plan.block_n == 128 ? sgb::launch_conv2d_pair_halo<128>(tm_a, tm_b, kp, (int)grid, stream)
+                                    : sgb::launch_conv2d_pair_halo<256>(tm_a, tm_b, kp, (int)grid, stream);
     else
         err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, kp, (int)grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;

@@ -166,6 +166,9 @@ struct ConvKernelParams {
     // CTA-pair kernel: divisions by the loop-invariant sizes (grid = pairs,
     // units, stages per tile, column blocks, P*Q, Q, C, S).
     FastDiv fd_grid, fd_units, fd_nkb, fd_ntiles, fd_pq, fd_q, fd_c, fd_s;
+    // CTA-pair halo loader: row-blocks per image, the padded row pitch, and
+    // two-tap weight stages per 64-channel chunk (tap_stages = ceil(R*S / 2)).
+    FastDiv fd_tpi, fd_wv, fd_tapst;
 };
 
 

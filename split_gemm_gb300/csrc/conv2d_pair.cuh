@@ -100,6 +100,9 @@ struct PairSmem {
     uint64_t* acc_full;  // 2 (both)
     uint64_t* acc_empty; // 2 (leader)
     uint64_t* mma_done;  // 1 (leader)
+    uint8_t* halo;         // halo loader: 2 buffers of kp.halo_bytes
+    uint64_t* halo_full;   // 2 (leader): both CTAs' halo landed
+    uint64_t* halo_empty;  // 2 (both): no MMA reads the buffer any more
     uint32_t* tmem_slot;
     volatile uint32_t* abort_flag;
     volatile uint32_t* epi_go;
@@ -325,12 +328,16 @@ __device__ void pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_
         __syncwarp();
         ptx::tc_fence_after();
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * BN);
+        // The whole warp runs the stage loop (uniform control flow, no shared-memory
+        // access between MMAs: such an access would wait for the queued MMAs to
+        // drain); one elected lane issues each MMA and commit.
+        const bool go = __shfl_sync(0xffffffffu, issue ? 1 : 0, 0) != 0;
         for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
             const int slot = it % STAGES;
             ptx::named_bar_sync(STAGE_BAR0 + slot, 64);
             ptx::tc_fence_after();
             if (lane == 0) SGB_PAIR_MARK(kp, it, 3);
-            if (lane == 0 && issue && !*sm.abort_flag) {
+            if (go) {
                 const int nkb = kb_total - st * KBS < KBS ? kb_total - st * KBS : KBS;
                 const uint64_t ad = a_desc0 + static_cast<uint64_t>((slot * Cfg::A_STAGE) >> 4);
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((slot * Cfg::B_STAGE) >> 4);
@@ -339,25 +346,23 @@ __device__ void pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_
                     if (j < nkb) {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
-                            ptx::mma_bf16_pair(tmem_d, ad + static_cast<uint64_t>((j * Cfg::A_KB + k * UMMA_K * 2) >> 4),
-                                               bd + static_cast<uint64_t>((j * Cfg::B_KB + k * UMMA_K * 2) >> 4),
-                                               Cfg::IDESC, (st > sg.kb_begin || j > 0 || k > 0) ? 1u : 0u);
+                            ptx::mma_bf16_pair_elect(tmem_d,
+                                                     ad + static_cast<uint64_t>((j * Cfg::A_KB + k * UMMA_K * 2) >> 4),
+                                                     bd + static_cast<uint64_t>((j * Cfg::B_KB + k * UMMA_K * 2) >> 4),
+                                                     Cfg::IDESC, (st > sg.kb_begin || j > 0 || k > 0) ? 1u : 0u);
                     }
                 }
             }
-            if (lane == 0) ptx::mma_commit_pair(&sm.empty[slot], 0x3);  // every stage, issuing or not
+            ptx::mma_commit_pair_elect(&sm.empty[slot], 0x3);  // every stage, issuing or not
             if (lane == 0) SGB_PAIR_MARK(kp, it, 4);
-            __syncwarp();
         }
-        if (lane == 0) ptx::mma_commit_pair(&sm.acc_full[buf], 0x3);
+        ptx::mma_commit_pair_elect(&sm.acc_full[buf], 0x3);
         __syncwarp();
         ++seg_idx;
     }
     // No MMA may be in flight when the pair reaches its teardown.
-    if (lane == 0) {
-        ptx::mma_commit_pair(sm.mma_done, 0x1);
-        ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
-    }
+    ptx::mma_commit_pair_elect(sm.mma_done, 0x1);  // the lane that issued the MMAs
+    if (lane == 0) ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
     __syncwarp();
 }
 
@@ -392,9 +397,47 @@ __device__ __forceinline__ void pair_pass_turn(const ConvKernelParams& kp, int s
     ptx::st_release_gpu(kp.sems + sem, next);
 }
 
+// The output rows of this CTA's half of a tile.  im2col loader: GEMM rows
+// m_tile*256 + rank*128 + r.  Halo loader: virtual pixels j0 + r of image
+// 2*i + rank, where row-block m_tile = i*tpi + b starts at j0 = 128*b; virtual
+// pixel j = p*wv + v is output pixel (p, v) when v < Q.
+template <bool HALO>
+struct PairRows {
+    int base;   // first GEMM row (im2col) or first virtual pixel (halo)
+    int n_img;  // halo: the image
+    bool any;   // the half holds at least one output row
+    __device__ __forceinline__ PairRows(const ConvKernelParams& kp, int m_tile, uint32_t rank)
+    {
+        if (HALO) {
+            const int i = static_cast<int>(kp.fd_tpi.div(static_cast<uint32_t>(m_tile)));
+            base = (m_tile - i * kp.tpi) * PAIR_ROWS;
+            n_img = 2 * i + static_cast<int>(rank);
+            any = n_img < kp.N;
+        } else {
+            base = m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS;
+            n_img = 0;
+            any = base < kp.M;
+        }
+    }
+    // GEMM row (output pixel) of row r of the half, or -1.
+    __device__ __forceinline__ int m(const ConvKernelParams& kp, int r) const
+    {
+        if (HALO) {
+            const int j = base + r;
+            if (j >= kp.vp) return -1;
+            const int p = static_cast<int>(kp.fd_wv.div(static_cast<uint32_t>(j)));
+            const int q = j - p * kp.wv;
+            if (q >= kp.Q || n_img >= kp.N) return -1;
+            return (n_img * kp.P + p) * kp.Q + q;
+        }
+        const int mm = base + r;
+        return mm < kp.M ? mm : -1;
+    }
+};
+
 // Zeroes this CTA's rows of every cut tile whose split 0 this pair owns, then
 // publishes them (all epilogue threads take part; one barrier).
-template <int BN>
+template <int BN, bool HALO>
 __device__ void pair_zero_cut_tiles(const ConvKernelParams& kp, uint32_t rank, int pair, int et)
 {
     constexpr int EPI_T = PairConfig<BN, 1>::EPI_T;
@@ -405,16 +448,17 @@ __device__ void pair_zero_cut_tiles(const ConvKernelParams& kp, uint32_t rank, i
         if (sg.nsplits < 2 || sg.split != 0) continue;
         int m_tile, n_tile;
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-        const int row0 = m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS;
-        if (row0 >= kp.M) continue;
+        const PairRows<HALO> rows(kp, m_tile, rank);
+        if (!rows.any) continue;
         const int n0 = n_tile * BN;
         const int vecs = ((n0 + BN < kp.K ? n0 + BN : kp.K) - n0) / 4;  // float4 per row (K % 4 == 0)
-        const int rows = kp.M - row0 < PAIR_ROWS ? kp.M - row0 : PAIR_ROWS;
-        for (int i = et; i < rows * vecs; i += EPI_T) {
+        for (int i = et; i < PAIR_ROWS * vecs; i += EPI_T) {
             const int r = i / vecs;
             const int v = i - r * vecs;
-            *reinterpret_cast<float4*>(kp.y + static_cast<int64_t>(row0 + r) * kp.ldy + n0 + 4 * v) =
-                make_float4(0.f, 0.f, 0.f, 0.f);
+            const int m = rows.m(kp, r);
+            if (m >= 0)
+                *reinterpret_cast<float4*>(kp.y + static_cast<int64_t>(m) * kp.ldy + n0 + 4 * v) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
         }
         any = true;
     }
@@ -426,13 +470,13 @@ __device__ void pair_zero_cut_tiles(const ConvKernelParams& kp, uint32_t rank, i
             if (sg.nsplits < 2 || sg.split != 0) continue;
             int m_tile, n_tile;
             pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-            if (m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS >= kp.M) continue;
+            if (!PairRows<HALO>(kp, m_tile, rank).any) continue;
             ptx::st_release_gpu(kp.sems + pair_sem_index(kp, m_tile, rank, n_tile), 1u);
         }
     }
 }
 
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, bool HALO>
 __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, uint32_t rank,
                               int pair)
 {
@@ -447,7 +491,7 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
     const int chunk = lane & 7;
     const uint32_t saddr = ptx::smem_addr(sm.epi + ew * EPI_SLOT_BYTES);
     const uint32_t acc_empty0 = ptx::mapa_shared(ptx::smem_addr(sm.acc_empty), 0u);  // the leader's
-    if (!FUSED) pair_zero_cut_tiles<BN>(kp, rank, pair, et);  // fused plans cut no tiles
+    if (!FUSED) pair_zero_cut_tiles<BN, HALO>(kp, rank, pair, et);  // fused plans cut no tiles
     int seg_idx = 0;
     PairWalker walk(kp, pair);
     Segment sg;
@@ -456,8 +500,8 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
         int m_tile, n_tile;
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-        const int row0 = m_tile * PAIR_TILE_M + static_cast<int>(rank) * PAIR_ROWS;
-        const bool has_rows = row0 < kp.M;  // a half past the output stores nothing and takes no turn
+        const PairRows<HALO> rows(kp, m_tile, rank);
+        const bool has_rows = rows.any;  // a half past the output stores nothing and takes no turn
         const int n0 = n_tile * BN;
         const int n_end = n0 + BN < kp.K ? n0 + BN : kp.K;
         const int sem = pair_sem_index(kp, m_tile, rank, n_tile);
@@ -487,10 +531,7 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         ptx::tc_fence_after();
         int mrow[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int m = row0 + quad * 32 + 4 * i + rsub;
-            mrow[i] = m < kp.M ? m : -1;
-        }
+        for (int i = 0; i < 8; ++i) mrow[i] = rows.m(kp, quad * 32 + 4 * i + rsub);
         const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
         for (int j = 0; j < SLABS; ++j) {
@@ -562,6 +603,9 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
     sm.acc_full = sm.empty + Cfg::STAGES;
     sm.acc_empty = sm.acc_full + 2;
     sm.mma_done = sm.acc_empty + 2;
+    sm.halo = nullptr;
+    sm.halo_full = nullptr;
+    sm.halo_empty = nullptr;
     sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.mma_done + 1);
     sm.abort_flag = sm.tmem_slot + 1;
     sm.epi_go = sm.tmem_slot + 2;
@@ -618,7 +662,7 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
     } else if (warp == 1) {
         if (rank == 0) pair_mma<BN, KBS>(kp, sm, tmem_base, pair);
     } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
-        pair_epilogue<BN, FUSED>(kp, sm, tmem_base, rank, pair);
+        pair_epilogue<BN, FUSED, false>(kp, sm, tmem_base, rank, pair);
     } else if (warp == WAITER_WARP) {
         if (rank == 0) pair_waiter<BN, KBS>(kp, sm, pair);
     }
@@ -632,6 +676,353 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
     }
     SGB_TRACE(kp, threadIdx.x == 0, 10);
 }
+
+// ---------------------------------------------------------------- halo loader on CTA pairs
+// Stride 1.  A CTA's 128 GEMM rows are 128 consecutive virtual pixels of one
+// image seen with the padded row pitch wv = W + 2*pw (virtual pixel j = p*wv + v
+// is output pixel (p, v) when v < Q; the others are computed and discarded),
+// and the pair takes the same block of images 2i and 2i+1, so that both CTAs'
+// operands sit at the same shared-memory offsets, as the 2-CTA MMA requires.
+// For each 64-channel chunk one tiled TMA box of whole padded input rows (zero
+// fill gives the padding) serves all R*S filter taps: tap (r, s) reads its 128
+// A rows in place, r*dh*wv + s*dw rows into the buffer (the 128-byte swizzle
+// follows absolute shared-memory addresses, so any start row works).  The
+// weight rows of two taps of one chunk come in one 4-D box per stage; the
+// reduction runs chunk-major, then over the taps two at a time.  Per k-block
+// this is about 0.1 TMA operation of activations (against one for the im2col
+// loader) and half an operation of weights.
+template <int BN>
+struct HaloPairConfig {
+    static constexpr int B_ROWS = BN / 2;
+    static constexpr int B_KB = B_ROWS * BK * 2;      // one tap's weight rows of this CTA
+    static constexpr int TAPS = 2;                    // taps (k-blocks) per stage
+    static constexpr int B_STAGE = TAPS * B_KB;
+    static constexpr int STAGES = 4;
+    static constexpr int RING = STAGES * B_STAGE;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_SLOT_BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 9) * 8 + 16;
+    static constexpr int FIXED_SMEM = RING + EPI_BYTES + BAR_BYTES + 1024;  // + the two halo buffers
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr int THREADS = (WAITER_WARP + 2) * 32;  // warps 0 .. 11
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR_TILE_M, BN);
+};
+
+// Chunk and first tap of stage st of a tile.
+__device__ __forceinline__ void halo_stage(const ConvKernelParams& kp, int st, int& chunk, int& tap0)
+{
+    chunk = static_cast<int>(kp.fd_tapst.div(static_cast<uint32_t>(st)));
+    tap0 = 2 * (st - chunk * static_cast<int>(kp.fd_tapst.d));
+}
+
+// First virtual pixel of the CTA's row-block and the first padded input row its halo holds.
+__device__ __forceinline__ void halo_block(const ConvKernelParams& kp, int m_tile, uint32_t rank, int& n_img, int& j0,
+                                           int& prow0)
+{
+    const int i = static_cast<int>(kp.fd_tpi.div(static_cast<uint32_t>(m_tile)));
+    j0 = (m_tile - i * kp.tpi) * PAIR_ROWS;
+    n_img = 2 * i + static_cast<int>(rank);
+    prow0 = static_cast<int>(kp.fd_wv.div(static_cast<uint32_t>(j0)));
+}
+
+// A halo use starts at a chunk's first stage or a segment's first stage and ends
+// at the chunk's last stage or the segment's last stage.
+__device__ __forceinline__ bool halo_use_starts(const Segment& sg, int st, int tap0) { return st == sg.kb_begin || tap0 == 0; }
+__device__ __forceinline__ bool halo_use_ends(const ConvKernelParams& kp, const Segment& sg, int st, int tap0)
+{
+    return st + 1 == sg.kb_end || tap0 + 2 >= kp.R * kp.S;
+}
+
+// Producer of the halos (warp 0, one thread, both CTAs).
+template <int BN>
+__device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelParams& kp, const PairSmem& sm,
+                                     uint32_t rank, int pair)
+{
+    const uint32_t hfull0 = ptx::mapa_shared(ptx::smem_addr(sm.halo_full), 0u);  // the leader's
+    int h = 0;  // halo uses issued
+    bool ok = true;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        int n_img, j0, prow0;
+        halo_block(kp, m_tile, rank, n_img, j0, prow0);
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st) {
+            int chunk, tap0;
+            halo_stage(kp, st, chunk, tap0);
+            if (!halo_use_starts(sg, st, tap0)) continue;
+            if (*sm.abort_flag) { ok = false; break; }
+            const int slot = h & 1;
+            if (!ptx::mbar_wait_spin(&sm.halo_empty[slot], (static_cast<uint32_t>(h >> 1) & 1u) ^ 1u, kp.wait_limit_ns)) {
+                pair_record_timeout(kp, sm, rank);
+                ok = false;
+                break;
+            }
+            if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.halo_full[slot], 2u * static_cast<uint32_t>(kp.halo_tx));
+            ptx::tma_load_4d_pair(sm.halo + slot * kp.halo_bytes, tm_a, hfull0 + static_cast<uint32_t>(slot) * 8u,
+                                  chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
+            SGB_PAIR_MARK(kp, 200 + h, static_cast<int>(rank));
+            ++h;
+        }
+    }
+    // Drain: each buffer's last use has been released by the MMA (so it landed).
+    for (int i = h > 2 ? h - 2 : 0; i < h; ++i)
+        ptx::mbar_wait(&sm.halo_empty[i & 1], static_cast<uint32_t>(i >> 1) & 1u, kp.wait_limit_ns);
+}
+
+// Producer of the weight stages (warp 11, one thread, both CTAs).
+template <int BN>
+__device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelParams& kp, const PairSmem& sm,
+                                     uint32_t rank, int pair)
+{
+    using Cfg = HaloPairConfig<BN>;
+    constexpr int STAGES = Cfg::STAGES;
+    const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(sm.full), 0u);
+    int it = 0;
+    bool ok = true;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (ok && walk.next(kp, sg)) {
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            if (*sm.abort_flag) { ok = false; break; }
+            if (!ptx::mbar_wait_spin(&sm.empty[slot], (static_cast<uint32_t>(it / STAGES) & 1u) ^ 1u, kp.wait_limit_ns)) {
+                pair_record_timeout(kp, sm, rank);
+                ok = false;
+                break;
+            }
+            int chunk, tap0;
+            halo_stage(kp, st, chunk, tap0);
+            // The box always counts two taps (a tap past R*S reads zeros).
+            if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(Cfg::B_STAGE));
+            ptx::tma_load_4d_pair(sm.b + slot * Cfg::B_STAGE, tm_b, full0 + static_cast<uint32_t>(slot) * 8u, 0, b_row,
+                                  chunk, tap0);
+            SGB_PAIR_MARK(kp, it, 5 + static_cast<int>(rank));
+        }
+    }
+    for (int i = it > STAGES ? it - STAGES : 0; i < it; ++i)
+        ptx::mbar_wait(&sm.empty[i % STAGES], static_cast<uint32_t>(i / STAGES) & 1u, kp.wait_limit_ns);
+}
+
+// Stage waiter (warp 10, leader): the chunk's halo, then the stage's weights.
+template <int BN>
+__device__ void halo_pair_waiter(const ConvKernelParams& kp, const PairSmem& sm, int pair)
+{
+    constexpr int STAGES = HaloPairConfig<BN>::STAGES;
+    const int lane = threadIdx.x & 31;
+    bool waiting = true;
+    int it = 0, h = 0;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            const uint32_t use = static_cast<uint32_t>(it / STAGES);
+            int chunk, tap0;
+            halo_stage(kp, st, chunk, tap0);
+            if (lane == 0) {
+                if (halo_use_starts(sg, st, tap0)) {
+                    if (waiting && (*sm.abort_flag ||
+                                    !ptx::mbar_wait_spin(&sm.halo_full[h & 1], static_cast<uint32_t>(h >> 1) & 1u,
+                                                         kp.wait_limit_ns))) {
+                        pair_record_timeout(kp, sm, 0u);
+                        waiting = false;
+                    }
+                    ++h;
+                }
+                if (waiting && (*sm.abort_flag || !ptx::mbar_wait_spin(&sm.full[slot], use & 1u, kp.wait_limit_ns))) {
+                    pair_record_timeout(kp, sm, 0u);
+                    waiting = false;
+                }
+                // After a timeout: pace the MMA warp by its own release of the previous use.
+                if (!waiting && use > 0)
+                    for (int t = 0; t < 16 && !ptx::mbar_wait(&sm.empty[slot], (use - 1u) & 1u, kp.wait_limit_ns); ++t) {
+                    }
+                SGB_PAIR_MARK(kp, it, 2);
+            }
+            __syncwarp();
+            ptx::named_bar_arrive(STAGE_BAR0 + slot, 64);
+        }
+    }
+}
+
+// MMA issuer (warp 1, leader).
+template <int BN>
+__device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, int pair)
+{
+    using Cfg = HaloPairConfig<BN>;
+    constexpr int STAGES = Cfg::STAGES;
+    const int lane = threadIdx.x & 31;
+    const int taps = kp.R * kp.S;
+    const uint64_t halo_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.halo));
+    const uint64_t b_desc0 = ptx::sw128_kmajor_desc(ptx::smem_addr(sm.b));
+    int it = 0, seg_idx = 0, h = 0;
+    bool issue = true;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    while (walk.next(kp, sg)) {
+        const int buf = seg_idx & 1;
+        const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+        if (lane == 0 && issue) {
+            if (*sm.abort_flag || !ptx::mbar_wait(&sm.acc_empty[buf], use ^ 1u, kp.wait_limit_ns)) {
+                pair_record_timeout(kp, sm, 0u);
+                issue = false;
+            }
+        }
+        __syncwarp();
+        ptx::tc_fence_after();
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(buf * BN);
+        const bool go = __shfl_sync(0xffffffffu, issue ? 1 : 0, 0) != 0;
+        int m_tile, n_tile;
+        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+        int n_img, j0, prow0;
+        halo_block(kp, m_tile, 0u, n_img, j0, prow0);
+        const int a0 = j0 - prow0 * kp.wv;  // the same in both CTAs
+        for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
+            const int slot = it % STAGES;
+            int chunk, tap0;
+            halo_stage(kp, st, chunk, tap0);
+            if (halo_use_starts(sg, st, tap0)) ++h;
+            const int hslot = (h - 1) & 1;
+            const bool hlast = halo_use_ends(kp, sg, st, tap0);
+            ptx::named_bar_sync(STAGE_BAR0 + slot, 64);
+            ptx::tc_fence_after();
+            if (lane == 0) SGB_PAIR_MARK(kp, it, 3);
+            if (go) {  // warp-uniform; one elected lane issues (see pair_mma)
+#pragma unroll
+                for (int jt = 0; jt < Cfg::TAPS; ++jt) {
+                    const int tap = tap0 + jt;
+                    if (tap < taps) {
+                        const int r = static_cast<int>(kp.fd_s.div(static_cast<uint32_t>(tap)));
+                        const int sx = tap - r * kp.S;
+                        const int a_row = a0 + r * kp.dh * kp.wv + sx * kp.dw;
+                        const uint64_t ad =
+                            halo_desc0 + static_cast<uint64_t>((hslot * kp.halo_bytes + a_row * 128) >> 4);
+                        const uint64_t bd = b_desc0 + static_cast<uint64_t>((slot * Cfg::B_STAGE + jt * Cfg::B_KB) >> 4);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            ptx::mma_bf16_pair_elect(tmem_d, ad + static_cast<uint64_t>((k * UMMA_K * 2) >> 4),
+                                                     bd + static_cast<uint64_t>((k * UMMA_K * 2) >> 4), Cfg::IDESC,
+                                                     (st > sg.kb_begin || jt > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+            }
+            ptx::mma_commit_pair_elect(&sm.empty[slot], 0x3);  // every stage, issuing or not
+            if (hlast) ptx::mma_commit_pair_elect(&sm.halo_empty[hslot], 0x3);
+            if (lane == 0) SGB_PAIR_MARK(kp, it, 4);
+        }
+        ptx::mma_commit_pair_elect(&sm.acc_full[buf], 0x3);
+        __syncwarp();
+        ++seg_idx;
+    }
+    ptx::mma_commit_pair_elect(sm.mma_done, 0x1);  // the lane that issued the MMAs
+    if (lane == 0) ptx::mbar_wait(sm.mma_done, 0u, kp.wait_limit_ns);
+    __syncwarp();
+}
+
+template <int BN, bool FUSED>
+__global__ void __launch_bounds__(HaloPairConfig<BN>::THREADS, 1)
+    conv2d_fwd_pair_halo_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                                const ConvKernelParams kp)
+{
+    using Cfg = HaloPairConfig<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairSmem sm;
+    sm.a = nullptr;
+    sm.b = smem;
+    sm.halo = smem + Cfg::RING;  // 2 buffers of kp.halo_bytes (1024-byte multiples)
+    sm.epi = sm.halo + 2 * kp.halo_bytes;
+    sm.full = reinterpret_cast<uint64_t*>(sm.epi + Cfg::EPI_BYTES);
+    sm.empty = sm.full + Cfg::STAGES;
+    sm.acc_full = sm.empty + Cfg::STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.mma_done = sm.acc_empty + 2;
+    sm.halo_full = sm.mma_done + 1;
+    sm.halo_empty = sm.halo_full + 2;
+    sm.tmem_slot = reinterpret_cast<uint32_t*>(sm.halo_empty + 2);
+    sm.abort_flag = sm.tmem_slot + 1;
+    sm.epi_go = sm.tmem_slot + 2;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int pair = static_cast<int>(ptx::cluster_id_x());
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Cfg::STAGES; ++i) {
+            ptx::mbar_init(&sm.full[i], 1);   // the leader's weight producer (expecting both CTAs' bytes)
+            ptx::mbar_init(&sm.empty[i], 1);  // the leader's MMA commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sm.acc_full[i], 1);
+            ptx::mbar_init(&sm.acc_empty[i], 2 * Cfg::EPI_WARPS);
+            ptx::mbar_init(&sm.halo_full[i], 1);   // the leader's halo producer
+            ptx::mbar_init(&sm.halo_empty[i], 1);  // the leader's MMA commit
+        }
+        ptx::mbar_init(sm.mma_done, 1);
+        *sm.abort_flag = 0u;
+        *sm.epi_go = 0u;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_a);
+        ptx::prefetch_tensormap(&tm_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(sm.tmem_slot, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *sm.tmem_slot;
+    SGB_TRACE(kp, threadIdx.x == 0, 0);
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+    SGB_TRACE(kp, threadIdx.x == 0, 1);
+
+    if (warp == 0) {
+        if (lane == 0) halo_pair_producer_a<BN>(&tm_a, kp, sm, rank, pair);
+    } else if (warp == WAITER_WARP + 1) {
+        if (lane == 0) halo_pair_producer_b<BN>(&tm_b, kp, sm, rank, pair);
+    } else if (warp == 1) {
+        if (rank == 0) halo_pair_mma<BN>(kp, sm, tmem_base, pair);
+    } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
+        pair_epilogue<BN, FUSED, true>(kp, sm, tmem_base, rank, pair);
+    } else if (warp == WAITER_WARP) {
+        if (rank == 0) halo_pair_waiter<BN>(kp, sm, pair);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+    SGB_TRACE(kp, threadIdx.x == 0, 10);
+}
+
+template <int BN>
+cudaError_t launch_conv2d_pair_halo(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const ConvKernelParams& kp,
+                                    int pairs, cudaStream_t stream);
+template <int BN>
+int conv2d_pair_halo_max_resident(bool fused, int smem_bytes);
+template <int BN>
+inline int conv2d_pair_halo_smem_bytes(int halo_bytes)
+{
+    return HaloPairConfig<BN>::FIXED_SMEM + 2 * halo_bytes;
+}
+#define SGB_PAIR_HALO_SIG(BN_)                                                                                   \
+    cudaError_t launch_conv2d_pair_halo<BN_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, int, \
+                                             cudaStream_t)
+#define SGB_PAIR_HALO_RES_SIG(BN_) int conv2d_pair_halo_max_resident<BN_>(bool, int)
 
 // Host-side launcher: `pairs` clusters of two CTAs.
 template <int BN, int KBS>
