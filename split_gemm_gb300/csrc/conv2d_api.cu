@@ -43,12 +43,16 @@ extern template SGB_PAIR_RES_SIG(256, 1);
 extern template SGB_PAIR_RES_SIG(64, 2);
 extern template SGB_PAIR_RES_SIG(128, 2);
 extern template SGB_PAIR_RES_SIG(256, 2);
-extern template SGB_PAIR_HALO_SIG(64);
-extern template SGB_PAIR_HALO_SIG(128);
-extern template SGB_PAIR_HALO_SIG(256);
-extern template SGB_PAIR_HALO_RES_SIG(64);
-extern template SGB_PAIR_HALO_RES_SIG(128);
-extern template SGB_PAIR_HALO_RES_SIG(256);
+extern template SGB_PAIR_HALO_SIG(64, 2);
+extern template SGB_PAIR_HALO_SIG(64, 3);
+extern template SGB_PAIR_HALO_SIG(128, 2);
+extern template SGB_PAIR_HALO_SIG(128, 3);
+extern template SGB_PAIR_HALO_SIG(256, 2);
+extern template SGB_PAIR_HALO_RES_SIG(64, 2);
+extern template SGB_PAIR_HALO_RES_SIG(64, 3);
+extern template SGB_PAIR_HALO_RES_SIG(128, 2);
+extern template SGB_PAIR_HALO_RES_SIG(128, 3);
+extern template SGB_PAIR_HALO_RES_SIG(256, 2);
 }  // namespace sgb
 
 namespace {
@@ -327,9 +331,10 @@ bool rowwin_config(const Shape& s, int bn_force, RowWinCfg* o)
 // chunk, one tiled TMA box of hr whole padded input rows holds every filter
 // tap's operand (the kernel header describes the layout).
 struct HaloGeom {
-    int wv, vp, tpi, hr, halo_bytes;
     int64_t m_tiles;
-};
+    int wv, vp, tpi, hr, halo_bytes;
+    int taps;  // CTA-pair halo loader: filter taps per pipeline stage (0 otherwise)
+};  // no padding bytes: the tensor-map cache compares keys bytewise
 
 // Halo geometry for output-channel tile width bn, or false when the shape does
 // not allow the halo loader: stride 1, C % 64 == 0, a padded row of at most 256
@@ -361,6 +366,7 @@ bool halo_geometry(const Shape& s, int bn, HaloGeom* g)
     g->hr = static_cast<int>(hr);
     g->halo_bytes = static_cast<int>(halo_bytes);
     g->m_tiles = s.n * tpi;
+    g->taps = 0;
     return true;
 }
 
@@ -374,7 +380,8 @@ struct Plan {
     long long units;  // (tile, stage) work units
     BoxGeom box;      // box loader only
     HaloGeom halo;    // halo loader only
-    int kbs;          // CTA-pair loader only: 64-wide k-blocks per pipeline stage (1 or 2)
+    int kbs;          // CTA-pair loaders: 64-wide k-blocks (filter taps for the halo loader) per pipeline stage
+    int unit_offset;  // CTA-pair loaders only: rotation of the pairs' unit ranges
 };
 
 // Semaphores the workspace holds: one per tile of the smallest tiles any plan
@@ -487,6 +494,26 @@ constexpr int64_t kPairStreamKStages = 8;
 constexpr int64_t PAIR_KBS_NORM = 2;  // units count stages of kbs k-blocks; the threshold counts pairs of k-blocks
 constexpr int64_t PAIR_M_SLACK = 512;  // pixel indices up to one tile past M are decoded
 
+// Rotation of the pairs' unit ranges (see PairWalker): the offset d, 0 < d <
+// stages, for which no range [floor(c*U/G) + d, ...) starts on a tile boundary
+// (a multiple of `stages`), searched outward from half a range; 0 when the plan
+// cuts no tile or no offset works.
+int64_t choose_unit_offset(int64_t units, int64_t grid, int64_t stages)
+{
+    if (grid <= 1 || stages <= 1 || (units % grid == 0 && (units / grid) % stages == 0)) return 0;
+    auto ok = [&](int64_t d) {
+        for (int64_t c = 0; c < grid; ++c)
+            if ((c * units / grid + d) % stages == 0) return false;
+        return true;
+    };
+    const int64_t mid = units / grid / 2 < stages ? units / grid / 2 : stages / 2;
+    for (int64_t step = 0; step < stages; ++step) {
+        if (mid + step >= 1 && mid + step < stages && ok(mid + step)) return mid + step;
+        if (mid - step >= 1 && mid - step < stages && ok(mid - step)) return mid - step;
+    }
+    return 0;
+}
+
 int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
 {
     if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
@@ -529,7 +556,8 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
             }
     }
     // The kernel splits the work with 32-bit arithmetic (FastDiv, n < 2^31).
-    if ((units + 1) * (grid + 1) >= (int64_t(1) << 31) || s.m >= (int64_t(1) << 31) - PAIR_M_SLACK)
+    const int64_t offset = choose_unit_offset(units, grid, stages);
+    if ((units + offset + 1) * (grid + 1) >= (int64_t(1) << 31) || s.m >= (int64_t(1) << 31) - PAIR_M_SLACK)
         return CONV2D_ERR_UNSUPPORTED;
     plan->block_m = sgb::PAIR_TILE_M;
     plan->block_n = bn;
@@ -543,6 +571,7 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     plan->box = BoxGeom{};
     plan->halo = HaloGeom{};
     plan->kbs = kbs;
+    plan->unit_offset = static_cast<int>(offset);
     if (plan_cuts_tiles(*plan)) {
         // A later split waits for an earlier one: every pair must be resident at once.
         if (grid > resident) return CONV2D_ERR_UNSUPPORTED;
@@ -552,8 +581,26 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     return CONV2D_OK;
 }
 
+// Shared memory of the CTA-pair halo kernel for tile width bn, taps per stage
+// and halo buffer size (0 for a combination that is not instantiated).
+int pair_halo_smem(int bn, int taps, int halo_bytes)
+{
+    if (taps == 3) {
+        if (bn == 64) return sgb::conv2d_pair_halo_smem_bytes<64, 3>(halo_bytes);
+        if (bn == 128) return sgb::conv2d_pair_halo_smem_bytes<128, 3>(halo_bytes);
+        return 0;
+    }
+    if (taps != 2) return 0;
+    if (bn == 64) return sgb::conv2d_pair_halo_smem_bytes<64, 2>(halo_bytes);
+    if (bn == 128) return sgb::conv2d_pair_halo_smem_bytes<128, 2>(halo_bytes);
+    if (bn == 256) return sgb::conv2d_pair_halo_smem_bytes<256, 2>(halo_bytes);
+    return 0;
+}
+
 // The CTA-pair halo loader: geometry (row pitch, row-blocks, halo rows and
-// bytes) for tile width bn, or false when the shape does not allow it.
+// bytes, taps per stage) for tile width bn, or false when the shape does not
+// allow it.  Stages hold three taps where the ring still fits beside the two
+// halo buffers (64- and 128-wide tiles), else two.
 bool halo_pair_geometry(const Shape& s, int bn, HaloGeom* g)
 {
     if (s.g != 1 || s.sh != 1 || s.sw != 1 || s.c % BK != 0 || s.k % 4 != 0 || s.p < 1) return false;
@@ -564,12 +611,10 @@ bool halo_pair_geometry(const Shape& s, int bn, HaloGeom* g)
     const int64_t hr = max_row / wv + 1;
     if (hr > 256) return false;
     const int64_t halo_bytes = (hr * wv * 128 + 1023) / 1024 * 1024;
-    int smem;
-    if (bn == 64) smem = sgb::conv2d_pair_halo_smem_bytes<64>(static_cast<int>(halo_bytes));
-    else if (bn == 128) smem = sgb::conv2d_pair_halo_smem_bytes<128>(static_cast<int>(halo_bytes));
-    else if (bn == 256) smem = sgb::conv2d_pair_halo_smem_bytes<256>(static_cast<int>(halo_bytes));
-    else return false;
-    if (smem > sgb::kMaxSmemBytes) return false;
+    if (bn != 64 && bn != 128 && bn != 256) return false;
+    int taps = bn == 256 ? 2 : 3;
+    if (pair_halo_smem(bn, taps, static_cast<int>(halo_bytes)) > sgb::kMaxSmemBytes) taps = 2;
+    if (pair_halo_smem(bn, taps, static_cast<int>(halo_bytes)) > sgb::kMaxSmemBytes) return false;
     const int64_t tpi = cdiv(vp, sgb::PAIR_ROWS);
     if (s.n * tpi > 2147483647ll / 1024) return false;
     g->wv = static_cast<int>(wv);
@@ -578,17 +623,37 @@ bool halo_pair_geometry(const Shape& s, int bn, HaloGeom* g)
     g->hr = static_cast<int>(hr);
     g->halo_bytes = static_cast<int>(halo_bytes);
     g->m_tiles = cdiv(s.n, 2) * tpi;  // a tile is one row-block of two images
+    g->taps = taps;
     return true;
 }
 
-int pair_halo_max_resident(int bn, bool fused, int halo_bytes)
+int pair_halo_max_resident(int bn, int taps, bool fused, int halo_bytes)
 {
-    if (bn == 64) return sgb::conv2d_pair_halo_max_resident<64>(fused, sgb::conv2d_pair_halo_smem_bytes<64>(halo_bytes));
-    if (bn == 128)
-        return sgb::conv2d_pair_halo_max_resident<128>(fused, sgb::conv2d_pair_halo_smem_bytes<128>(halo_bytes));
-    if (bn == 256)
-        return sgb::conv2d_pair_halo_max_resident<256>(fused, sgb::conv2d_pair_halo_smem_bytes<256>(halo_bytes));
+    const int smem = pair_halo_smem(bn, taps, halo_bytes);
+    if (smem <= 0) return 0;
+    if (taps == 3) {
+        if (bn == 64) return sgb::conv2d_pair_halo_max_resident<64, 3>(fused, smem);
+        if (bn == 128) return sgb::conv2d_pair_halo_max_resident<128, 3>(fused, smem);
+        return 0;
+    }
+    if (bn == 64) return sgb::conv2d_pair_halo_max_resident<64, 2>(fused, smem);
+    if (bn == 128) return sgb::conv2d_pair_halo_max_resident<128, 2>(fused, smem);
+    if (bn == 256) return sgb::conv2d_pair_halo_max_resident<256, 2>(fused, smem);
     return 0;
+}
+
+cudaError_t launch_pair_halo(int bn, int taps, const CUtensorMap& a, const CUtensorMap& b,
+                             const sgb::ConvKernelParams& kp, int pairs, cudaStream_t stream)
+{
+    if (taps == 3) {
+        if (bn == 64) return sgb::launch_conv2d_pair_halo<64, 3>(a, b, kp, pairs, stream);
+        if (bn == 128) return sgb::launch_conv2d_pair_halo<128, 3>(a, b, kp, pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (bn == 64) return sgb::launch_conv2d_pair_halo<64, 2>(a, b, kp, pairs, stream);
+    if (bn == 128) return sgb::launch_conv2d_pair_halo<128, 2>(a, b, kp, pairs, stream);
+    if (bn == 256) return sgb::launch_conv2d_pair_halo<256, 2>(a, b, kp, pairs, stream);
+    return cudaErrorInvalidValue;
 }
 
 int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
@@ -601,9 +666,9 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
     const int64_t m_tiles = g.m_tiles;
     const int64_t n_tiles = cdiv(s.k, bn);
     const int64_t tiles = m_tiles * n_tiles;
-    const int64_t stages = (s.c / BK) * cdiv(s.r * s.s, 2);  // chunk-major, two taps per stage
+    const int64_t stages = (s.c / BK) * cdiv(s.r * s.s, g.taps);  // chunk-major
     const int64_t units = tiles * stages;
-    const int64_t resident = pair_halo_max_resident(bn, whole_tiles, g.halo_bytes);
+    const int64_t resident = pair_halo_max_resident(bn, g.taps, whole_tiles, g.halo_bytes);
     if (resident <= 0) return CONV2D_ERR_CUDA;
     const int64_t fsplits = force ? force->splits : 0;
     const int64_t fgrid = force ? force->grid : 0;
@@ -626,11 +691,13 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
                 break;
             }
     }
-    if ((units + 1) * (grid + 1) >= (int64_t(1) << 31)) return CONV2D_ERR_UNSUPPORTED;
+    const int64_t offset = choose_unit_offset(units, grid, stages);
+    if ((units + offset + 1) * (grid + 1) >= (int64_t(1) << 31)) return CONV2D_ERR_UNSUPPORTED;
     plan->block_m = sgb::PAIR_TILE_M;
     plan->block_n = bn;
     plan->splits = static_cast<int>(fsplits);
     plan->loader = CONV2D_LOADER_PAIR_HALO;
+    plan->unit_offset = static_cast<int>(offset);
     plan->m_tiles = static_cast<int>(m_tiles);
     plan->n_tiles = static_cast<int>(n_tiles);
     plan->num_kb = static_cast<int>(stages);
@@ -638,7 +705,7 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
     plan->units = units;
     plan->box = BoxGeom{};
     plan->halo = g;
-    plan->kbs = 2;
+    plan->kbs = g.taps;
     if (plan_cuts_tiles(*plan)) {
         if (grid > resident) return CONV2D_ERR_UNSUPPORTED;
         if (whole_tiles) return CONV2D_ERR_UNSUPPORTED;
@@ -859,7 +926,7 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
         const cuuint64_t wd[4] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.c / BK), (cuuint64_t)(s.r * s.s)};
         const cuuint64_t ws[3] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2), (cuuint64_t)(s.c * 2)};
-        const cuuint32_t wb[4] = {(cuuint32_t)BK, (cuuint32_t)(plan.block_n / 2), 1, 2};
+        const cuuint32_t wb[4] = {(cuuint32_t)BK, (cuuint32_t)(plan.block_n / 2), 1, (cuuint32_t)plan.kbs};
         const cuuint32_t we[4] = {1, 1, 1, 1};
         rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), wd, ws, wb, we,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1281,9 +1348,10 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
         kp.halo_tx = plan.halo.hr * plan.halo.wv * 128;
         kp.fd_tpi = sgb::FastDiv(static_cast<uint32_t>(plan.halo.tpi));
         kp.fd_wv = sgb::FastDiv(static_cast<uint32_t>(plan.halo.wv));
-        kp.fd_tapst = sgb::FastDiv(static_cast<uint32_t>(cdiv(s.r * s.s, 2)));
+        kp.fd_tapst = sgb::FastDiv(static_cast<uint32_t>(cdiv(s.r * s.s, plan.kbs)));
     }
     if (plan.loader == CONV2D_LOADER_TMA_PAIR || plan.loader == CONV2D_LOADER_PAIR_HALO) {
+        kp.unit_offset = plan.unit_offset;
         kp.fd_grid = sgb::FastDiv(static_cast<uint32_t>(plan.grid));
         kp.fd_units = sgb::FastDiv(static_cast<uint32_t>(plan.units));
         kp.fd_nkb = sgb::FastDiv(static_cast<uint32_t>(plan.num_kb));
@@ -1303,9 +1371,7 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     if (plan.loader == CONV2D_LOADER_TMA_PAIR)
         err = launch_pair(plan.block_n, plan.kbs, tm_a, tm_b, kp, (int)grid, stream);
     else if (plan.loader == CONV2D_LOADER_PAIR_HALO)
-        err = plan.block_n == 64    ? sgb::launch_conv2d_pair_halo<64>(tm_a, tm_b, kp, (int)grid, stream)
-              : plan.block_n == 128 ? sgb::launch_conv2d_pair_halo<128>(tm_a, tm_b, kp, (int)grid, stream)
-                                    : sgb::launch_conv2d_pair_halo<256>(tm_a, tm_b, kp, (int)grid, stream);
+        err = launch_pair_halo(plan.block_n, plan.kbs, tm_a, tm_b, kp, (int)grid, stream);
     else
         err = dispatch(plan.block_m, plan.block_n, plan.loader, tm_a, tm_b, kp, (int)grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;

@@ -169,6 +169,10 @@ struct ConvKernelParams {
     // CTA-pair halo loader: row-blocks per image, the padded row pitch, and
     // two-tap weight stages per 64-channel chunk (tap_stages = ceil(R*S / 2)).
     FastDiv fd_tpi, fd_wv, fd_tapst;
+    // CTA-pair kernels: the pairs' unit ranges are rotated by this many units
+    // (0 <= unit_offset < stages per tile) so that no range starts on a tile
+    // boundary (see PairWalker).
+    int unit_offset;
 };
 
 
@@ -292,6 +296,61 @@ struct SegmentWalker {
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16)
 {
     return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
+
+// How an epilogue writes a 32 x 32 slab of the accumulator: plain fp32 stores,
+// fp32 vector atomic adds (a later split of a cut tile, or a partial-sum
+// buffer), or bf16 stores (fused output conversion).
+enum SlabMode : int { SLAB_F32 = 0, SLAB_RED = 1, SLAB_BF16 = 2 };
+
+// One warp's 32 x 32 fp32 slab (lane l holds row l, columns 0..31 in v) goes out
+// through the warp's swizzled 4 KB staging slot as 16-byte row-segment writes: 8
+// lanes cover one 128-byte row segment, four rows per instruction.  Lane (rsub,
+// chunk) = (lane / 8, lane % 8) writes rows 4*i + rsub, i < 8, at column chunk
+// `chunk`; rowp[i] + slab_off is that row's byte address for this slab (offset
+// to the lane's chunk), bit i of row_ok says whether the row exists, col_ok
+// whether the chunk's columns do.  All eight slot reads are issued before the first
+// global write so that their latencies overlap, and missing rows and columns
+// are predicated off rather than branched around: the epilogue warps are few
+// and their instruction stream is the critical path once the last accumulator
+// is ready.
+template <int MODE>
+__device__ __forceinline__ void slab_out(uint32_t saddr, const uint32_t (&v)[32], const uint64_t (&rowp)[8],
+                                         int64_t slab_off, uint32_t row_ok, bool col_ok, bool add_bias, float4 bias,
+                                         bool relu)
+{
+    const int lane = threadIdx.x & 31;
+    const int rsub = lane >> 3;
+    const int chunk = lane & 7;
+    __syncwarp();  // the previous slab's reads of the slot are done
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    __syncwarp();
+    uint4 val[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) val[i] = ptx::ld_shared_v4(saddr + sw128_offset(4 * i + rsub, chunk));
+    if (add_bias) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            val[i].x = __float_as_uint(__uint_as_float(val[i].x) + bias.x);
+            val[i].y = __float_as_uint(__uint_as_float(val[i].y) + bias.y);
+            val[i].z = __float_as_uint(__uint_as_float(val[i].z) + bias.z);
+            val[i].w = __float_as_uint(__uint_as_float(val[i].w) + bias.w);
+        }
+    }
+    if (relu) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) val[i] = ptx::relu4(val[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool p = col_ok && ((row_ok >> i) & 1u);
+        const uint64_t at = rowp[i] + static_cast<uint64_t>(slab_off);
+        if constexpr (MODE == SLAB_F32) ptx::st_global_v4_if(at, val[i], p);
+        else if constexpr (MODE == SLAB_RED) ptx::red_add_v4_f32_if(at, val[i], p);
+        else ptx::st_global_v2_if(at, ptx::pack_bf16x4(val[i]), p);
+    }
 }
 
 // Pixel (n, p, q) of GEMM row m.
@@ -1257,10 +1316,22 @@ __device__ void run_epilogue_impl(const ConvKernelParams& kp, const SmemView& sm
                 // splits.  The writes use the load/store path, leaving the TMA unit
                 // to the im2col and weight loads.
                 const uint32_t saddr = ptx::smem_addr(slots);
-                int mrow[8];  // output row of each of this lane's eight rows (-1: none)
+                // Byte address of each of this lane's eight rows at the warp's first slab
+                // (in the partial-sum buffer for a cut tile of a fused epilogue).
+                const bool bf16_out = FUSED && kp.out_bf16 && !via_part;
+                const int64_t esize = bf16_out ? 2 : 4;
+                const uint64_t base = reinterpret_cast<uint64_t>(via_part ? kp.part : kp.y);
+                uint64_t rowp[8];
+                uint32_t row_ok = 0u;
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    mrow[i] = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + quad * 32 + 4 * i + rsub, bx_n, bx_p, bx_q);
+                for (int i = 0; i < 8; ++i) {
+                    const int m = tile_row_m<BM, LOADER>(kp, m_tile, trow0 + quad * 32 + 4 * i + rsub, bx_n, bx_p, bx_q);
+                    row_ok |= (m >= 0 ? 1u : 0u) << i;
+                    rowp[i] = base + static_cast<uint64_t>(
+                                         (static_cast<int64_t>(m >= 0 ? m : 0) * kp.ldy + n0 + jbeg * 32 + chunk * 4) * esize);
+                }
+                const int mode = bf16_out ? SLAB_BF16 : ((via_part || sg.split > 0) ? SLAB_RED : SLAB_F32);
+                const bool relu = FUSED && kp.relu && !via_part;
 #pragma unroll
                 for (int j = 0; j < SLABS; ++j) {
                     uint32_t v[32];
@@ -1272,37 +1343,15 @@ __device__ void run_epilogue_impl(const ConvKernelParams& kp, const SmemView& sm
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&sm.acc_empty[buf]);
                     }
-                    SGB_CYCLES_BEGIN(t_st);
-                    __syncwarp();  // the previous slab's reads of the slot are done
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2],
-                                          v[4 * c + 3]);
-                    __syncwarp();
-                    SGB_CYCLES_END(c_st, t_st);
                     SGB_CYCLES_BEGIN(t_slot);
-                    const int col = n0 + (jbeg + j) * 32 + chunk * 4;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = 4 * i + rsub;  // row within the warp's 32 rows
-                        const int m = mrow[i];
-                        uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(r, chunk));
-                        if (add_bias) {
-                            val.x = __float_as_uint(__uint_as_float(val.x) + bias4[j].x);
-                            val.y = __float_as_uint(__uint_as_float(val.y) + bias4[j].y);
-                            val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
-                            val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
-                        }
-                        if (FUSED && kp.relu && !via_part) val = ptx::relu4(val);
-                        if (m >= 0 && col < n_end) {
-                            const int64_t at = static_cast<int64_t>(m) * kp.ldy + col;
-                            if (via_part) ptx::red_add_v4_f32(kp.part + at, val);
-                            else if (FUSED && kp.out_bf16)
-                                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
-                            else if (sg.split == 0) *reinterpret_cast<uint4*>(kp.y + at) = val;
-                            else ptx::red_add_v4_f32(kp.y + at, val);
-                        }
-                    }
+                    const bool col_ok = n0 + (jbeg + j) * 32 + chunk * 4 < n_end;
+                    const int64_t off = static_cast<int64_t>(j) * 32 * esize;
+                    if (FUSED && mode == SLAB_BF16)
+                        slab_out<SLAB_BF16>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
+                    else if (mode == SLAB_F32)
+                        slab_out<SLAB_F32>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
+                    else
+                        slab_out<SLAB_RED>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
                     SGB_CYCLES_END(c_slot, t_slot);
                 }
             } else {
@@ -1473,6 +1522,7 @@ __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
         ptx::tmem_alloc(sm.tmem_slot, Cfg::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    if (warp == 2) ptx::touch_params(&kp, static_cast<int>(sizeof(kp)));
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();

@@ -33,8 +33,8 @@
 // SM pairs get the same number of MMAs.  A tile cut between pairs is reduced in
 // place in y, each 128-row half with its own semaphore (NVIDIA/Fuser issue #1316
 // "Split-K matmul is slow even for few partitions", Eliminating the workspace):
-// the owner of split 0 zeroes the rows early, then every split adds (see the
-// epilogue).
+// split 0 stores, later splits add; the ranges are rotated so that split 0 is
+// always computed first (see PairWalker and the epilogue).
 //
 // Warp roles, the same in both CTAs (the MMA issuer and the stage waiter are
 // idle in the peer):
@@ -117,11 +117,22 @@ __device__ __forceinline__ void pair_record_timeout(const ConvKernelParams& kp, 
 }
 
 // This pair's segments, from the end of its unit range to the start.  kp.grid
-// is the number of pairs and kp.num_kb the number of stages per tile.  All
-// arithmetic is 32-bit and every division goes through a FastDiv: the host
-// admits only plans with (units + 1) * (grid + 1) < 2^31.
+// is the number of pairs and kp.num_kb the number of stages per tile.
+//
+// The units (tile, stage), numbered tile-major, are split into equal ranges
+// along an axis rotated by d = kp.unit_offset: pair c takes the units
+// [floor(c*U/G) + d, floor((c+1)*U/G) + d), the ones at U and above standing
+// for units 0 .. d-1 (the first d stages of tile 0, whose other stages open
+// pair 0's range).  The host picks d so that no range starts on a tile
+// boundary: then split 0 of a cut tile -- the tile's first stages, where a
+// range starts inside the tile -- is the highest segment of its pair's range
+// and is computed first, so its stores are done long before the tile's later
+// splits add to them, and no pair holds a split 0 as its only segment.
+//
+// All arithmetic is 32-bit and every division goes through a FastDiv: the host
+// admits only plans with (units + d + 1) * (grid + 1) < 2^31.
 struct PairWalker {
-    uint32_t lo, cur, nkb, grid, units;
+    uint32_t lo, cur, nkb, grid, units, off, tiles;
     int pair;
     __device__ __forceinline__ PairWalker(const ConvKernelParams& kp, int pair_idx)
     {
@@ -129,27 +140,46 @@ struct PairWalker {
         units = static_cast<uint32_t>(kp.units);
         grid = static_cast<uint32_t>(kp.grid);
         nkb = static_cast<uint32_t>(kp.num_kb);
-        lo = kp.fd_grid.div(static_cast<uint32_t>(pair) * units);
-        cur = kp.fd_grid.div((static_cast<uint32_t>(pair) + 1u) * units);
+        off = static_cast<uint32_t>(kp.unit_offset);
+        tiles = units / nkb;
+        lo = kp.fd_grid.div(static_cast<uint32_t>(pair) * units) + off;
+        cur = kp.fd_grid.div((static_cast<uint32_t>(pair) + 1u) * units) + off;
     }
-    // The pair whose unit range holds unit u: the largest c with floor(c*U/G) <= u.
-    __device__ __forceinline__ uint32_t pair_of_unit(const ConvKernelParams& kp, uint32_t u) const
+    // The pair whose range holds unit e of the rotated axis (off <= e < units + off).
+    __device__ __forceinline__ uint32_t pair_of(const ConvKernelParams& kp, uint32_t e) const
     {
+        const uint32_t u = e - off;
         return kp.fd_units.div((u + 1u) * grid + units - 1u) - 1u;
     }
     __device__ __forceinline__ bool next(const ConvKernelParams& kp, Segment& sg)
     {
         if (cur <= lo) return false;
-        const uint32_t t = kp.fd_nkb.div(cur - 1u);
-        const uint32_t base = t * nkb;
+        const uint32_t te = kp.fd_nkb.div(cur - 1u);  // tile index on the rotated axis
+        const uint32_t base = te * nkb;
         const uint32_t seg_lo = lo > base ? lo : base;
-        sg.tile = static_cast<int>(t);
+        sg.tile = static_cast<int>(te < tiles ? te : te - tiles);
         sg.kb_begin = static_cast<int>(seg_lo - base);
         sg.kb_end = static_cast<int>(cur - base);
-        const uint32_t first = pair_of_unit(kp, base);
-        const uint32_t last = pair_of_unit(kp, base + nkb - 1u);
-        sg.split = pair - static_cast<int>(first);
-        sg.nsplits = static_cast<int>(last - first + 1u);
+        if (off == 0u) {
+            const uint32_t first = pair_of(kp, base);
+            const uint32_t last = pair_of(kp, base + nkb - 1u);
+            sg.split = pair - static_cast<int>(first);
+            sg.nsplits = static_cast<int>(last - first + 1u);
+        } else {
+            // Tile 0 is the only tile that straddles the rotation: its stages 0 .. off-1
+            // are the top of the last pair's range, the rest open pair 0's.
+            const bool wrapped_tile = te == 0u || te == tiles;
+            if (!wrapped_tile) {
+                const uint32_t first = pair_of(kp, base);
+                const uint32_t last = pair_of(kp, base + nkb - 1u);
+                sg.split = pair - static_cast<int>(first);
+                sg.nsplits = static_cast<int>(last - first + 1u);
+            } else {
+                const uint32_t last = pair_of(kp, nkb - 1u);  // the last pair holding part of stages off .. nkb-1
+                sg.nsplits = static_cast<int>(last) + 2;
+                sg.split = te == tiles ? 0 : pair + 1;
+            }
+        }
         cur = seg_lo;
         return true;
     }
@@ -367,18 +397,15 @@ __device__ void pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_
 }
 
 // ---------------------------------------------------------------- epilogue (warps 2..9, both CTAs)
-// Cut tiles are reduced in place in y without any split waiting for another
-// split's stores.  The pair that owns split 0 of a cut tile zeroes its rows of
-// y at the start of the kernel, while its first MMAs run and its store path is
-// otherwise idle, and publishes that on the tile half's semaphore (value 1).
-// Every split -- split 0 with the bias -- then adds its partial sums with
-// vector atomic adds once the semaphore is non-zero and counts itself in
-// (value 1 + splits done); the last one resets the semaphore to 0.  In the
-// ordered mode split j waits for the value j + 1 and publishes j + 2 after a
-// fence (the last resets), so the adds land in k order: bitwise reproducible.
-// (A split that stored first and let the others add would chain one tile
-// half's store -- ~2.5 us for 128 KB at one SM's ~60 GB/s store rate -- in
-// front of the other splits' adds at the end of the kernel.)
+// Cut tiles are reduced in place in y (NVIDIA/Fuser issue #1316, Eliminating
+// the workspace), each 128-row half on its own semaphore: split 0 stores its
+// partial sums with the bias and publishes; in the concurrent mode every later
+// split waits only for that, adds with vector atomic adds and counts itself
+// in (the last resets the semaphore to 0); in the ordered mode split j waits
+// for the value j, adds, fences and publishes j + 1 (the last resets), so the
+// adds land in k order: bitwise reproducible.  The rotated work split makes
+// split 0 the first segment its pair computes (PairWalker), so its stores are
+// complete long before a later split asks.
 //
 // Semaphore of one 128-row half of a tile: [row half][column block].
 __device__ __forceinline__ int pair_sem_index(const ConvKernelParams& kp, int m_tile, uint32_t rank, int n_tile)
@@ -388,12 +415,13 @@ __device__ __forceinline__ int pair_sem_index(const ConvKernelParams& kp, int m_
 
 __device__ __forceinline__ void pair_pass_turn(const ConvKernelParams& kp, int sem, const Segment& sg)
 {
+    if ((kp.debug_flags & 1) && sg.split == 0) return;  // test hook: never signal
     if (kp.reduce_concurrent) {
         const uint32_t before = atomicAdd(kp.sems + sem, 1u);
-        if (before == static_cast<uint32_t>(sg.nsplits)) atomicExch(kp.sems + sem, 0u);
+        if (before + 1u == static_cast<uint32_t>(sg.nsplits)) atomicExch(kp.sems + sem, 0u);
         return;
     }
-    const uint32_t next = (sg.split + 1 == sg.nsplits) ? 0u : static_cast<uint32_t>(sg.split + 2);
+    const uint32_t next = (sg.split + 1 == sg.nsplits) ? 0u : static_cast<uint32_t>(sg.split + 1);
     ptx::st_release_gpu(kp.sems + sem, next);
 }
 
@@ -435,47 +463,6 @@ struct PairRows {
     }
 };
 
-// Zeroes this CTA's rows of every cut tile whose split 0 this pair owns, then
-// publishes them (all epilogue threads take part; one barrier).
-template <int BN, bool HALO>
-__device__ void pair_zero_cut_tiles(const ConvKernelParams& kp, uint32_t rank, int pair, int et)
-{
-    constexpr int EPI_T = PairConfig<BN, 1>::EPI_T;
-    bool any = false;
-    PairWalker walk(kp, pair);
-    Segment sg;
-    while (walk.next(kp, sg)) {
-        if (sg.nsplits < 2 || sg.split != 0) continue;
-        int m_tile, n_tile;
-        pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-        const PairRows<HALO> rows(kp, m_tile, rank);
-        if (!rows.any) continue;
-        const int n0 = n_tile * BN;
-        const int vecs = ((n0 + BN < kp.K ? n0 + BN : kp.K) - n0) / 4;  // float4 per row (K % 4 == 0)
-        for (int i = et; i < PAIR_ROWS * vecs; i += EPI_T) {
-            const int r = i / vecs;
-            const int v = i - r * vecs;
-            const int m = rows.m(kp, r);
-            if (m >= 0)
-                *reinterpret_cast<float4*>(kp.y + static_cast<int64_t>(m) * kp.ldy + n0 + 4 * v) =
-                    make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        any = true;
-    }
-    if (any) __threadfence();
-    ptx::named_bar_sync(1, EPI_T);
-    if (et == 0 && any && !(kp.debug_flags & 1)) {  // test hook: never signal
-        PairWalker again(kp, pair);
-        while (again.next(kp, sg)) {
-            if (sg.nsplits < 2 || sg.split != 0) continue;
-            int m_tile, n_tile;
-            pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-            if (!PairRows<HALO>(kp, m_tile, rank).any) continue;
-            ptx::st_release_gpu(kp.sems + pair_sem_index(kp, m_tile, rank, n_tile), 1u);
-        }
-    }
-}
-
 template <int BN, bool FUSED, bool HALO>
 __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, uint32_t rank,
                               int pair)
@@ -491,7 +478,6 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
     const int chunk = lane & 7;
     const uint32_t saddr = ptx::smem_addr(sm.epi + ew * EPI_SLOT_BYTES);
     const uint32_t acc_empty0 = ptx::mapa_shared(ptx::smem_addr(sm.acc_empty), 0u);  // the leader's
-    if (!FUSED) pair_zero_cut_tiles<BN, HALO>(kp, rank, pair, et);  // fused plans cut no tiles
     int seg_idx = 0;
     PairWalker walk(kp, pair);
     Segment sg;
@@ -514,13 +500,31 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
             bias4[j] = (add_bias && col < n_end) ? __ldg(reinterpret_cast<const float4*>(kp.bias + col))
                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // Byte address of each of this lane's eight rows at the warp's first slab,
+        // computed while the accumulator is still being produced.
+        const bool bf16_out = FUSED && kp.out_bf16;
+        const int64_t esize = bf16_out ? 2 : 4;
+        uint64_t rowp[8];
+        uint32_t row_ok = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int m = rows.m(kp, quad * 32 + 4 * i + rsub);
+            row_ok |= (m >= 0 ? 1u : 0u) << i;
+            rowp[i] = reinterpret_cast<uint64_t>(kp.y) +
+                      static_cast<uint64_t>((static_cast<int64_t>(m >= 0 ? m : 0) * kp.ldy + n0 + jbeg * 32 + chunk * 4) *
+                                            esize);
+        }
+        const int mode = bf16_out ? SLAB_BF16 : (sg.split == 0 ? SLAB_F32 : SLAB_RED);
+        const bool relu = FUSED && kp.relu;
+        const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+
         if (et == 0 && !ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) pair_record_timeout(kp, sm, rank);
         ptx::named_bar_sync(1, Cfg::EPI_T);
         if (et == 0) {
             bool go = *sm.abort_flag == 0u;
-            if (go && has_rows && cut) {  // the rows are zeroed (concurrent) or it is this split's turn (ordered)
+            if (go && has_rows && cut && sg.split > 0) {  // split 0 has stored (concurrent) or it is this split's turn
                 go = kp.reduce_concurrent ? wait_base(kp, sem, sm.abort_flag)
-                                          : wait_turn(kp, sem, sg.split + 1, sm.abort_flag);
+                                          : wait_turn(kp, sem, sg.split, sm.abort_flag);
                 if (!go) pair_record_timeout(kp, sm, rank);  // the turn never came: flag the peer too
             }
             *sm.epi_go = go ? 1u : 0u;
@@ -529,54 +533,37 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         SGB_TRACE(kp, et == 0 && seg_idx < 4, 2 + 2 * seg_idx);  // segment: accumulator ready, turn granted
         const bool store = *sm.epi_go != 0u && has_rows;
         ptx::tc_fence_after();
-        int mrow[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mrow[i] = rows.m(kp, quad * 32 + 4 * i + rsub);
-        const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+#ifdef SGB_TRACE_ENABLED
+        const uint64_t c0 = ptx::clock64();
+#endif
 #pragma unroll
         for (int j = 0; j < SLABS; ++j) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(taddr + (jbeg + j) * 32, v);
             ptx::tmem_ld_wait();
+            SGB_TRACE_VALUE(kp, et == 0 && seg_idx < 2 && j < 4, 12 + 8 * seg_idx + 2 * j,
+                            ptx::clock64() - c0);  // slab j in registers (SM cycles after the grant)
             if (j == SLABS - 1) {  // this warp's part of the accumulator is in registers: tell the leader
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(buf) * 8u);
+                if (lane == 0) ptx::mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(buf) * 8u);
             }
             if (!store) continue;
-            // Registers -> this warp's 32 x 32 swizzled slot -> 16-byte global writes
-            // (8 lanes per 128-byte row segment, four rows per instruction).
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                ptx::st_shared_v4(saddr + sw128_offset(lane, c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            __syncwarp();
-            const int col = n0 + (jbeg + j) * 32 + chunk * 4;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint4 val = ptx::ld_shared_v4(saddr + sw128_offset(4 * i + rsub, chunk));
-                if (add_bias) {
-                    val.x = __float_as_uint(__uint_as_float(val.x) + bias4[j].x);
-                    val.y = __float_as_uint(__uint_as_float(val.y) + bias4[j].y);
-                    val.z = __float_as_uint(__uint_as_float(val.z) + bias4[j].z);
-                    val.w = __float_as_uint(__uint_as_float(val.w) + bias4[j].w);
-                }
-                if (FUSED && kp.relu) val = ptx::relu4(val);
-                const int m = mrow[i];
-                if (m >= 0 && col < n_end) {
-                    const int64_t at = static_cast<int64_t>(m) * kp.ldy + col;
-                    if (FUSED && kp.out_bf16)
-                        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + at) = ptx::pack_bf16x4(val);
-                    else if (!cut)
-                        *reinterpret_cast<uint4*>(kp.y + at) = val;
-                    else
-                        ptx::red_add_v4_f32(kp.y + at, val);
-                }
-            }
+            const bool col_ok = n0 + (jbeg + j) * 32 + chunk * 4 < n_end;
+            const int64_t off = static_cast<int64_t>(j) * 32 * esize;
+            if (FUSED && mode == SLAB_BF16)
+                slab_out<SLAB_BF16>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
+            else if (mode == SLAB_F32)
+                slab_out<SLAB_F32>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
+            else
+                slab_out<SLAB_RED>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], relu);
+            SGB_TRACE_VALUE(kp, et == 0 && seg_idx < 2 && j < 4, 13 + 8 * seg_idx + 2 * j,
+                            ptx::clock64() - c0);  // slab j's stores issued
         }
         if (store && cut) {
-            // Ordered mode: this split's adds must be performed before the next split's.
-            if (!kp.reduce_concurrent) __threadfence();
+            // Split 0's stores (both modes) and every split's adds in the ordered mode must be
+            // performed before the next split adds.
+            if (sg.split == 0 || !kp.reduce_concurrent) __threadfence();
             ptx::named_bar_sync(1, Cfg::EPI_T);
             if (et == 0) pair_pass_turn(kp, sem, sg);
         }
@@ -639,6 +626,7 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
         ptx::tmem_alloc_pair(sm.tmem_slot, Cfg::TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
+    if (warp == 2) ptx::touch_params(&kp, static_cast<int>(sizeof(kp)));
     ptx::tc_fence_before();
     __syncthreads();
     ptx::cluster_sync();  // both CTAs' barriers are initialised before any remote arrive or TMA completion
@@ -687,15 +675,19 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
 // fill gives the padding) serves all R*S filter taps: tap (r, s) reads its 128
 // A rows in place, r*dh*wv + s*dw rows into the buffer (the 128-byte swizzle
 // follows absolute shared-memory addresses, so any start row works).  The
-// weight rows of two taps of one chunk come in one 4-D box per stage; the
-// reduction runs chunk-major, then over the taps two at a time.  Per k-block
+// weight rows of two or three taps of one chunk come in one 4-D box per stage;
+// the reduction runs chunk-major, then over the taps.  Per k-block
 // this is about 0.1 TMA operation of activations (against one for the im2col
 // loader) and half an operation of weights.
-template <int BN>
+template <int BN, int TAPS_>
 struct HaloPairConfig {
     static constexpr int B_ROWS = BN / 2;
     static constexpr int B_KB = B_ROWS * BK * 2;      // one tap's weight rows of this CTA
-    static constexpr int TAPS = 2;                    // taps (k-blocks) per stage
+    // Taps (k-blocks) per stage: enough MMA work per stage that the MMA warp's
+    // per-stage handshake (~0.1 us) stays small.  Two for 256-wide tiles (1024 MMA
+    // cycles per SM); three for narrower ones where the ring still fits beside the
+    // two halos (a 3x3 filter then takes three full stages per chunk).
+    static constexpr int TAPS = TAPS_;
     static constexpr int B_STAGE = TAPS * B_KB;
     static constexpr int STAGES = 4;
     static constexpr int RING = STAGES * B_STAGE;
@@ -708,11 +700,12 @@ struct HaloPairConfig {
     static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(PAIR_TILE_M, BN);
 };
 
-// Chunk and first tap of stage st of a tile.
+// Chunk and first tap of stage st of a tile (TAPS taps per stage).
+template <int TAPS>
 __device__ __forceinline__ void halo_stage(const ConvKernelParams& kp, int st, int& chunk, int& tap0)
 {
     chunk = static_cast<int>(kp.fd_tapst.div(static_cast<uint32_t>(st)));
-    tap0 = 2 * (st - chunk * static_cast<int>(kp.fd_tapst.d));
+    tap0 = TAPS * (st - chunk * static_cast<int>(kp.fd_tapst.d));
 }
 
 // First virtual pixel of the CTA's row-block and the first padded input row its halo holds.
@@ -728,13 +721,39 @@ __device__ __forceinline__ void halo_block(const ConvKernelParams& kp, int m_til
 // A halo use starts at a chunk's first stage or a segment's first stage and ends
 // at the chunk's last stage or the segment's last stage.
 __device__ __forceinline__ bool halo_use_starts(const Segment& sg, int st, int tap0) { return st == sg.kb_begin || tap0 == 0; }
+template <int TAPS>
 __device__ __forceinline__ bool halo_use_ends(const ConvKernelParams& kp, const Segment& sg, int st, int tap0)
 {
-    return st + 1 == sg.kb_end || tap0 + 2 >= kp.R * kp.S;
+    return st + 1 == sg.kb_end || tap0 + TAPS >= kp.R * kp.S;
+}
+
+// L2 prefetch of this CTA's first halo and first weight stages, issued before
+// the grid-dependency wait so that the loads after it find them in L2 (a
+// prefetch reads nothing into the CTA, and L2 is coherent: a later load still
+// sees whatever the previous kernel writes).
+template <int BN, int TAPS>
+__device__ void halo_pair_prefetch(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const ConvKernelParams& kp,
+                                   uint32_t rank, int pair)
+{
+    using Cfg = HaloPairConfig<BN, TAPS>;
+    PairWalker walk(kp, pair);
+    Segment sg;
+    if (!walk.next(kp, sg)) return;
+    int m_tile, n_tile;
+    pair_tile_coords(kp, sg.tile, m_tile, n_tile);
+    int n_img, j0, prow0, chunk, tap0;
+    halo_block(kp, m_tile, rank, n_img, j0, prow0);
+    halo_stage<TAPS>(kp, sg.kb_begin, chunk, tap0);
+    if (n_img < kp.N) ptx::tma_prefetch_4d(tm_a, chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
+    const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+    for (int st = sg.kb_begin; st < sg.kb_end && st < sg.kb_begin + Cfg::STAGES; ++st) {
+        halo_stage<TAPS>(kp, st, chunk, tap0);
+        ptx::tma_prefetch_4d(tm_b, 0, b_row, chunk, tap0);
+    }
 }
 
 // Producer of the halos (warp 0, one thread, both CTAs).
-template <int BN>
+template <int BN, int TAPS>
 __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelParams& kp, const PairSmem& sm,
                                      uint32_t rank, int pair)
 {
@@ -750,7 +769,7 @@ __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelPa
         halo_block(kp, m_tile, rank, n_img, j0, prow0);
         for (int st = sg.kb_begin; st < sg.kb_end; ++st) {
             int chunk, tap0;
-            halo_stage(kp, st, chunk, tap0);
+            halo_stage<TAPS>(kp, st, chunk, tap0);
             if (!halo_use_starts(sg, st, tap0)) continue;
             if (*sm.abort_flag) { ok = false; break; }
             const int slot = h & 1;
@@ -772,11 +791,11 @@ __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelPa
 }
 
 // Producer of the weight stages (warp 11, one thread, both CTAs).
-template <int BN>
+template <int BN, int TAPS>
 __device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelParams& kp, const PairSmem& sm,
                                      uint32_t rank, int pair)
 {
-    using Cfg = HaloPairConfig<BN>;
+    using Cfg = HaloPairConfig<BN, TAPS>;
     constexpr int STAGES = Cfg::STAGES;
     const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(sm.full), 0u);
     int it = 0;
@@ -796,8 +815,8 @@ __device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelPa
                 break;
             }
             int chunk, tap0;
-            halo_stage(kp, st, chunk, tap0);
-            // The box always counts two taps (a tap past R*S reads zeros).
+            halo_stage<TAPS>(kp, st, chunk, tap0);
+            // The box always counts TAPS taps (a tap past R*S reads zeros).
             if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(Cfg::B_STAGE));
             ptx::tma_load_4d_pair(sm.b + slot * Cfg::B_STAGE, tm_b, full0 + static_cast<uint32_t>(slot) * 8u, 0, b_row,
                                   chunk, tap0);
@@ -809,10 +828,10 @@ __device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelPa
 }
 
 // Stage waiter (warp 10, leader): the chunk's halo, then the stage's weights.
-template <int BN>
+template <int BN, int TAPS>
 __device__ void halo_pair_waiter(const ConvKernelParams& kp, const PairSmem& sm, int pair)
 {
-    constexpr int STAGES = HaloPairConfig<BN>::STAGES;
+    constexpr int STAGES = HaloPairConfig<BN, TAPS>::STAGES;
     const int lane = threadIdx.x & 31;
     bool waiting = true;
     int it = 0, h = 0;
@@ -823,7 +842,7 @@ __device__ void halo_pair_waiter(const ConvKernelParams& kp, const PairSmem& sm,
             const int slot = it % STAGES;
             const uint32_t use = static_cast<uint32_t>(it / STAGES);
             int chunk, tap0;
-            halo_stage(kp, st, chunk, tap0);
+            halo_stage<TAPS>(kp, st, chunk, tap0);
             if (lane == 0) {
                 if (halo_use_starts(sg, st, tap0)) {
                     if (waiting && (*sm.abort_flag ||
@@ -851,10 +870,10 @@ __device__ void halo_pair_waiter(const ConvKernelParams& kp, const PairSmem& sm,
 }
 
 // MMA issuer (warp 1, leader).
-template <int BN>
+template <int BN, int TAPS>
 __device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, int pair)
 {
-    using Cfg = HaloPairConfig<BN>;
+    using Cfg = HaloPairConfig<BN, TAPS>;
     constexpr int STAGES = Cfg::STAGES;
     const int lane = threadIdx.x & 31;
     const int taps = kp.R * kp.S;
@@ -885,10 +904,10 @@ __device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, ui
         for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
             const int slot = it % STAGES;
             int chunk, tap0;
-            halo_stage(kp, st, chunk, tap0);
+            halo_stage<TAPS>(kp, st, chunk, tap0);
             if (halo_use_starts(sg, st, tap0)) ++h;
             const int hslot = (h - 1) & 1;
-            const bool hlast = halo_use_ends(kp, sg, st, tap0);
+            const bool hlast = halo_use_ends<TAPS>(kp, sg, st, tap0);
             ptx::named_bar_sync(STAGE_BAR0 + slot, 64);
             ptx::tc_fence_after();
             if (lane == 0) SGB_PAIR_MARK(kp, it, 3);
@@ -924,12 +943,12 @@ __device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, ui
     __syncwarp();
 }
 
-template <int BN, bool FUSED>
-__global__ void __launch_bounds__(HaloPairConfig<BN>::THREADS, 1)
+template <int BN, int TAPS, bool FUSED>
+__global__ void __launch_bounds__(HaloPairConfig<BN, TAPS>::THREADS, 1)
     conv2d_fwd_pair_halo_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                                 const ConvKernelParams kp)
 {
-    using Cfg = HaloPairConfig<BN>;
+    using Cfg = HaloPairConfig<BN, TAPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     PairSmem sm;
@@ -972,11 +991,13 @@ __global__ void __launch_bounds__(HaloPairConfig<BN>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tm_a);
         ptx::prefetch_tensormap(&tm_b);
+        halo_pair_prefetch<BN, TAPS>(&tm_a, &tm_b, kp, rank, pair);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(sm.tmem_slot, Cfg::TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
+    if (warp == 2) ptx::touch_params(&kp, static_cast<int>(sizeof(kp)));
     ptx::tc_fence_before();
     __syncthreads();
     ptx::cluster_sync();
@@ -988,15 +1009,15 @@ __global__ void __launch_bounds__(HaloPairConfig<BN>::THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
-        if (lane == 0) halo_pair_producer_a<BN>(&tm_a, kp, sm, rank, pair);
+        if (lane == 0) halo_pair_producer_a<BN, TAPS>(&tm_a, kp, sm, rank, pair);
     } else if (warp == WAITER_WARP + 1) {
-        if (lane == 0) halo_pair_producer_b<BN>(&tm_b, kp, sm, rank, pair);
+        if (lane == 0) halo_pair_producer_b<BN, TAPS>(&tm_b, kp, sm, rank, pair);
     } else if (warp == 1) {
-        if (rank == 0) halo_pair_mma<BN>(kp, sm, tmem_base, pair);
+        if (rank == 0) halo_pair_mma<BN, TAPS>(kp, sm, tmem_base, pair);
     } else if (warp < EPI_WARP0 + Cfg::EPI_WARPS) {
         pair_epilogue<BN, FUSED, true>(kp, sm, tmem_base, rank, pair);
     } else if (warp == WAITER_WARP) {
-        if (rank == 0) halo_pair_waiter<BN>(kp, sm, pair);
+        if (rank == 0) halo_pair_waiter<BN, TAPS>(kp, sm, pair);
     }
 
     ptx::tc_fence_before();
@@ -1009,20 +1030,20 @@ __global__ void __launch_bounds__(HaloPairConfig<BN>::THREADS, 1)
     SGB_TRACE(kp, threadIdx.x == 0, 10);
 }
 
-template <int BN>
+template <int BN, int TAPS>
 cudaError_t launch_conv2d_pair_halo(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const ConvKernelParams& kp,
                                     int pairs, cudaStream_t stream);
-template <int BN>
+template <int BN, int TAPS>
 int conv2d_pair_halo_max_resident(bool fused, int smem_bytes);
-template <int BN>
+template <int BN, int TAPS>
 inline int conv2d_pair_halo_smem_bytes(int halo_bytes)
 {
-    return HaloPairConfig<BN>::FIXED_SMEM + 2 * halo_bytes;
+    return HaloPairConfig<BN, TAPS>::FIXED_SMEM + 2 * halo_bytes;
 }
-#define SGB_PAIR_HALO_SIG(BN_)                                                                                   \
-    cudaError_t launch_conv2d_pair_halo<BN_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, int, \
-                                             cudaStream_t)
-#define SGB_PAIR_HALO_RES_SIG(BN_) int conv2d_pair_halo_max_resident<BN_>(bool, int)
+#define SGB_PAIR_HALO_SIG(BN_, TAPS_)                                                                        \
+    cudaError_t launch_conv2d_pair_halo<BN_, TAPS_>(const CUtensorMap&, const CUtensorMap&, const ConvKernelParams&, \
+                                                    int, cudaStream_t)
+#define SGB_PAIR_HALO_RES_SIG(BN_, TAPS_) int conv2d_pair_halo_max_resident<BN_, TAPS_>(bool, int)
 
 // Host-side launcher: `pairs` clusters of two CTAs.
 template <int BN, int KBS>

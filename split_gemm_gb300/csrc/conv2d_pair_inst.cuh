@@ -97,15 +97,15 @@ int conv2d_pair_max_resident(bool fused)
 #error "define SGB_PAIR_KBS (k-blocks per stage) before including this file"
 #endif
 #if SGB_PAIR_KBS == 2
-// The halo loader's kernel (its stages always hold two taps) lives in this translation unit.
+// The halo loader's kernels (two or three taps per stage) live in this translation unit.
 namespace {
-template <int BN>
+template <int BN, int TAPS>
 auto pair_halo_kernel(bool fused)
 {
-    return fused ? conv2d_fwd_pair_halo_kernel<BN, true> : conv2d_fwd_pair_halo_kernel<BN, false>;
+    return fused ? conv2d_fwd_pair_halo_kernel<BN, TAPS, true> : conv2d_fwd_pair_halo_kernel<BN, TAPS, false>;
 }
 
-template <int BN>
+template <int BN, int TAPS>
 cudaError_t pair_halo_configure(bool fused)
 {
     static unsigned long long configured[2] = {0ull, 0ull};
@@ -114,19 +114,19 @@ cudaError_t pair_halo_configure(bool fused)
     if (err != cudaSuccess) return err;
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
     if (bit && (__atomic_load_n(&configured[fused], __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
-    err = cudaFuncSetAttribute(pair_halo_kernel<BN>(fused), cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemBytes);
+    err = cudaFuncSetAttribute(pair_halo_kernel<BN, TAPS>(fused), cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemBytes);
     if (err != cudaSuccess) return err;
     if (bit) __atomic_fetch_or(&configured[fused], bit, __ATOMIC_RELEASE);
     return cudaSuccess;
 }
 
-template <int BN>
+template <int BN, int TAPS>
 void pair_halo_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, int smem,
                              cudaStream_t stream)
 {
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg->blockDim = dim3(HaloPairConfig<BN>::THREADS);
+    cfg->blockDim = dim3(HaloPairConfig<BN, TAPS>::THREADS);
     cfg->dynamicSmemBytes = static_cast<size_t>(smem);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -140,23 +140,23 @@ void pair_halo_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
 }
 }  // namespace
 
-template <int BN>
+template <int BN, int TAPS>
 cudaError_t launch_conv2d_pair_halo(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const ConvKernelParams& kp,
                                     int pairs, cudaStream_t stream)
 {
     const bool fused = (kp.relu | kp.out_bf16) != 0;
-    const int smem = conv2d_pair_halo_smem_bytes<BN>(kp.halo_bytes);
+    const int smem = conv2d_pair_halo_smem_bytes<BN, TAPS>(kp.halo_bytes);
     if (smem > kMaxSmemBytes) return cudaErrorInvalidValue;
-    cudaError_t err = pair_halo_configure<BN>(fused);
+    cudaError_t err = pair_halo_configure<BN, TAPS>(fused);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    pair_halo_launch_config<BN>(&cfg, attr, pairs, smem, stream);
-    return cudaLaunchKernelEx(&cfg, pair_halo_kernel<BN>(fused), tm_a, tm_b, kp);
+    pair_halo_launch_config<BN, TAPS>(&cfg, attr, pairs, smem, stream);
+    return cudaLaunchKernelEx(&cfg, pair_halo_kernel<BN, TAPS>(fused), tm_a, tm_b, kp);
 }
 
 // Resident CTA pairs at this shared-memory size; a few sizes are remembered per device.
-template <int BN>
+template <int BN, int TAPS>
 int conv2d_pair_halo_max_resident(bool fused, int smem)
 {
     struct Entry { int dev, fused, smem, n; };
@@ -170,13 +170,13 @@ int conv2d_pair_halo_max_resident(bool fused, int smem)
         for (const Entry& e : cache)
             if (e.n > 0 && e.dev == dev && e.fused == static_cast<int>(fused) && e.smem == smem) return e.n;
     }
-    if (pair_halo_configure<BN>(fused) != cudaSuccess) return 0;
+    if (pair_halo_configure<BN, TAPS>(fused) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    pair_halo_launch_config<BN>(&cfg, attr, 1, smem, nullptr);
+    pair_halo_launch_config<BN, TAPS>(&cfg, attr, 1, smem, nullptr);
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_halo_kernel<BN>(fused), &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_halo_kernel<BN, TAPS>(fused), &cfg) != cudaSuccess) return 0;
     if (n > 0) {
         std::lock_guard<std::mutex> lock(mu);
         cache[next] = Entry{dev, static_cast<int>(fused), smem, n};
@@ -185,12 +185,16 @@ int conv2d_pair_halo_max_resident(bool fused, int smem)
     return n;
 }
 
-template SGB_PAIR_HALO_SIG(64);
-template SGB_PAIR_HALO_SIG(128);
-template SGB_PAIR_HALO_SIG(256);
-template SGB_PAIR_HALO_RES_SIG(64);
-template SGB_PAIR_HALO_RES_SIG(128);
-template SGB_PAIR_HALO_RES_SIG(256);
+template SGB_PAIR_HALO_SIG(64, 2);
+template SGB_PAIR_HALO_SIG(64, 3);
+template SGB_PAIR_HALO_SIG(128, 2);
+template SGB_PAIR_HALO_SIG(128, 3);
+template SGB_PAIR_HALO_SIG(256, 2);
+template SGB_PAIR_HALO_RES_SIG(64, 2);
+template SGB_PAIR_HALO_RES_SIG(64, 3);
+template SGB_PAIR_HALO_RES_SIG(128, 2);
+template SGB_PAIR_HALO_RES_SIG(128, 3);
+template SGB_PAIR_HALO_RES_SIG(256, 2);
 #endif
 
 template SGB_PAIR_SIG(64, SGB_PAIR_KBS);

@@ -762,6 +762,7 @@ __global__ void __launch_bounds__(RW_THREADS, 1) conv2d_rowwin_kernel(const __gr
         ptx::tmem_alloc(sm.tmem_slot, kp.tmem_cols);
         ptx::tmem_relinquish();
     }
+    if (warp == RW_MMA_WARP + 1) ptx::touch_params(&kp, static_cast<int>(sizeof(kp)));
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();

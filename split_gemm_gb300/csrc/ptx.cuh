@@ -311,6 +311,36 @@ __device__ __forceinline__ uint16_t bf16_bits(float f)
     return *reinterpret_cast<const uint16_t*>(&b);
 }
 
+// Predicated global writes (no branch around a store that a lane may skip):
+// 16 bytes, 8 bytes, or a 16-byte vector fp32 atomic add, at byte address addr.
+__device__ __forceinline__ void st_global_v4_if(uint64_t addr, uint4 v, bool p)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "@p st.global.v4.b32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(addr),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(static_cast<uint32_t>(p))
+        : "memory");
+}
+
+__device__ __forceinline__ void st_global_v2_if(uint64_t addr, uint2 v, bool p)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
+        "@p st.global.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(addr),
+        "r"(v.x), "r"(v.y), "r"(static_cast<uint32_t>(p))
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4_f32_if(uint64_t addr, uint4 v, bool p)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "@p red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n\t}" ::"l"(addr),
+        "f"(__uint_as_float(v.x)), "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w)),
+        "r"(static_cast<uint32_t>(p))
+        : "memory");
+}
+
 // Vector fp32 atomic add to global memory (no return value).
 __device__ __forceinline__ void red_add_v4_f32(float* dst, uint4 v)
 {
@@ -346,6 +376,20 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
 // ---------------------------------------------------------------- programmatic dependent launch
 // Blocks until the grids this one depends on have completed and their memory
 // writes are visible (a no-op when the launch carried no such dependency).
+// Loads every 16th byte of a kernel parameter block of `bytes` bytes (lane l
+// reads the word at 16*l, then 16*(l+32), ...) and waits for the values, so
+// that the block's lines are in the SM's constant cache before the roles start:
+// a role's first dependent parameter reads would otherwise each miss in turn.
+// Call from one whole warp, before the grid-dependency wait (parameters never
+// depend on the previous kernel).
+__device__ __forceinline__ void touch_params(const void* params, int bytes)
+{
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(params);
+    uint32_t acc = 0u;
+    for (int off = 16 * static_cast<int>(threadIdx.x & 31); off < bytes; off += 16 * 32) acc ^= w[off / 4];
+    asm volatile("" ::"r"(acc));
+}
+
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Lets the next grid in the stream begin launching once every CTA of this grid
 // has executed this (its CTAs then run their prologue and wait in grid_dependency_wait).
@@ -515,6 +559,15 @@ __device__ __forceinline__ void cluster_sync()
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrival without release semantics: for a signal that orders no memory
+// writes (e.g. "this warp's accumulator reads have completed", which
+// tcgen05.wait::ld already guarantees), so that it need not wait for the
+// thread's earlier global stores to be performed.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 32-bit store into the shared memory of a CTA of the cluster (shared::cluster address).

@@ -63,16 +63,20 @@ GEOMETRIES = {
 SMEM_LIMIT = 232448  # dynamic shared memory one CTA may opt in to
 
 
-def _halo_fits(wl, bn):
-    """Whether the two halo buffers and the weight ring of a forced tile width fit one CTA's
-    shared memory (the host refuses the plan otherwise): four stages of two taps of bn/2
-    weight rows, eight 4 KB epilogue slots, barriers and 1 KB alignment slack."""
+def _halo_smem(wl, bn, taps):
+    """Shared memory of the halo kernel: two halo buffers, four stages of `taps` taps of
+    bn/2 weight rows, eight 4 KB epilogue slots, barriers and 1 KB alignment slack."""
     wv = wl.w + 2 * wl.pad_w
     max_row = (wv - 1) + (wl.r - 1) * wl.dil_h * wv + (wl.s - 1) * wl.dil_w + 127
     hr = max_row // wv + 1
     halo = (hr * wv * 128 + 1023) // 1024 * 1024
-    fixed = 4 * bn * 128 + 8 * 4096 + (2 * 4 + 9) * 8 + 16 + 1024
-    return fixed + 2 * halo <= SMEM_LIMIT
+    return 4 * taps * (bn // 2) * 128 + 8 * 4096 + (2 * 4 + 9) * 8 + 16 + 1024 + 2 * halo
+
+
+def _halo_fits(wl, bn):
+    """Whether a forced tile width fits one CTA's shared memory (the host refuses the plan
+    otherwise): stages of three taps for 64- and 128-wide tiles where they fit, else two."""
+    return _halo_smem(wl, bn, 2) <= SMEM_LIMIT
 
 
 @pytest.mark.parametrize("bn", [64, 128, 256])
