@@ -713,9 +713,69 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
     return CONV2D_OK;
 }
 
+// The heuristic's CTA-pair choices (loader AUTO with no shape field forced), in
+// the two regimes where the pair kernels measured faster than the single-CTA
+// kernel on GB300; anything else returns CONV2D_ERR_UNSUPPORTED and the
+// single-CTA planner decides.
+//  - Few output tiles and a long reduction (split-K): 256-pixel pair tiles, each
+//    tile cut into an equal number of splits so that tiles x splits fills the
+//    resident pairs (every pair computes one segment and reduces it once), each
+//    split at least 8 stages long; only when the 256-row tiles waste at most 35%
+//    of their rows and the epilogue is not fused (a fused epilogue needs whole
+//    tiles).
+//  - Whole-tile stride-1 layers with at least 128 input channels whose halo
+//    tiles fill at least 70% of the resident pairs' waves and whose
+//    virtual pixels (padded row pitch, image pairs) exceed the output pixels by
+//    at most 20%: the halo loader, one tile per pair per wave.
+int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
+{
+    if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    conv2d_algo f;
+    std::memset(&f, 0, sizeof(f));
+    if (force) f = *force;
+    const int bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+    if (!whole_tiles) {
+        const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
+        const int64_t tiles = m_tiles * cdiv(s.k, bn);
+        const int64_t stages = cdiv(s.crs / BK, 2);
+        const int64_t res = pair_max_resident(bn, 2, false);
+        if (res > 0 && tiles * 2 <= res && stages >= 16 && m_tiles * sgb::PAIR_TILE_M * 20 <= s.m * 27) {
+            int64_t splits = res / tiles;
+            if (splits > stages / 8) splits = stages / 8;
+            if (splits >= 2) {
+                f.loader = CONV2D_LOADER_TMA_PAIR;
+                f.block_n = bn;
+                f.splits = static_cast<int32_t>(splits);
+                if (choose_pair_plan(s, &f, plan, false) == CONV2D_OK) return CONV2D_OK;
+            }
+        }
+    }
+    HaloGeom g;
+    if (s.c >= 128 && halo_pair_geometry(s, bn, &g)) {
+        const int64_t tiles = g.m_tiles * cdiv(s.k, bn);
+        const int64_t res = pair_halo_max_resident(bn, g.taps, whole_tiles, g.halo_bytes);
+        const int64_t virt = cdiv(s.n, 2) * 2 * static_cast<int64_t>(g.tpi) * sgb::PAIR_ROWS;
+        if (res > 0) {
+            const int64_t waves = cdiv(tiles, res);
+            if (tiles * 10 >= waves * res * 7 && virt * 5 <= s.m * 6) {
+                f.loader = CONV2D_LOADER_PAIR_HALO;
+                f.block_n = bn;
+                f.splits = 0;
+                f.grid = 0;
+                if (choose_pair_halo_plan(s, &f, plan, true) == CONV2D_OK) return CONV2D_OK;
+            }
+        }
+    }
+    return CONV2D_ERR_UNSUPPORTED;
+}
+
 int choose_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles = false)
 {
     const int sms = sm_count_current();
+    if (!force || (force->loader == CONV2D_LOADER_AUTO && force->block_m == 0 && force->block_n == 0 &&
+                   force->splits == 0 && force->grid == 0)) {
+        if (choose_auto_pair(s, force, plan, whole_tiles) == CONV2D_OK) return CONV2D_OK;
+    }
     // Loader.
     int loader = force ? force->loader : 0;
     RowWinCfg rw;

@@ -113,6 +113,7 @@ __device__ __forceinline__ void pair_record_timeout(const ConvKernelParams& kp, 
 {
     *sm.abort_flag = 1u;
     ptx::st_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t*>(sm.abort_flag)), rank ^ 1u), 1u);
+    ptx::grid_dependency_wait();  // the status word is global memory (a no-op once waited)
     if (kp.status) atomicMax(kp.status, STATUS_TIMEOUT);
 }
 
@@ -249,6 +250,7 @@ __device__ void pair_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
     const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(sm.full), 0u);  // the leader's full[0]
     int it = 0;  // stages issued (all segments)
     bool ok = true;
+    bool released = false;  // past the grid-dependency wait
     PairWalker walk(kp, pair);
     Segment sg;
     while (ok && walk.next(kp, sg)) {
@@ -274,6 +276,11 @@ __device__ void pair_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
                 break;
             }
             const uint32_t bar = full0 + static_cast<uint32_t>(slot) * 8u;
+            if (!released) {  // everything before this point reads only parameters and shared memory
+                ptx::grid_dependency_wait();
+                released = true;
+                SGB_TRACE(kp, threadIdx.x == 0, 1);
+            }
             if (OP == PAIR_A) {
                 // The leader expects the activation bytes of both CTAs.
                 if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(nkb * Cfg::A_KB));
@@ -493,6 +500,7 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         const int sem = pair_sem_index(kp, m_tile, rank, n_tile);
         const bool cut = sg.nsplits > 1;
         const bool add_bias = kp.bias != nullptr && sg.split == 0;
+        if (seg_idx == 0) ptx::grid_dependency_wait();  // bias and output are global memory
         float4 bias4[SLABS];
 #pragma unroll
         for (int j = 0; j < SLABS; ++j) {
@@ -635,9 +643,12 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
     // Everything above touches only shared memory, tensor memory, parameters and
     // (by prefetches) L2, so it may overlap the previous kernel in the stream.
     SGB_TRACE(kp, threadIdx.x == 0, 0);
+    // Each role waits for the previous kernel in the stream (griddepcontrol.wait)
+    // right before its first global-memory access, after whatever setup needs
+    // only parameters and shared memory: the producers before their first TMA
+    // load, the epilogue before its first bias read.  The MMA issuer and the
+    // stage waiter touch shared and tensor memory only.
     ptx::grid_launch_dependents();
-    ptx::grid_dependency_wait();
-    SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
         if (lane == 0) pair_producer<BN, KBS, PAIR_A>(&tm_a, &tm_b, kp, sm, rank, pair, 0);
@@ -778,6 +789,10 @@ __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelPa
                 ok = false;
                 break;
             }
+            if (h == 0) {  // everything before reads only parameters and shared memory
+                ptx::grid_dependency_wait();
+                SGB_TRACE(kp, threadIdx.x == 0, 1);
+            }
             if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.halo_full[slot], 2u * static_cast<uint32_t>(kp.halo_tx));
             ptx::tma_load_4d_pair(sm.halo + slot * kp.halo_bytes, tm_a, hfull0 + static_cast<uint32_t>(slot) * 8u,
                                   chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
@@ -797,25 +812,32 @@ __device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelPa
 {
     using Cfg = HaloPairConfig<BN, TAPS>;
     constexpr int STAGES = Cfg::STAGES;
+    SGB_TRACE(kp, true, 6);  // weight producer: entered
     const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(sm.full), 0u);
     int it = 0;
     bool ok = true;
     PairWalker walk(kp, pair);
     Segment sg;
+    SGB_TRACE(kp, true, 7);  // weight producer: walker ready
     while (ok && walk.next(kp, sg)) {
+        SGB_TRACE(kp, it == 0, 9);  // weight producer: first segment
         int m_tile, n_tile;
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
         const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
             const int slot = it % STAGES;
             if (*sm.abort_flag) { ok = false; break; }
+            SGB_TRACE(kp, it == 0, 11);  // weight producer: abort flag read
             if (!ptx::mbar_wait_spin(&sm.empty[slot], (static_cast<uint32_t>(it / STAGES) & 1u) ^ 1u, kp.wait_limit_ns)) {
                 pair_record_timeout(kp, sm, rank);
                 ok = false;
                 break;
             }
+            SGB_TRACE(kp, it == 0, 30);  // weight producer: slot free
             int chunk, tap0;
             halo_stage<TAPS>(kp, st, chunk, tap0);
+            SGB_TRACE(kp, it == 0, 8);  // weight producer: first stage's coordinates
+            if (it == 0) ptx::grid_dependency_wait();  // everything before reads only parameters and shared memory
             // The box always counts TAPS taps (a tap past R*S reads zeros).
             if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(Cfg::B_STAGE));
             ptx::tma_load_4d_pair(sm.b + slot * Cfg::B_STAGE, tm_b, full0 + static_cast<uint32_t>(slot) * 8u, 0, b_row,
@@ -1004,9 +1026,12 @@ __global__ void __launch_bounds__(HaloPairConfig<BN, TAPS>::THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *sm.tmem_slot;
     SGB_TRACE(kp, threadIdx.x == 0, 0);
+    // Each role waits for the previous kernel in the stream (griddepcontrol.wait)
+    // right before its first global-memory access, after whatever setup needs
+    // only parameters and shared memory: the producers before their first TMA
+    // load, the epilogue before its first bias read.  The MMA issuer and the
+    // stage waiter touch shared and tensor memory only.
     ptx::grid_launch_dependents();
-    ptx::grid_dependency_wait();
-    SGB_TRACE(kp, threadIdx.x == 0, 1);
 
     if (warp == 0) {
         if (lane == 0) halo_pair_producer_a<BN, TAPS>(&tm_a, kp, sm, rank, pair);
