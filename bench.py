@@ -449,12 +449,15 @@ def _algo_report(heuristic, forced):
 
 
 def _forced_algo(sg, args):
-    if not (args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction or args.pair_kb):
+    if not (args.block_n or args.splits or args.loader or args.grid or args.block_m or args.reduction or args.pair_kb
+            or args.tma_store):
         return None
     a = sg.Algo()
     a.block_n, a.splits, a.loader, a.grid = args.block_n, args.splits, args.loader, args.grid
     a.block_m, a.reduction = args.block_m, args.reduction
     a.debug_flags = {1: 2, 2: 4}.get(args.pair_kb, 0)  # CONV2D_DEBUG_PAIR_KB1 / KB2
+    if args.tma_store:
+        a.debug_flags |= sg.DEBUG_TMA_STORE
     return a
 
 
@@ -791,6 +794,8 @@ def parse_args(argv=None):
     ap.add_argument("--block-m", type=int, default=0, help="force the output-pixel tile height (128/256)")
     ap.add_argument("--pair-kb", type=int, default=0, choices=[0, 1, 2],
                     help="CTA-pair loader: force 1 or 2 k-blocks per pipeline stage (0: the heuristic's)")
+    ap.add_argument("--tma-store", action="store_true",
+                    help="CTA-pair loaders: write y through TMA stores (a measurement hook)")
     ap.add_argument("--op", default="fwd", choices=["fwd", "wgrad", "dgrad"],
                     help="fwd: the forward convolution (the headline); wgrad / dgrad: its weight / input gradient")
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "bf16", "relu_bf16"],

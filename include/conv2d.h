@@ -153,6 +153,10 @@ typedef enum {
  * or two 64-wide k-blocks per pipeline stage instead of the heuristic's choice. */
 #define CONV2D_DEBUG_PAIR_KB1 2
 #define CONV2D_DEBUG_PAIR_KB2 4
+/* Measurement hook of the CTA-pair loaders: write fp32 y through TMA stores
+ * and TMA reductions of staged 64-row boxes instead of per-thread vector
+ * stores (measured slower on GB300, so not the default). */
+#define CONV2D_DEBUG_TMA_STORE 8
 
 /* Output extents P and Q (pure host computation).  Returns CONV2D_OK or
  * CONV2D_ERR_INVALID (bad options, or the filter window does not fit). */

@@ -26,7 +26,7 @@ __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
     "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "LOADER_DIRECT", "LOADER_TMA_PAIR", "LOADER_PAIR_HALO", "REDUCTION_AUTO", "REDUCTION_ORDERED",
     "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
-    "DEBUG_SKIP_SIGNAL", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
+    "DEBUG_SKIP_SIGNAL", "DEBUG_TMA_STORE", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "epi_workspace_bytes", "conv2d_bwd_weight", "conv2d_bwd_weight_into",
     "wgrad_workspace_bytes", "query_wgrad_algo", "conv2d_bwd_data", "conv2d_bwd_data_into", "dgrad_workspace_bytes",
     "query_dgrad_algo", "conv_transpose2d", "conv2d_fwd", "conv2d_fwd_into", "conv2d_fwd_host", "host_staging_bytes", "status",
@@ -43,6 +43,7 @@ REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
 ACT_NONE, ACT_RELU = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 DEBUG_SKIP_SIGNAL = 1
+DEBUG_TMA_STORE = 8  # CTA-pair loaders: write y through TMA stores (measurement hook; slower)
 STATUS_NAMES = {0: "CONV2D_OK", 1: "CONV2D_ERR_INVALID", 2: "CONV2D_ERR_UNSUPPORTED", 3: "CONV2D_ERR_ALIGNMENT",
                 4: "CONV2D_ERR_WORKSPACE", 5: "CONV2D_ERR_CUDA", 6: "CONV2D_ERR_TIMEOUT",
                 7: "CONV2D_ERR_SCRATCH_LIMIT"}

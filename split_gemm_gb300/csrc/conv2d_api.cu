@@ -1132,6 +1132,58 @@ MapKey make_map_key(const Shape& s, const Plan& plan, const void* x, const void*
     return k;
 }
 
+// y as a 2-D fp32 tensor {K, M} with row pitch ldy, boxes of 32 columns x 64
+// rows in the 128-byte swizzle (the CTA-pair epilogue's TMA stores), cached by
+// (pointer, sizes, device) like the operand maps.
+struct YMapEntry {
+    const void* y;
+    int64_t m, k, ldy;
+    int device;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kYMapEntries = 32;
+YMapEntry g_ymap_cache[kYMapEntries];
+int g_ymap_next = 0;
+
+int encode_y_map_cached(float* y, int64_t m, int64_t k, int64_t ldy, CUtensorMap* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
+    if (m < 1 || k < 1 || (ldy * 4) % 16 != 0) return CONV2D_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (const YMapEntry& e : g_ymap_cache)
+            if (e.used && e.y == y && e.m == m && e.k == k && e.ldy == ldy && e.device == dev) {
+                *out = e.map;
+                ++g_map_hits;
+                return CONV2D_OK;
+            }
+    }
+    if (!load_encoders()) return CONV2D_ERR_CUDA;
+    std::memset(out, 0, sizeof(*out));
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ldy * 4)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)sgb::EPI_BOX_ROWS};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult rc = g_encode_tiled(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+                                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    YMapEntry& e = g_ymap_cache[g_ymap_next];
+    g_ymap_next = (g_ymap_next + 1) % kYMapEntries;
+    e.y = y;
+    e.m = m;
+    e.k = k;
+    e.ldy = ldy;
+    e.device = dev;
+    e.map = *out;
+    e.used = true;
+    ++g_map_misses;
+    return CONV2D_OK;
+}
+
 int encode_maps_cached(const Shape& s, const Plan& plan, const void* x, const void* w, CUtensorMap* tm_a,
                        CUtensorMap* tm_b)
 {
@@ -1411,6 +1463,13 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
         kp.fd_tapst = sgb::FastDiv(static_cast<uint32_t>(cdiv(s.r * s.s, plan.kbs)));
     }
     if (plan.loader == CONV2D_LOADER_TMA_PAIR || plan.loader == CONV2D_LOADER_PAIR_HALO) {
+        // fp32 output through the TMA unit: a measurement hook (16-byte aligned y).
+        // Per-thread vector stores measured faster on GB300 (the boxes' staging
+        // handshakes cost more than the shared-memory reads they save).
+        kp.tma_y = 0;
+        if (!out_bf16 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && (kp.debug_flags & CONV2D_DEBUG_TMA_STORE) &&
+            encode_y_map_cached(y, s.m, s.k, kp.ldy, &kp.tm_y) == CONV2D_OK)
+            kp.tma_y = 1;
         kp.unit_offset = plan.unit_offset;
         kp.fd_grid = sgb::FastDiv(static_cast<uint32_t>(plan.grid));
         kp.fd_units = sgb::FastDiv(static_cast<uint32_t>(plan.units));

@@ -167,12 +167,17 @@ struct ConvKernelParams {
     // units, stages per tile, column blocks, P*Q, Q, C, S).
     FastDiv fd_grid, fd_units, fd_nkb, fd_ntiles, fd_pq, fd_q, fd_c, fd_s;
     // CTA-pair halo loader: row-blocks per image, the padded row pitch, and
-    // two-tap weight stages per 64-channel chunk (tap_stages = ceil(R*S / 2)).
+    // weight stages per 64-channel chunk (ceil(R*S / taps per stage)).
     FastDiv fd_tpi, fd_wv, fd_tapst;
     // CTA-pair kernels: the pairs' unit ranges are rotated by this many units
     // (0 <= unit_offset < stages per tile) so that no range starts on a tile
     // boundary (see PairWalker).
     int unit_offset;
+    // CTA-pair kernels: y as a 2-D fp32 tensor {K, M} (row pitch ldy) for TMA
+    // stores and reductions of 32-column x 64-row boxes in the 128-byte swizzle;
+    // tma_y = 0 when it is not encoded (the epilogue then writes with st.global).
+    int tma_y;
+    CUtensorMap tm_y;
 };
 
 
@@ -1461,7 +1466,7 @@ __device__ void run_epilogue_impl(const ConvKernelParams& kp, const SmemView& sm
 template <int BM, int BN, int LOADER, bool FUSED>
 __global__ void __launch_bounds__(TileConfig<BM, BN, LOADER>::THREADS, 1)
     conv2d_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const ConvKernelParams kp)
+                         const __grid_constant__ ConvKernelParams kp)
 {
     using Cfg = TileConfig<BM, BN, LOADER>;
     extern __shared__ uint8_t smem_raw[];

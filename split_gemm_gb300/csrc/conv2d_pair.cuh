@@ -57,6 +57,9 @@ namespace sgb {
 
 constexpr int PAIR_ROWS = 128;  // output pixels (GEMM rows) each CTA of the pair holds
 constexpr int PAIR_TILE_M = 2 * PAIR_ROWS;
+constexpr int EPI_GRP_BAR0 = 12;      // named barriers of the epilogue's two column groups (TMA stores)
+constexpr int EPI_BOX_ROWS = 64;      // rows of one staged y box
+constexpr int EPI_BOX_BYTES = EPI_BOX_ROWS * 128;
 // 64-wide k-blocks per pipeline stage (KBS): 2 gives three 64 KB stages at BN =
 // 256 with one producer thread per operand; 1 gives six 32 KB stages with two
 // producer threads per operand taking alternate stages.
@@ -470,6 +473,53 @@ struct PairRows {
     }
 };
 
+// The output rows of a CTA's half tile are consecutive GEMM rows [m_a, m_a + cnt):
+// im2col loader, rows base .. base + 127 clipped to M; halo loader, the valid
+// virtual pixels of the row-block, which are consecutive output pixels of one
+// image once the junk columns (q >= Q) are dropped.  cnt = 0 when there are none.
+template <bool HALO>
+__device__ __forceinline__ void pair_row_span(const ConvKernelParams& kp, const PairRows<HALO>& rows, int& m_a,
+                                              int& cnt)
+{
+    m_a = 0;
+    cnt = 0;
+    if (!HALO) {
+        m_a = rows.base;
+        const int left = kp.M - rows.base;
+        cnt = left < PAIR_ROWS ? (left > 0 ? left : 0) : PAIR_ROWS;
+        return;
+    }
+    if (rows.n_img >= kp.N) return;
+    const int j_first = rows.base;
+    const int j_last = rows.base + PAIR_ROWS - 1 < kp.vp - 1 ? rows.base + PAIR_ROWS - 1 : kp.vp - 1;
+    if (j_first > j_last) return;
+    int p0 = static_cast<int>(kp.fd_wv.div(static_cast<uint32_t>(j_first)));
+    int v0 = j_first - p0 * kp.wv;
+    if (v0 >= kp.Q) {  // starts in a junk column: the next row's first pixel
+        ++p0;
+        v0 = 0;
+    }
+    const int p1 = static_cast<int>(kp.fd_wv.div(static_cast<uint32_t>(j_last)));
+    int v1 = j_last - p1 * kp.wv;
+    if (v1 >= kp.Q) v1 = kp.Q - 1;  // ends in a junk column: the row's last pixel
+    const int img = rows.n_img * kp.P * kp.Q;
+    m_a = img + p0 * kp.Q + v0;
+    const int m_last = img + p1 * kp.Q + v1;
+    cnt = m_last >= m_a ? m_last - m_a + 1 : 0;
+}
+
+// Stages one 32-column slab row (this thread's accumulator row, bias and ReLU
+// applied) into row d of a 64-row staging box at `box` (1024-byte aligned), in
+// the 128-byte swizzle the y tensor map expects.
+__device__ __forceinline__ void stage_row(uint32_t box, int d, const uint32_t (&v)[32])
+{
+    const uint32_t rowb = box + static_cast<uint32_t>(d) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        ptx::st_shared_v4(rowb + static_cast<uint32_t>((c ^ (d & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                          v[4 * c + 3]);
+}
+
 template <int BN, bool FUSED, bool HALO>
 __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, uint32_t tmem_base, uint32_t rank,
                               int pair)
@@ -485,6 +535,15 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
     const int chunk = lane & 7;
     const uint32_t saddr = ptx::smem_addr(sm.epi + ew * EPI_SLOT_BYTES);
     const uint32_t acc_empty0 = ptx::mapa_shared(ptx::smem_addr(sm.acc_empty), 0u);  // the leader's
+    // TMA stores: warps 2..5 and 6..9 form two column groups; each group stages a
+    // slab's 128 rows in two 64-row boxes (its four warps' 4 KB slots) that one
+    // thread of the group hands to the TMA unit.
+    const int grp = ew >> 2;
+    const bool issuer = (ew & 3) == 0 && lane == 0;
+    const uint32_t box_a = ptx::smem_addr(sm.epi) + static_cast<uint32_t>(grp * 2 * EPI_BOX_BYTES);
+    const uint32_t box_b = box_a + EPI_BOX_BYTES;
+    const int trow = quad * 32 + lane;  // this thread's accumulator row
+    bool tma_used = false;
     int seg_idx = 0;
     PairWalker walk(kp, pair);
     Segment sg;
@@ -525,6 +584,22 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         const int mode = bf16_out ? SLAB_BF16 : (sg.split == 0 ? SLAB_F32 : SLAB_RED);
         const bool relu = FUSED && kp.relu;
         const uint32_t taddr = tmem_base + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+        // TMA path (fp32 output): box A takes span rows 0..63.  Plain stores: box B
+        // takes the span's last 64 rows (overlapping A with the same values when the
+        // span is shorter than 128), so the span needs at least 64 rows.  Adds (a
+        // later split): box B takes rows 64..127 and rows past the span are added as
+        // zeros, which leaves whatever they hold unchanged.
+        int m_a, cnt;
+        pair_row_span<HALO>(kp, rows, m_a, cnt);
+        const bool use_tma = kp.tma_y != 0 && !bf16_out && (mode == SLAB_RED ? cnt >= 1 : cnt >= EPI_BOX_ROWS);
+        const bool overlap = mode == SLAB_F32 && cnt < PAIR_ROWS;
+        const int b_first = overlap ? cnt - EPI_BOX_ROWS : EPI_BOX_ROWS;  // span row at box B's row 0
+        const bool need_b = overlap || cnt > EPI_BOX_ROWS;
+        const int my_m = rows.m(kp, trow);
+        const int idx = my_m >= 0 ? my_m - m_a : -1;  // this row's place in the span
+        const int row_a = idx >= 0 && idx < EPI_BOX_ROWS ? idx : -1;
+        const int row_b = idx >= b_first ? idx - b_first : -1;
+        const int zero_row = mode == SLAB_RED && trow >= cnt ? trow : -1;  // padding rows cnt..127 of an add
 
         if (et == 0 && !ptx::mbar_wait(&sm.acc_full[buf], use, kp.wait_limit_ns)) pair_record_timeout(kp, sm, rank);
         ptx::named_bar_sync(1, Cfg::EPI_T);
@@ -557,6 +632,53 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
                 if (lane == 0) ptx::mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(buf) * 8u);
             }
             if (!store) continue;
+            if (use_tma) {
+                const int col0 = n0 + (jbeg + j) * 32;
+                if (col0 >= n_end) continue;  // a slab wholly past the last column (uniform in the group)
+                if (add_bias) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 b4 = col0 + 4 * c < n_end ? __ldg(reinterpret_cast<const float4*>(kp.bias + col0) + c)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[4 * c] = __float_as_uint(__uint_as_float(v[4 * c]) + b4.x);
+                        v[4 * c + 1] = __float_as_uint(__uint_as_float(v[4 * c + 1]) + b4.y);
+                        v[4 * c + 2] = __float_as_uint(__uint_as_float(v[4 * c + 2]) + b4.z);
+                        v[4 * c + 3] = __float_as_uint(__uint_as_float(v[4 * c + 3]) + b4.w);
+                    }
+                }
+                if (relu) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(fmaxf(__uint_as_float(v[q]), 0.0f));
+                }
+                if (issuer) ptx::bulk_wait_read<0>();  // the previous slab's boxes have been read
+                ptx::named_bar_sync(EPI_GRP_BAR0 + grp, 128);
+                if (row_a >= 0) stage_row(box_a, row_a, v);
+                if (row_b >= 0) stage_row(box_b, row_b, v);
+                if (zero_row >= 0) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) z[q] = 0u;
+                    if (zero_row < EPI_BOX_ROWS) stage_row(box_a, zero_row, z);
+                    else stage_row(box_b, zero_row - EPI_BOX_ROWS, z);
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(EPI_GRP_BAR0 + grp, 128);
+                if (issuer) {
+                    if (mode == SLAB_RED) {
+                        // Split 0's writes were seen (generic proxy) before this segment began;
+                        // order that before the TMA's read-modify-writes of the same rows.
+                        if (j == 0) ptx::fence_proxy_async_global();
+                        ptx::tma_reduce_add_2d_s(&kp.tm_y, box_a, col0, m_a);
+                        if (need_b) ptx::tma_reduce_add_2d_s(&kp.tm_y, box_b, col0, m_a + EPI_BOX_ROWS);
+                    } else {
+                        ptx::tma_store_2d_s(&kp.tm_y, box_a, col0, m_a);
+                        if (need_b) ptx::tma_store_2d_s(&kp.tm_y, box_b, col0, m_a + b_first);
+                    }
+                    ptx::bulk_commit();
+                }
+                tma_used = true;
+                continue;
+            }
             const bool col_ok = n0 + (jbeg + j) * 32 + chunk * 4 < n_end;
             const int64_t off = static_cast<int64_t>(j) * 32 * esize;
             if (FUSED && mode == SLAB_BF16)
@@ -568,6 +690,14 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
             SGB_TRACE_VALUE(kp, et == 0 && seg_idx < 2 && j < 4, 13 + 8 * seg_idx + 2 * j,
                             ptx::clock64() - c0);  // slab j's stores issued
         }
+        if (store && use_tma && issuer) {
+            if (cut && (sg.split == 0 || !kp.reduce_concurrent)) {
+                ptx::bulk_wait_all();  // the TMA writes are performed before the turn passes
+                ptx::fence_proxy_async_global();
+            } else {
+                ptx::bulk_wait_read<0>();  // the boxes may be reused (either path) by the next segment
+            }
+        }
         if (store && cut) {
             // Split 0's stores (both modes) and every split's adds in the ordered mode must be
             // performed before the next split adds.
@@ -578,13 +708,14 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         SGB_TRACE(kp, et == 0 && seg_idx < 4, 3 + 2 * seg_idx);  // segment: epilogue done
         ++seg_idx;
     }
+    if (tma_used && issuer) ptx::bulk_wait_all();  // no TMA store outlives the CTA
 }
 
 // ---------------------------------------------------------------- the kernel
 template <int BN, int KBS, bool FUSED>
 __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
     conv2d_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                           const ConvKernelParams kp)
+                           const __grid_constant__ ConvKernelParams kp)
 {
     using Cfg = PairConfig<BN, KBS>;
     extern __shared__ uint8_t smem_raw[];
@@ -968,7 +1099,7 @@ __device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, ui
 template <int BN, int TAPS, bool FUSED>
 __global__ void __launch_bounds__(HaloPairConfig<BN, TAPS>::THREADS, 1)
     conv2d_fwd_pair_halo_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                                const ConvKernelParams kp)
+                                const __grid_constant__ ConvKernelParams kp)
 {
     using Cfg = HaloPairConfig<BN, TAPS>;
     extern __shared__ uint8_t smem_raw[];

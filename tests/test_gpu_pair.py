@@ -68,6 +68,22 @@ def test_pair_geometries_each_width(sg, name, bn, kb):
     _check(sg, wl, x, w, b, algo, f"{name} bn={bn} kb={kb}")
 
 
+@pytest.mark.parametrize("split", [0, 3])
+@pytest.mark.parametrize("bn", [64, 256])
+@pytest.mark.parametrize("name", sorted(GEOMETRIES))
+def test_pair_tma_store_path(sg, name, bn, split):
+    """The TMA store path (a measurement hook): whole tiles and, with three splits, TMA stores
+    of split 0 and TMA reductions of the later splits (rows past a span added as zeros)."""
+    n, h, w_, c, k, r, s, stride, pad, dil = GEOMETRIES[name]
+    wl, x, w, b = _case(n, h, w_, c, k, r, s, stride, pad, dil, seed=sum(map(ord, name)) % 997)
+    algo = make_algo(sg, loader=PAIR, block_n=bn, wait_limit_ns=WAIT, debug_flags=sg.DEBUG_TMA_STORE,
+                     splits=split)
+    try:
+        _check(sg, wl, x, w, b, algo, f"{name} bn={bn} splits={split} TMA stores")
+    except sg.Conv2dError as e:  # more splits than stages
+        assert split and e.code == 2
+
+
 @pytest.mark.parametrize("name", ["m588_k136_3x3", "1x1_c192_k320", "m200_k80_3x3", "asym_3x2_k48"])
 def test_pair_integer_inputs_exact(sg, name):
     """Small integers: every product and partial sum is exact in fp32, so the result must equal

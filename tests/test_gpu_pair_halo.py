@@ -93,6 +93,19 @@ def test_halo_geometries_each_width(sg, name, bn):
     _check(sg, wl, x, w, b, algo, f"{name} bn={bn}")
 
 
+@pytest.mark.parametrize("split", [0, 3])
+@pytest.mark.parametrize("name", sorted(GEOMETRIES))
+def test_halo_tma_store_path(sg, name, split):
+    """The TMA store path (a measurement hook), whole and cut tiles."""
+    n, h, w_, c, k, r, s, pad, dil = GEOMETRIES[name]
+    wl, x, w, b = _case(n, h, w_, c, k, r, s, pad, dil, seed=sum(map(ord, name)) % 991)
+    algo = make_algo(sg, loader=HALO, wait_limit_ns=WAIT, debug_flags=sg.DEBUG_TMA_STORE, splits=split)
+    try:
+        _check(sg, wl, x, w, b, algo, f"{name} splits={split} TMA stores")
+    except sg.Conv2dError as e:  # more splits than stages, or the halos do not fit
+        assert e.code == 2
+
+
 @pytest.mark.parametrize("name", ["n3_14x14_c128_k136", "n4_9x9_1x1_c192_k320", "n2_8x12_3x2_pad10_k48",
                                   "n1_16x16_5x5_c256_k128"])
 def test_halo_integer_inputs_exact(sg, name):
