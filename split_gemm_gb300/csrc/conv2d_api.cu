@@ -1184,9 +1184,21 @@ int encode_y_map_cached(float* y, int64_t m, int64_t k, int64_t ldy, CUtensorMap
     return CONV2D_OK;
 }
 
+// CONV2D_NO_MAP_CACHE=1 in the environment encodes every call's maps afresh
+// (a measurement switch: the cache's effect on host time per call).
+bool map_cache_enabled()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("CONV2D_NO_MAP_CACHE");
+        return !(v && v[0] == '1');
+    }();
+    return on;
+}
+
 int encode_maps_cached(const Shape& s, const Plan& plan, const void* x, const void* w, CUtensorMap* tm_a,
                        CUtensorMap* tm_b)
 {
+    if (!map_cache_enabled()) return encode_maps(s, plan, x, w, tm_a, tm_b);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CONV2D_ERR_CUDA;
     const MapKey key = make_map_key(s, plan, x, w, dev);
