@@ -384,12 +384,9 @@ __device__ void pair_mma(const ConvKernelParams& kp, const PairSmem& sm, uint32_
 #pragma unroll
                 for (int j = 0; j < KBS; ++j) {
                     if (j < nkb) {
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            ptx::mma_bf16_pair_elect(tmem_d,
-                                                     ad + static_cast<uint64_t>((j * Cfg::A_KB + k * UMMA_K * 2) >> 4),
-                                                     bd + static_cast<uint64_t>((j * Cfg::B_KB + k * UMMA_K * 2) >> 4),
-                                                     Cfg::IDESC, (st > sg.kb_begin || j > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_bf16_pair_elect_kb(tmem_d, ad + static_cast<uint64_t>((j * Cfg::A_KB) >> 4),
+                                                    bd + static_cast<uint64_t>((j * Cfg::B_KB) >> 4), Cfg::IDESC,
+                                                    (st > sg.kb_begin || j > 0) ? 1u : 0u);
                     }
                 }
             }
@@ -1075,11 +1072,8 @@ __device__ void halo_pair_mma(const ConvKernelParams& kp, const PairSmem& sm, ui
                         const uint64_t ad =
                             halo_desc0 + static_cast<uint64_t>((hslot * kp.halo_bytes + a_row * 128) >> 4);
                         const uint64_t bd = b_desc0 + static_cast<uint64_t>((slot * Cfg::B_STAGE + jt * Cfg::B_KB) >> 4);
-#pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            ptx::mma_bf16_pair_elect(tmem_d, ad + static_cast<uint64_t>((k * UMMA_K * 2) >> 4),
-                                                     bd + static_cast<uint64_t>((k * UMMA_K * 2) >> 4), Cfg::IDESC,
-                                                     (st > sg.kb_begin || jt > 0 || k > 0) ? 1u : 0u);
+                        static_assert(BK / UMMA_K == 4 && UMMA_K * 2 == 32, "four MMAs of 32 bytes per k-block");
+                        ptx::mma_bf16_pair_elect_kb(tmem_d, ad, bd, Cfg::IDESC, (st > sg.kb_begin || jt > 0) ? 1u : 0u);
                     }
                 }
             }

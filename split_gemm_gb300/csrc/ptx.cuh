@@ -675,6 +675,28 @@ __device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d_tmem, uint64_t a_
         : "memory");
 }
 
+// The four MMAs of one 64-wide k-block (K = 16 each, the operands advancing 32
+// bytes = 2 descriptor units per step) from one elected lane, in one block so
+// that the election and the descriptor arithmetic are paid once per k-block.
+// The first MMA accumulates when `accumulate` is nonzero; the other three always do.
+__device__ __forceinline__ void mma_bf16_pair_elect_kb(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair_elect(uint64_t* bar, uint16_t cta_mask)
 {
     asm volatile(
