@@ -324,18 +324,25 @@ int conv2d_bwd_weight_query_algo(const conv2d_params* params, conv2d_algo* out);
  *       over the taps with h + ph - r*dh = p*sh, w + pw - s*dw = q*sw, 0 <= p < P, 0 <= q < Q.
  *
  * It is also conv_transpose2d: conv_transpose2d of an input [N][Hi][Wi][Cin]
- * with weights [Cin][R][S][Cout] (padding p, dilation d, stride 1) is this call
- * with params {n = N, h = Hi - 2p + d(R-1), w = Wi - 2p + d(S-1), c = Cout,
- * k = Cin, r = R, s = S, pad p, dil d, stride 1} and dy = the input.
+ * with weights [Cin][R][S][Cout] (stride st, padding p, dilation d, output
+ * padding op < st) is this call with params {n = N, h = (Hi-1)*st - 2p +
+ * d(R-1) + 1 + op, w likewise, c = Cout, k = Cin, r = R, s = S, stride st,
+ * pad p, dil d} and dy = the input.
  * params describe the forward convolution (x [N][H][W][C], weight
  * [K][R][S][C]); dy_dev: bf16 [N][P][Q][K]; w_dev: bf16 [K][R][S][C]; dx_dev:
- * fp32 [N][H][W][C], fully overwritten.  Computed at stride 1 as the forward
- * convolution of dy with the flipped, transposed weight w'[c][r][s][k] =
- * w[k][R-1-r][S-1-s][c] and padding dil*(R-1) - pad, which the kernel reads
- * from w directly (no transformed copy).  Supported, as burn's implicit GEMM:
- * stride 1, groups == 1; and K % 64 == 0 (im2col TMA boxes of dy), C % 8 == 0,
- * pad <= dil*(R-1) per axis; otherwise CONV2D_ERR_UNSUPPORTED.  algo as for
- * conv2d_fwd_ex (block_m 0/128, loader 0 or CONV2D_LOADER_TMA_IM2COL). */
+ * fp32 [N][H][W][C], fully overwritten.  Computed as forward convolutions of
+ * dy with the flipped, transposed weight w'[c][r][s][k] = w[k][R-1-r][S-1-s][c],
+ * which the kernel reads from w directly (no transformed copy): at stride 1
+ * one launch with padding dil*(R-1) - pad; at stride (sh, sw) one launch per
+ * output phase (a, b), 0 <= a < sh, 0 <= b < sw (the sub-pixel decomposition):
+ * the rows h = a + sh*i receive only the taps r with a + ph - r*dh divisible
+ * by sh, which are every (sh / gcd(sh, dh))-th tap, and form a stride-1
+ * convolution of dy at dilation dh / gcd(sh, dh); a phase that no tap reaches
+ * is zero (dx is cleared first when there is one).  Supported: groups == 1,
+ * K % 64 == 0 (im2col TMA boxes of dy), C % 8 == 0, and every phase's padding
+ * d'(R'-1) - c >= 0 (at stride 1: pad <= dil*(R-1)); otherwise
+ * CONV2D_ERR_UNSUPPORTED.  algo as for conv2d_fwd_ex (block_m 0/128, loader 0
+ * or CONV2D_LOADER_TMA_IM2COL), applied to every phase. */
 size_t conv2d_bwd_data_workspace_bytes(const conv2d_params* params);
 
 int conv2d_bwd_data(const conv2d_params* params, const void* dy_dev, const void* w_dev, float* dx_dev,

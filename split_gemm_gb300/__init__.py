@@ -429,17 +429,25 @@ def conv2d_bwd_data(dy, w, x_shape, stride=1, padding=0, dilation=1, groups=1, *
     return dx
 
 
-def conv_transpose2d(x, w, padding=0, dilation=1, *, workspace=None, algo: Optional[Algo] = None, stream=None):
-    """conv_transpose2d at stride 1: x [N,Hi,Wi,Cin] bf16, w [Cin,R,S,Cout] bf16 ->
-    y [N,Hi-2p+d(R-1), Wi-2p+d(S-1), Cout] fp32, through the data-gradient kernel (dy = x)."""
+def conv_transpose2d(x, w, padding=0, dilation=1, *, stride=1, output_padding=0, workspace=None,
+                     algo: Optional[Algo] = None, stream=None):
+    """conv_transpose2d: x [N,Hi,Wi,Cin] bf16, w [Cin,R,S,Cout] bf16 -> y [N,Ho,Wo,Cout] fp32 with
+    Ho = (Hi-1)*stride - 2*padding + dilation*(R-1) + 1 + output_padding (likewise Wo), through the
+    data-gradient kernel (dy = x): the input gradient of the forward conv from Ho x Wo to Hi x Wi."""
+    sh, sw = _pair(stride)
     ph, pw = _pair(padding)
     dh, dw = _pair(dilation)
+    oph, opw = _pair(output_padding)
+    if not (0 <= oph < sh and 0 <= opw < sw):
+        raise ValueError("output_padding must lie in [0, stride)")
     n, hi, wi, cin = (int(v) for v in x.shape)
     cin_w, r, s, cout = (int(v) for v in w.shape)
     if cin_w != cin:
         raise ValueError(f"weight has {cin_w} input channels, x has {cin}")
-    return conv2d_bwd_data(x, w, (n, hi - 2 * ph + dh * (r - 1), wi - 2 * pw + dw * (s - 1), cout), 1, (ph, pw),
-                           (dh, dw), workspace=workspace, algo=algo, stream=stream)
+    ho = (hi - 1) * sh - 2 * ph + dh * (r - 1) + 1 + oph
+    wo = (wi - 1) * sw - 2 * pw + dw * (s - 1) + 1 + opw
+    return conv2d_bwd_data(x, w, (n, ho, wo, cout), (sh, sw), (ph, pw), (dh, dw), workspace=workspace, algo=algo,
+                           stream=stream)
 
 
 def conv2d_fwd_host(x_host, w_host, bias_host, y_host, params: Params, staging, stream=None) -> None:

@@ -1593,13 +1593,84 @@ bool wgrad_cuts_tiles(const WgradPlan& p)
 // dx = conv(dy, w') with w'[c][r][s][k] = w[k][R-1-r][S-1-s][c], stride 1, the same
 // dilation and padding dil*(R-1) - pad: a forward convolution of the output
 // gradient, whose weight operand the kernel reads from w itself (LOADER_DGRAD).
-bool dgrad_eligible(const Shape& s)
+// The data gradient runs as a forward convolution of dy (channels K) that
+// produces dx (channels C), one launch per output phase.  At stride 1 there is
+// one phase: dx[h] = sum_r dy[h + ph - r*dh] w[r], a stride-1 convolution of dy
+// with the flipped filter.  At stride sh the rows h = a + sh*i of phase a
+// (0 <= a < sh) receive only the taps r with a + ph - r*dh divisible by sh:
+// r = r0 + m*u (m = sh / gcd(sh, dh)), and then
+//     dx[a + sh*i] = sum_u dy[i + c - u*d'] w[r0 + m*u],   c = (a + ph - r0*dh) / sh,
+// with d' = dh / gcd(sh, dh): a stride-1 convolution of dy over the phase's
+// R' taps at dilation d' (the sub-pixel decomposition); columns likewise.  A
+// phase with no tap is all zero.
+struct DgradAxis {
+    int r0, m, taps, dil, pad;  // first tap, tap step, tap count, dilation d', forward-form padding d'(R'-1) - c
+    int64_t out;                // phase output extent ceil((H - a) / sh)
+};
+
+int64_t gcd64(int64_t a, int64_t b) { return b == 0 ? a : gcd64(b, a % b); }
+
+// Phase `a` along one axis of extent h (stride st, padding pad, dilation dil,
+// kernel ker).  false when the phase has no pixel; taps == 0 for no tap.
+bool dgrad_axis(int64_t a, int64_t h, int64_t st, int64_t pad, int64_t dil, int64_t ker, DgradAxis* ax)
 {
-    return s.g == 1 && s.sh == 1 && s.sw == 1 && s.k % BK == 0 && s.c % 8 == 0 && s.ph <= s.dh * (s.r - 1) &&
-           s.pw <= s.dw * (s.s - 1);
+    if (a >= h) return false;
+    ax->out = (h - a + st - 1) / st;
+    const int64_t g = gcd64(st, dil);
+    ax->m = static_cast<int>(st / g);
+    ax->dil = static_cast<int>(dil / g);
+    ax->taps = 0;
+    ax->r0 = 0;
+    ax->pad = 0;
+    int64_t r0 = -1;
+    for (int64_t r = 0; r < ker; ++r)
+        if (((a + pad - r * dil) % st + st) % st == 0) {
+            r0 = r;
+            break;
+        }
+    if (r0 < 0) return true;
+    ax->r0 = static_cast<int>(r0);
+    ax->taps = static_cast<int>((ker - 1 - r0) / ax->m + 1);
+    const int64_t c = (a + pad - r0 * dil) / st;  // exact
+    ax->pad = static_cast<int>(static_cast<int64_t>(ax->dil) * (ax->taps - 1) - c);
+    return true;
 }
 
-// The forward problem the data gradient is: input dy [N][P][Q][K], output dx [N][H][W][C].
+bool dgrad_eligible(const Shape& s)
+{
+    if (s.g != 1 || s.k % BK != 0 || s.c % 8 != 0) return false;
+    // Every phase's forward-form padding d'(R'-1) - c must be >= 0 (the im2col
+    // box's lower corner at or below 0), as ph <= dh*(R-1) is at stride 1.
+    for (int64_t a = 0; a < s.sh; ++a) {
+        DgradAxis ax;
+        if (dgrad_axis(a, s.h, s.sh, s.ph, s.dh, s.r, &ax) && ax.taps > 0 && ax.pad < 0) return false;
+    }
+    for (int64_t b = 0; b < s.sw; ++b) {
+        DgradAxis ax;
+        if (dgrad_axis(b, s.w, s.sw, s.pw, s.dw, s.s, &ax) && ax.taps > 0 && ax.pad < 0) return false;
+    }
+    return true;
+}
+
+// The forward problem of one phase: input dy [N][P][Q][K], output the phase's
+// [N][out_h][out_w][C] pixels, R' x S' taps at dilations d'.
+Shape dgrad_phase_shape(const Shape& s, const DgradAxis& ah, const DgradAxis& aw)
+{
+    Shape t = s;
+    t.h = s.p; t.w = s.q; t.c = s.k; t.k = s.c;
+    t.r = ah.taps; t.s = aw.taps;
+    t.sh = 1; t.sw = 1;
+    t.dh = ah.dil; t.dw = aw.dil;
+    t.ph = ah.pad; t.pw = aw.pad;
+    t.g = 1; t.cg = t.c; t.kg = t.k;
+    t.p = ah.out; t.q = aw.out;
+    t.m = s.n * t.p * t.q;
+    t.crs = t.c * t.r * t.s;
+    return t;
+}
+
+// The whole-gradient forward problem (stride 1), used to size the workspace: every
+// phase has at most its output pixels and so needs at most its semaphores.
 Shape dgrad_forward_shape(const Shape& s)
 {
     Shape t = s;
@@ -1626,46 +1697,28 @@ int dgrad_plan(const Shape& t, const conv2d_algo* algo, Plan* plan)
     return choose_plan(t, &f, plan);
 }
 
-int run_dgrad(const conv2d_params* params, const void* dy, const void* w, float* dx, void* workspace,
-              size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+// One launch: phase (a, b) with axes ah, aw (stride 1: a = b = 0, the whole dx).
+int launch_dgrad_phase(const Shape& s, const DgradAxis& ah, const DgradAxis& aw, int64_t a, int64_t b, const void* dy,
+                       const void* w, float* dx, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                       const conv2d_algo* algo)
 {
-    g_last_launches = 0;
-    Shape s;
-    int rc = make_shape(params, &s);
-    if (rc != CONV2D_OK) return rc;
-    if (s.n == 0 || s.c == 0) return CONV2D_OK;  // empty input gradient
-    if (!dx || (s.k > 0 && (!dy || !w))) return CONV2D_ERR_INVALID;
-    if (!aligned16(dx) || (dy && !aligned16(dy)) || (w && !aligned16(w)) || (workspace && !aligned16(workspace)))
-        return CONV2D_ERR_ALIGNMENT;
-    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
-                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
-                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
-        return CONV2D_ERR_INVALID;
-    if (s.k == 0) {  // no filters: the gradient is zero
-        if (cudaMemsetAsync(dx, 0, static_cast<size_t>(s.n * s.h * s.w * s.c) * sizeof(float), stream) != cudaSuccess)
-            return CONV2D_ERR_CUDA;
-        return CONV2D_OK;
-    }
-    if (!dgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
-    const Shape t = dgrad_forward_shape(s);
+    const Shape t = dgrad_phase_shape(s, ah, aw);
     Plan plan;
-    rc = dgrad_plan(t, algo, &plan);
+    int rc = dgrad_plan(t, algo, &plan);
     if (rc != CONV2D_OK) return rc;
     const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(t);
-    const bool cuts = plan_cuts_tiles(plan);
-    if (cuts && !have_ws) return CONV2D_ERR_WORKSPACE;
-    if (workspace && !have_ws) return CONV2D_ERR_WORKSPACE;
-    if (!load_encoders()) return CONV2D_ERR_CUDA;
+    if (plan_cuts_tiles(plan) && !have_ws) return CONV2D_ERR_WORKSPACE;
 
     CUtensorMap tm_a, tm_b;
     std::memset(&tm_a, 0, sizeof(tm_a));
     std::memset(&tm_b, 0, sizeof(tm_b));
-    {   // dy through the forward im2col map of problem t (128-pixel columns, 64 channels)
+    {   // dy through an im2col map whose window origins run over the phase's t.p x t.q
+        // output pixels: lower corner -pad, upper corner (out - in) - pad per axis.
         const cuuint64_t dims[4] = {(cuuint64_t)t.c, (cuuint64_t)t.w, (cuuint64_t)t.h, (cuuint64_t)t.n};
         const cuuint64_t strides[3] = {(cuuint64_t)(t.c * 2), (cuuint64_t)(t.w * t.c * 2),
                                        (cuuint64_t)(t.h * t.w * t.c * 2)};
         const int lower[2] = {(int)-t.pw, (int)-t.ph};
-        const int upper[2] = {(int)(t.pw - (t.s - 1) * t.dw), (int)(t.ph - (t.r - 1) * t.dh)};
+        const int upper[2] = {(int)(t.q - t.w - t.pw), (int)(t.p - t.h - t.ph)};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
         if (g_encode_im2col(&tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, lower,
                             upper, BK, static_cast<cuuint32_t>(plan.block_m), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1710,19 +1763,73 @@ int run_dgrad(const conv2d_params* params, const void* dy, const void* w, float*
     kp.debug_flags = algo ? algo->debug_flags : 0;
     kp.reduce_concurrent = (algo && algo->reduction == CONV2D_REDUCTION_ORDERED) ? 0 : 1;
     kp.wait_limit_ns = (algo && algo->wait_limit_ns > 0) ? (unsigned long long)algo->wait_limit_ns : kDefaultWaitNs;
+    kp.dg_r0 = ah.r0; kp.dg_rm = ah.m; kp.dg_s0 = aw.r0; kp.dg_sm = aw.m; kp.dg_S = (int)s.s;
+    kp.dg_phase = (s.sh > 1 || s.sw > 1) ? 1 : 0;
+    kp.dg_H = (int)s.h; kp.dg_W = (int)s.w; kp.dg_a = (int)a; kp.dg_b = (int)b;
+    kp.dg_sh = (int)s.sh; kp.dg_sw = (int)s.sw;
     kp.trace = nullptr;
 #ifdef SGB_TRACE_ENABLED
     kp.trace = g_trace;
 #endif
     if (log_enabled())
-        std::fprintf(stderr, "[conv2d dgrad] M=%lld C=%lld KRS=%lld -> BN=%d splits=%d grid=%d\n", (long long)t.m,
-                     (long long)t.k, (long long)t.crs, plan.block_n, plan.splits, plan.grid);
+        std::fprintf(stderr, "[conv2d dgrad] phase (%lld,%lld) M=%lld C=%lld KRS=%lld -> BN=%d splits=%d grid=%d\n",
+                     (long long)a, (long long)b, (long long)t.m, (long long)t.k, (long long)t.crs, plan.block_n,
+                     plan.splits, plan.grid);
     cudaError_t err;
     if (plan.block_n == 64) err = sgb::launch_conv2d_tc<128, 64, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
     else if (plan.block_n == 128) err = sgb::launch_conv2d_tc<128, 128, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
     else err = sgb::launch_conv2d_tc<128, 256, sgb::LOADER_DGRAD>(tm_a, tm_b, kp, plan.grid, stream);
     if (err != cudaSuccess) return CONV2D_ERR_CUDA;
-    g_last_launches = 1;
+    ++g_last_launches;
+    return CONV2D_OK;
+}
+
+int run_dgrad(const conv2d_params* params, const void* dy, const void* w, float* dx, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.n == 0 || s.c == 0) return CONV2D_OK;  // empty input gradient
+    if (!dx || (s.k > 0 && (!dy || !w))) return CONV2D_ERR_INVALID;
+    if (!aligned16(dx) || (dy && !aligned16(dy)) || (w && !aligned16(w)) || (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_ALIGNMENT;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
+                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
+                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
+        return CONV2D_ERR_INVALID;
+    const size_t dx_bytes = static_cast<size_t>(s.n * s.h * s.w * s.c) * sizeof(float);
+    if (s.k == 0) {  // no filters: the gradient is zero
+        if (cudaMemsetAsync(dx, 0, dx_bytes, stream) != cudaSuccess) return CONV2D_ERR_CUDA;
+        return CONV2D_OK;
+    }
+    if (!dgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    const Shape full = dgrad_forward_shape(s);
+    if (workspace && workspace_bytes < workspace_bytes_for(full)) return CONV2D_ERR_WORKSPACE;
+    if (!load_encoders()) return CONV2D_ERR_CUDA;
+    // Phases with no tap contribute nothing: dx starts at zero when there is one.
+    bool empty_phase = false;
+    for (int64_t a = 0; a < s.sh; ++a)
+        for (int64_t b = 0; b < s.sw; ++b) {
+            DgradAxis ah, aw;
+            if (!dgrad_axis(a, s.h, s.sh, s.ph, s.dh, s.r, &ah) || !dgrad_axis(b, s.w, s.sw, s.pw, s.dw, s.s, &aw))
+                continue;
+            if (ah.taps == 0 || aw.taps == 0) empty_phase = true;
+        }
+    if (empty_phase && cudaMemsetAsync(dx, 0, dx_bytes, stream) != cudaSuccess) return CONV2D_ERR_CUDA;
+    int launches = 0;
+    for (int64_t a = 0; a < s.sh; ++a)
+        for (int64_t b = 0; b < s.sw; ++b) {
+            DgradAxis ah, aw;
+            if (!dgrad_axis(a, s.h, s.sh, s.ph, s.dh, s.r, &ah) || !dgrad_axis(b, s.w, s.sw, s.pw, s.dw, s.s, &aw))
+                continue;
+            if (ah.taps == 0 || aw.taps == 0) continue;
+            rc = launch_dgrad_phase(s, ah, aw, a, b, dy, w, dx, workspace, workspace_bytes, stream, algo);
+            if (rc != CONV2D_OK) return rc;
+            ++launches;
+        }
+    g_last_launches = launches;
     return CONV2D_OK;
 }
 
@@ -1938,8 +2045,20 @@ int conv2d_bwd_data_query_algo(const conv2d_params* params, conv2d_algo* out)
     int rc = make_shape(params, &s);
     if (rc != CONV2D_OK) return rc;
     if (!dgrad_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
+    // The plan of the first phase with taps (stride 1: the only one).
+    Shape t = dgrad_forward_shape(s);
+    bool found = false;
+    for (int64_t a = 0; a < s.sh && !found; ++a)
+        for (int64_t b = 0; b < s.sw && !found; ++b) {
+            DgradAxis ah, aw;
+            if (dgrad_axis(a, s.h, s.sh, s.ph, s.dh, s.r, &ah) && dgrad_axis(b, s.w, s.sw, s.pw, s.dw, s.s, &aw) &&
+                ah.taps > 0 && aw.taps > 0) {
+                t = dgrad_phase_shape(s, ah, aw);
+                found = true;
+            }
+        }
     Plan plan;
-    rc = dgrad_plan(dgrad_forward_shape(s), nullptr, &plan);
+    rc = dgrad_plan(t, nullptr, &plan);
     if (rc != CONV2D_OK) return rc;
     std::memset(out, 0, sizeof(*out));
     out->block_m = plan.block_m;

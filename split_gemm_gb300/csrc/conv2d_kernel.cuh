@@ -173,6 +173,13 @@ struct ConvKernelParams {
     // (0 <= unit_offset < stages per tile) so that no range starts on a tile
     // boundary (see PairWalker).
     int unit_offset;
+    // Data gradient (LOADER_DGRAD).  Filter tap (r, s) of the launch (kernel order,
+    // flipped) reads the original tap (dg_r0 + dg_rm*(R-1-r), dg_s0 + dg_sm*(S-1-s))
+    // of a filter with dg_S columns; stride 1 is (0, 1, 0, 1, S).  At stride > 1 a
+    // launch computes one output phase (dg_phase = 1): its pixel (n, i, j) is dx
+    // pixel (n, dg_a + dg_sh*i, dg_b + dg_sw*j) of a dx with dg_H x dg_W pixels.
+    int dg_r0, dg_rm, dg_s0, dg_sm, dg_S;
+    int dg_phase, dg_H, dg_W, dg_a, dg_b, dg_sh, dg_sw;
     // CTA-pair kernels: y as a 2-D fp32 tensor {K, M} (row pitch ldy) for TMA
     // stores and reductions of 32-column x 64-row boxes in the 128-byte swizzle;
     // tma_y = 0 when it is not encoded (the epilogue then writes with st.global).
@@ -428,6 +435,14 @@ __device__ __forceinline__ void halo_origin(const ConvKernelParams& kp, int m_ti
 // GEMM row (output pixel index) of row `row` of tile row-block m_tile, or -1
 // when the row lies past the output.  (n0, p0, q0) is the box origin (box
 // loader only).
+// Data gradient: the original filter tap (index into R*S) that kernel tap (r, s)
+// reads (the taps run flipped; at stride > 1 a phase's taps are every dg_rm-th row
+// and dg_sm-th column of the filter).
+__device__ __forceinline__ int dgrad_tap(const ConvKernelParams& kp, int r, int s)
+{
+    return (kp.dg_r0 + kp.dg_rm * (kp.R - 1 - r)) * kp.dg_S + (kp.dg_s0 + kp.dg_sm * (kp.S - 1 - s));
+}
+
 template <int BM, int LOADER>
 __device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile, int row, int n0, int p0, int q0)
 {
@@ -448,6 +463,17 @@ __device__ __forceinline__ int tile_row_m(const ConvKernelParams& kp, int m_tile
         const int n = n0 + t / kp.bh;
         if (q >= kp.Q || p >= kp.P || n >= kp.N) return -1;
         return (n * kp.P + p) * kp.Q + q;
+    } else if constexpr (LOADER == LOADER_DGRAD) {
+        (void)n0; (void)p0; (void)q0;
+        const int m = m_tile * BM + row;
+        if (m >= kp.M) return -1;
+        if (!kp.dg_phase) return m;
+        // Phase pixel (n, i, j) -> dx pixel (n, a + sh*i, b + sw*j).
+        const int j = m % kp.Q;
+        const int t = m / kp.Q;
+        const int i = t % kp.P;
+        const int n = t / kp.P;
+        return (n * kp.dg_H + kp.dg_a + kp.dg_sh * i) * kp.dg_W + kp.dg_b + kp.dg_sw * j;
     } else {
         (void)n0; (void)p0; (void)q0;
         const int m = m_tile * BM + row;
@@ -548,7 +574,7 @@ struct LoadCursor {
         } else if constexpr (LOADER == LOADER_DGRAD) {
             // w as {C, R*S, K}: for the flipped tap, output channels n0 + 64i .. +63 (contiguous)
             // x dy channels c .. c+63 (rows): BN / 64 boxes of 64 rows of 128 bytes, 8 KB apart.
-            const int tap = (kp.R - 1 - r) * kp.S + (kp.S - 1 - s);
+            const int tap = dgrad_tap(kp, r, s);
 #pragma unroll
             for (int i = 0; i < BN / 64; ++i) ptx::tma_load_3d(b_dst + i * BK * 128, tm_b, bar, n0 + 64 * i, tap, c);
         } else if constexpr (LOADER == LOADER_BOX) ptx::tma_load_3d(b_dst, tm_b, bar, 0, n0, kb * KC);  // KC k-blocks
@@ -570,7 +596,7 @@ struct LoadCursor {
         } else if constexpr (LOADER == LOADER_DGRAD) {
             ptx::tma_prefetch_im2col_4d(tm_a, c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),
                                         static_cast<uint16_t>(r * kp.dh));
-            const int tap = (kp.R - 1 - r) * kp.S + (kp.S - 1 - s);
+            const int tap = dgrad_tap(kp, r, s);
             for (int i = 0; i < BN / 64; ++i) ptx::tma_prefetch_3d(tm_b, n0 + 64 * i, tap, c);
         } else {
             ptx::tma_prefetch_im2col_4d(tm_a, c_base + c, w_org, h_org, n_img, static_cast<uint16_t>(s * kp.dw),

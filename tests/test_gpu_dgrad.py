@@ -1,5 +1,6 @@
-"""Data gradient (conv2d_bwd_data) and conv_transpose2d at stride 1 against the CPU
-oracle, element by element, through the C ABI (needs a GB300).
+"""Data gradient (conv2d_bwd_data) and conv_transpose2d against the CPU oracle, element
+by element, through the C ABI (needs a GB300): stride 1 (one launch) and strides 2 and 3
+(one launch per output phase, the sub-pixel decomposition).
 
 Inputs: dy ~ N(0, 1), weights He-init as the forward workloads draw them, so each
 term dy*w has the forward terms' scale and the forward bar applies with C*R*S
@@ -37,11 +38,11 @@ def _extent(i, pad, dil, ker, st):
     return 0 if room < 0 else room // st + 1
 
 
-def _case(n, h, w, c, k, r, s, pad=0, dil=1, seed=0, ints=False):
+def _case(n, h, w, c, k, r, s, pad=0, dil=1, seed=0, ints=False, stride=1):
     def pair(v):
         return v if isinstance(v, tuple) else (v, v)
-    (ph, pw), (dh, dw) = pair(pad), pair(dil)
-    p, q = _extent(h, ph, dh, r, 1), _extent(w, pw, dw, s, 1)
+    (ph, pw), (dh, dw), (sh, sw) = pair(pad), pair(dil), pair(stride)
+    p, q = _extent(h, ph, dh, r, sh), _extent(w, pw, dw, s, sw)
     g = torch.Generator().manual_seed(2000 + seed)
     if ints:
         dy = torch.randint(-3, 4, (n, p, q, k), generator=g).to(torch.bfloat16)
@@ -49,7 +50,7 @@ def _case(n, h, w, c, k, r, s, pad=0, dil=1, seed=0, ints=False):
     else:
         dy = torch.randn((n, p, q, k), generator=g).to(torch.bfloat16)
         wt = (torch.randn((k, r, s, c), generator=g) * math.sqrt(2.0 / (c * r * s))).to(torch.bfloat16)
-    opts = dict(stride=1, padding=(ph, pw), dilation=(dh, dw))
+    opts = dict(stride=(sh, sw), padding=(ph, pw), dilation=(dh, dw))
     return dy, wt, (n, h, w, c), opts
 
 
@@ -138,7 +139,7 @@ def test_dgrad_no_filters_gives_zero(sg):
 
 
 @pytest.mark.parametrize("xs,ws,stride,pad,groups", [
-    ((1, 8, 8, 64), (64, 3, 3, 64), 2, 1, 1),   # stride 2
+    ((1, 8, 8, 64), (64, 3, 3, 64), 2, 2, 1),   # stride 2, pad 2: phase 1 has one tap and padding -1
     ((1, 8, 8, 64), (32, 3, 3, 64), 1, 1, 1),   # K % 64 != 0
     ((1, 8, 8, 12), (64, 3, 3, 12), 1, 1, 1),   # C % 8 != 0
     ((1, 8, 8, 128), (64, 3, 3, 64), 1, 1, 2),  # groups
@@ -154,20 +155,98 @@ def test_dgrad_unsupported_shapes_refused(sg, xs, ws, stride, pad, groups):
     assert e.value.code == 2
 
 
-FULL = ["resnet_56x56_c64", "resnet_28x28_c256", "splitk_7x7_c2048", "dil2_64_c128"]
+def _phases_with_taps(h, st, pad, dil, ker):
+    """Output phases a (rows h = a + st*i exist) that some filter tap reaches."""
+    return [a for a in range(min(st, h)) if any((a + pad - r * dil) % st == 0 for r in range(ker))]
+
+
+STRIDED = [
+    ("s2_3x3_pad1", dict(n=2, h=14, w=14, c=64, k=64, r=3, s=3, pad=1, stride=2)),
+    ("s2_1x1", dict(n=2, h=15, w=16, c=128, k=64, r=1, s=1, pad=0, stride=2)),      # phases with no tap
+    ("s2_7x7_pad3", dict(n=1, h=22, w=20, c=64, k=64, r=7, s=7, pad=3, stride=2)),
+    ("s2_dil2", dict(n=2, h=13, w=12, c=64, k=128, r=3, s=3, pad=2, dil=2, stride=2)),  # gcd(2, 2) = 2
+    ("s3_5x3", dict(n=2, h=17, w=16, c=72, k=64, r=5, s=3, pad=(2, 0), stride=3)),
+    ("s23_asym", dict(n=3, h=11, w=13, c=64, k=192, r=3, s=4, pad=(1, 1), stride=(2, 3))),
+    ("s2_valid", dict(n=2, h=9, w=10, c=96, k=64, r=3, s=3, pad=0, stride=2)),
+    ("s2_ragged_h", dict(n=1, h=7, w=9, c=8, k=64, r=4, s=2, pad=(1, 0), stride=(3, 2))),
+]
+
+
+@pytest.mark.parametrize("bn", [0, 64, 256])
+@pytest.mark.parametrize("geom", STRIDED, ids=[g[0] for g in STRIDED])
+def test_dgrad_strided_geometries(sg, geom, bn):
+    """Stride > 1: one launch per output phase that a tap reaches; the rest of dx is zero."""
+    name, kw = geom
+    kw = dict(kw)
+    def pair(v):
+        return v if isinstance(v, tuple) else (v, v)
+    k, r, s = kw["k"], kw["r"], kw["s"]
+    (sh, sw), (ph, pw), (dh, dw) = pair(kw["stride"]), pair(kw["pad"]), pair(kw.get("dil", 1))
+    dy, wt, xs, opts = _case(kw.pop("n"), kw.pop("h"), kw.pop("w"), kw.pop("c"), kw.pop("k"), kw.pop("r"),
+                             kw.pop("s"), seed=zlib.crc32(name.encode()) % 1000, **kw)
+    got = _gpu(sg, dy, wt, xs, opts, algo=make_algo(sg, block_n=bn, wait_limit_ns=WAIT))
+    phases = len(_phases_with_taps(xs[1], sh, ph, dh, r)) * len(_phases_with_taps(xs[2], sw, pw, dw, s))
+    assert sg.last_launch_count() == phases
+    ref = od.conv2d_dgrad(dy, wt, xs, **opts)
+    check_close(got, ref, k, r, s, f"dgrad {name} bn={bn}")
+
+
+@pytest.mark.parametrize("stride,pad", [(2, 1), (3, 0)])
+def test_dgrad_strided_integer_inputs_exact(sg, stride, pad):
+    dy, wt, xs, opts = _case(2, 13, 14, 64, 128, 3, 3, pad=pad, seed=17 + stride, ints=True, stride=stride)
+    got = _gpu(sg, dy, wt, xs, opts, algo=make_algo(sg, wait_limit_ns=WAIT))
+    ref = od.conv2d_dgrad(dy, wt, xs, **opts)
+    assert np.array_equal(got, ref), f"{int(np.count_nonzero(got != ref))} of {got.size} differ"
+
+
+@pytest.mark.parametrize("forced", [dict(splits=3), dict(grid=3), dict(splits=2, reduction=1)],
+                         ids=["splits3", "grid3", "splits2_ordered"])
+def test_dgrad_strided_cut_tiles(sg, forced):
+    """Cut tiles in every phase (the one-tap phase has 4 k-blocks), the phases reusing one
+    workspace in stream order."""
+    dy, wt, xs, opts = _case(2, 12, 12, 128, 256, 3, 3, pad=1, seed=9, stride=2)
+    params = sg.make_params(xs, wt.shape, **opts)
+    ws = torch.zeros(sg.dgrad_workspace_bytes(params), dtype=torch.uint8, device="cuda")
+    got = _gpu(sg, dy, wt, xs, opts, algo=make_algo(sg, wait_limit_ns=WAIT, **forced), workspace=ws)
+    ref = od.conv2d_dgrad(dy, wt, xs, **opts)
+    check_close(got, ref, 256, 3, 3, f"strided dgrad forced {forced}")
+    assert int(torch.count_nonzero(ws)) == 0
+    assert sg.status(ws) == 0
+
+
+@pytest.mark.parametrize("geom", [(2, 7, 7, 64, 64, 3, 3, 1, 1, 2, 1), (1, 6, 5, 64, 32, 4, 4, 1, 1, 2, 0),
+                                  (2, 5, 6, 128, 64, 3, 3, 0, 1, 3, 2)])
+def test_conv_transpose2d_strided(sg, geom):
+    """conv_transpose2d with stride and output padding: the data gradient of the forward
+    conv from the transposed output size back to the input's (oracle definition)."""
+    n, hi, wi, cin, cout, r, s, pad, dil, st, op = geom
+    g = torch.Generator().manual_seed(sum(geom))
+    x = torch.randn((n, hi, wi, cin), generator=g).to(torch.bfloat16)
+    wt = (torch.randn((cin, r, s, cout), generator=g) * math.sqrt(2.0 / (cin * r * s))).to(torch.bfloat16)
+    y = sg.conv_transpose2d(x.cuda(), wt.cuda(), padding=pad, dilation=dil, stride=st, output_padding=op)
+    torch.cuda.synchronize()
+    ho = (hi - 1) * st - 2 * pad + dil * (r - 1) + 1 + op
+    wo = (wi - 1) * st - 2 * pad + dil * (s - 1) + 1 + op
+    assert tuple(y.shape) == (n, ho, wo, cout)
+    ref = od.conv2d_dgrad(x, wt, (n, ho, wo, cout), st, pad, dil)
+    check_close(y.cpu().numpy(), ref, cin, r, s, f"conv_transpose2d {geom}")
+
+
+FULL = ["resnet_56x56_c64", "resnet_28x28_c256", "splitk_7x7_c2048", "dil2_64_c128", "proj_56_c256_1x1s2"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_dgrad_full_size_workloads(sg, name):
-    """The data gradient of each eligible (stride-1) workload at full size (the heuristic's
-    plan), checked on sampled elements against the oracle one by one."""
+    """The data gradient of each eligible workload at full size (the heuristic's plan; the
+    1x1 stride-2 projection through its one phase with a tap, the other three zero), checked
+    on sampled elements against the oracle one by one."""
     wl = workloads.get(name)
     _, w, _ = workloads.make_inputs(wl)
     dy = workloads.make_output_grad(wl, variance=1.0)
     o = wl.options()
     xs = (wl.n, wl.h, wl.w, wl.c)
     got = _gpu(sg, dy, w, xs, dict(stride=o["stride"], padding=o["padding"], dilation=o["dilation"]))
-    assert sg.last_launch_count() == 1
+    assert sg.last_launch_count() == 1  # stride 1, or one phase with a tap
     flat = got.reshape(-1, wl.c)
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     mi = np.concatenate([rng.integers(0, flat.shape[0], 3000), [0, 0, flat.shape[0] - 1, flat.shape[0] - 1]])
