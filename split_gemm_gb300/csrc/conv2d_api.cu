@@ -727,6 +727,8 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
 //    tiles fill at least 70% of the resident pairs' waves and whose
 //    virtual pixels (padded row pitch, image pairs) exceed the output pixels by
 //    at most 20%: the halo loader, one tile per pair per wave.
+//  - Otherwise, where the pair tiles cover at least half the resident pairs
+//    (and waste at most 35% of their rows): the im2col pair loader.
 int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
 {
     if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
@@ -765,6 +767,17 @@ int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
                 if (choose_pair_halo_plan(s, &f, plan, true) == CONV2D_OK) return CONV2D_OK;
             }
         }
+    }
+    // Otherwise the im2col pair kernel with its own schedule, where its 256-row tiles
+    // cover at least half the resident pairs and waste at most 35% of their rows.
+    const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
+    const int64_t res = pair_max_resident(bn, 2, whole_tiles);
+    if (res > 0 && m_tiles * cdiv(s.k, bn) * 2 >= res && m_tiles * sgb::PAIR_TILE_M * 20 <= s.m * 27) {
+        f.loader = CONV2D_LOADER_TMA_PAIR;
+        f.block_n = bn;
+        f.splits = 0;
+        f.grid = 0;
+        if (choose_pair_plan(s, &f, plan, whole_tiles) == CONV2D_OK) return CONV2D_OK;
     }
     return CONV2D_ERR_UNSUPPORTED;
 }

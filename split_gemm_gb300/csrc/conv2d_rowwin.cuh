@@ -53,6 +53,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "slab_store.cuh"
 #include "trace.cuh"
 
 namespace sgb {
@@ -584,12 +585,14 @@ __device__ void rw_epilogue_impl(const RowWinParams& kp, const RwSmem& sm, uint3
     if (lane == 0) ptx::mbar_arrive(sm.w_ready);
     SGB_TRACE(kp, et == 0, 2);
     int g_end = 0, freed = 0, freed_slot = 0;  // row release bookkeeping (thread et == 0)
-    // Bias of the output channels: lane l holds channels 32*j + l.
-    float bias_r[BN / 32];
+    // Bias for the vector stores: lane l adds channels 32*j + 4*(l % 8) .. +3 after the
+    // slot transpose.  (The row stores of K % 4 != 0 read theirs per slab.)
+    float4 bias4[BN / 32];
 #pragma unroll
     for (int j = 0; j < BN / 32; ++j) {
-        const int n = j * 32 + lane;
-        bias_r[j] = (add_bias && n < kp.K) ? __ldg(kp.bias + n) : 0.0f;
+        const int n4 = j * 32 + (lane & 7) * 4;
+        bias4[j] = (add_bias && kp.vec_store && n4 < kp.K) ? __ldg(reinterpret_cast<const float4*>(kp.bias + n4))
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     int ti = 0;
     for (int t = t_lo; t < t_hi; ++t, ++ti) {
@@ -629,10 +632,21 @@ __device__ void rw_epilogue_impl(const RowWinParams& kp, const RwSmem& sm, uint3
                                    (static_cast<uint32_t>(quad * 32) << 16);
             const bool last_b = b == rows_valid - 1;
             if (kp.vec_store) {
-                // TMEM -> registers (+bias) -> this warp's 32 x 32 swizzled staging slot ->
-                // 16-byte global stores, 8 lanes per 128-byte row piece.
+                // TMEM -> registers -> this warp's 32 x 32 swizzled staging slot -> 16-byte
+                // global stores, 8 lanes per 128-byte row piece, the bias added per 16-byte
+                // chunk after the transpose (slab_out: slot reads batched, stores predicated).
                 const int rsub = lane >> 3;
                 const int chunk = lane & 7;
+                const int64_t esize = (FUSED && kp.out_bf16) ? 2 : 4;
+                uint64_t rowp[8];
+                uint32_t row_ok = 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = quad * 32 + 4 * i + rsub;
+                    row_ok |= (row < nv ? 1u : 0u) << i;
+                    rowp[i] = reinterpret_cast<uint64_t>(kp.y) +
+                              static_cast<uint64_t>(((m0 + (row < nv ? row : 0)) * kp.K + chunk * 4) * esize);
+                }
 #pragma unroll
                 for (int j = 0; j < BN / 32; ++j) {
                     uint32_t v[32];
@@ -644,34 +658,13 @@ __device__ void rw_epilogue_impl(const RowWinParams& kp, const RwSmem& sm, uint3
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(&sm.acc_empty[buf]);
                     }
-                    if (add_bias) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
-                    }
-                    __syncwarp();  // the previous slab's reads of the slot are done
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        ptx::st_shared_v4(saddr + static_cast<uint32_t>(lane * 128 + ((c ^ (lane & 7)) << 4)),
-                                          v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                    __syncwarp();
-                    const int col = j * 32 + chunk * 4;
                     SGB_CYCLES_BEGIN(t_st);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = 4 * i + rsub;  // row within the warp's 32 rows
-                        const int row = quad * 32 + rr;
-                        uint4 val =
-                            ptx::ld_shared_v4(saddr + static_cast<uint32_t>(rr * 128 + ((chunk ^ (rr & 7)) << 4)));
-                        if (FUSED && kp.relu) val = ptx::relu4(val);
-                        if (row < nv && col < kp.K) {
-                            if (FUSED && kp.out_bf16)
-                                *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(kp.y) + (m0 + row) * kp.K + col) =
-                                    ptx::pack_bf16x4(val);
-                            else
-                                *reinterpret_cast<uint4*>(kp.y + (m0 + row) * kp.K + col) = val;
-                        }
-                    }
+                    const bool col_ok = j * 32 + chunk * 4 < kp.K;
+                    const int64_t off = static_cast<int64_t>(j) * 32 * esize;
+                    if (FUSED && kp.out_bf16)
+                        slab_out<SLAB_BF16>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], FUSED && kp.relu);
+                    else
+                        slab_out<SLAB_F32>(saddr, v, rowp, off, row_ok, col_ok, add_bias, bias4[j], FUSED && kp.relu);
                     SGB_CYCLES_END(c_st, t_st);
                 }
             } else {
@@ -688,9 +681,11 @@ __device__ void rw_epilogue_impl(const RowWinParams& kp, const RwSmem& sm, uint3
                         ptx::mbar_arrive(&sm.acc_empty[buf]);
                     }
                     if (add_bias) {
+                        const int n = j * 32 + lane;
+                        const float bias_l = n < kp.K ? __ldg(kp.bias + n) : 0.0f;  // lane l: channel 32*j + l
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_r[j], e));
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __shfl_sync(0xffffffffu, bias_l, e));
                     }
                     if (row >= nv) continue;
 #pragma unroll

@@ -44,7 +44,7 @@ def test_map_cache_hits_and_reencodes(sg):
     dev = torch.device("cuda", 0)
     wl, x, w, b = _case(2, 14, 14, 31)
     params = sg.make_params(x.shape, w.shape, **wl.options())
-    assert sg.query_algo(params).loader == sg.LOADER_TMA_IM2COL  # a loader that encodes maps
+    assert sg.query_algo(params).loader in (sg.LOADER_TMA_IM2COL, sg.LOADER_TMA_PAIR)  # loaders that encode maps
     xd, wd, bd = x.to(dev), w.to(dev), b.to(dev)
 
     h0, m0 = sg.tensor_map_cache_stats()
