@@ -110,14 +110,23 @@ typedef enum {
                                      K % 4 == 0; block_m is 256 (or 0); grid counts CTA pairs; a fused
                                      epilogue runs on whole tiles only.  The heuristic takes it for such
                                      shapes when nothing else is forced */
-    CONV2D_LOADER_PAIR_HALO = 10  /* stride 1 on clusters of two CTAs: each CTA holds 128 consecutive pixels of
+    CONV2D_LOADER_PAIR_HALO = 10, /* stride 1 on clusters of two CTAs: each CTA holds 128 consecutive pixels of
                                      one image seen with the padded row pitch W + 2*pad_w (pixels past Q are
                                      computed and discarded), the pair the same pixels of two images; per
                                      64-channel chunk one tiled TMA box of whole padded input rows serves every
                                      filter tap, read in place by 2-CTA tensor-core MMAs, and the weights of
-                                     two taps come in one box per stage.  Needs groups == 1, stride 1,
+                                     two or three taps come in one box per stage.  Needs groups == 1, stride 1,
                                      C % 64 == 0, K % 4 == 0, W + 2*pad_w <= 256 and the two halo buffers within
                                      shared memory; block_m is 256 (or 0); grid counts CTA pairs */
+    CONV2D_LOADER_BLOCKDIAG = 11  /* grouped convolution with C/groups == K/groups = cg in {8, 16, 32} and groups a
+                                     multiple of 64/cg: 64/cg groups merged into one 64-channel group whose weight
+                                     is block-diagonal (zeros outside each output channel's own group), expanded
+                                     into the workspace by a first launch (K*R*S*64 bf16 after the semaphores;
+                                     conv2d_fwd_workspace_bytes includes it), then the grouped implicit GEMM on
+                                     TMA im2col boxes.  The heuristic's choice for such layers when the
+                                     workspace has room (else the direct kernel); forcing it needs the room.
+                                     Only reported by the query functions or forced: no other field may be set
+                                     with it */
 } conv2d_loader;
 
 /* Kernel configuration.  All-zero fields mean "let the heuristic choose".

@@ -24,7 +24,7 @@ from . import _build
 
 __all__ = [
     "Conv2dError", "Params", "Algo", "LOADER_AUTO", "LOADER_TMA_IM2COL", "LOADER_CPASYNC", "LOADER_SCALAR",
-    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "LOADER_DIRECT", "LOADER_TMA_PAIR", "LOADER_PAIR_HALO", "REDUCTION_AUTO", "REDUCTION_ORDERED",
+    "LOADER_HYBRID", "LOADER_ROW_WINDOW", "LOADER_TMA_BOX", "LOADER_HALO", "LOADER_DIRECT", "LOADER_TMA_PAIR", "LOADER_PAIR_HALO", "LOADER_BLOCKDIAG", "REDUCTION_AUTO", "REDUCTION_ORDERED",
     "REDUCTION_CONCURRENT", "Epilogue", "ACT_NONE", "ACT_RELU", "OUT_F32", "OUT_BF16",
     "DEBUG_SKIP_SIGNAL", "DEBUG_TMA_STORE", "load_library", "library_path", "make_params", "output_shape", "workspace_bytes",
     "query_algo", "epi_workspace_bytes", "conv2d_bwd_weight", "conv2d_bwd_weight_into",
@@ -39,6 +39,7 @@ LOADER_HALO = 7
 LOADER_DIRECT = 8
 LOADER_TMA_PAIR = 9
 LOADER_PAIR_HALO = 10
+LOADER_BLOCKDIAG = 11
 REDUCTION_AUTO, REDUCTION_ORDERED, REDUCTION_CONCURRENT = 0, 1, 2
 ACT_NONE, ACT_RELU = 0, 1
 OUT_F32, OUT_BF16 = 0, 1

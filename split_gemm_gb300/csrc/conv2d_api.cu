@@ -969,6 +969,8 @@ size_t workspace_bytes_for(const Shape& s)
 // Where the fused epilogue's fp32 partial-sum buffer starts in the workspace.
 size_t part_offset(const Shape& s) { return (workspace_bytes_for(s) + 255) & ~size_t(255); }
 
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
 // Workspace one call needs: status and semaphores, plus under a fused epilogue
 // an fp32 [M][K] partial-sum buffer when the plan cuts tiles.
 size_t workspace_bytes_for_plan(const Shape& s, const Plan& plan, bool fused)
@@ -1321,38 +1323,40 @@ int run_direct(const Shape& s, const void* x, const void* w, const float* bias, 
     return CONV2D_OK;
 }
 
-int run_conv(const conv2d_params* params, const void* x, const void* w, const float* bias, float* y,
-             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo,
-             const conv2d_epilogue* epi = nullptr)
+// Block-diagonal grouped tiles: groups of cg = 8, 16 or 32 channels (cg input and
+// cg output channels each) merged 64 / cg at a time into groups of 64, the
+// weight expanded to [K][R][S][64] with zeros outside each output channel's own
+// group (launch_expand_blockdiag).  The tensor cores then do 64 / cg times the
+// multiplications, but through TMA im2col boxes and 128 x 64 MMAs instead of
+// CUDA-core FMAs.
+bool blockdiag_eligible(const Shape& s)
 {
-    g_last_launches = 0;
-    Shape s;
-    int rc = make_shape(params, &s);
-    if (rc != CONV2D_OK) return rc;
-    if (s.m == 0 || s.k == 0) return CONV2D_OK;  // empty batch or no filters: nothing to compute
-    if (!x || !w || !y) return CONV2D_ERR_INVALID;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
-        (workspace && !aligned16(workspace)))
-        return CONV2D_ERR_ALIGNMENT;
-    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
-                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
-                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
-        return CONV2D_ERR_INVALID;
-    if (epi && (epi->activation < CONV2D_ACT_NONE || epi->activation > CONV2D_ACT_RELU ||
-                epi->out_dtype < CONV2D_OUT_F32 || epi->out_dtype > CONV2D_OUT_BF16))
-        return CONV2D_ERR_INVALID;
-    const bool relu = epi && epi->activation == CONV2D_ACT_RELU;
-    const bool out_bf16 = epi && epi->out_dtype == CONV2D_OUT_BF16;
+    if (s.g < 2 || s.cg != s.kg || (s.cg != 8 && s.cg != 16 && s.cg != 32)) return false;
+    const int64_t f = 64 / s.cg;
+    return s.g % f == 0;
+}
+
+Shape blockdiag_shape(const Shape& s)
+{
+    Shape t = s;
+    const int64_t f = 64 / s.cg;
+    t.g = s.g / f;
+    t.cg = 64;
+    t.kg = 64;
+    t.crs = t.r * t.s * t.cg;
+    return t;
+}
+
+size_t blockdiag_weight_bytes(const Shape& s) { return static_cast<size_t>(s.k * s.r * s.s * 64) * 2; }
+
+// Launches one planned forward convolution (encodes the maps, fills the kernel
+// parameters, dispatches on the loader).
+int run_plan(const Shape& s, const Plan& plan, const void* x, const void* w, const float* bias, float* y,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo, bool relu,
+             bool out_bf16)
+{
+    int rc = CONV2D_OK;
     const bool fused = relu || out_bf16;
-    const bool force_direct = algo && algo->loader == CONV2D_LOADER_DIRECT;
-    if (force_direct || (nothing_forced(algo) && direct_eligible(s))) {
-        if (!direct_eligible(s) || (algo && (algo->splits > 1 || algo->block_m != 0)))
-            return CONV2D_ERR_UNSUPPORTED;
-        return run_direct(s, x, w, bias, y, stream, algo, relu, out_bf16);
-    }
-    Plan plan;
-    rc = choose_plan(s, algo, &plan, fused);
-    if (rc != CONV2D_OK) return rc;
     const bool have_ws = workspace && workspace_bytes >= workspace_bytes_for(s);
     // Any tile cut between CTAs needs the semaphores (and, under a fused
     // epilogue, the partial-sum buffer).
@@ -1523,7 +1527,74 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
     return CONV2D_OK;
 }
 
-size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+int run_conv(const conv2d_params* params, const void* x, const void* w, const float* bias, float* y,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream, const conv2d_algo* algo,
+             const conv2d_epilogue* epi = nullptr)
+{
+    g_last_launches = 0;
+    Shape s;
+    int rc = make_shape(params, &s);
+    if (rc != CONV2D_OK) return rc;
+    if (s.m == 0 || s.k == 0) return CONV2D_OK;  // empty batch or no filters: nothing to compute
+    if (!x || !w || !y) return CONV2D_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+        (workspace && !aligned16(workspace)))
+        return CONV2D_ERR_ALIGNMENT;
+    if (algo && (algo->splits < 0 || algo->block_n < 0 || algo->block_m < 0 || algo->grid < 0 ||
+                 algo->wait_limit_ns < 0 || algo->reduction < CONV2D_REDUCTION_AUTO ||
+                 algo->reduction > CONV2D_REDUCTION_CONCURRENT))
+        return CONV2D_ERR_INVALID;
+    if (epi && (epi->activation < CONV2D_ACT_NONE || epi->activation > CONV2D_ACT_RELU ||
+                epi->out_dtype < CONV2D_OUT_F32 || epi->out_dtype > CONV2D_OUT_BF16))
+        return CONV2D_ERR_INVALID;
+    const bool relu = epi && epi->activation == CONV2D_ACT_RELU;
+    const bool out_bf16 = epi && epi->out_dtype == CONV2D_OUT_BF16;
+    const bool fused = relu || out_bf16;
+    const bool force_direct = algo && algo->loader == CONV2D_LOADER_DIRECT;
+    // Block-diagonal grouped tiles (before the direct kernel, which they beat):
+    // groups of cg = 8, 16 or 32 channels merged 64 / cg at a time into 64-channel
+    // groups, on a weight expanded into the workspace with zeros off the diagonal
+    // blocks; the rest is the grouped implicit GEMM.  Needs the room in the workspace
+    // (else the direct kernel or the plain grouped path runs).
+    const bool force_bd = algo && algo->loader == CONV2D_LOADER_BLOCKDIAG;
+    if (force_bd && (!blockdiag_eligible(s) || algo->splits || algo->grid || algo->block_n || algo->block_m))
+        return CONV2D_ERR_UNSUPPORTED;
+    if (force_bd || (!force_direct && nothing_forced(algo) && blockdiag_eligible(s))) {
+        const Shape t = blockdiag_shape(s);
+        conv2d_algo tf;
+        std::memset(&tf, 0, sizeof(tf));
+        if (algo) {  // keep the caller's waits, hooks and reduction mode
+            tf.wait_limit_ns = algo->wait_limit_ns;
+            tf.debug_flags = algo->debug_flags;
+            tf.reduction = algo->reduction;
+        }
+        Plan tplan;
+        if (choose_plan(t, &tf, &tplan, fused) == CONV2D_OK) {
+            const size_t off = round256(workspace_bytes_for_plan(t, tplan, fused));
+            if (force_bd && !(workspace && workspace_bytes >= off + blockdiag_weight_bytes(s)))
+                return CONV2D_ERR_WORKSPACE;
+            if (workspace && workspace_bytes >= off + blockdiag_weight_bytes(s)) {
+                uint16_t* wb = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + off);
+                if (sgb::launch_expand_blockdiag(static_cast<const uint16_t*>(w), wb, (int)s.k, (int)(s.r * s.s),
+                                                 (int)s.cg, stream) != cudaSuccess)
+                    return CONV2D_ERR_CUDA;
+                rc = run_plan(t, tplan, x, wb, bias, y, workspace, workspace_bytes, stream, &tf, relu, out_bf16);
+                if (rc == CONV2D_OK) g_last_launches = 2;  // the expansion and the convolution
+                return rc;
+            }
+        }
+    }
+    if (force_direct || (nothing_forced(algo) && direct_eligible(s))) {
+        if (!direct_eligible(s) || (algo && (algo->splits > 1 || algo->block_m != 0)))
+            return CONV2D_ERR_UNSUPPORTED;
+        return run_direct(s, x, w, bias, y, stream, algo, relu, out_bf16);
+    }
+    Plan plan;
+    rc = choose_plan(s, algo, &plan, fused);
+    if (rc != CONV2D_OK) return rc;
+    return run_plan(s, plan, x, w, bias, y, workspace, workspace_bytes, stream, algo, relu, out_bf16);
+}
+
 
 // ------------------------------------------------------------------ weight gradient
 // dw[k][(r*S + s)*C + c] = sum over output pixels l of dy[l][k] * im2col(x)[l][(r, s, c)]:
@@ -1948,6 +2019,17 @@ int run_wgrad(const conv2d_params* params, const void* x, const void* dy, float*
 
 }  // namespace
 
+namespace sgb {
+// The smallest workspace a plain forward call can run with (no block-diagonal
+// weight: grouped layers then take the direct kernel or the plain grouped path).
+size_t fwd_workspace_bytes_min(const conv2d_params* params)
+{
+    Shape s;
+    if (make_shape(params, &s) != CONV2D_OK) return 0;
+    return workspace_bytes_for(s);
+}
+}  // namespace sgb
+
 extern "C" {
 
 int conv2d_fwd_output_shape(const conv2d_params* params, int64_t* p, int64_t* q)
@@ -1964,8 +2046,14 @@ size_t conv2d_fwd_workspace_bytes(const conv2d_params* params)
 {
     Shape s;
     if (make_shape(params, &s) != CONV2D_OK) return 0;
-    return workspace_bytes_for(s);
+    size_t need = workspace_bytes_for(s);
+    if (blockdiag_eligible(s)) {  // room for the block-diagonal weight after the semaphores
+        const size_t bd = round256(workspace_bytes_for(blockdiag_shape(s))) + blockdiag_weight_bytes(s);
+        if (bd > need) need = bd;
+    }
+    return need;
 }
+
 
 int conv2d_fwd_ex(const conv2d_params* params, const void* x_dev, const void* w_dev, const float* bias_dev,
                   float* y_dev, void* workspace_dev, size_t workspace_bytes, conv2d_stream_t stream,
@@ -2000,6 +2088,14 @@ int conv2d_fwd_query_algo_epi(const conv2d_params* params, const conv2d_epilogue
     Shape s;
     int rc = make_shape(params, &s);
     if (rc != CONV2D_OK) return rc;
+    if (blockdiag_eligible(s)) {  // with the workspace conv2d_fwd(_epi)_workspace_bytes asks for
+        Plan tplan;
+        if (choose_plan(blockdiag_shape(s), nullptr, &tplan, fused) == CONV2D_OK) {
+            std::memset(out, 0, sizeof(*out));
+            out->loader = CONV2D_LOADER_BLOCKDIAG;
+            return CONV2D_OK;
+        }
+    }
     if (direct_eligible(s)) {
         std::memset(out, 0, sizeof(*out));
         out->loader = CONV2D_LOADER_DIRECT;
@@ -2026,10 +2122,19 @@ size_t conv2d_fwd_epi_workspace_bytes(const conv2d_params* params, const conv2d_
     Shape s;
     if (make_shape(params, &s) != CONV2D_OK) return 0;
     const bool fused = epi && (epi->activation != CONV2D_ACT_NONE || epi->out_dtype != CONV2D_OUT_F32);
-    if (!fused) return workspace_bytes_for(s);
+    if (!fused) return conv2d_fwd_workspace_bytes(params);
     Plan plan;
-    if (s.m == 0 || s.k == 0 || choose_plan(s, algo, &plan, true) != CONV2D_OK) return workspace_bytes_for(s);
-    return workspace_bytes_for_plan(s, plan, true);
+    size_t need = workspace_bytes_for(s);
+    if (s.m > 0 && s.k > 0 && choose_plan(s, algo, &plan, true) == CONV2D_OK) need = workspace_bytes_for_plan(s, plan, true);
+    if (s.m > 0 && s.k > 0 && blockdiag_eligible(s) && (nothing_forced(algo) || algo->loader == CONV2D_LOADER_BLOCKDIAG)) {
+        const Shape t = blockdiag_shape(s);
+        Plan tplan;
+        if (choose_plan(t, nullptr, &tplan, true) == CONV2D_OK) {
+            const size_t bd = round256(workspace_bytes_for_plan(t, tplan, true)) + blockdiag_weight_bytes(s);
+            if (bd > need) need = bd;
+        }
+    }
+    return need;
 }
 
 int conv2d_fwd_query_algo(const conv2d_params* params, conv2d_algo* out)

@@ -165,4 +165,11 @@ cudaError_t launch_conv2d_direct(const DirectParams& kp, int grid, cudaStream_t 
 
 #define SGB_DIRECT_SIG(CG_) cudaError_t launch_conv2d_direct<CG_>(const DirectParams&, int, cudaStream_t)
 
+// Block-diagonal weight for grouped convolution on the tensor cores: groups of
+// cg channels (cg = 8, 16 or 32) merged 64 / cg at a time into groups of 64.
+// w [K][taps][cg] bf16 becomes wb [K][taps][64] bf16, output channel k's row
+// holding its cg weights at columns ((k / cg) % (64 / cg)) * cg .. + cg - 1 of
+// its 64-channel block and zeros elsewhere.  One thread per 16-byte chunk.
+cudaError_t launch_expand_blockdiag(const uint16_t* w, uint16_t* wb, int K, int taps, int cg, cudaStream_t stream);
+
 }  // namespace sgb

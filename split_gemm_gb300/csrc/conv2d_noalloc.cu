@@ -21,6 +21,10 @@
 
 #include "conv2d.h"
 
+namespace sgb {
+size_t fwd_workspace_bytes_min(const conv2d_params* params);  // conv2d_api.cu
+}
+
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CONV2D_NOALLOC_SCRATCH_BYTES];
@@ -50,7 +54,7 @@ int scratch_on_current_device(void** out)
 extern "C" int conv2d_fwd_noalloc(const conv2d_params* params, const void* x_dev, const void* w_dev,
                                   const float* bias_dev, float* y_dev, conv2d_stream_t stream)
 {
-    const size_t need = conv2d_fwd_workspace_bytes(params);
+    const size_t need = sgb::fwd_workspace_bytes_min(params);
     if (need == 0)  // invalid params: let the regular entry point report exactly why
         return conv2d_fwd(params, x_dev, w_dev, bias_dev, y_dev, nullptr, 0, stream);
     if (need > CONV2D_NOALLOC_SCRATCH_BYTES) return CONV2D_ERR_SCRATCH_LIMIT;

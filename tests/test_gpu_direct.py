@@ -1,6 +1,8 @@
 """The direct (CUDA-core) kernel for groups of few channels -- C/groups = K/groups in
 {1, 2, 4, 8, 16}, depthwise included -- against the CPU oracle, element by element,
-through the C ABI (needs a GB300)."""
+through the C ABI (needs a GB300).  Where block-diagonal tensor-core tiles apply
+(C/groups in {8, 16, 32}) the heuristic takes those instead; these tests force the
+direct kernel."""
 import numpy as np
 import pytest
 import torch
@@ -54,8 +56,10 @@ def test_direct_geometries(sg, geom):
     wl, x, w, b = _case(kw.pop("n"), kw.pop("h"), kw.pop("w"), kw.pop("c"), kw.pop("k"), kw.pop("r"), kw.pop("s"),
                         kw.pop("groups"), seed=51, **kw)
     params = sg.make_params(x.shape, w.shape, **wl.options())
-    assert sg.query_algo(params).loader == sg.LOADER_DIRECT
-    got = gpu_conv(sg, x, w, b, wl.options())
+    cg = wl.c // wl.groups
+    bd = cg in (8, 16, 32) and wl.groups % (64 // cg) == 0  # block-diagonal tiles take these layers
+    assert sg.query_algo(params).loader == (sg.LOADER_BLOCKDIAG if bd else sg.LOADER_DIRECT)
+    got = gpu_conv(sg, x, w, b, wl.options(), algo=make_algo(sg, loader=sg.LOADER_DIRECT))
     assert sg.last_launch_count() == 1
     ref = oracle.conv2d_fwd(x, w, b, **wl.options())
     check_close(got, ref, wl.c // wl.groups, wl.r, wl.s, f"direct {name}")
@@ -72,11 +76,12 @@ def test_direct_integer_inputs_exact(sg, groups, c):
 @pytest.mark.parametrize("mode", [(True, False), (False, True), (True, True)], ids=["relu", "bf16", "relu_bf16"])
 def test_direct_fused_epilogue(sg, mode):
     wl, x, w, b = _case(2, 14, 14, 256, 256, 3, 3, 32, pad=1, seed=53)
-    got = gpu_conv_epi(sg, x, w, b, wl.options(), *mode)
+    direct = make_algo(sg, loader=sg.LOADER_DIRECT)
+    got = gpu_conv_epi(sg, x, w, b, wl.options(), *mode, algo=direct)
     u = oracle.conv2d_fwd(x, w, b, **wl.options())
     check_epilogue(got, u, wl.c // wl.groups, wl.r, wl.s, *mode, "direct fused")
     # Same kernel, same summation order: the fused output is the plain one put through the epilogue.
-    plain = gpu_conv_epi(sg, x, w, b, wl.options(), False, False)
+    plain = gpu_conv_epi(sg, x, w, b, wl.options(), False, False, algo=direct)
     assert np.array_equal(got, epilogue.apply(plain, *mode))
 
 
