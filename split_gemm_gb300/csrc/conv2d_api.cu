@@ -456,7 +456,9 @@ bool plan_cuts_tiles(const Plan& p);
 
 // The CTA-pair kernel (conv2d_pair.cuh): 256-pixel tiles on clusters of two
 // CTAs, TMA im2col loads of 128 pixels per CTA, 16-byte vector stores.
-bool pair_eligible(const Shape& s) { return s.g == 1 && tma_im2col_eligible(s) && s.k % 4 == 0; }
+// The im2col pair kernel: C/groups % 64 == 0 (im2col boxes inside one group), K/groups % 4 == 0
+// (16-byte stores inside one group's columns).  The halo pair kernel needs groups == 1.
+bool pair_eligible(const Shape& s) { return tma_im2col_eligible(s) && s.kg % 4 == 0; }
 
 int pair_max_resident(int bn, int kbs, bool fused)
 {
@@ -518,7 +520,7 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
 {
     if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
     if (force && force->block_m != 0 && force->block_m != sgb::PAIR_TILE_M) return CONV2D_ERR_UNSUPPORTED;
-    int bn = force && force->block_n ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+    int bn = force && force->block_n ? force->block_n : (s.kg <= 64 ? 64 : (s.kg <= 128 ? 128 : 256));
     if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
     // Stage depth: two k-blocks per stage (three 64 KB stages at block_n = 256, one
     // producer thread per operand): 1.5 TMA operations per k-block against 2 with one
@@ -527,7 +529,7 @@ int choose_pair_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     const int dbg = force ? force->debug_flags : 0;
     const int kbs = (dbg & CONV2D_DEBUG_PAIR_KB1) ? 1 : 2;
     const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
-    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t n_tiles = s.g * cdiv(s.kg, bn);  // column blocks never straddle a group
     const int64_t tiles = m_tiles * n_tiles;
     const int64_t stages = cdiv(s.crs / BK, kbs);
     const int64_t units = tiles * stages;
@@ -735,10 +737,11 @@ int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     conv2d_algo f;
     std::memset(&f, 0, sizeof(f));
     if (force) f = *force;
-    const int bn = s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256);
+    const int bn = s.kg <= 64 ? 64 : (s.kg <= 128 ? 128 : 256);
+    const int64_t col_blocks = s.g * cdiv(s.kg, bn);
     if (!whole_tiles) {
         const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
-        const int64_t tiles = m_tiles * cdiv(s.k, bn);
+        const int64_t tiles = m_tiles * col_blocks;
         const int64_t stages = cdiv(s.crs / BK, 2);
         const int64_t res = pair_max_resident(bn, 2, false);
         if (res > 0 && tiles * 2 <= res && stages >= 16 && m_tiles * sgb::PAIR_TILE_M * 20 <= s.m * 27) {
@@ -772,7 +775,7 @@ int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
     // cover at least half the resident pairs and waste at most 35% of their rows.
     const int64_t m_tiles = cdiv(s.m, sgb::PAIR_TILE_M);
     const int64_t res = pair_max_resident(bn, 2, whole_tiles);
-    if (res > 0 && m_tiles * cdiv(s.k, bn) * 2 >= res && m_tiles * sgb::PAIR_TILE_M * 20 <= s.m * 27) {
+    if (res > 0 && m_tiles * col_blocks * 2 >= res && m_tiles * sgb::PAIR_TILE_M * 20 <= s.m * 27) {
         f.loader = CONV2D_LOADER_TMA_PAIR;
         f.block_n = bn;
         f.splits = 0;
@@ -1506,7 +1509,7 @@ int run_plan(const Shape& s, const Plan& plan, const void* x, const void* w, con
         kp.fd_ntiles = sgb::FastDiv(static_cast<uint32_t>(plan.n_tiles));
         kp.fd_pq = sgb::FastDiv(static_cast<uint32_t>(s.p * s.q));
         kp.fd_q = sgb::FastDiv(static_cast<uint32_t>(s.q));
-        kp.fd_c = sgb::FastDiv(static_cast<uint32_t>(s.c));
+        kp.fd_c = sgb::FastDiv(static_cast<uint32_t>(s.cg));
         kp.fd_s = sgb::FastDiv(static_cast<uint32_t>(s.s));
     }
 

@@ -202,15 +202,15 @@ struct PairCursor {
     __device__ __forceinline__ void at(const ConvKernelParams& kp, int kb)
     {
         const int kk = kb * BK;
-        const int rs = static_cast<int>(kp.fd_c.div(static_cast<uint32_t>(kk)));
-        c = kk - rs * kp.C;
+        const int rs = static_cast<int>(kp.fd_c.div(static_cast<uint32_t>(kk)));  // fd_c divides by Cg
+        c = kk - rs * kp.Cg;
         r = static_cast<int>(kp.fd_s.div(static_cast<uint32_t>(rs)));
         s = rs - r * kp.S;
     }
     __device__ __forceinline__ void step(const ConvKernelParams& kp)
     {
         c += BK;
-        if (c >= kp.C) {
+        if (c >= kp.Cg) {
             c = 0;
             if (++s == kp.S) {
                 s = 0;
@@ -219,6 +219,19 @@ struct PairCursor {
         }
     }
 };
+
+// Output channels of column block n_tile: block nb of group g = n_tile / ntpg
+// covers channels g*Kg + nb*BN .. up to the group's end; its reduction reads the
+// group's input channels from g*Cg.  One group: n0 = n_tile*BN, n_end <= K.
+template <int BN>
+__device__ __forceinline__ void pair_columns(const ConvKernelParams& kp, int n_tile, int& n0, int& n_end, int& c_base)
+{
+    const int g = n_tile / kp.ntpg;
+    n0 = g * kp.Kg + (n_tile - g * kp.ntpg) * BN;
+    const int g_end = (g + 1) * kp.Kg;
+    n_end = n0 + BN < g_end ? n0 + BN : g_end;
+    c_base = g * kp.Cg;
+}
 
 // Window origin of this CTA's first pixel in tile row-block m_tile (pixels
 // past the output decode to images >= N, which the TMA zero-fills).
@@ -261,7 +274,9 @@ __device__ void pair_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
         int n_img = 0, w_org = 0, h_org = 0;
         if (OP == PAIR_A) pair_origin(kp, m_tile, rank, n_img, w_org, h_org);
-        const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        int n0, n_end, c_base;
+        pair_columns<BN>(kp, n_tile, n0, n_end, c_base);
+        const int b_row = n0 + static_cast<int>(rank) * Cfg::B_ROWS;
         PairCursor cur;
         if (OP == PAIR_A) cur.at(kp, sg.kb_begin * KBS);
         for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
@@ -289,7 +304,7 @@ __device__ void pair_producer(const CUtensorMap* tm_a, const CUtensorMap* tm_b, 
                 if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.full[slot], 2u * static_cast<uint32_t>(nkb * Cfg::A_KB));
                 uint8_t* a_dst = sm.a + slot * Cfg::A_STAGE;
                 for (int j = 0; j < nkb; ++j) {
-                    ptx::tma_load_im2col_4d_pair(a_dst + j * Cfg::A_KB, tm_a, bar, cur.c, w_org, h_org, n_img,
+                    ptx::tma_load_im2col_4d_pair(a_dst + j * Cfg::A_KB, tm_a, bar, c_base + cur.c, w_org, h_org, n_img,
                                                  static_cast<uint16_t>(cur.s * kp.dw), static_cast<uint16_t>(cur.r * kp.dh));
                     cur.step(kp);
                 }
@@ -551,8 +566,8 @@ __device__ void pair_epilogue(const ConvKernelParams& kp, const PairSmem& sm, ui
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
         const PairRows<HALO> rows(kp, m_tile, rank);
         const bool has_rows = rows.any;  // a half past the output stores nothing and takes no turn
-        const int n0 = n_tile * BN;
-        const int n_end = n0 + BN < kp.K ? n0 + BN : kp.K;
+        int n0, n_end, c_base_unused;
+        pair_columns<BN>(kp, n_tile, n0, n_end, c_base_unused);
         const int sem = pair_sem_index(kp, m_tile, rank, n_tile);
         const bool cut = sg.nsplits > 1;
         const bool add_bias = kp.bias != nullptr && sg.split == 0;

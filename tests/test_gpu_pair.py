@@ -174,8 +174,47 @@ def test_pair_fused_epilogue_refuses_cut_tiles(sg, long_k):
     assert e.value.code == 2  # CONV2D_ERR_UNSUPPORTED
 
 
+GROUPED = {
+    "g2_cg64_kg64": (2, 10, 10, 128, 128, 3, 3, 1, 1, 1, 2),
+    "g4_cg64_kg128_s2": (2, 13, 11, 256, 512, 3, 3, 2, 1, 1, 4),
+    "g2_cg128_kg96": (1, 9, 12, 256, 192, 3, 3, 1, 1, 2, 2),
+    "g8_cg64_kg64_1x1": (3, 8, 8, 512, 512, 1, 1, 1, 0, 1, 8),
+}
+
+
+@pytest.mark.parametrize("split", [0, 3])
+@pytest.mark.parametrize("name", sorted(GROUPED))
+def test_pair_grouped(sg, name, split):
+    """Groups of 64+ channels on the pair kernel: column blocks never straddle a group, each
+    group's im2col boxes start at its first input channel; whole and cut tiles."""
+    n, h, w_, c, k, r, s, stride, pad, dil, groups = GROUPED[name]
+    wl = workloads.Workload(f"pg{groups}", n, h, w_, c, k, r, s, stride, stride, pad, pad, dil, dil,
+                            x_dist="normal", w_dist="he", bias="normal:0.1", seed=sum(map(ord, name)) % 1000,
+                            groups=groups)
+    x, w, b = workloads.make_inputs(wl)
+    algo = make_algo(sg, loader=PAIR, wait_limit_ns=WAIT, splits=split)
+    stages = -(-(c // groups * r * s // 64) // 2)
+    if split > stages:  # every split needs a stage
+        with pytest.raises(sg.Conv2dError) as e:
+            gpu_conv(sg, x, w, b, wl.options(), algo=algo)
+        assert e.value.code == 2
+        return
+    got = gpu_conv(sg, x, w, b, wl.options(), algo=algo)
+    ref = oracle.conv2d_fwd(x, w, b, **wl.options())
+    check_close(got, ref, c // groups, r, s, f"pair grouped {name} splits={split}")
+
+
+def test_pair_grouped_integer_exact(sg):
+    wl = workloads.Workload("pgi", 2, 9, 10, 256, 256, 3, 3, 1, 1, 1, 1, 1, 1, x_dist="int:-3:3", w_dist="int:-3:3",
+                            bias="int:-3:3", seed=5, groups=4)
+    x, w, b = workloads.make_inputs(wl)
+    got = gpu_conv(sg, x, w, b, wl.options(), algo=make_algo(sg, loader=PAIR, wait_limit_ns=WAIT))
+    ref = oracle.conv2d_fwd(x, w, b, **wl.options())
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("shape", [
-    (1, 8, 8, 64, 64, 3, 3, 1, 1, 1, 2),    # groups
+    (1, 8, 8, 64, 64, 3, 3, 1, 1, 1, 2),    # groups of 32 channels
     (1, 8, 8, 32, 64, 3, 3, 1, 1, 1, 1),    # C % 64 != 0
     (1, 8, 8, 64, 66, 3, 3, 1, 1, 1, 1),    # K % 4 != 0
 ])
