@@ -1582,8 +1582,12 @@ int run_conv(const conv2d_params* params, const void* x, const void* w, const fl
                                                  (int)s.cg, stream) != cudaSuccess)
                     return CONV2D_ERR_CUDA;
                 rc = run_plan(t, tplan, x, wb, bias, y, workspace, workspace_bytes, stream, &tf, relu, out_bf16);
-                if (rc == CONV2D_OK) g_last_launches = 2;  // the expansion and the convolution
-                return rc;
+                if (rc != CONV2D_OK) return rc;
+                // The workspace is zero at rest (a later call's semaphores or partial-sum
+                // buffer may lie where the expanded weight was): clear it in stream order.
+                if (cudaMemsetAsync(wb, 0, blockdiag_weight_bytes(s), stream) != cudaSuccess) return CONV2D_ERR_CUDA;
+                g_last_launches = 2;  // the expansion and the convolution
+                return CONV2D_OK;
             }
         }
     }

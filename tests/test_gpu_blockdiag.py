@@ -62,6 +62,18 @@ def test_blockdiag_geometries(sg, geom):
     check_close(got, ref, wl.c // wl.groups, wl.r, wl.s, f"block-diagonal {name}")
 
 
+def test_blockdiag_leaves_the_workspace_zero(sg):
+    """The expanded weight lives in the workspace only during the call: the workspace is
+    zero afterwards (a later call's semaphores and partial sums assume it)."""
+    wl, x, w, b = _case(2, 10, 10, 256, 256, 3, 3, 32, pad=1, seed=65)
+    params = sg.make_params(x.shape, w.shape, **wl.options())
+    ws = torch.zeros(sg.workspace_bytes(params), dtype=torch.uint8, device="cuda")
+    got = gpu_conv(sg, x, w, b, wl.options(), workspace=ws)
+    assert sg.last_launch_count() == 2
+    check_close(got, oracle.conv2d_fwd(x, w, b, **wl.options()), 8, 3, 3, "block-diagonal")
+    assert int(torch.count_nonzero(ws)) == 0
+
+
 @pytest.mark.parametrize("groups,c", [(32, 256), (8, 128), (4, 128)])
 def test_blockdiag_integer_inputs_exact(sg, groups, c):
     """Small integers: the zero blocks add exact zeros, so the result equals the oracle's."""
