@@ -1,4 +1,4 @@
-// Kernel instantiations for 256-channel output tiles (all three loaders).
+// Kernel instantiations of the one-CTA kernel for 256-channel output tiles (every loader kind, plain and fused epilogue).
 #include "conv2d_kernel.cuh"
 
 namespace sgb {

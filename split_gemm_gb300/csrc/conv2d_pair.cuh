@@ -3,9 +3,9 @@
 // The GEMM view is the one-CTA kernel's (burn PR #2287 "Introduce autotuning to
 // conv2d ...", Changes; burn PR #2545 "[Optimization] Implicit gemm rewrite",
 // Changes): rows m = (n*P + p)*Q + q are output pixels, columns are output
-// channels, the reduction index is kk = (r*S + s)*C + c, A is the im2col matrix
-// gathered tile by tile by TMA in im2col mode and B the KRSC weight viewed as
-// [K][C*R*S].
+// channels, the reduction index is kk = (r*S + s)*Cg + c (Cg = C / groups; a
+// column block stays inside one group), A is the im2col matrix gathered tile by
+// tile by TMA in im2col mode and B the KRSC weight viewed as [K][Cg*R*S].
 //
 // A tile is 256 output pixels x BN output channels, computed by a cluster of
 // two CTAs on two SMs.  Each CTA loads into its own shared memory the im2col
