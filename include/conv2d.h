@@ -115,9 +115,11 @@ typedef enum {
                                      computed and discarded), the pair the same pixels of two images; per
                                      64-channel chunk one tiled TMA box of whole padded input rows serves every
                                      filter tap, read in place by 2-CTA tensor-core MMAs, and the weights of
-                                     two or three taps come in one box per stage.  Needs groups == 1, stride 1,
-                                     C % 64 == 0, K % 4 == 0, W + 2*pad_w <= 256 and the two halo buffers within
-                                     shared memory; block_m is 256 (or 0); grid counts CTA pairs */
+                                     two or three taps come in one box per stage.  Needs stride 1,
+                                     C/groups % 64 == 0, K/groups % 4 == 0 (a column block lies in one group),
+                                     W + 2*pad_w <= 256 and the two halo buffers within shared memory; block_m
+                                     is 256 (or 0); grid counts CTA pairs.  The heuristic takes it for
+                                     ungrouped layers only */
     CONV2D_LOADER_BLOCKDIAG = 11  /* grouped convolution with C/groups == K/groups = cg in {8, 16, 32} and groups a
                                      multiple of 64/cg: 64/cg groups merged into one 64-channel group whose weight
                                      is block-diagonal (zeros outside each output channel's own group), expanded

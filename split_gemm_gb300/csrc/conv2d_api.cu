@@ -602,10 +602,11 @@ int pair_halo_smem(int bn, int taps, int halo_bytes)
 // The CTA-pair halo loader: geometry (row pitch, row-blocks, halo rows and
 // bytes, taps per stage) for tile width bn, or false when the shape does not
 // allow it.  Stages hold three taps where the ring still fits beside the two
-// halo buffers (64- and 128-wide tiles), else two.
+// halo buffers (64- and 128-wide tiles), else two.  Groups need Cg, the chunked
+// reduction of one group, to be whole 64-channel chunks.
 bool halo_pair_geometry(const Shape& s, int bn, HaloGeom* g)
 {
-    if (s.g != 1 || s.sh != 1 || s.sw != 1 || s.c % BK != 0 || s.k % 4 != 0 || s.p < 1) return false;
+    if (s.sh != 1 || s.sw != 1 || s.cg % BK != 0 || s.kg % 4 != 0 || s.p < 1) return false;
     const int64_t wv = s.w + 2 * s.pw;
     if (wv > 256) return false;
     const int64_t vp = s.p * wv;
@@ -661,14 +662,14 @@ cudaError_t launch_pair_halo(int bn, int taps, const CUtensorMap& a, const CUten
 int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
 {
     if (force && force->block_m != 0 && force->block_m != sgb::PAIR_TILE_M) return CONV2D_ERR_UNSUPPORTED;
-    int bn = force && force->block_n ? force->block_n : (s.k <= 64 ? 64 : (s.k <= 128 ? 128 : 256));
+    int bn = force && force->block_n ? force->block_n : (s.kg <= 64 ? 64 : (s.kg <= 128 ? 128 : 256));
     if (bn != 64 && bn != 128 && bn != 256) return CONV2D_ERR_INVALID;
     HaloGeom g;
     if (!halo_pair_geometry(s, bn, &g)) return CONV2D_ERR_UNSUPPORTED;
     const int64_t m_tiles = g.m_tiles;
-    const int64_t n_tiles = cdiv(s.k, bn);
+    const int64_t n_tiles = s.g * cdiv(s.kg, bn);  // column blocks within each group
     const int64_t tiles = m_tiles * n_tiles;
-    const int64_t stages = (s.c / BK) * cdiv(s.r * s.s, g.taps);  // chunk-major
+    const int64_t stages = (s.cg / BK) * cdiv(s.r * s.s, g.taps);  // chunk-major
     const int64_t units = tiles * stages;
     const int64_t resident = pair_halo_max_resident(bn, g.taps, whole_tiles, g.halo_bytes);
     if (resident <= 0) return CONV2D_ERR_CUDA;
@@ -725,12 +726,15 @@ int choose_pair_halo_plan(const Shape& s, const conv2d_algo* force, Plan* plan, 
 //    split at least 8 stages long; only when the 256-row tiles waste at most 35%
 //    of their rows and the epilogue is not fused (a fused epilogue needs whole
 //    tiles).
-//  - Whole-tile stride-1 layers with at least 128 input channels whose halo
+//  - Whole-tile stride-1 ungrouped layers with at least 128 input channels whose halo
 //    tiles fill at least 70% of the resident pairs' waves and whose
 //    virtual pixels (padded row pitch, image pairs) exceed the output pixels by
 //    at most 20%: the halo loader, one tile per pair per wave.
 //  - Otherwise, where the pair tiles cover at least half the resident pairs
-//    (and waste at most 35% of their rows): the im2col pair loader.
+//    (and waste at most 35% of their rows): the im2col pair loader.  Grouped
+//    layers stay on it: with 64-wide group tiles the halo kernel's MMAs and stage
+//    handshakes (35-40 ns per 256x64x16 MMA) set the same pace as the im2col
+//    kernel's activation loads, and its virtual pixels add 14% on a 28x28 layer.
 int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool whole_tiles)
 {
     if (!pair_eligible(s)) return CONV2D_ERR_UNSUPPORTED;
@@ -756,8 +760,8 @@ int choose_auto_pair(const Shape& s, const conv2d_algo* force, Plan* plan, bool 
         }
     }
     HaloGeom g;
-    if (s.c >= 128 && halo_pair_geometry(s, bn, &g)) {
-        const int64_t tiles = g.m_tiles * cdiv(s.k, bn);
+    if (s.g == 1 && s.c >= 128 && halo_pair_geometry(s, bn, &g)) {
+        const int64_t tiles = g.m_tiles * col_blocks;
         const int64_t res = pair_halo_max_resident(bn, g.taps, whole_tiles, g.halo_bytes);
         const int64_t virt = cdiv(s.n, 2) * 2 * static_cast<int64_t>(g.tpi) * sgb::PAIR_ROWS;
         if (res > 0) {
@@ -990,8 +994,8 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
     if (!load_encoders()) return CONV2D_ERR_CUDA;
     if (plan.loader == CONV2D_LOADER_PAIR_HALO) {
         // A: x as {C, W, H, N}; a box is one 64-channel chunk of hr whole padded rows (wv columns
-        // from -pad_w), landing pixel-major in 128-byte rows.  B: w as {64, K, C/64, R*S}; a box
-        // is block_n/2 weight rows of one chunk at two consecutive taps (a tap past R*S reads zeros).
+        // from -pad_w), landing pixel-major in 128-byte rows.  B: w as {64, K, Cg/64, R*S}; a box
+        // is block_n/2 weight rows of one chunk at kbs consecutive taps (a tap past R*S reads zeros).
         const HaloGeom& g = plan.halo;
         const cuuint64_t dims[4] = {(cuuint64_t)s.c, (cuuint64_t)s.w, (cuuint64_t)s.h, (cuuint64_t)s.n};
         const cuuint64_t strides[3] = {(cuuint64_t)(s.c * 2), (cuuint64_t)(s.w * s.c * 2),
@@ -1002,8 +1006,8 @@ int encode_maps(const Shape& s, const Plan& plan, const void* x, const void* w, 
                                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (rc != CUDA_SUCCESS) return CONV2D_ERR_CUDA;
-        const cuuint64_t wd[4] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.c / BK), (cuuint64_t)(s.r * s.s)};
-        const cuuint64_t ws[3] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2), (cuuint64_t)(s.c * 2)};
+        const cuuint64_t wd[4] = {(cuuint64_t)BK, (cuuint64_t)s.k, (cuuint64_t)(s.cg / BK), (cuuint64_t)(s.r * s.s)};
+        const cuuint64_t ws[3] = {(cuuint64_t)(s.crs * 2), (cuuint64_t)(BK * 2), (cuuint64_t)(s.cg * 2)};
         const cuuint32_t wb[4] = {(cuuint32_t)BK, (cuuint32_t)(plan.block_n / 2), 1, (cuuint32_t)plan.kbs};
         const cuuint32_t we[4] = {1, 1, 1, 1};
         rc = g_encode_tiled(tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), wd, ws, wb, we,

@@ -832,7 +832,9 @@ __global__ void __launch_bounds__(PairConfig<BN, KBS>::THREADS, 1)
 // weight rows of two or three taps of one chunk come in one 4-D box per stage;
 // the reduction runs chunk-major, then over the taps.  Per k-block
 // this is about 0.1 TMA operation of activations (against one for the im2col
-// loader) and half an operation of weights.
+// loader) and half an operation of weights.  Under groups a column block lies
+// in one group (pair_columns) and its chunks are that group's Cg input
+// channels, from channel g*Cg of x and from the group's weight rows.
 template <int BN, int TAPS_>
 struct HaloPairConfig {
     static constexpr int B_ROWS = BN / 2;
@@ -895,11 +897,12 @@ __device__ void halo_pair_prefetch(const CUtensorMap* tm_a, const CUtensorMap* t
     if (!walk.next(kp, sg)) return;
     int m_tile, n_tile;
     pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-    int n_img, j0, prow0, chunk, tap0;
+    int n_img, j0, prow0, chunk, tap0, n0, n_end, c_base;
     halo_block(kp, m_tile, rank, n_img, j0, prow0);
     halo_stage<TAPS>(kp, sg.kb_begin, chunk, tap0);
-    if (n_img < kp.N) ptx::tma_prefetch_4d(tm_a, chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
-    const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+    pair_columns<BN>(kp, n_tile, n0, n_end, c_base);
+    if (n_img < kp.N) ptx::tma_prefetch_4d(tm_a, c_base + chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
+    const int b_row = n0 + static_cast<int>(rank) * Cfg::B_ROWS;
     for (int st = sg.kb_begin; st < sg.kb_end && st < sg.kb_begin + Cfg::STAGES; ++st) {
         halo_stage<TAPS>(kp, st, chunk, tap0);
         ptx::tma_prefetch_4d(tm_b, 0, b_row, chunk, tap0);
@@ -919,8 +922,9 @@ __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelPa
     while (ok && walk.next(kp, sg)) {
         int m_tile, n_tile;
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-        int n_img, j0, prow0;
+        int n_img, j0, prow0, n0, n_end, c_base;
         halo_block(kp, m_tile, rank, n_img, j0, prow0);
+        pair_columns<BN>(kp, n_tile, n0, n_end, c_base);  // the group's channels start at c_base
         for (int st = sg.kb_begin; st < sg.kb_end; ++st) {
             int chunk, tap0;
             halo_stage<TAPS>(kp, st, chunk, tap0);
@@ -938,7 +942,7 @@ __device__ void halo_pair_producer_a(const CUtensorMap* tm_a, const ConvKernelPa
             }
             if (rank == 0) ptx::mbar_arrive_expect_tx(&sm.halo_full[slot], 2u * static_cast<uint32_t>(kp.halo_tx));
             ptx::tma_load_4d_pair(sm.halo + slot * kp.halo_bytes, tm_a, hfull0 + static_cast<uint32_t>(slot) * 8u,
-                                  chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
+                                  c_base + chunk * BK, -kp.pw, prow0 - kp.ph, n_img);
             SGB_PAIR_MARK(kp, 200 + h, static_cast<int>(rank));
             ++h;
         }
@@ -966,7 +970,9 @@ __device__ void halo_pair_producer_b(const CUtensorMap* tm_b, const ConvKernelPa
         SGB_TRACE(kp, it == 0, 9);  // weight producer: first segment
         int m_tile, n_tile;
         pair_tile_coords(kp, sg.tile, m_tile, n_tile);
-        const int b_row = n_tile * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        int n0, n_end, c_base;
+        pair_columns<BN>(kp, n_tile, n0, n_end, c_base);
+        const int b_row = n0 + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int st = sg.kb_begin; st < sg.kb_end; ++st, ++it) {
             const int slot = it % STAGES;
             if (*sm.abort_flag) { ok = false; break; }

@@ -62,13 +62,14 @@ def test_auto_plans_random_layers(sg, seed):
 
 
 def test_auto_plans_cover_the_pair_kernels(sg):
-    """The draw above reaches the im2col pair kernel and the block-diagonal tiles (so a change
-    of the rules that stopped exercising them would show here rather than pass silently; the
-    halo pair kernel is the heuristic's plan for the full-size 28x28 and dilated layers,
-    which the workload tests run)."""
+    """The draw above reaches a CTA-pair kernel and the block-diagonal tiles (so a change of
+    the rules that stopped exercising them would show here rather than pass silently; the
+    workload tests run both pair kernels at full size: the im2col one on the 56x56, split-K,
+    projection and grouped layers, the halo one on the 28x28 and dilated layers, and forced on
+    the grouped layer)."""
     loaders = set()
     for seed in range(16):
         wl = _draw(seed)
         loaders.add(sg.query_algo(sg.make_params((wl.n, wl.h, wl.w, wl.c), (wl.k, wl.r, wl.s, wl.c // wl.groups),
                                                  **wl.options())).loader)
-    assert {sg.LOADER_TMA_PAIR, sg.LOADER_BLOCKDIAG} <= loaders, loaders
+    assert sg.LOADER_BLOCKDIAG in loaders and loaders & {sg.LOADER_TMA_PAIR, sg.LOADER_PAIR_HALO}, loaders

@@ -25,13 +25,14 @@ def sg():
     return split_gemm_gb300
 
 
-def _case(n, h, w, c, k, r, s, pad=0, dil=1, bias=True, seed=0, dist="normal"):
+def _case(n, h, w, c, k, r, s, pad=0, dil=1, bias=True, seed=0, dist="normal", groups=1):
     def two(v):
         return v if isinstance(v, tuple) else (v, v)
     (ph, pw), (dh, dw) = two(pad), two(dil)
     wl = workloads.Workload(f"halo{seed}", n, h, w, c, k, r, s, 1, 1, ph, pw, dh, dw,
                             x_dist=dist, w_dist="he" if dist == "normal" else dist,
-                            bias=("normal:0.1" if dist == "normal" else dist) if bias else None, seed=seed)
+                            bias=("normal:0.1" if dist == "normal" else dist) if bias else None, seed=seed,
+                            groups=groups)
     x, wt, b = workloads.make_inputs(wl)
     return wl, x, wt, b
 
@@ -39,7 +40,7 @@ def _case(n, h, w, c, k, r, s, pad=0, dil=1, bias=True, seed=0, dist="normal"):
 def _check(sg, wl, x, w, b, algo, what):
     got = gpu_conv(sg, x, w, b, wl.options(), algo=algo)
     ref = oracle.conv2d_fwd(x, w, b, **wl.options())
-    check_close(got, ref, wl.c, wl.r, wl.s, what)
+    check_close(got, ref, wl.c // wl.groups, wl.r, wl.s, what)
     return got, ref
 
 
@@ -174,22 +175,61 @@ def test_halo_fused_epilogue_whole_tiles(sg, name, mode):
     check_epilogue(got.astype(np.float64), u, wl.c, wl.r, wl.s, *mode, f"{name} fused {mode}")
 
 
+# Groups on the halo kernel (n, h, w, c, k, r, s, pad, dil, groups): one and two chunks per
+# group, an odd image count, a group narrower than the tile (its block reads the next group's
+# weight rows and stores only its own columns), a group width that is not a tile multiple,
+# dilation and 1x1.
+GROUPED = {
+    "g2_cg64_kg64": (2, 10, 10, 128, 128, 3, 3, 1, 1, 2),
+    "g4_cg64_kg128_n3": (3, 13, 11, 256, 512, 3, 3, 1, 1, 4),
+    "g2_cg128_kg96_dil2": (1, 9, 12, 256, 192, 3, 3, 2, 2, 2),
+    "g8_cg64_kg64_1x1": (3, 8, 8, 512, 512, 1, 1, 0, 1, 8),
+    "g4_cg64_kg16": (2, 7, 7, 256, 64, 3, 3, 1, 1, 4),
+}
+
+
+@pytest.mark.parametrize("split", [0, 3])
+@pytest.mark.parametrize("name", sorted(GROUPED))
+def test_halo_grouped(sg, name, split):
+    """Column blocks never straddle a group; each group's halos start at its first input
+    channel and its weight boxes at its own rows; whole and cut tiles."""
+    n, h, w_, c, k, r, s, pad, dil, groups = GROUPED[name]
+    wl, x, w, b = _case(n, h, w_, c, k, r, s, pad, dil, seed=sum(map(ord, name)) % 997, groups=groups)
+    algo = make_algo(sg, loader=HALO, wait_limit_ns=WAIT, splits=split)
+    stages = (c // groups // 64) * -(-(r * s) // 3)  # at most this many (three taps per stage)
+    if split > stages:
+        with pytest.raises(sg.Conv2dError) as e:
+            gpu_conv(sg, x, w, b, wl.options(), algo=algo)
+        assert e.value.code == 2
+        return
+    _check(sg, wl, x, w, b, algo, f"halo grouped {name} splits={split}")
+
+
+def test_halo_grouped_integer_exact(sg):
+    wl, x, w, b = _case(3, 9, 10, 256, 256, 3, 3, 1, 1, seed=7, dist="int:-3:3", groups=4)
+    got = gpu_conv(sg, x, w, b, wl.options(), algo=make_algo(sg, loader=HALO, wait_limit_ns=WAIT))
+    ref = oracle.conv2d_fwd(x, w, b, **wl.options())
+    assert np.array_equal(got.astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("shape", [
-    (1, 8, 8, 64, 64, 3, 3, 2, 1, 1),    # stride 2
-    (1, 8, 8, 32, 64, 3, 3, 1, 1, 1),    # C % 64 != 0
-    (1, 8, 300, 64, 64, 3, 3, 1, 1, 1),  # padded row longer than a TMA box dimension
+    (1, 8, 8, 64, 64, 3, 3, 2, 1, 1, 1),    # stride 2
+    (1, 8, 8, 32, 64, 3, 3, 1, 1, 1, 1),    # C % 64 != 0
+    (1, 8, 300, 64, 64, 3, 3, 1, 1, 1, 1),  # padded row longer than a TMA box dimension
+    (1, 8, 8, 128, 64, 3, 3, 1, 1, 1, 4),   # groups of 32 channels
 ])
 def test_halo_refuses_ineligible_shapes(sg, shape):
-    n, h, w_, c, k, r, s, stride, pad, dil = shape
+    n, h, w_, c, k, r, s, stride, pad, dil, groups = shape
     dev = torch.device("cuda", 0)
     x = torch.zeros((n, h, w_, c), dtype=torch.bfloat16, device=dev)
-    w = torch.zeros((k, r, s, c), dtype=torch.bfloat16, device=dev)
+    w = torch.zeros((k, r, s, c // groups), dtype=torch.bfloat16, device=dev)
     with pytest.raises(sg.Conv2dError) as e:
-        sg.conv2d_fwd(x, w, None, stride, pad, dil, 1, algo=make_algo(sg, loader=HALO))
+        sg.conv2d_fwd(x, w, None, stride, pad, dil, groups, algo=make_algo(sg, loader=HALO))
     assert e.value.code == 2
 
 
-@pytest.mark.parametrize("name", ["resnet_56x56_c64", "resnet_28x28_c256", "splitk_7x7_c2048", "dil2_64_c128"])
+@pytest.mark.parametrize("name", ["resnet_56x56_c64", "resnet_28x28_c256", "splitk_7x7_c2048", "dil2_64_c128",
+                                  "grouped_28x28_c512_g8"])
 def test_halo_full_size_workloads(sg, name):
     wl = workloads.get(name)
     x, w, b = workloads.make_inputs(wl)
