@@ -457,7 +457,8 @@ bool plan_cuts_tiles(const Plan& p);
 // The CTA-pair kernel (conv2d_pair.cuh): 256-pixel tiles on clusters of two
 // CTAs, TMA im2col loads of 128 pixels per CTA, 16-byte vector stores.
 // The im2col pair kernel: C/groups % 64 == 0 (im2col boxes inside one group), K/groups % 4 == 0
-// (16-byte stores inside one group's columns).  The halo pair kernel needs groups == 1.
+// (16-byte stores inside one group's columns); the halo pair kernel adds its own
+// geometry conditions (halo_pair_geometry).
 bool pair_eligible(const Shape& s) { return tma_im2col_eligible(s) && s.kg % 4 == 0; }
 
 int pair_max_resident(int bn, int kbs, bool fused)
