@@ -53,3 +53,25 @@ def test_reference_arm_prints_one_json_line(op):
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert ("wgrad" in d["metric"]) == (op == "wgrad") and ("dgrad" in d["metric"]) == (op == "dgrad")
+
+
+def test_traffic_table_format_and_hash_gate(monkeypatch):
+    """profiles/ncu_traffic.txt: one line per workload (optionally :wgrad / :dgrad) with the kernel
+    sources' hash and a positive byte count; the bench reports a figure only while the hash matches."""
+    lines = [l.split() for l in open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")).read().splitlines()
+             if l.strip() and not l.startswith("#")]
+    assert lines
+    hashes = set()
+    for name, h, nbytes in lines:
+        wl_name, _, op = name.partition(":")
+        assert wl_name in workloads.WORKLOADS and op in ("", "wgrad", "dgrad"), name
+        assert len(h) == 16 and int(h, 16) >= 0
+        assert int(nbytes) > 0
+        hashes.add(h)
+    assert len(hashes) == 1  # one capture of one source tree
+    table_hash = hashes.pop()
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: table_hash)
+    want = {name: float(nbytes) for name, _, nbytes in lines}
+    assert bench.recorded_traffic("resnet_28x28_c256") == want["resnet_28x28_c256"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic("resnet_28x28_c256") is None
